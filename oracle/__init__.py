@@ -1,0 +1,164 @@
+"""fp64 CPU oracle for paged split-KV decode attention -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
+baseline / reference arm may import this package. The CUDA library never
+links it and it imports nothing from the CUDA library's package: it takes
+plain CPU arrays (torch CPU tensors or numpy arrays) and returns fp64 numpy
+arrays.
+
+The arithmetic lives in ``pdo_oracle.c`` (plain C, fp64, OpenMP over output
+items); this module compiles it with gcc on first use and wraps it with
+ctypes. The method it states, and the readings of the pages it takes, are in
+that file's header: per-row causal limit p_i = L - R + i, optional sliding
+window of W keys, contiguous GQA groups, bf16 or OCP E4M3 cache values with
+per-tensor or per-(token, kv head) scales ("perf(attention): run up to 8
+query rows per request in the triton decode kernel", section "Changes";
+"fp8 support", section "Functionality"; "Naive Support for Hopper FP8
+Prefill Kernel with Per-Head Quantization", item 3).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pdo_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LOCK = threading.Lock()
+_LIBS: dict = {}
+
+PDO_OK = 0
+PDO_ERR_ARG = -1
+PDO_ERR_KVLEN = -2
+
+
+def lib_path(mutation: int = 0) -> str:
+    name = "libpdo.so" if mutation == 0 else f"libpdo_mut{mutation}.so"
+    return os.path.join(_BUILD, name)
+
+
+def build(mutation: int = 0, force: bool = False) -> str:
+    """Compile the oracle (gcc, -O2, no FP contraction) into oracle/_build.
+
+    ``mutation`` > 0 builds a copy with one deliberate mistake planted
+    (``PDO_MUTATION``); the test suite uses those copies to show that the
+    pins catch each such mistake. The default build has none.
+    """
+    out = lib_path(mutation)
+    with _LOCK:
+        if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
+            return out
+        os.makedirs(_BUILD, exist_ok=True)
+        tmp = out + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
+               _SRC, "-o", tmp, "-lm"]
+        if mutation:
+            cmd.insert(1, f"-DPDO_MUTATION={mutation}")
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, out)
+    return out
+
+
+def _load(mutation: int = 0):
+    if mutation in _LIBS:
+        return _LIBS[mutation]
+    lib = ctypes.CDLL(build(mutation))
+    i32, i64, vp, dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_double
+    lib.pdo_attention.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i64, i64, i64, i64,
+                                  vp, vp, vp, vp, vp, vp, vp, vp, dbl, vp, vp, i64, vp, i64,
+                                  vp, vp, i32]
+    lib.pdo_attention.restype = i32
+    lib.pdo_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.pdo_e4m3_to_double.restype = dbl
+    lib.pdo_max_threads.restype = i32
+    _LIBS[mutation] = lib
+    return lib
+
+
+def _np(x, dtype=None):
+    """Contiguous numpy view of a CPU torch tensor / numpy array (None stays None)."""
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor: reinterpret 16-/8-bit payloads as integers
+        import torch
+        t = x.detach().cpu().contiguous()
+        if t.dtype == torch.bfloat16:
+            t = t.view(torch.int16)
+        elif t.dtype in (getattr(torch, "float8_e4m3fn", None),):
+            t = t.view(torch.uint8)
+        x = t.numpy()
+    x = np.ascontiguousarray(x)
+    if dtype is not None:
+        x = x.astype(dtype, copy=False)
+    return x
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def e4m3_to_double(code: int, mutation: int = 0) -> float:
+    return _load(mutation).pdo_e4m3_to_double(int(code) & 0xFF)
+
+
+def max_threads() -> int:
+    return int(_load().pdo_max_threads())
+
+
+def attention(*, q, k_pages, v_pages, page_table, kv_indptr, kv_len, qo_indptr, window,
+              sm_scale, k_scale=None, v_scale=None, num_qo_heads, num_kv_heads, head_dim,
+              page_size, q_e4m3, kv_e4m3, scale_mode, strides, num_pages, items=None,
+              split_tokens=0, num_threads=0, mutation=0, check=True):
+    """fp64 attention for the given (row, q head) items.
+
+    Arrays are CPU tensors / numpy arrays holding raw cache payloads (bf16 as
+    16-bit words, e4m3 as bytes). ``strides`` = (page, token, head) in
+    elements. ``items`` = flat indices row*Hq + h (None: every item).
+    Returns (out [n, D] float64, lse [n] float64, status).
+    """
+    lib = _load(mutation)
+    q_ = _np(q)
+    k_ = _np(k_pages)
+    v_ = _np(v_pages)
+    pt = _np(page_table, np.int32)
+    ki = _np(kv_indptr, np.int32)
+    kl = _np(kv_len, np.int32)
+    qi = _np(qo_indptr, np.int32)
+    win = _np(window, np.int32)
+    ks = _np(k_scale, np.float32)
+    vs = _np(v_scale, np.float32)
+    it = _np(items, np.int64)
+    batch = int(kl.shape[0])
+    total_rows = int(qi[batch]) if batch else 0
+    n = int(it.shape[0]) if it is not None else total_rows * num_qo_heads
+    out = np.zeros((max(n, 0), head_dim), dtype=np.float64)
+    lse = np.zeros((max(n, 0),), dtype=np.float64)
+    sp, st, sh = (int(s) for s in strides)
+    rc = lib.pdo_attention(batch, num_qo_heads, num_kv_heads, head_dim, page_size, int(q_e4m3),
+                           int(kv_e4m3), int(scale_mode), sp, st, sh, int(num_pages), _ptr(q_),
+                           _ptr(k_), _ptr(v_), _ptr(pt), _ptr(ki), _ptr(kl), _ptr(qi), _ptr(win),
+                           float(sm_scale), _ptr(ks), _ptr(vs), int(split_tokens), _ptr(it),
+                           n if it is not None else 0, _ptr(out), _ptr(lse), int(num_threads))
+    if check and rc == PDO_ERR_ARG:
+        raise ValueError("oracle rejected its arguments")
+    return out, lse, rc
+
+
+def attention_for(wl, items=None, split_tokens=0, num_threads=0, mutation=0, **overrides):
+    """``attention`` on a workload object that carries the fields by name
+    (q, k_pages, ..., num_qo_heads, ...). The object only transports arrays;
+    nothing of its arithmetic is used."""
+    args = dict(q=wl.q, k_pages=wl.k_pages, v_pages=wl.v_pages, page_table=wl.page_table,
+                kv_indptr=wl.kv_indptr, kv_len=wl.kv_len, qo_indptr=wl.qo_indptr,
+                window=wl.window, sm_scale=wl.sm_scale, k_scale=wl.k_scale, v_scale=wl.v_scale,
+                num_qo_heads=wl.num_qo_heads, num_kv_heads=wl.num_kv_heads,
+                head_dim=wl.head_dim, page_size=wl.page_size, q_e4m3=wl.q_e4m3,
+                kv_e4m3=wl.kv_e4m3, scale_mode=wl.scale_mode, strides=wl.strides,
+                num_pages=wl.num_pages)
+    args.update(overrides)
+    return attention(items=items, split_tokens=split_tokens, num_threads=num_threads,
+                     mutation=mutation, **args)

@@ -1,0 +1,256 @@
+/*
+ * pdo_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, fp64 CPU statement of what paged split-KV decode attention
+ * computes. Only the test suite, the smoke check and the benchmark's CPU
+ * baseline load this file's library; the CUDA library never links it, and it
+ * includes nothing from the CUDA library (its own types, its own decoders).
+ *
+ * What it follows:
+ *  - "perf(attention): run up to 8 query rows per request in the triton
+ *    decode kernel" (FreeToken PR #900), section "Changes": each request has
+ *    up to 8 causal query rows (qo_indptr, max_q_len); every row sees keys up
+ *    to its own position and inside its window; the KV split is merged per
+ *    row. Query head h reads kv head h / (Hq/Hkv) (contiguous GQA groups).
+ *  - "fp8 support" (FlashMLA PR #54), section "Functionality": symmetric
+ *    per-tensor FP8 scales.
+ *  - FreeToken PR #900, section "End-to-end A/B": the fp8_per_token_head KV
+ *    dtype, i.e. one fp32 scale per (token, kv head).
+ *  - "Naive Support for Hopper FP8 Prefill Kernel with Per-Head Quantization"
+ *    (FlashInfer PR #869), item 3 "Fused Dequantization": the dequant scales
+ *    are plain multipliers on the QK logits and on the PV output, so the
+ *    oracle applies them to the decoded K and V values directly.
+ *
+ * Readings of the pages taken here (the pages leave these open):
+ *  - Row i of a request with R rows and L cached tokens sits at position
+ *    p_i = L - R + i (the R new tokens are already in the cache).
+ *  - A window W > 0 counts keys including the row's own: p_i-W+1 <= j <= p_i.
+ *    W <= 0, or no window array, means no lower bound.
+ *  - lse is the natural log of sum_j exp(s_j) over the scaled logits.
+ *  - FP8 is OCP E4M3 ("e4m3fn": bias 7, no infinities, S.1111.111 is NaN).
+ *
+ * Split mode (split_tokens > 0) cuts the key axis into chunks
+ * [c*T, (c+1)*T), computes (o_c, lse_c) per chunk with the same two-pass
+ * softmax and merges them: M = max lse_c, w_c = exp(lse_c - M),
+ * o = sum w_c o_c / sum w_c, lse = M + ln sum w_c; a chunk with no visible
+ * key has lse_c = -inf and weight 0 (the per-row merge of "Changes").
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Mutation hooks. The normal build defines PDO_MUTATION as 0, so every MUT(k)
+ * below is the constant 0 and changes nothing. The test suite compiles extra
+ * copies with one PDO_MUTATION = k each: every such copy carries one
+ * plausible mistake, and the suite checks that the oracle's pins reject it. */
+#ifndef PDO_MUTATION
+#define PDO_MUTATION 0
+#endif
+#define MUT(k) (PDO_MUTATION == (k))
+
+#define PDO_OK 0
+#define PDO_ERR_ARG (-1)
+#define PDO_ERR_KVLEN (-2) /* a request has kv_len < rows: its outputs are NaN */
+
+/* bf16 is the upper half of an IEEE binary32 word. */
+static double pdo_bf16_to_double(uint16_t bits) {
+  uint32_t w = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &w, sizeof f);
+  return (double)f;
+}
+
+/* OCP 8-bit floating point, E4M3: sign bit 7, exponent bits 6..3 with bias 7,
+ * mantissa bits 2..0. Exponent field 0 is subnormal (2^-6 * m/8). The pattern
+ * with exponent 15 and mantissa 7 is NaN; there is no infinity. */
+double pdo_e4m3_to_double(uint8_t code) {
+  int sign = (code >> 7) & 1;
+  int e = (code >> 3) & 0xF;
+  int m = code & 0x7;
+  double mag;
+  if (e == 0xF && m == 0x7) return NAN;
+  if (e == 0)
+    mag = ldexp((double)m / 8.0, -6 - MUT(7));
+  else
+    mag = ldexp(1.0 + (double)m / 8.0, e - 7 - MUT(6));
+  return sign ? -mag : mag;
+}
+
+typedef struct {
+  int batch, hq, hkv, d, page_size;
+  int q_e4m3, kv_e4m3, scale_mode; /* scale_mode: 0 none, 1 per tensor, 2 per (token, kv head) */
+  int64_t sp, st, sh;              /* cache strides in elements: page, token-in-page, kv head */
+  int64_t num_pages;
+  const void *q, *k, *v;
+  const int32_t *page_table, *kv_indptr, *kv_len, *qo_indptr, *window;
+  double sm_scale;
+  const float *k_scale, *v_scale;
+} pdo_problem;
+
+static double pdo_q_elem(const pdo_problem* p, int64_t row, int h, int d) {
+  int64_t idx = ((row - MUT(14) * (row > 0)) * p->hq + h) * (int64_t)p->d + d;
+  if (p->q_e4m3) return pdo_e4m3_to_double(((const uint8_t*)p->q)[idx]);
+  return pdo_bf16_to_double(((const uint16_t*)p->q)[idx]);
+}
+
+/* Dequantised K or V element of kv head g at token j of request b. */
+static double pdo_kv_elem(const pdo_problem* p, const void* cache, const float* scale, int b,
+                          int64_t j, int g, int d) {
+  int64_t page = p->page_table[p->kv_indptr[b] + j / p->page_size + MUT(13)];
+  int64_t slot = j % p->page_size;
+  int64_t idx = MUT(10) ? page * p->sp + slot * p->sh + (int64_t)g * p->st + d
+                        : page * p->sp + slot * p->st + (int64_t)g * p->sh + d;
+  double x;
+  if (p->kv_e4m3)
+    x = pdo_e4m3_to_double(((const uint8_t*)cache)[idx]);
+  else
+    x = pdo_bf16_to_double(((const uint16_t*)cache)[idx]);
+  if (p->scale_mode == 1) x *= (double)scale[0];
+  if (p->scale_mode == 2) x *= (double)scale[(page * p->page_size + slot) * p->hkv + (MUT(4) ? 0 : g)];
+  return x;
+}
+
+/* Two-pass softmax attention of one query row over keys [lo, hi] (inclusive)
+ * of request b, kv head g. Writes o[0..d) and returns lse; an empty range
+ * gives o = 0 and lse = -inf. */
+static double pdo_attend_range(const pdo_problem* p, int b, int64_t row, int h, int g,
+                               int64_t lo, int64_t hi, double* s, double* o) {
+  int64_t n = hi - lo + 1;
+  for (int d = 0; d < p->d; ++d) o[d] = 0.0;
+  if (n <= 0) return -INFINITY;
+  double m = -INFINITY;
+  for (int64_t j = 0; j < n; ++j) {
+    double acc = 0.0;
+    for (int d = 0; d < p->d; ++d) acc += pdo_q_elem(p, row, h, d) * pdo_kv_elem(p, p->k, p->k_scale, b, lo + j, g, d);
+    s[j] = MUT(12) ? acc : p->sm_scale * acc;
+    if (s[j] > m) m = s[j];
+  }
+  double l = 0.0;
+  for (int64_t j = 0; j < n; ++j) {
+    double w = exp(s[j] - m);
+    l += w;
+    for (int d = 0; d < p->d; ++d) o[d] += w * pdo_kv_elem(p, p->v, MUT(9) ? p->k_scale : p->v_scale, b, lo + j, g, d);
+  }
+  if (!MUT(15))
+    for (int d = 0; d < p->d; ++d) o[d] /= l;
+  return MUT(5) ? log(l) : m + log(l);
+}
+
+/* One (query row, q head) item; returns PDO_OK or PDO_ERR_KVLEN. */
+static int pdo_item(const pdo_problem* p, int64_t row, int h, int64_t split_tokens, double* s,
+                    double* oc, double* out, double* lse_out) {
+  int b = 0;
+  while (b < p->batch && p->qo_indptr[b + 1] <= row) ++b; /* request owning this row */
+  int64_t rows_b = p->qo_indptr[b + 1] - p->qo_indptr[b];
+  int64_t i = row - p->qo_indptr[b];
+  int64_t L = p->kv_len[b];
+  if (L < rows_b) {
+    for (int d = 0; d < p->d; ++d) out[d] = NAN;
+    *lse_out = NAN;
+    return PDO_ERR_KVLEN;
+  }
+  int64_t pos = L - rows_b + i - MUT(11);
+  int64_t w = p->window ? p->window[b] : 0;
+  int64_t lo = (w > 0) ? pos - w + 1 - MUT(1) : 0;
+  if (lo < 0) lo = 0;
+  if (MUT(2)) pos = L - 1;
+  int g = MUT(3) ? h % p->hkv : h / (p->hq / p->hkv);
+  if (split_tokens <= 0) {
+    *lse_out = pdo_attend_range(p, b, row, h, g, lo, pos, s, out);
+    return PDO_OK;
+  }
+  /* Split mode: per-chunk partials, then the log-sum-exp merge. */
+  int64_t nchunks = pos / split_tokens + 1;
+  double* lse_c = (double*)malloc(sizeof(double) * (size_t)nchunks);
+  double* o_c = (double*)malloc(sizeof(double) * (size_t)nchunks * (size_t)p->d);
+  double big = -INFINITY;
+  for (int64_t c = 0; c < nchunks; ++c) {
+    int64_t a = c * split_tokens, e = a + split_tokens - 1;
+    if (a < lo) a = lo;
+    if (e > pos) e = pos;
+    lse_c[c] = pdo_attend_range(p, b, row, h, g, a, e, s, oc);
+    memcpy(o_c + c * p->d, oc, sizeof(double) * (size_t)p->d);
+    if (lse_c[c] > big) big = lse_c[c];
+  }
+  double wsum = 0.0;
+  for (int d = 0; d < p->d; ++d) out[d] = 0.0;
+  for (int64_t c = 0; c < nchunks; ++c) {
+    if (lse_c[c] == -INFINITY) continue; /* weight 0 */
+    double wc = exp(lse_c[c] - big);
+    wsum += wc;
+    for (int d = 0; d < p->d; ++d) out[d] += wc * o_c[c * p->d + d];
+  }
+  if (!MUT(8))
+    for (int d = 0; d < p->d; ++d) out[d] /= wsum;
+  *lse_out = big + log(wsum);
+  free(lse_c);
+  free(o_c);
+  return PDO_OK;
+}
+
+/*
+ * Attention output for the requested (query row, q head) items.
+ *   q        [total_rows, hq, d]   bf16 bits (uint16) or e4m3 codes (uint8)
+ *   k, v     paged cache, element (page, slot, kv head, c) at
+ *            page*sp + slot*st + head*sh + c; bf16 bits or e4m3 codes
+ *   k_scale, v_scale: NULL (scale_mode 0), [1] (1) or
+ *            [num_pages, page_size, hkv] (2)
+ *   items    NULL: all total_rows*hq items in order; else flat indices
+ *            row*hq + h, n_items of them
+ *   out      [n_items, d] fp64; lse [n_items] fp64 (natural log)
+ * Returns PDO_OK, PDO_ERR_ARG, or PDO_ERR_KVLEN (some rows set to NaN).
+ */
+int pdo_attention(int batch, int hq, int hkv, int d, int page_size, int q_e4m3, int kv_e4m3,
+                  int scale_mode, int64_t sp, int64_t st, int64_t sh, int64_t num_pages,
+                  const void* q, const void* k, const void* v, const int32_t* page_table,
+                  const int32_t* kv_indptr, const int32_t* kv_len, const int32_t* qo_indptr,
+                  const int32_t* window, double sm_scale, const float* k_scale,
+                  const float* v_scale, int64_t split_tokens, const int64_t* items,
+                  int64_t n_items, double* out, double* lse, int num_threads) {
+  if (batch < 0 || hq <= 0 || hkv <= 0 || hq % hkv || d <= 0 || page_size <= 0) return PDO_ERR_ARG;
+  if (scale_mode < 0 || scale_mode > 2 || (scale_mode && !kv_e4m3)) return PDO_ERR_ARG;
+  pdo_problem p = {batch, hq, hkv, d, page_size, q_e4m3, kv_e4m3, scale_mode, sp, st, sh, num_pages,
+                   q, k, v, page_table, kv_indptr, kv_len, qo_indptr, window, sm_scale,
+                   k_scale, v_scale};
+  int64_t total_rows = batch > 0 ? qo_indptr[batch] : 0;
+  int64_t n = items ? n_items : total_rows * hq;
+  int64_t max_len = 0;
+  for (int b = 0; b < batch; ++b)
+    if (kv_len[b] > max_len) max_len = kv_len[b];
+  int status = PDO_OK;
+#ifdef _OPENMP
+  if (num_threads > 0) omp_set_num_threads(num_threads);
+#else
+  (void)num_threads;
+#endif
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)(max_len + 1));
+    double* oc = (double*)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t t = 0; t < n; ++t) {
+      int64_t flat = items ? items[t] : t;
+      int rc = pdo_item(&p, flat / hq, (int)(flat % hq), split_tokens, s, oc, out + t * d, lse + t);
+      if (rc != PDO_OK) {
+#pragma omp atomic write
+        status = rc;
+      }
+    }
+    free(s);
+    free(oc);
+  }
+  return status;
+}
+
+/* Threads the OpenMP runtime would use for a parallel region. */
+int pdo_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

@@ -1,0 +1,301 @@
+"""Seeded synthetic workloads for paged decode attention.
+
+This module only draws inputs: query rows, a paged K/V cache (bf16, or OCP
+E4M3 codes with their scales), a shuffled page table and the CSR offsets. It
+holds none of the attention arithmetic. Both the CUDA library's callers and
+the fp64 oracle consume the arrays it returns, so neither side's arithmetic
+can leak into the other's inputs.
+
+Recipe (stated once here, used by the tests and the benchmark):
+  * values: Q, K, V ~ N(0, 1) from a torch.Generator seeded per workload;
+  * bf16 payloads are the round-to-nearest-even bf16 of those values;
+  * FP8 payloads: scale = amax / 448 (1 if amax == 0), per tensor or per
+    (token, kv head) over head_dim; code = e4m3(clamp(x / scale, +-448))
+    by torch's float8_e4m3fn cast (RNE). A per-tensor E4M3 query folds its
+    scale into the returned sm_scale, so a consumer multiplies decoded codes
+    by sm_scale only;
+  * optional K outliers: round(frac * head_dim) channels per kv head, chosen
+    by the seed and fixed across tokens, multiplied by ``k_outlier_mult``
+    before quantisation;
+  * the page table is a random permutation of the physical pages; every
+    request's CSR list gets ``extra_table_entries`` trailing entries that
+    point at poison pages, and ``extra_pages`` poison pages exist;
+  * poison: pages no request uses and the tail slots of each request's last
+    page hold NaN (bf16 0x7FC0, e4m3 0x7F), and so do their per-token scales,
+    so that any read of them shows up as NaN in the output.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Optional, Sequence, Union
+
+import torch
+
+E4M3_MAX = 448.0
+BF16_NAN_BITS = 0x7FC0
+E4M3_NAN_CODE = 0x7F
+
+SCALE_NONE, SCALE_TENSOR, SCALE_TOKEN_HEAD = 0, 1, 2
+
+
+@dataclass
+class Workload:
+    name: str
+    num_qo_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    num_pages: int
+    q_e4m3: bool
+    kv_e4m3: bool
+    scale_mode: int
+    layout: str                      # "NHD" = [page, slot, head, d]; "HND" = [page, head, slot, d]
+    strides: tuple                   # (page, token, head) strides in elements
+    q: torch.Tensor                  # [total_rows, Hq, D] bf16 or uint8 codes
+    k_pages: torch.Tensor            # cache, bf16 or uint8 codes, layout as above
+    v_pages: torch.Tensor
+    k_scale: Optional[torch.Tensor]  # None, [1] or [num_pages, page_size, Hkv] float32
+    v_scale: Optional[torch.Tensor]
+    page_table: torch.Tensor         # int32 CSR page ids
+    kv_indptr: torch.Tensor          # int32 [B+1]
+    kv_len: torch.Tensor             # int32 [B]
+    qo_indptr: torch.Tensor          # int32 [B+1]
+    window: Optional[torch.Tensor]   # int32 [B] (<= 0: none) or None
+    sm_scale: float
+    q_scale: float = 1.0             # already folded into sm_scale when q_e4m3
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def batch(self) -> int:
+        return int(self.kv_len.shape[0])
+
+    @property
+    def total_rows(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def max_q_len(self) -> int:
+        r = self.qo_indptr[1:] - self.qo_indptr[:-1]
+        return int(r.max().item()) if r.numel() else 0
+
+    @property
+    def group(self) -> int:
+        return self.num_qo_heads // self.num_kv_heads
+
+    def rows_per_request(self):
+        return (self.qo_indptr[1:] - self.qo_indptr[:-1]).tolist()
+
+    def to(self, device) -> "Workload":
+        def mv(t):
+            return None if t is None else t.to(device)
+        return Workload(self.name, self.num_qo_heads, self.num_kv_heads, self.head_dim,
+                        self.page_size, self.num_pages, self.q_e4m3, self.kv_e4m3,
+                        self.scale_mode, self.layout, self.strides, mv(self.q), mv(self.k_pages),
+                        mv(self.v_pages), mv(self.k_scale), mv(self.v_scale),
+                        mv(self.page_table), mv(self.kv_indptr), mv(self.kv_len),
+                        mv(self.qo_indptr), mv(self.window), self.sm_scale, self.q_scale,
+                        dict(self.meta))
+
+
+def _as_list(x, n):
+    if isinstance(x, (list, tuple)):
+        assert len(x) == n
+        return [int(v) for v in x]
+    return [int(x)] * n
+
+
+def _quant_e4m3(x: torch.Tensor, amax_dims) -> tuple:
+    """(codes uint8, scale float32) with scale = amax/448 over ``amax_dims``
+    (None: whole tensor)."""
+    if amax_dims is None:
+        amax = x.abs().amax().float()
+    else:
+        amax = x.abs().amax(dim=amax_dims).float()
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    if amax_dims is None:
+        y = x / scale
+    else:
+        y = x / scale.unsqueeze(-1)
+    codes = y.clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, scale.to(torch.float32)
+
+
+def make_workload(*, name: str = "custom", batch: int, rows: Union[int, Sequence[int]],
+                  kv_lens: Union[int, Sequence[int]], num_qo_heads: int, num_kv_heads: int,
+                  head_dim: int, page_size: int, kv_dtype: str = "bf16", q_dtype: str = "bf16",
+                  scale_mode: int = SCALE_NONE, windows=None, sm_scale: Optional[float] = None,
+                  layout: str = "NHD", seed: int = 0, device="cpu",
+                  k_outlier_frac: float = 0.0, k_outlier_mult: float = 20.0,
+                  q_mult: float = 1.0, extra_pages: int = 4, extra_table_entries: int = 1,
+                  poison: bool = True, value_fn=None) -> Workload:
+    """Draw one workload. ``value_fn(kind, shape, gen)`` may replace N(0,1)
+    draws for structured tests (kind in {"q", "k", "v"}, logical shapes
+    [rows, Hq, D] and [num_pages, P, Hkv, D])."""
+    assert kv_dtype in ("bf16", "e4m3") and q_dtype in ("bf16", "e4m3")
+    assert num_qo_heads % num_kv_heads == 0
+    if kv_dtype == "bf16":
+        assert scale_mode == SCALE_NONE
+    else:
+        assert scale_mode in (SCALE_TENSOR, SCALE_TOKEN_HEAD)
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(int(seed))
+    R = _as_list(rows, batch)
+    L = _as_list(kv_lens, batch)
+    P, H, D = page_size, num_kv_heads, head_dim
+    qo_indptr = [0]
+    for r in R:
+        qo_indptr.append(qo_indptr[-1] + r)
+    npages_b = [-(-l // P) for l in L]
+    used = sum(npages_b)
+    num_pages = used + int(extra_pages)
+    perm = torch.randperm(num_pages, generator=gen, device=dev).to(torch.int32).cpu().tolist()
+    poison_pages = perm[used:]
+    table, kv_indptr, cursor = [], [0], 0
+    for b in range(batch):
+        table.extend(perm[cursor:cursor + npages_b[b]])
+        cursor += npages_b[b]
+        for e in range(extra_table_entries):
+            table.append(poison_pages[(b + e) % len(poison_pages)] if poison_pages else perm[0])
+        kv_indptr.append(len(table))
+
+    def draw(kind, shape):
+        if value_fn is not None:
+            return value_fn(kind, shape, gen).to(dev, torch.float32)
+        return torch.randn(shape, generator=gen, device=dev, dtype=torch.float32)
+
+    total_rows = qo_indptr[-1]
+    qf = draw("q", (total_rows, num_qo_heads, D)) * q_mult
+    kf = draw("k", (num_pages, P, H, D))
+    vf = draw("v", (num_pages, P, H, D))
+    outlier_channels = None
+    if k_outlier_frac > 0:
+        n_out = max(1, int(round(k_outlier_frac * D)))
+        outlier_channels = torch.stack([torch.randperm(D, generator=gen, device=dev)[:n_out]
+                                        for _ in range(H)])
+        for h in range(H):
+            kf[:, :, h, outlier_channels[h]] *= k_outlier_mult
+
+    # valid-slot mask [num_pages, P]: which slots hold a real token
+    valid = torch.zeros(num_pages, P, dtype=torch.bool, device=dev)
+    cursor = 0
+    for b in range(batch):
+        pages = torch.tensor(perm[cursor:cursor + npages_b[b]], dtype=torch.long, device=dev)
+        cursor += npages_b[b]
+        if npages_b[b]:
+            valid[pages] = True
+            tail = L[b] - (npages_b[b] - 1) * P
+            valid[pages[-1], tail:] = False
+
+    q_scale = 1.0
+    if q_dtype == "bf16":
+        q = qf.to(torch.bfloat16)
+    else:
+        q, qs = _quant_e4m3(qf, None)
+        q_scale = float(qs.item())
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    sm_eff = float(sm_scale) * q_scale
+
+    k_scale = v_scale = None
+    if kv_dtype == "bf16":
+        kc, vc = kf.to(torch.bfloat16), vf.to(torch.bfloat16)
+    elif scale_mode == SCALE_TENSOR:
+        kc, k_scale = _quant_e4m3(kf, None)
+        vc, v_scale = _quant_e4m3(vf, None)
+        k_scale, v_scale = k_scale.reshape(1), v_scale.reshape(1)
+    else:
+        kc, k_scale = _quant_e4m3(kf, -1)
+        vc, v_scale = _quant_e4m3(vf, -1)
+    del kf, vf, qf
+
+    if poison:
+        bad = ~valid
+        if kv_dtype == "bf16":
+            nanb = torch.tensor(BF16_NAN_BITS, dtype=torch.int16, device=dev).view(torch.bfloat16)
+            kc[bad] = nanb
+            vc[bad] = nanb
+        else:
+            kc[bad] = E4M3_NAN_CODE
+            vc[bad] = E4M3_NAN_CODE
+        if scale_mode == SCALE_TOKEN_HEAD:
+            k_scale[bad] = float("nan")
+            v_scale[bad] = float("nan")
+
+    if layout == "NHD":
+        strides = (P * H * D, H * D, D)
+    elif layout == "HND":
+        kc = kc.permute(0, 2, 1, 3).contiguous()
+        vc = vc.permute(0, 2, 1, 3).contiguous()
+        strides = (H * P * D, D, P * D)
+    else:
+        raise ValueError(layout)
+
+    win = None
+    if windows is not None:
+        win = torch.tensor(_as_list(windows, batch), dtype=torch.int32, device=dev)
+
+    i32 = dict(dtype=torch.int32, device=dev)
+    return Workload(
+        name=name, num_qo_heads=num_qo_heads, num_kv_heads=H, head_dim=D, page_size=P,
+        num_pages=num_pages, q_e4m3=(q_dtype == "e4m3"), kv_e4m3=(kv_dtype == "e4m3"),
+        scale_mode=scale_mode, layout=layout, strides=strides, q=q, k_pages=kc, v_pages=vc,
+        k_scale=k_scale, v_scale=v_scale, page_table=torch.tensor(table, **i32),
+        kv_indptr=torch.tensor(kv_indptr, **i32), kv_len=torch.tensor(L, **i32),
+        qo_indptr=torch.tensor(qo_indptr, **i32), window=win, sm_scale=sm_eff, q_scale=q_scale,
+        meta=dict(seed=seed, rows=R, kv_lens=L, outlier_channels=outlier_channels,
+                  poison_pages=poison_pages))
+
+
+# ---------------------------------------------------------------------------
+# The five workloads the benchmark and the parity tests use.
+
+CONFIG_NAMES = ("tiny", "fp8_decode", "mtp_verify_bf16", "longctx_fp8_pth", "mixed")
+
+
+def config_workload(name: str, *, R: Optional[int] = None, bs: Optional[int] = None,
+                    device="cpu", seed: Optional[int] = None, **kw) -> Workload:
+    """The named workload at its stated sizes (seed 1000 + its index).
+
+    tiny            bs 1, R 1, 16/2 heads, D 128, ctx 512, page 16, bf16, 4 poison pages
+    fp8_decode      bs 128, R 1, 64/8 heads, D 128, ctx 2048, page 64, Q/K/V e4m3
+                    with per-tensor scales, bf16 output
+    mtp_verify_bf16 16/2 heads, D 256, R 4 (1, 8), ctx 32768, bs 1 or 16, page 16, bf16
+    longctx_fp8_pth 16/2 heads, D 256, R 1 or 8 (4), ctx 131072, bs 1 or 16, page 16,
+                    e4m3 K/V with a scale per (token, kv head), 1% K channels x20, Q bf16
+    mixed           bs 64, 48/2 heads, D 128, R_b ~ U{1..8}, ctx_b ~ U[1024, 65536],
+                    window 64 on half the requests, page 32, bf16
+    """
+    idx = CONFIG_NAMES.index(name)
+    seed = 1000 + idx if seed is None else seed
+    if name == "tiny":
+        args = dict(batch=1, rows=1, kv_lens=512, num_qo_heads=16, num_kv_heads=2, head_dim=128,
+                    page_size=16)
+    elif name == "fp8_decode":
+        args = dict(batch=128, rows=1, kv_lens=2048, num_qo_heads=64, num_kv_heads=8,
+                    head_dim=128, page_size=64, kv_dtype="e4m3", q_dtype="e4m3",
+                    scale_mode=SCALE_TENSOR)
+    elif name == "mtp_verify_bf16":
+        args = dict(batch=bs or 16, rows=R or 4, kv_lens=32768, num_qo_heads=16, num_kv_heads=2,
+                    head_dim=256, page_size=16)
+    elif name == "longctx_fp8_pth":
+        args = dict(batch=bs or 16, rows=R or 8, kv_lens=131072, num_qo_heads=16,
+                    num_kv_heads=2, head_dim=256, page_size=16, kv_dtype="e4m3",
+                    q_dtype="bf16", scale_mode=SCALE_TOKEN_HEAD, k_outlier_frac=0.01)
+    elif name == "mixed":
+        g = torch.Generator().manual_seed(seed + 7)
+        b = bs or 64
+        rows = torch.randint(1, 9, (b,), generator=g).tolist()
+        lens = torch.randint(1024, 65537, (b,), generator=g).tolist()
+        order = torch.randperm(b, generator=g).tolist()
+        win = [0] * b
+        for pos, req in enumerate(order):
+            if pos % 2 == 0:
+                win[req] = 64
+        args = dict(batch=b, rows=rows, kv_lens=lens, num_qo_heads=48, num_kv_heads=2,
+                    head_dim=128, page_size=32, windows=win)
+    else:
+        raise KeyError(name)
+    args.update(kw)
+    return make_workload(name=name, seed=seed, device=device, **args)

@@ -1,0 +1,411 @@
+"""Benchmark of paged split-KV decode attention (stage 1 + stage 2 per call).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one pda_decode call (all of stage 1 and stage 2) over the
+fp8_decode workload: bs 128, R 1, 64 query / 8 kv heads, head_dim 128,
+ctx 2048, page 64, Q/K/V E4M3 with per-tensor scales, bf16 output. The call is
+captured once in a CUDA graph and replayed; before every step L2 is flushed by
+a memset of twice its size, outside the CUDA events that time the step.
+`value` is the algorithmic HBM bytes of the call (paged_split_kv_03_gb300.
+traffic) over its measured time, summed over ranks; the line also carries the
+R = 1 / 4 / 8 sweep of the two bs-16 workloads at 16 query / 2 kv heads and
+head_dim 256 (bf16 ctx 32768 and E4M3 per-(token, head) ctx 131072).
+
+`--impl reference` times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of (row, q head) items per step, scaled to the same metric.
+With N > 1 (torchrun) every rank runs an independent replica: the path needs
+no collective.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("paged decode attn µs/call and achieved HBM GB/s (% of GB300 peak) at R=1/4/8")
+HEADLINE = "fp8_decode"
+HEADLINE_DESC = ("fp8_decode: bs128, R1, 64 q / 8 kv heads, head_dim 128, ctx 2048 each, "
+                 "page 64, Q/K/V e4m3 per-tensor scales, bf16 out")
+PAGES_NUMBER = {"value": 3672.1, "unit": "GB/s",
+                "source": "hpc-ops FP8 decode on H200 (other hardware; context only)"}
+SWEEP = [("mtp_verify_bf16", 16, R) for R in (1, 4, 8)] + \
+        [("longctx_fp8_pth", 16, R) for R in (1, 4, 8)]
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def source_sha() -> str:
+    """Hash of the CUDA sources: ncu traffic figures apply only to this code."""
+    h = hashlib.sha256()
+    cs = os.path.join(ROOT, "paged_split_kv_03_gb300", "csrc")
+    for f in sorted(os.listdir(cs)):
+        h.update(f.encode())
+        h.update(open(os.path.join(cs, f), "rb").read())
+    return h.hexdigest()[:12]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """dram read+write bytes per launch from the committed ncu summary, or
+    None when the summary is for other sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = source_sha()
+    for line in open(path):
+        m = re.match(r"\s*(\S+)\s+(\S+)\s+(\S+)\s+(\d+)", line)
+        if m and m.group(1) == kernel and m.group(2) == workload and m.group(3) == sha:
+            return int(m.group(4))
+    return None
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+def time_graph(fn, steps, warmup, flush, stream):
+    """Per-step CUDA-event times (ms) of ``fn`` replayed on ``stream``, with an
+    L2 flush enqueued before every step outside the events."""
+    import torch
+    for _ in range(warmup):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            flush()
+            a.record(stream)
+            fn()
+            b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def setup_call(wl, dev):
+    """Plan, scratch, outputs and a captured CUDA graph of one pda_decode."""
+    import torch
+    from paged_split_kv_03_gb300 import binding as B
+    dec = B.Decoder(B.params_for(wl, device=dev.index or 0), device=dev)
+    out = torch.empty(wl.total_rows, wl.num_qo_heads, wl.head_dim, dtype=torch.bfloat16,
+                      device=dev)
+    lse = torch.empty(wl.total_rows, wl.num_qo_heads, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        dec.run(wl, out, lse, stream=stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        dec.run(wl, out, lse, stream=stream)
+    return dec, out, lse, stream, graph
+
+
+def e2e_time(wl, dec, steps, warmup, dev):
+    """End to end through the C ABI: pinned host inputs copied to the device,
+    pda_decode, outputs copied back, all inside the timed region."""
+    import torch
+    names = ["q", "k_pages", "v_pages", "k_scale", "v_scale", "page_table", "kv_indptr",
+             "kv_len", "qo_indptr", "window"]
+    host = {n: getattr(wl, n).cpu().pin_memory() for n in names if getattr(wl, n) is not None}
+    devb = {n: torch.empty_like(getattr(wl, n)) for n in host}
+    out = torch.empty(wl.total_rows, wl.num_qo_heads, wl.head_dim, dtype=torch.bfloat16,
+                      device=dev)
+    lse = torch.empty(wl.total_rows, wl.num_qo_heads, dtype=torch.float32, device=dev)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    stream = torch.cuda.Stream(device=dev)
+
+    class View:
+        pass
+    v = View()
+    for n in names:
+        setattr(v, n, devb.get(n))
+    v.sm_scale, v.max_q_len = wl.sm_scale, wl.max_q_len
+
+    def step():
+        for n, t in host.items():
+            devb[n].copy_(t, non_blocking=True)
+        dec.run(v, out, lse, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(steps):
+            step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+def oracle_rate(wl, budget_s: float, seed: int = 0, max_items=None):
+    """Oracle GB/s on ``wl``: times a random sample of (row, q head) items
+    sized to about ``budget_s`` seconds and scales to the whole call."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from paged_split_kv_03_gb300.traffic import call_bytes
+    host = wl.to("cpu")
+    total = host.total_rows * host.num_qo_heads
+    g = torch.Generator().manual_seed(seed)
+    calib = np.sort(torch.randperm(total, generator=g)[: min(total, 32)].numpy()).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.attention_for(host, items=calib)
+    per = (time.perf_counter() - t0) / len(calib)
+    n = int(min(total, max(len(calib), budget_s / max(per, 1e-9))))
+    if max_items:
+        n = min(n, max_items)
+    items = np.sort(torch.randperm(total, generator=g)[:n].numpy()).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.attention_for(host, items=items)
+    dt = time.perf_counter() - t0
+    full_s = dt * total / n
+    gbs = call_bytes(host)["total"] / full_s / 1e9
+    return gbs, full_s, n, total, oracle.max_threads()
+
+
+def run_ours(args, rank, world, dev):
+    import torch
+
+    from paged_split_kv_03_gb300.synth import config_workload
+    from paged_split_kv_03_gb300.traffic import call_bytes, call_flops
+    torch.cuda.set_device(dev)
+    peak, peak_kind = peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.zero_()
+
+    wl = config_workload(HEADLINE, device=dev)
+    dec, out, lse, stream, graph = setup_call(wl, dev)
+    nbytes = call_bytes(wl, dec.plan.chunk_pages)
+    flops = call_flops(wl)
+    launches_per_step = 1 + (1 if dec.plan.max_splits > 1 else 0)
+
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+        tdist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index or 0) as clk:
+        times = time_graph(graph.replay, args.steps, args.warmup, flush, stream)
+    torch.cuda.synchronize()
+    if dist:
+        tdist.barrier()
+    ms = sum(times) / len(times)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = nbytes["total"] * world / (ms * 1e-3) / 1e9
+    assert dec.status() == 0, "device status bits set during the benchmark"
+
+    # the dominant kernel: stage 1 (the only launch when the call has one split)
+    stage1_ms = ms if launches_per_step == 1 else None
+    stage1_bytes = nbytes["total"] - nbytes["scratch"] // 2
+    roof = {"bound": "hbm", "kernel": "stage1", "peak": peak, "unit": "GB/s",
+            "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+            "traffic": recorded_traffic("stage1", HEADLINE)}
+    if stage1_ms:
+        roof["achieved"] = stage1_bytes / (stage1_ms * 1e-3) / 1e9
+        roof["frac"] = roof["achieved"] / peak
+        roof["algorithmic_bytes"] = stage1_bytes
+
+    sweep = []
+    if rank == 0 and not args.no_sweep:
+        for name, bs, R in SWEEP:
+            w2 = config_workload(name, R=R, bs=bs, device=dev)
+            d2, o2, l2_, s2, g2 = setup_call(w2, dev)
+            t2 = time_graph(g2.replay, max(10, args.steps), 3, flush, s2)
+            b2 = call_bytes(w2, d2.plan.chunk_pages)["total"]
+            med = statistics.median(t2)
+            sweep.append({"workload": f"{name} bs{bs} R{R}", "us_per_call": med * 1e3,
+                          "GB_s": b2 / (med * 1e-3) / 1e9,
+                          "frac_of_peak": b2 / (med * 1e-3) / 1e9 / peak, "bytes": b2,
+                          "splits": d2.plan.max_splits})
+            del w2, d2, o2, l2_, g2
+            torch.cuda.empty_cache()
+        by = {s["workload"]: s["us_per_call"] for s in sweep}
+        for name in ("mtp_verify_bf16", "longctx_fp8_pth"):
+            r1, r8 = by.get(f"{name} bs16 R1"), by.get(f"{name} bs16 R8")
+            if r1 and r8:
+                sweep.append({"workload": f"{name} bs16", "R8_over_R1": r8 / r1})
+
+    e2e = None
+    if rank == 0:
+        e_ms, h2d, d2h = e2e_time(wl, dec, max(5, args.steps // 2), 2, dev)
+        e2e = {"value": nbytes["total"] / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "ms_per_step": e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, full_s, n, total, cores = oracle_rate(wl, budget_s=args.cpu_seconds)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"{n} of {total} (row, q head) items of {HEADLINE}, timed and scaled "
+                         f"to the whole call ({full_s:.1f} s per call)"}
+
+    if rank != 0:
+        return None
+    return {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "us_per_call": ms * 1e3,
+        "frac_of_peak": value / world / peak, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": value / world / PAGES_NUMBER["value"],
+        "vs_baseline_ref": PAGES_NUMBER, "dtype": "e4m3 codes, f16 MMA, fp32 accumulate",
+        "data": "synthetic (seeded N(0,1), e4m3 per-tensor)",
+        "config": {"workload": HEADLINE_DESC, "parallelism": f"replicas x{world}",
+                   "l2": "flushed before every step (memset of 2x L2), outside the events",
+                   "graph": "stage 1 + stage 2 captured in one CUDA graph",
+                   "splits": dec.plan.max_splits, "chunk_pages": dec.plan.chunk_pages,
+                   "grid_ctas": dec.plan.grid_ctas, "bytes_per_call": nbytes,
+                   "flops_per_call": flops, "tflops": flops / (ms * 1e-3) / 1e12},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps, "clocks": clk.summary(),
+        "r_sweep": sweep, "source_sha": source_sha(),
+    }
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, timed on the host cores: each step a bounded
+    sample of the headline workload scaled to the call."""
+    import torch
+
+    from paged_split_kv_03_gb300.synth import config_workload
+    if rank != 0:
+        return None
+    wl = config_workload(HEADLINE, device="cpu")
+    budget = args.reference_seconds
+    for i in range(args.warmup):
+        oracle_rate(wl, budget_s=min(budget, 2.0), seed=100 + i)
+    rates, secs = [], []
+    n = total = cores = 0
+    for i in range(args.steps):
+        gbs, full_s, n, total, cores = oracle_rate(wl, budget_s=budget, seed=i)
+        rates.append(gbs)
+        secs.append(full_s)
+    value = statistics.mean(rates)
+    sample = (f"per step {n} of {total} (row, q head) items of {HEADLINE}, scaled to the call")
+    ms = statistics.mean(secs) * 1e3
+    return {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": HEADLINE_DESC},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "kind": "oracle", "cores": cores,
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--reference-seconds", type=float, default=4.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        import torch
+        if world > 1:
+            import torch.distributed as tdist
+            torch.cuda.set_device(local)
+            tdist.init_process_group("nccl")
+        res = run_ours(args, rank, world, torch.device("cuda", local))
+        if world > 1:
+            import torch.distributed as tdist
+            tdist.destroy_process_group()
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

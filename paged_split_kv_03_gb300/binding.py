@@ -1,0 +1,208 @@
+"""Thin ctypes binding of the C ABI in include/pda.h (argument marshalling only).
+
+The names mirror the C entry points: ``pda_plan``, ``pda_decode``,
+``pda_get_status``, ``pda_reset_status``, ``pda_strerror``. Tensors are
+passed as raw pointers (``data_ptr()``) and streams as their CUDA handle;
+every step of the computation runs in the library's kernels. There is no
+fallback: if ``_lib/libpda.so`` has not been built, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_lib", "libpda.so")
+
+PDA_BF16, PDA_E4M3 = 0, 1
+PDA_SCALE_NONE, PDA_SCALE_TENSOR, PDA_SCALE_TOKEN_HEAD = 0, 1, 2
+PDA_KERNEL_AUTO, PDA_KERNEL_MMA, PDA_KERNEL_TC = 0, 1, 2
+PDA_OK = 0
+PDA_ERR_NULL, PDA_ERR_INVALID, PDA_ERR_UNSUPPORTED = -1, -2, -3
+PDA_ERR_ALIGNMENT, PDA_ERR_SCRATCH, PDA_ERR_CUDA, PDA_ERR_PLAN = -4, -5, -6, -7
+PDA_STATUS_KV_LEN_LT_ROWS = 0x1
+PDA_STATUS_ROWS_GT_MAX = 0x2
+PDA_STATUS_KV_LEN_GT_MAX = 0x4
+PDA_STATUS_PAGE_OOB = 0x8
+PDA_STATUS_ROWS_GT_CAP = 0x10
+PDA_PLAN_MAGIC = 0x50444131
+
+EXPORTED = ("pda_plan", "pda_decode", "pda_get_status", "pda_reset_status", "pda_strerror",
+            "pda_version", "pda_struct_sizes")
+
+_i32, _i64, _u32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_void_p
+
+
+class PdaParams(ctypes.Structure):
+    _fields_ = [("num_qo_heads", _i32), ("num_kv_heads", _i32), ("head_dim", _i32),
+                ("page_size", _i32), ("q_dtype", _i32), ("kv_dtype", _i32),
+                ("scale_mode", _i32), ("max_batch", _i32), ("max_q_len", _i32),
+                ("max_kv_len", _i32), ("num_pages", _i32), ("kv_stride_page", _i64),
+                ("kv_stride_token", _i64), ("kv_stride_head", _i64), ("device", _i32),
+                ("num_sms", _i32), ("host_kv_len", ctypes.POINTER(_i32)), ("batch", _i32),
+                ("chunk_pages", _i32), ("kernel", _i32)]
+
+
+class PdaPlan(ctypes.Structure):
+    _fields_ = [("magic", _u32), ("num_qo_heads", _i32), ("num_kv_heads", _i32),
+                ("head_dim", _i32), ("page_size", _i32), ("q_dtype", _i32), ("kv_dtype", _i32),
+                ("scale_mode", _i32), ("max_batch", _i32), ("max_q_len", _i32),
+                ("max_kv_len", _i32), ("num_pages", _i32), ("batch", _i32),
+                ("kv_stride_page", _i64), ("kv_stride_token", _i64), ("kv_stride_head", _i64),
+                ("group", _i32), ("kernel", _i32), ("rows_per_cta", _i32),
+                ("heads_per_cta", _i32 * 9), ("head_blocks", _i32), ("chunk_pages", _i32),
+                ("max_splits", _i32), ("num_sms", _i32), ("grid_ctas", _i64),
+                ("rows_cap", _i64), ("scratch_bytes", _i64), ("scratch_lse_offset", _i64),
+                ("scratch_o_offset", _i64), ("stage1_smem_bytes", _i32),
+                ("reserved", _i32 * 15)]
+
+
+class PdaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where} failed: {pda_strerror(code)} ({code})")
+
+
+_LIB = None
+
+
+def load_library(path: Optional[str] = None):
+    """Load libpda.so (built by paged_split_kv_03_gb300.build); raises if absent."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it with paged_split_kv_03_gb300.build.build() "
+                           "(there is no fallback implementation)")
+    lib = ctypes.CDLL(p)
+    lib.pda_plan.argtypes = [ctypes.POINTER(PdaParams), ctypes.POINTER(PdaPlan),
+                             ctypes.POINTER(ctypes.c_size_t)]
+    lib.pda_plan.restype = ctypes.c_int
+    lib.pda_decode.argtypes = [ctypes.POINTER(PdaPlan), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                               _i32, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.pda_decode.restype = ctypes.c_int
+    lib.pda_get_status.argtypes = [ctypes.POINTER(PdaPlan), _vp, ctypes.POINTER(_u32), _vp]
+    lib.pda_get_status.restype = ctypes.c_int
+    lib.pda_reset_status.argtypes = [ctypes.POINTER(PdaPlan), _vp, _vp]
+    lib.pda_reset_status.restype = ctypes.c_int
+    lib.pda_strerror.argtypes = [ctypes.c_int]
+    lib.pda_strerror.restype = ctypes.c_char_p
+    lib.pda_version.restype = ctypes.c_int
+    lib.pda_struct_sizes.argtypes = [ctypes.POINTER(ctypes.c_size_t),
+                                     ctypes.POINTER(ctypes.c_size_t)]
+    lib.pda_struct_sizes.restype = ctypes.c_int
+    if path is None:
+        _LIB = lib
+    return lib
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def pda_strerror(code: int) -> str:
+    return load_library().pda_strerror(int(code)).decode()
+
+
+def pda_plan(params: PdaParams, check: bool = True):
+    """-> (PdaPlan, scratch_bytes, rc)."""
+    plan = PdaPlan()
+    nbytes = ctypes.c_size_t(0)
+    rc = load_library().pda_plan(ctypes.byref(params), ctypes.byref(plan), ctypes.byref(nbytes))
+    if check and rc != PDA_OK:
+        raise PdaError(rc, "pda_plan")
+    return plan, int(nbytes.value), rc
+
+
+def pda_decode(plan: PdaPlan, q, k_pages, v_pages, page_table, kv_indptr, kv_len, qo_indptr,
+               max_q_len: int, window, sm_scale: float, k_scale, v_scale, out, lse,
+               split_scratch, stream=None, check: bool = True) -> int:
+    rc = load_library().pda_decode(
+        ctypes.byref(plan), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+        _ptr(kv_indptr), _ptr(kv_len), _ptr(qo_indptr), int(max_q_len), _ptr(window),
+        float(sm_scale), _ptr(k_scale), _ptr(v_scale), _ptr(out), _ptr(lse), _ptr(split_scratch),
+        _stream(stream))
+    if check and rc != PDA_OK:
+        raise PdaError(rc, "pda_decode")
+    return rc
+
+
+def pda_get_status(plan: PdaPlan, split_scratch, stream=None) -> int:
+    bits = _u32(0)
+    rc = load_library().pda_get_status(ctypes.byref(plan), _ptr(split_scratch),
+                                       ctypes.byref(bits), _stream(stream))
+    if rc != PDA_OK:
+        raise PdaError(rc, "pda_get_status")
+    return int(bits.value)
+
+
+def pda_reset_status(plan: PdaPlan, split_scratch, stream=None) -> None:
+    rc = load_library().pda_reset_status(ctypes.byref(plan), _ptr(split_scratch),
+                                         _stream(stream))
+    if rc != PDA_OK:
+        raise PdaError(rc, "pda_reset_status")
+
+
+# ---------------------------------------------------------------- helpers
+
+def params_for(wl, *, max_batch=None, max_q_len=None, max_kv_len=None, device=0, num_sms=0,
+               chunk_pages=0, kernel=PDA_KERNEL_AUTO, batch=0) -> PdaParams:
+    """PdaParams describing a workload object (synth.Workload or alike)."""
+    p = PdaParams()
+    p.num_qo_heads = wl.num_qo_heads
+    p.num_kv_heads = wl.num_kv_heads
+    p.head_dim = wl.head_dim
+    p.page_size = wl.page_size
+    p.q_dtype = PDA_E4M3 if wl.q_e4m3 else PDA_BF16
+    p.kv_dtype = PDA_E4M3 if wl.kv_e4m3 else PDA_BF16
+    p.scale_mode = wl.scale_mode
+    p.max_batch = max_batch or wl.batch
+    p.max_q_len = max_q_len or max(1, wl.max_q_len)
+    p.max_kv_len = max_kv_len or max(1, int(wl.kv_len.max().item()))
+    p.num_pages = wl.num_pages
+    p.kv_stride_page, p.kv_stride_token, p.kv_stride_head = (int(s) for s in wl.strides)
+    p.device = device
+    p.num_sms = num_sms
+    p.batch = batch or wl.batch
+    p.chunk_pages = chunk_pages
+    p.kernel = kernel
+    return p
+
+
+class Decoder:
+    """A plan plus its split scratch (allocated once with torch) for one
+    workload shape; ``run`` enqueues one pda_decode on the current stream."""
+
+    def __init__(self, params: PdaParams, device="cuda"):
+        import torch
+        self.params = params
+        self.plan, self.scratch_bytes, _ = pda_plan(params)
+        n = (max(self.scratch_bytes, 256) + 255) // 256 * 256
+        self.scratch = torch.zeros(n, dtype=torch.uint8, device=device)
+
+    def run(self, wl, out, lse, max_q_len=None, stream=None, sm_scale=None):
+        return pda_decode(self.plan, wl.q, wl.k_pages, wl.v_pages, wl.page_table, wl.kv_indptr,
+                          wl.kv_len, wl.qo_indptr, max_q_len or max(1, wl.max_q_len), wl.window,
+                          wl.sm_scale if sm_scale is None else sm_scale, wl.k_scale, wl.v_scale,
+                          out, lse, self.scratch, stream)
+
+    def status(self, stream=None) -> int:
+        return pda_get_status(self.plan, self.scratch, stream)
+
+    def reset_status(self, stream=None) -> None:
+        pda_reset_status(self.plan, self.scratch, stream)

@@ -1,0 +1,73 @@
+// pda_internal.h -- shared between the planner (host C++) and the CUDA
+// translation units. Not part of the public ABI.
+#pragma once
+
+#include <stdint.h>
+
+#include "pda.h"
+
+#ifdef __CUDACC__
+#define PDA_HD __host__ __device__ __forceinline__
+#else
+#define PDA_HD inline
+#endif
+
+namespace pda {
+
+constexpr int kStatusHeaderBytes = 256;  // status word + padding at the start of split_scratch
+constexpr int kMaxQLen = 8;              // rows per request ("up to 8 query rows")
+constexpr int kMmaRowsPerCta = 64;       // mma.sync path: 4 warps x m16 tiles
+constexpr int kTcRowsPerCta = 128;       // tcgen05 path: N of the swapped QK^T MMA
+
+// Arguments of both stage-1 variants and of stage 2 (passed by value).
+struct DecodeArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const int32_t* page_table;
+  const int32_t* kv_indptr;
+  const int32_t* kv_len;
+  const int32_t* qo_indptr;
+  const int32_t* window;
+  const float* k_scale;
+  const float* v_scale;
+  void* out;
+  float* lse;
+  float* part_o;      // [max_splits][rows_cap][Hq][D] fp32, normalised partial output
+  float* part_lse;    // [max_splits][rows_cap][Hq] fp32, log2-domain partial LSE
+  uint32_t* status;   // sticky device status bits
+  float sm_scale;
+  int64_t sp, st, sh; // cache strides (elements)
+  int batch, hq, hkv, group, head_dim, page_size, num_pages;
+  int max_q_len, max_kv_len, max_splits, head_blocks, chunk_pages;
+  int64_t rows_cap;
+  int hpc[kMaxQLen + 1];  // q heads per CTA for R rows
+};
+
+// The KV range one (request, split) covers. Every kernel derives it from the
+// device-resident kv_len / qo_indptr / window, so one plan (and one captured
+// graph) serves any lengths up to the plan's maxima.
+struct SplitRange {
+  int32_t lo;          // first visible key of any row of the request
+  int32_t lo_page;     // page holding lo
+  int32_t num_pages;   // ceil(L / P)
+  int32_t num_splits;  // splits with at least one page of [lo_page, num_pages)
+};
+
+PDA_HD SplitRange split_range(int32_t L, int32_t R, int32_t W, int32_t P, int32_t chunk_pages) {
+  SplitRange s;
+  int32_t p0 = L - R;  // position of the first query row
+  s.lo = (W > 0) ? (p0 - W + 1 > 0 ? p0 - W + 1 : 0) : 0;
+  s.lo_page = s.lo / P;
+  s.num_pages = (L + P - 1) / P;
+  int32_t span = s.num_pages - s.lo_page;
+  s.num_splits = span > 0 ? (span + chunk_pages - 1) / chunk_pages : 0;
+  return s;
+}
+
+// Resolved launch choices (filled by the planner, read by the launcher).
+int launch_decode(const pda_plan_t* plan, const DecodeArgs& args, pda_stream_t stream);
+int stage1_smem_bytes(const pda_plan_t* plan);
+int stage1_ctas_per_sm(const pda_plan_t* plan);
+
+}  // namespace pda

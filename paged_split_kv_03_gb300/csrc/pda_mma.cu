@@ -1,0 +1,698 @@
+// pda_mma.cu -- stage 1 (per-chunk partial attention) on the mma.sync tensor
+// path, and stage 2 (per-row log-sum-exp merge), for sm_103a.
+//
+// Method: "perf(attention): run up to 8 query rows per request in the triton
+// decode kernel" (FreeToken PR #900), "Changes". One CTA owns one
+// (request, kv head, head block, KV chunk). It packs the request's R query
+// rows times its q heads onto the MMA M axis (row m = i * heads + hh), so the
+// kv head's K/V pages are read once for all of them; it streams the chunk's
+// pages through a shared-memory ring filled by 16-byte cp.async gathers that
+// follow the page table; it masks every row at its own causal position and
+// window; it keeps an online softmax per row; and it writes either the final
+// output (one chunk) or a normalised partial (o, lse) for stage 2.
+// FP8 (OCP E4M3) caches are widened exactly to 16 bits in shared memory;
+// per-tensor K scales fold into the logit scale and per-tensor V scales into
+// the finalize step ("Naive Support for Hopper FP8 Prefill Kernel with
+// Per-Head Quantization", item 3); per-(token, kv head) scales multiply the
+// logit column (K) and the probability column (V) of their token.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "pda_internal.h"
+
+namespace pda {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kWarps = 4;
+constexpr int kT = 64;  // tokens per shared-memory tile
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte async gather; src_bytes 0 zero-fills the destination.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+               "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src),
+               "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+template <bool kF16>
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  if constexpr (kF16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+
+// Two floats -> packed 16-bit pair (low = x, high = y), RNE.
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack2(float x, float y) {
+  if constexpr (kF16) {
+    __half2 h = __floats2half2_rn(x, y);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+// Two OCP E4M3 codes (low byte = first element) -> packed f16 pair. Exact:
+// every E4M3 value is an f16 normal number.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(codes));
+  return r;
+}
+
+// Two E4M3 codes -> packed value pair of the compute type (exact both ways).
+template <bool kF16>
+__device__ __forceinline__ uint32_t e4m3x2_to_ct(uint16_t codes) {
+  uint32_t h = e4m3x2_to_f16x2(codes);
+  if constexpr (kF16) {
+    return h;
+  } else {
+    float2 f = __half22float2(*reinterpret_cast<__half2*>(&h));
+    return pack2<false>(f.x, f.y);
+  }
+}
+
+__device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
+
+// Swizzled byte offset of 16-byte chunk `c` of row `r` in a tile whose rows
+// are `row_bytes` (a multiple of 128) long: XOR of the chunk's low 3 bits with
+// the row's keeps every 8-row ldmatrix access on distinct bank groups.
+__device__ __forceinline__ uint32_t swz(int r, int c, int row_bytes) {
+  return static_cast<uint32_t>(r * row_bytes + ((c ^ (r & 7)) << 4));
+}
+
+// ------------------------------------------------------------ configuration
+template <int D, int KVT, int QT, int SMODE>
+struct Cfg {
+  static constexpr bool kKvFp8 = KVT == PDA_E4M3;
+  static constexpr bool kQFp8 = QT == PDA_E4M3;
+  static constexpr bool kF16 = kQFp8;  // MMA operand type: f16 for E4M3 queries, else bf16
+  static constexpr int kKvBytes = kKvFp8 ? 1 : 2;
+  static constexpr int kTileBytes = kT * D * kKvBytes;  // one of K, V
+  static constexpr int kStages = (2 * kTileBytes <= 16384) ? 4 : (2 * kTileBytes <= 32768 ? 3 : 2);
+  static constexpr int kRow16 = D * 2;                  // bytes of one 16-bit row
+  static constexpr int kQBytes = kMmaRowsPerCta * kRow16;
+  static constexpr int kRingBytes = kStages * 2 * kTileBytes;
+  static constexpr int kMergeStride = D + 8;            // fp32 words per merge row (padded)
+  static constexpr int kMergeBytes = kWarps * 16 * kMergeStride * 4 + kWarps * 16 * 2 * 4;
+  static constexpr int kRingOrMerge = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
+  static constexpr int kConvBytes = kKvFp8 ? 2 * kT * kRow16 : 0;
+  static constexpr int kScaleBytes = SMODE == PDA_SCALE_TOKEN_HEAD ? kStages * 2 * kT * 4 : 0;
+  static constexpr int kSmem = kQBytes + kRingOrMerge + kConvBytes + kScaleBytes;
+  static constexpr int kCpr = D * kKvBytes / 16;        // 16-byte chunks per cached row
+  static_assert(kSmem <= 227 * 1024, "stage-1 tile does not fit shared memory");
+};
+
+struct RowInfo {
+  int lo, hi;  // visible key range [lo, hi] of the row inside this chunk (empty if lo > hi)
+};
+
+// ------------------------------------------------------------------ stage 1
+template <int D, int KVT, int QT, int SMODE>
+__global__ void __launch_bounds__(kThreads, 1) stage1_mma(const __grid_constant__ DecodeArgs a) {
+  using C = Cfg<D, KVT, QT, SMODE>;
+  constexpr bool kF16 = C::kF16;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* q_s = smem;
+  uint8_t* ring = smem + C::kQBytes;
+  uint8_t* conv = ring + C::kRingOrMerge;
+  float* scl = reinterpret_cast<float*>(conv + C::kConvBytes);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // ---- which work item
+  int64_t bid = blockIdx.x;
+  const int hb = static_cast<int>(bid % a.head_blocks);
+  bid /= a.head_blocks;
+  const int split = static_cast<int>(bid % a.max_splits);
+  bid /= a.max_splits;
+  const int hkv = static_cast<int>(bid % a.hkv);
+  const int b = static_cast<int>(bid / a.hkv);
+  if (b >= a.batch) return;
+  const int q0 = a.qo_indptr[b];
+  const int R = a.qo_indptr[b + 1] - q0;
+  const int L = a.kv_len[b];
+  if (R <= 0 || R > a.max_q_len || L < R || L > a.max_kv_len || q0 + R > a.rows_cap) {
+    if (tid == 0 && split == 0 && hb == 0 && hkv == 0) {
+      uint32_t bits = 0;
+      if (R < 0 || R > a.max_q_len) bits |= PDA_STATUS_ROWS_GT_MAX;
+      else if (R > 0 && L < R) bits |= PDA_STATUS_KV_LEN_LT_ROWS;
+      else if (R > 0 && L > a.max_kv_len) bits |= PDA_STATUS_KV_LEN_GT_MAX;
+      else if (R > 0 && q0 + R > a.rows_cap) bits |= PDA_STATUS_ROWS_GT_CAP;
+      if (bits) atomicOr(a.status, bits);
+    }
+    return;
+  }
+  const int hpc = a.hpc[R];
+  if (hb >= a.group / hpc) return;  // fewer head blocks are needed for fewer rows
+  const int W = a.window ? a.window[b] : 0;
+  const int P = a.page_size;
+  const SplitRange sr = split_range(L, R, W, P, a.chunk_pages);
+  if (split >= sr.num_splits) return;
+  const int page_begin = sr.lo_page + split * a.chunk_pages;
+  const int page_end = min(page_begin + a.chunk_pages, sr.num_pages);
+  const int t_begin = page_begin * P;              // first token of the chunk (tile origin)
+  const int t_end = min(page_end * P, L);          // one past the chunk's last real token
+  const int ntiles = (t_end - t_begin + kT - 1) / kT;
+  const int M = R * hpc;
+  const int head0 = hkv * a.group + hb * hpc;      // first q head of this CTA
+  const int32_t* ptab = a.page_table + a.kv_indptr[b];
+
+  // ---- scales folded into the logit scale / the finalize step
+  float qk_scale = a.sm_scale * kLog2e;            // logits in log2 units
+  float v_final = 1.f;
+  if constexpr (SMODE == PDA_SCALE_TENSOR) {
+    qk_scale *= __ldg(a.k_scale);
+    v_final = __ldg(a.v_scale);
+  }
+
+  // ---- query tile: rows m < M, zero rows up to the warp tiles in use
+  const int mt = (M + 15) >> 4;
+  const int mt_eff = mt == 3 ? 4 : mt;
+  {
+    constexpr int qchunks = D * (C::kQFp8 ? 1 : 2) / 16;  // 16-byte chunks per global row
+    for (int idx = tid; idx < mt_eff * 16 * qchunks; idx += kThreads) {
+      const int m = idx / qchunks, c = idx % qchunks;
+      if constexpr (C::kQFp8) {
+        uint4 raw = make_uint4(0, 0, 0, 0);
+        if (m < M) {
+          const uint8_t* src = static_cast<const uint8_t*>(a.q) +
+                               ((int64_t)(q0 + m / hpc) * a.hq + head0 + m % hpc) * D + c * 16;
+          raw = __ldg(reinterpret_cast<const uint4*>(src));
+        }
+        const uint16_t* cw = reinterpret_cast<const uint16_t*>(&raw);
+        uint4 lo, hi;
+        lo.x = e4m3x2_to_ct<kF16>(cw[0]); lo.y = e4m3x2_to_ct<kF16>(cw[1]);
+        lo.z = e4m3x2_to_ct<kF16>(cw[2]); lo.w = e4m3x2_to_ct<kF16>(cw[3]);
+        hi.x = e4m3x2_to_ct<kF16>(cw[4]); hi.y = e4m3x2_to_ct<kF16>(cw[5]);
+        hi.z = e4m3x2_to_ct<kF16>(cw[6]); hi.w = e4m3x2_to_ct<kF16>(cw[7]);
+        *reinterpret_cast<uint4*>(q_s + swz(m, 2 * c, C::kRow16)) = lo;
+        *reinterpret_cast<uint4*>(q_s + swz(m, 2 * c + 1, C::kRow16)) = hi;
+      } else {
+        uint4 raw = make_uint4(0, 0, 0, 0);
+        if (m < M) {
+          const uint8_t* src = static_cast<const uint8_t*>(a.q) +
+                               (((int64_t)(q0 + m / hpc) * a.hq + head0 + m % hpc) * D) * 2 + c * 16;
+          raw = __ldg(reinterpret_cast<const uint4*>(src));
+        }
+        *reinterpret_cast<uint4*>(q_s + swz(m, c, C::kRow16)) = raw;
+      }
+    }
+  }
+
+  // ---- K/V tile gather: tile `jt` into ring stage `st`
+  const uint8_t* kbase = static_cast<const uint8_t*>(a.k);
+  const uint8_t* vbase = static_cast<const uint8_t*>(a.v);
+  const int64_t head_off = (int64_t)hkv * a.sh;
+  auto issue_tile = [&](int jt, int st) {
+    if (jt < ntiles) {
+      const int tok0 = t_begin + jt * kT;
+      uint8_t* kst = ring + st * 2 * C::kTileBytes;
+      uint8_t* vst = kst + C::kTileBytes;
+      for (int idx = tid; idx < kT * C::kCpr; idx += kThreads) {
+        const int r = idx / C::kCpr, c = idx % C::kCpr;
+        const int tok = tok0 + r;
+        int bytes = 0;
+        int64_t off = 0;
+        if (tok < t_end) {
+          const int page = __ldg(ptab + tok / P);
+          if (page >= 0 && page < a.num_pages) {
+            bytes = 16;
+            off = ((int64_t)page * a.sp + (int64_t)(tok % P) * a.st + head_off) * C::kKvBytes +
+                  c * 16;
+          } else {
+            atomicOr(a.status, PDA_STATUS_PAGE_OOB);
+          }
+        }
+        uint32_t dk, dv;
+        if constexpr (C::kKvFp8) {  // raw bytes, row-major; widened later
+          dk = smem_u32(kst + r * D + c * 16);
+          dv = smem_u32(vst + r * D + c * 16);
+        } else {
+          dk = smem_u32(kst + swz(r, c, C::kRow16));
+          dv = smem_u32(vst + swz(r, c, C::kRow16));
+        }
+        cp_async16(dk, kbase + off, bytes);
+        cp_async16(dv, vbase + off, bytes);
+      }
+      if constexpr (SMODE == PDA_SCALE_TOKEN_HEAD) {
+        if (tid < kT) {
+          const int tok = tok0 + tid;
+          int bytes = 0;
+          int64_t sidx = 0;
+          if (tok < t_end) {
+            const int page = __ldg(ptab + tok / P);
+            if (page >= 0 && page < a.num_pages) {
+              bytes = 4;
+              sidx = ((int64_t)page * P + tok % P) * a.hkv + hkv;
+            }
+          }
+          cp_async4(smem_u32(scl + st * 2 * kT + tid), a.k_scale + sidx, bytes);
+          cp_async4(smem_u32(scl + st * 2 * kT + kT + tid), a.v_scale + sidx, bytes);
+        }
+      }
+    }
+    cp_async_commit();
+  };
+
+  // ---- per-warp role: m-tile `mi`, token slice `ts` of every tile
+  const int nslices = kWarps / mt_eff;
+  const int mi = warp % mt_eff;
+  const int ts = warp / mt_eff;
+  const int blocks_per_slice = (kT / 16) / nslices;  // 16-token blocks per warp per tile
+  const bool active = mi < mt;
+  const int g = lane >> 2, t4 = lane & 3;
+  RowInfo ri[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int m = mi * 16 + g + 8 * h;
+    if (m < M) {
+      const int pos = L - R + m / hpc;
+      ri[h].lo = W > 0 ? pos - W + 1 : 0;
+      ri[h].hi = min(pos, t_end - 1);
+    } else {
+      ri[h].lo = 1;
+      ri[h].hi = 0;  // padded row: sees nothing
+    }
+  }
+  // tokens every real row of the CTA sees: [all_lo, all_hi]
+  const int all_hi = min(L - R, t_end - 1);
+  const int all_lo = W > 0 ? L - 1 - W + 1 : 0;
+
+  float o[D / 8][4];
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float row_max[2] = {-INFINITY, -INFINITY};
+  float row_sum[2] = {0.f, 0.f};
+
+  const uint32_t q_base = smem_u32(q_s) + mi * 16 * C::kRow16;
+  // ldmatrix lane roles
+  const int a_row = lane & 15, a_chunk = lane >> 4;                 // Q as A (m16 x k16)
+  const int bk_row = ((lane >> 4) << 3) + (lane & 7), bk_chunk = (lane >> 3) & 1;  // K as B
+  const int bv_row = (lane & 7) + (((lane >> 3) & 1) << 3), bv_chunk = lane >> 4;  // V as B^T
+
+#pragma unroll 1
+  for (int s = 0; s < C::kStages - 1; ++s) issue_tile(s, s);
+
+#pragma unroll 1
+  for (int j = 0; j < ntiles; ++j) {
+    const int st = j % C::kStages;
+    issue_tile(j + C::kStages - 1, (j + C::kStages - 1) % C::kStages);
+    cp_async_wait<C::kStages - 1>();
+    __syncthreads();
+    const uint8_t* kt;
+    const uint8_t* vt;
+    if constexpr (C::kKvFp8) {
+      // widen the E4M3 tile pair to the 16-bit compute type, swizzled
+      const uint8_t* kraw = ring + st * 2 * C::kTileBytes;
+      const uint8_t* vraw = kraw + C::kTileBytes;
+      uint8_t* k16 = conv;
+      uint8_t* v16 = conv + kT * C::kRow16;
+      for (int idx = tid; idx < 2 * kT * C::kCpr; idx += kThreads) {
+        const int which = idx / (kT * C::kCpr);
+        const int rem = idx % (kT * C::kCpr);
+        const int r = rem / C::kCpr, c = rem % C::kCpr;
+        const uint4 raw = *reinterpret_cast<const uint4*>((which ? vraw : kraw) + r * D + c * 16);
+        const uint16_t* cw = reinterpret_cast<const uint16_t*>(&raw);
+        uint4 lo, hi;
+        lo.x = e4m3x2_to_ct<kF16>(cw[0]); lo.y = e4m3x2_to_ct<kF16>(cw[1]);
+        lo.z = e4m3x2_to_ct<kF16>(cw[2]); lo.w = e4m3x2_to_ct<kF16>(cw[3]);
+        hi.x = e4m3x2_to_ct<kF16>(cw[4]); hi.y = e4m3x2_to_ct<kF16>(cw[5]);
+        hi.z = e4m3x2_to_ct<kF16>(cw[6]); hi.w = e4m3x2_to_ct<kF16>(cw[7]);
+        uint8_t* dst = which ? v16 : k16;
+        *reinterpret_cast<uint4*>(dst + swz(r, 2 * c, C::kRow16)) = lo;
+        *reinterpret_cast<uint4*>(dst + swz(r, 2 * c + 1, C::kRow16)) = hi;
+      }
+      __syncthreads();
+      kt = k16;
+      vt = v16;
+    } else {
+      kt = ring + st * 2 * C::kTileBytes;
+      vt = kt + C::kTileBytes;
+    }
+    const float* ks_t = scl + st * 2 * kT;
+    const float* vs_t = ks_t + kT;
+    const int tile_tok0 = t_begin + j * kT;
+
+    if (active) {
+      const uint32_t k_base = smem_u32(kt), v_base = smem_u32(vt);
+#pragma unroll 1
+      for (int blk = 0; blk < blocks_per_slice; ++blk) {
+        const int r0 = (ts * blocks_per_slice + blk) * 16;  // first token row in the tile
+        const int tok0 = tile_tok0 + r0;
+        // S = Q K^T for 16 rows x 16 tokens (two n8 tiles)
+        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          uint32_t qa[4];
+          ldsm_x4(q_base + swz(a_row, 2 * kk + a_chunk, C::kRow16), qa[0], qa[1], qa[2], qa[3]);
+          uint32_t kb0, kb1, kb2, kb3;
+          ldsm_x4(k_base + swz(r0 + bk_row, 2 * kk + bk_chunk, C::kRow16), kb0, kb1, kb2, kb3);
+          mma16816<kF16>(sc[0], qa, kb0, kb1);
+          mma16816<kF16>(sc[1], qa, kb2, kb3);
+        }
+        // logit scale (+ per-token K scale), causal/window mask
+        const bool full = tok0 >= all_lo && tok0 + 15 <= all_hi;
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int col = n * 8 + 2 * t4 + (e & 1);
+            float x = sc[n][e] * qk_scale;
+            if constexpr (SMODE == PDA_SCALE_TOKEN_HEAD) x *= ks_t[r0 + col];
+            if (!full) {
+              const int tok = tok0 + col;
+              const RowInfo& rr = ri[e >> 1];
+              if (tok < rr.lo || tok > rr.hi) x = -INFINITY;
+            }
+            sc[n][e] = x;
+          }
+        }
+        // online softmax per row (rows g and g+8 of the m-tile)
+        float alpha[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float mx = fmaxf(fmaxf(sc[0][2 * h], sc[0][2 * h + 1]), fmaxf(sc[1][2 * h], sc[1][2 * h + 1]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          const float m_new = fmaxf(row_max[h], mx);
+          const float m_use = m_new == -INFINITY ? 0.f : m_new;
+          alpha[h] = fast_exp2(row_max[h] - m_use);
+          row_max[h] = m_new;
+#pragma unroll
+          for (int n = 0; n < 2; ++n) {
+            sc[n][2 * h] = fast_exp2(sc[n][2 * h] - m_use);
+            sc[n][2 * h + 1] = fast_exp2(sc[n][2 * h + 1] - m_use);
+          }
+          row_sum[h] = row_sum[h] * alpha[h] + sc[0][2 * h] + sc[0][2 * h + 1] + sc[1][2 * h] +
+                       sc[1][2 * h + 1];
+        }
+        if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+          for (int n = 0; n < D / 8; ++n) {
+            o[n][0] *= alpha[0];
+            o[n][1] *= alpha[0];
+            o[n][2] *= alpha[1];
+            o[n][3] *= alpha[1];
+          }
+        }
+        if constexpr (SMODE == PDA_SCALE_TOKEN_HEAD) {
+#pragma unroll
+          for (int n = 0; n < 2; ++n) {
+            const float v0 = vs_t[r0 + n * 8 + 2 * t4], v1 = vs_t[r0 + n * 8 + 2 * t4 + 1];
+            sc[n][0] *= v0; sc[n][1] *= v1; sc[n][2] *= v0; sc[n][3] *= v1;
+          }
+        }
+        // O += P V  (P from the S accumulators: the m16n8 C layout of two n8
+        // tiles is the m16k16 A layout)
+        uint32_t pa[4];
+        pa[0] = pack2<kF16>(sc[0][0], sc[0][1]);
+        pa[1] = pack2<kF16>(sc[0][2], sc[0][3]);
+        pa[2] = pack2<kF16>(sc[1][0], sc[1][1]);
+        pa[3] = pack2<kF16>(sc[1][2], sc[1][3]);
+#pragma unroll
+        for (int nn = 0; nn < D / 16; ++nn) {
+          uint32_t vb0, vb1, vb2, vb3;
+          ldsm_x4_t(v_base + swz(r0 + bv_row, 2 * nn + bv_chunk, C::kRow16), vb0, vb1, vb2, vb3);
+          mma16816<kF16>(o[2 * nn], pa, vb0, vb1);
+          mma16816<kF16>(o[2 * nn + 1], pa, vb2, vb3);
+        }
+      }
+    }
+    __syncthreads();  // stage `st` (and the widened tile) may be refilled now
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  // Let stage 2 start launching; it waits for this grid's memory anyway.
+  asm volatile("griddepcontrol.launch_dependents;\n" ::);
+
+  // ---- merge the token slices of each m-tile through shared memory
+  float* mo = reinterpret_cast<float*>(ring);
+  float* mml = mo + kWarps * 16 * C::kMergeStride;  // [warp][16][2] = (max, sum)
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    row_sum[h] += __shfl_xor_sync(0xffffffffu, row_sum[h], 1);
+    row_sum[h] += __shfl_xor_sync(0xffffffffu, row_sum[h], 2);
+  }
+  if (active) {
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      float* r0p = mo + (warp * 16 + g) * C::kMergeStride + n * 8 + 2 * t4;
+      float* r1p = r0p + 8 * C::kMergeStride;
+      *reinterpret_cast<float2*>(r0p) = make_float2(o[n][0], o[n][1]);
+      *reinterpret_cast<float2*>(r1p) = make_float2(o[n][2], o[n][3]);
+    }
+    if (t4 == 0) {
+      mml[(warp * 16 + g) * 2] = row_max[0];
+      mml[(warp * 16 + g) * 2 + 1] = row_sum[0];
+      mml[(warp * 16 + g + 8) * 2] = row_max[1];
+      mml[(warp * 16 + g + 8) * 2 + 1] = row_sum[1];
+    }
+  }
+  __syncthreads();
+
+  const bool single = sr.num_splits == 1;
+  constexpr int kC4 = D / 4;
+  for (int idx = tid; idx < M * kC4; idx += kThreads) {
+    const int m = idx / kC4, c4 = idx % kC4;
+    const int mtile = m >> 4, r = m & 15;
+    float mstar = -INFINITY;
+    for (int s2 = 0; s2 < nslices; ++s2)
+      mstar = fmaxf(mstar, mml[((s2 * mt_eff + mtile) * 16 + r) * 2]);
+    float lsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (mstar != -INFINITY) {
+      for (int s2 = 0; s2 < nslices; ++s2) {
+        const int w = s2 * mt_eff + mtile;
+        const float ms = mml[(w * 16 + r) * 2];
+        if (ms == -INFINITY) continue;
+        const float f = fast_exp2(ms - mstar);
+        lsum += f * mml[(w * 16 + r) * 2 + 1];
+        const float4 x = *reinterpret_cast<const float4*>(mo + (w * 16 + r) * C::kMergeStride + c4 * 4);
+        acc.x += f * x.x; acc.y += f * x.y; acc.z += f * x.z; acc.w += f * x.w;
+      }
+    }
+    const float inv = lsum > 0.f ? v_final / lsum : 0.f;
+    acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+    const float lse2 = lsum > 0.f ? mstar + __log2f(lsum) : -INFINITY;
+    const int64_t row = q0 + m / hpc;
+    const int head = head0 + m % hpc;
+    if (single) {
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + (row * a.hq + head) * D + c4 * 4;
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(dst) = pk;
+      if (c4 == 0 && a.lse) a.lse[row * a.hq + head] = lse2 * kLn2;
+    } else {
+      const int64_t prow = ((int64_t)split * a.rows_cap + row) * a.hq + head;
+      *reinterpret_cast<float4*>(a.part_o + prow * D + c4 * 4) = acc;
+      if (c4 == 0) a.part_lse[prow] = lse2;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ stage 2
+// One warp per (request, row, q head): log-sum-exp merge of the chunk
+// partials ("Stage 2 merges per row").
+template <int D>
+__global__ void __launch_bounds__(128) stage2_merge(const __grid_constant__ DecodeArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t item = (int64_t)blockIdx.x * 4 + warp;
+  const int64_t per_b = (int64_t)a.max_q_len * a.hq;
+  const int b = static_cast<int>(item / per_b);
+  if (b >= a.batch) return;
+  const int rem = static_cast<int>(item % per_b);
+  const int i = rem / a.hq, head = rem % a.hq;
+  const int q0 = a.qo_indptr[b];
+  const int R = a.qo_indptr[b + 1] - q0;
+  const int L = a.kv_len[b];
+  if (i >= R || R > a.max_q_len || L < R || L > a.max_kv_len || q0 + R > a.rows_cap) return;
+  const int W = a.window ? a.window[b] : 0;
+  const SplitRange sr = split_range(L, R, W, a.page_size, a.chunk_pages);
+  if (sr.num_splits <= 1) return;  // stage 1 wrote the final result
+  const int64_t row = q0 + i;
+  const int n = sr.num_splits;
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  const int64_t stride = a.rows_cap * a.hq;  // partial rows per split
+  const int64_t base = row * a.hq + head;
+  float mx = -INFINITY;
+  for (int s = lane; s < n; s += 32) mx = fmaxf(mx, a.part_lse[s * stride + base]);
+#pragma unroll
+  for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  constexpr int kPer = D / 32;  // floats per lane
+  float acc[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  if (mx != -INFINITY) {
+    for (int s = 0; s < n; ++s) {
+      const float ls = a.part_lse[s * stride + base];
+      if (ls == -INFINITY) continue;
+      const float w = exp2f(ls - mx);
+      wsum += w;
+      const float* src = a.part_o + (s * stride + base) * D + lane * kPer;
+#pragma unroll
+      for (int e = 0; e < kPer; e += 4) {
+        if constexpr (kPer >= 4) {
+          const float4 x = *reinterpret_cast<const float4*>(src + e);
+          acc[e] += w * x.x; acc[e + 1] += w * x.y; acc[e + 2] += w * x.z; acc[e + 3] += w * x.w;
+        }
+      }
+      if constexpr (kPer == 2) {
+        const float2 x = *reinterpret_cast<const float2*>(src);
+        acc[0] += w * x.x; acc[1] += w * x.y;
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + base * D + lane * kPer;
+#pragma unroll
+  for (int e = 0; e < kPer; e += 2) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+    *reinterpret_cast<__nv_bfloat162*>(dst + e) = v;
+  }
+  if (lane == 0 && a.lse) a.lse[base] = wsum > 0.f ? (mx + __log2f(wsum)) * kLn2 : -INFINITY;
+}
+
+// ---------------------------------------------------------------- dispatch
+using KernelFn = void (*)(DecodeArgs);
+
+template <int D>
+KernelFn pick_stage1(int kv, int qd, int sm) {
+  if (kv == PDA_BF16) return stage1_mma<D, PDA_BF16, PDA_BF16, PDA_SCALE_NONE>;
+  if (qd == PDA_BF16) {
+    if (sm == PDA_SCALE_TENSOR) return stage1_mma<D, PDA_E4M3, PDA_BF16, PDA_SCALE_TENSOR>;
+    return stage1_mma<D, PDA_E4M3, PDA_BF16, PDA_SCALE_TOKEN_HEAD>;
+  }
+  if (sm == PDA_SCALE_TENSOR) return stage1_mma<D, PDA_E4M3, PDA_E4M3, PDA_SCALE_TENSOR>;
+  return stage1_mma<D, PDA_E4M3, PDA_E4M3, PDA_SCALE_TOKEN_HEAD>;
+}
+
+template <int D>
+int smem_of(int kv, int qd, int sm) {
+  if (kv == PDA_BF16) return Cfg<D, PDA_BF16, PDA_BF16, PDA_SCALE_NONE>::kSmem;
+  if (qd == PDA_BF16) {
+    if (sm == PDA_SCALE_TENSOR) return Cfg<D, PDA_E4M3, PDA_BF16, PDA_SCALE_TENSOR>::kSmem;
+    return Cfg<D, PDA_E4M3, PDA_BF16, PDA_SCALE_TOKEN_HEAD>::kSmem;
+  }
+  if (sm == PDA_SCALE_TENSOR) return Cfg<D, PDA_E4M3, PDA_E4M3, PDA_SCALE_TENSOR>::kSmem;
+  return Cfg<D, PDA_E4M3, PDA_E4M3, PDA_SCALE_TOKEN_HEAD>::kSmem;
+}
+
+KernelFn stage1_for(const pda_plan_t* p) {
+  switch (p->head_dim) {
+    case 64: return pick_stage1<64>(p->kv_dtype, p->q_dtype, p->scale_mode);
+    case 128: return pick_stage1<128>(p->kv_dtype, p->q_dtype, p->scale_mode);
+    default: return pick_stage1<256>(p->kv_dtype, p->q_dtype, p->scale_mode);
+  }
+}
+
+KernelFn stage2_for(const pda_plan_t* p) {
+  switch (p->head_dim) {
+    case 64: return stage2_merge<64>;
+    case 128: return stage2_merge<128>;
+    default: return stage2_merge<256>;
+  }
+}
+
+}  // namespace
+
+int stage1_smem_bytes(const pda_plan_t* p) {
+  switch (p->head_dim) {
+    case 64: return smem_of<64>(p->kv_dtype, p->q_dtype, p->scale_mode);
+    case 128: return smem_of<128>(p->kv_dtype, p->q_dtype, p->scale_mode);
+    default: return smem_of<256>(p->kv_dtype, p->q_dtype, p->scale_mode);
+  }
+}
+
+int stage1_ctas_per_sm(const pda_plan_t* p) {
+  // 228 KB of shared memory per SM, 1 KB reserved per CTA; the kernel is
+  // built for at most 255 registers x 128 threads, so shared memory decides.
+  const int per = stage1_smem_bytes(p) + 1024;
+  int n = (228 * 1024) / per;
+  return n < 1 ? 1 : (n > 4 ? 4 : n);
+}
+
+int launch_decode(const pda_plan_t* plan, const DecodeArgs& args, pda_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  KernelFn k1 = stage1_for(plan);
+  const int smem = plan->stage1_smem_bytes;
+  if (cudaFuncSetAttribute(reinterpret_cast<const void*>(k1),
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return PDA_ERR_CUDA;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(plan->grid_ctas));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  if (cudaLaunchKernelEx(&cfg, k1, args) != cudaSuccess) {
+    cudaGetLastError();
+    return PDA_ERR_CUDA;
+  }
+  if (plan->max_splits > 1) {
+    const int64_t items = (int64_t)plan->batch * args.max_q_len * plan->num_qo_heads;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t c2 = {};
+    c2.gridDim = dim3(static_cast<unsigned>((items + 3) / 4));
+    c2.blockDim = dim3(128);
+    c2.dynamicSmemBytes = 0;
+    c2.stream = s;
+    c2.attrs = attr;
+    c2.numAttrs = 1;
+    if (cudaLaunchKernelEx(&c2, stage2_for(plan), args) != cudaSuccess) {
+      cudaGetLastError();
+      return PDA_ERR_CUDA;
+    }
+  }
+  return PDA_OK;
+}
+
+}  // namespace pda

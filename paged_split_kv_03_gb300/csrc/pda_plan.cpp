@@ -1,0 +1,258 @@
+// pda_plan.cpp -- host side of the C ABI: the split planner, argument
+// validation, status access and error strings.
+//
+// The planner keeps the KV split of "perf(attention): run up to 8 query rows
+// per request in the triton decode kernel" (FreeToken PR #900, "Changes") and
+// sizes it for this GPU: it picks how many KV pages one CTA streams
+// (chunk_pages) from the batch, the context and the SM count, and it picks
+// how many query heads one CTA packs next to the request's rows so that the
+// heads always divide the GQA group (the same section's fix for groups such
+// as 48 query / 2 kv heads).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "pda_internal.h"
+
+namespace {
+
+bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int elem_bytes(int dtype) { return dtype == PDA_E4M3 ? 1 : 2; }
+
+}  // namespace
+
+extern "C" int pda_version(void) { return 100; }
+
+extern "C" int pda_struct_sizes(size_t* params_bytes, size_t* plan_bytes) {
+  if (params_bytes) *params_bytes = sizeof(pda_params);
+  if (plan_bytes) *plan_bytes = sizeof(pda_plan_t);
+  return PDA_OK;
+}
+
+extern "C" const char* pda_strerror(int code) {
+  switch (code) {
+    case PDA_OK: return "ok";
+    case PDA_ERR_NULL: return "a required pointer is NULL";
+    case PDA_ERR_INVALID: return "a size or count is out of range";
+    case PDA_ERR_UNSUPPORTED: return "head_dim / page_size / dtype combination not supported";
+    case PDA_ERR_ALIGNMENT: return "a base address or stride is not 16-byte aligned";
+    case PDA_ERR_SCRATCH: return "split_scratch is NULL or not 256-byte aligned";
+    case PDA_ERR_CUDA: return "a CUDA runtime call failed";
+    case PDA_ERR_PLAN: return "plan was not produced by pda_plan of this library version";
+    default: return "unknown pda error code";
+  }
+}
+
+extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scratch_bytes) {
+  if (!p || !out) return PDA_ERR_NULL;
+  pda_plan_t pl;
+  std::memset(&pl, 0, sizeof pl);
+  // ---- shape checks
+  if (p->num_qo_heads <= 0 || p->num_kv_heads <= 0 || p->num_qo_heads % p->num_kv_heads)
+    return PDA_ERR_INVALID;
+  if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256) return PDA_ERR_UNSUPPORTED;
+  if (!is_pow2(p->page_size) || p->page_size > 256) return PDA_ERR_UNSUPPORTED;
+  if (p->kv_dtype != PDA_BF16 && p->kv_dtype != PDA_E4M3) return PDA_ERR_UNSUPPORTED;
+  if (p->q_dtype != PDA_BF16 && p->q_dtype != PDA_E4M3) return PDA_ERR_UNSUPPORTED;
+  if (p->q_dtype == PDA_E4M3 && p->kv_dtype != PDA_E4M3) return PDA_ERR_UNSUPPORTED;
+  if (p->kv_dtype == PDA_BF16 && p->scale_mode != PDA_SCALE_NONE) return PDA_ERR_UNSUPPORTED;
+  if (p->kv_dtype == PDA_E4M3 && p->scale_mode != PDA_SCALE_TENSOR &&
+      p->scale_mode != PDA_SCALE_TOKEN_HEAD)
+    return PDA_ERR_UNSUPPORTED;
+  if (p->max_batch <= 0 || p->max_q_len < 1 || p->max_q_len > pda::kMaxQLen) return PDA_ERR_INVALID;
+  if (p->max_kv_len < 1 || p->num_pages < 1) return PDA_ERR_INVALID;
+  if (p->batch < 0 || p->batch > p->max_batch) return PDA_ERR_INVALID;
+  if (p->kv_stride_page <= 0 || p->kv_stride_token <= 0 || p->kv_stride_head <= 0)
+    return PDA_ERR_INVALID;
+  if (p->chunk_pages < 0) return PDA_ERR_INVALID;
+  if (p->kernel < PDA_KERNEL_AUTO || p->kernel > PDA_KERNEL_TC) return PDA_ERR_INVALID;
+  // 16-byte alignment of every stride ("require 16-byte aligned cache bases
+  // and strides", follow-up commit on the FreeToken page)
+  const int eb = elem_bytes(p->kv_dtype);
+  if ((p->kv_stride_page * eb) % 16 || (p->kv_stride_token * eb) % 16 ||
+      (p->kv_stride_head * eb) % 16)
+    return PDA_ERR_ALIGNMENT;
+
+  int num_sms = p->num_sms;
+  if (num_sms <= 0) {
+    if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, p->device) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return PDA_ERR_CUDA;
+    }
+  }
+
+  pl.magic = PDA_PLAN_MAGIC;
+  pl.num_qo_heads = p->num_qo_heads;
+  pl.num_kv_heads = p->num_kv_heads;
+  pl.head_dim = p->head_dim;
+  pl.page_size = p->page_size;
+  pl.q_dtype = p->q_dtype;
+  pl.kv_dtype = p->kv_dtype;
+  pl.scale_mode = p->scale_mode;
+  pl.max_batch = p->max_batch;
+  pl.max_q_len = p->max_q_len;
+  pl.max_kv_len = p->max_kv_len;
+  pl.num_pages = p->num_pages;
+  pl.batch = p->batch ? p->batch : p->max_batch;
+  pl.kv_stride_page = p->kv_stride_page;
+  pl.kv_stride_token = p->kv_stride_token;
+  pl.kv_stride_head = p->kv_stride_head;
+  pl.group = p->num_qo_heads / p->num_kv_heads;
+  pl.num_sms = num_sms;
+  pl.kernel = p->kernel == PDA_KERNEL_AUTO ? PDA_KERNEL_MMA : p->kernel;
+  if (pl.kernel == PDA_KERNEL_TC) return PDA_ERR_UNSUPPORTED;  // not built yet
+  pl.rows_per_cta = pda::kMmaRowsPerCta;
+
+  // Query heads per CTA for a request with R rows: the largest divisor of the
+  // GQA group whose R x heads tile fits the CTA's rows.
+  for (int R = 1; R <= pda::kMaxQLen; ++R) {
+    int best = 1;
+    for (int d = 1; d <= pl.group; ++d)
+      if (pl.group % d == 0 && R * d <= pl.rows_per_cta) best = d;
+    pl.heads_per_cta[R] = best;
+  }
+  pl.heads_per_cta[0] = pl.heads_per_cta[1];
+  pl.head_blocks = pl.group / pl.heads_per_cta[pl.max_q_len];
+
+  // Context to plan for: the maximum, or the exact host lengths when given.
+  int64_t max_len = p->max_kv_len;
+  if (p->host_kv_len) {
+    int64_t m = 1;
+    for (int b = 0; b < pl.batch; ++b) m = std::max<int64_t>(m, p->host_kv_len[b]);
+    max_len = std::min<int64_t>(m, p->max_kv_len);
+    pl.max_kv_len = (int32_t)max_len;
+  }
+  const int64_t pages_max = ceil_div(max_len, p->page_size);
+
+  // Split planning. A chunk is a whole number of 64-token tiles when pages
+  // are smaller than a tile, so that only a request's last chunk is ragged.
+  pl.stage1_smem_bytes = pda::stage1_smem_bytes(&pl);
+  const int per_sm = std::max(1, pda::stage1_ctas_per_sm(&pl));
+  const int64_t slots = (int64_t)num_sms * per_sm;
+  const int64_t units = (int64_t)pl.batch * pl.num_kv_heads * pl.head_blocks;
+  const int64_t tile_pages = std::max<int64_t>(1, 64 / p->page_size);
+  const int64_t min_chunk = std::max<int64_t>(tile_pages, ceil_div(256, p->page_size));
+  int64_t chunk;
+  if (p->chunk_pages > 0) {
+    chunk = ceil_div(p->chunk_pages, tile_pages) * tile_pages;
+  } else {
+    const int64_t want_splits = std::max<int64_t>(1, ceil_div(2 * slots, units));
+    chunk = ceil_div(pages_max, want_splits);
+    chunk = ceil_div(chunk, tile_pages) * tile_pages;
+    chunk = std::max(chunk, min_chunk);
+  }
+  chunk = std::min<int64_t>(chunk, std::max<int64_t>(pages_max, 1));
+  chunk = ceil_div(chunk, tile_pages) * tile_pages;
+  pl.chunk_pages = (int32_t)chunk;
+  pl.max_splits = (int32_t)ceil_div(pages_max, chunk);
+  pl.grid_ctas = units * pl.max_splits;
+  if (pl.grid_ctas > 0x7fffffffLL) return PDA_ERR_INVALID;
+
+  pl.rows_cap = (int64_t)pl.max_batch * pl.max_q_len;
+  int64_t off = pda::kStatusHeaderBytes;
+  pl.scratch_lse_offset = off;
+  if (pl.max_splits > 1) {
+    off += ceil_div((int64_t)pl.max_splits * pl.rows_cap * pl.num_qo_heads * 4, 256) * 256;
+    pl.scratch_o_offset = off;
+    off += (int64_t)pl.max_splits * pl.rows_cap * pl.num_qo_heads * pl.head_dim * 4;
+  } else {
+    pl.scratch_o_offset = off;
+  }
+  pl.scratch_bytes = off;
+  *out = pl;
+  if (split_scratch_bytes) *split_scratch_bytes = (size_t)pl.scratch_bytes;
+  return PDA_OK;
+}
+
+extern "C" int pda_decode(const pda_plan_t* plan, const void* q, const void* k_pages,
+                          const void* v_pages, const int32_t* page_table,
+                          const int32_t* kv_indptr, const int32_t* kv_len,
+                          const int32_t* qo_indptr, int32_t max_q_len, const int32_t* window,
+                          float sm_scale, const float* k_scale, const float* v_scale, void* out,
+                          float* lse, void* split_scratch, pda_stream_t stream) {
+  if (!plan) return PDA_ERR_NULL;
+  if (plan->magic != PDA_PLAN_MAGIC) return PDA_ERR_PLAN;
+  if (!q || !k_pages || !v_pages || !page_table || !kv_indptr || !kv_len || !qo_indptr || !out)
+    return PDA_ERR_NULL;
+  if (!split_scratch) return PDA_ERR_SCRATCH;
+  if (reinterpret_cast<uintptr_t>(split_scratch) % 256) return PDA_ERR_SCRATCH;
+  if (max_q_len < 1 || max_q_len > plan->max_q_len) return PDA_ERR_INVALID;
+  if (plan->scale_mode != PDA_SCALE_NONE && (!k_scale || !v_scale)) return PDA_ERR_NULL;
+  auto a16 = [](const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
+  if (!a16(q) || !a16(k_pages) || !a16(v_pages) || !a16(out)) return PDA_ERR_ALIGNMENT;
+  if (lse && reinterpret_cast<uintptr_t>(lse) % 4) return PDA_ERR_ALIGNMENT;
+  if (plan->scale_mode != PDA_SCALE_NONE &&
+      (reinterpret_cast<uintptr_t>(k_scale) % 4 || reinterpret_cast<uintptr_t>(v_scale) % 4))
+    return PDA_ERR_ALIGNMENT;
+  if (plan->batch == 0) return PDA_OK;
+
+  pda::DecodeArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.q = q;
+  a.k = k_pages;
+  a.v = v_pages;
+  a.page_table = page_table;
+  a.kv_indptr = kv_indptr;
+  a.kv_len = kv_len;
+  a.qo_indptr = qo_indptr;
+  a.window = window;
+  a.k_scale = plan->scale_mode != PDA_SCALE_NONE ? k_scale : nullptr;
+  a.v_scale = plan->scale_mode != PDA_SCALE_NONE ? v_scale : nullptr;
+  a.out = out;
+  a.lse = lse;
+  char* base = static_cast<char*>(split_scratch);
+  a.status = reinterpret_cast<uint32_t*>(base);
+  a.part_lse = reinterpret_cast<float*>(base + plan->scratch_lse_offset);
+  a.part_o = reinterpret_cast<float*>(base + plan->scratch_o_offset);
+  a.sm_scale = sm_scale;
+  a.sp = plan->kv_stride_page;
+  a.st = plan->kv_stride_token;
+  a.sh = plan->kv_stride_head;
+  a.batch = plan->batch;
+  a.hq = plan->num_qo_heads;
+  a.hkv = plan->num_kv_heads;
+  a.group = plan->group;
+  a.head_dim = plan->head_dim;
+  a.page_size = plan->page_size;
+  a.num_pages = plan->num_pages;
+  a.max_q_len = max_q_len;
+  a.max_kv_len = plan->max_kv_len;
+  a.max_splits = plan->max_splits;
+  a.head_blocks = plan->head_blocks;
+  a.chunk_pages = plan->chunk_pages;
+  a.rows_cap = plan->rows_cap;
+  for (int r = 0; r <= pda::kMaxQLen; ++r) a.hpc[r] = plan->heads_per_cta[r];
+  return pda::launch_decode(plan, a, stream);
+}
+
+extern "C" int pda_get_status(const pda_plan_t* plan, const void* split_scratch,
+                              uint32_t* host_bits, pda_stream_t stream) {
+  if (!plan || !host_bits) return PDA_ERR_NULL;
+  if (plan->magic != PDA_PLAN_MAGIC) return PDA_ERR_PLAN;
+  if (!split_scratch) return PDA_ERR_SCRATCH;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(host_bits, split_scratch, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return PDA_ERR_CUDA;
+  }
+  return PDA_OK;
+}
+
+extern "C" int pda_reset_status(const pda_plan_t* plan, void* split_scratch, pda_stream_t stream) {
+  if (!plan) return PDA_ERR_NULL;
+  if (plan->magic != PDA_PLAN_MAGIC) return PDA_ERR_PLAN;
+  if (!split_scratch) return PDA_ERR_SCRATCH;
+  if (cudaMemsetAsync(split_scratch, 0, sizeof(uint32_t),
+                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return PDA_ERR_CUDA;
+  }
+  return PDA_OK;
+}

@@ -121,6 +121,14 @@ def _quant_e4m3(x: torch.Tensor, amax_dims) -> tuple:
     return codes, scale.to(torch.float32)
 
 
+def _exact_e4m3(x: torch.Tensor) -> torch.Tensor:
+    """E4M3 codes of values that E4M3 represents exactly (asserted)."""
+    codes = x.to(torch.float8_e4m3fn)
+    back = codes.to(torch.float32)
+    assert torch.equal(back, x), "value not exactly representable in E4M3"
+    return codes.view(torch.uint8)
+
+
 def make_workload(*, name: str = "custom", batch: int, rows: Union[int, Sequence[int]],
                   kv_lens: Union[int, Sequence[int]], num_qo_heads: int, num_kv_heads: int,
                   head_dim: int, page_size: int, kv_dtype: str = "bf16", q_dtype: str = "bf16",
@@ -128,10 +136,19 @@ def make_workload(*, name: str = "custom", batch: int, rows: Union[int, Sequence
                   layout: str = "NHD", seed: int = 0, device="cpu",
                   k_outlier_frac: float = 0.0, k_outlier_mult: float = 20.0,
                   q_mult: float = 1.0, extra_pages: int = 4, extra_table_entries: int = 1,
-                  poison: bool = True, value_fn=None) -> Workload:
-    """Draw one workload. ``value_fn(kind, shape, gen)`` may replace N(0,1)
-    draws for structured tests (kind in {"q", "k", "v"}, logical shapes
-    [rows, Hq, D] and [num_pages, P, Hkv, D])."""
+                  poison: bool = True, value_fn=None, token_fn=None,
+                  unit_scale: bool = False, scale_fn=None) -> Workload:
+    """Draw one workload.
+
+    Structured tests may replace the N(0,1) draws:
+      ``value_fn(kind, shape, gen)`` -- kind in {"q", "k", "v"}, logical
+          shapes [rows, Hq, D] and [num_pages, P, Hkv, D];
+      ``token_fn(kind, b, L)`` -- kind in {"k", "v"}: values [L, Hkv, D] of
+          request b's tokens in order, scattered through the page table;
+      ``unit_scale`` -- E4M3 scales fixed at 1 (values must be exact E4M3);
+      ``scale_fn(kind, b, L)`` -- per-(token, kv head) scales [L, Hkv] of
+          request b (with ``unit_scale``), e.g. to ramp logits per token.
+    """
     assert kv_dtype in ("bf16", "e4m3") and q_dtype in ("bf16", "e4m3")
     assert num_qo_heads % num_kv_heads == 0
     if kv_dtype == "bf16":
@@ -169,6 +186,16 @@ def make_workload(*, name: str = "custom", batch: int, rows: Union[int, Sequence
     qf = draw("q", (total_rows, num_qo_heads, D)) * q_mult
     kf = draw("k", (num_pages, P, H, D))
     vf = draw("v", (num_pages, P, H, D))
+    if token_fn is not None or scale_fn is not None:
+        cursor = 0
+        for b in range(batch):
+            pages = torch.tensor(perm[cursor:cursor + npages_b[b]], dtype=torch.long, device=dev)
+            cursor += npages_b[b]
+            tok = torch.arange(L[b], device=dev)
+            pg, sl = pages[tok // P], tok % P
+            if token_fn is not None:
+                kf[pg, sl] = token_fn("k", b, L[b]).to(dev, torch.float32)
+                vf[pg, sl] = token_fn("v", b, L[b]).to(dev, torch.float32)
     outlier_channels = None
     if k_outlier_frac > 0:
         n_out = max(1, int(round(k_outlier_frac * D)))
@@ -191,6 +218,8 @@ def make_workload(*, name: str = "custom", batch: int, rows: Union[int, Sequence
     q_scale = 1.0
     if q_dtype == "bf16":
         q = qf.to(torch.bfloat16)
+    elif unit_scale:
+        q = _exact_e4m3(qf)
     else:
         q, qs = _quant_e4m3(qf, None)
         q_scale = float(qs.item())
@@ -201,6 +230,24 @@ def make_workload(*, name: str = "custom", batch: int, rows: Union[int, Sequence
     k_scale = v_scale = None
     if kv_dtype == "bf16":
         kc, vc = kf.to(torch.bfloat16), vf.to(torch.bfloat16)
+    elif unit_scale:
+        kc, vc = _exact_e4m3(kf), _exact_e4m3(vf)
+        if scale_mode == SCALE_TENSOR:
+            k_scale = torch.ones(1, dtype=torch.float32, device=dev)
+            v_scale = torch.ones(1, dtype=torch.float32, device=dev)
+        else:
+            k_scale = torch.ones(num_pages, P, H, dtype=torch.float32, device=dev)
+            v_scale = torch.ones(num_pages, P, H, dtype=torch.float32, device=dev)
+            if scale_fn is not None:
+                cursor = 0
+                for b in range(batch):
+                    pages = torch.tensor(perm[cursor:cursor + npages_b[b]], dtype=torch.long,
+                                         device=dev)
+                    cursor += npages_b[b]
+                    tok = torch.arange(L[b], device=dev)
+                    pg, sl = pages[tok // P], tok % P
+                    k_scale[pg, sl] = scale_fn("k", b, L[b]).to(dev, torch.float32)
+                    v_scale[pg, sl] = scale_fn("v", b, L[b]).to(dev, torch.float32)
     elif scale_mode == SCALE_TENSOR:
         kc, k_scale = _quant_e4m3(kf, None)
         vc, v_scale = _quant_e4m3(vf, None)

@@ -1,0 +1,88 @@
+"""Algorithmic bytes and flops of one paged decode call (the roofline's
+numerator).
+
+Byte model, per call (GB = 1e9 bytes):
+  * K and V: every token a CTA has to stream, i.e. for each request the
+    tokens [lo_page * P, L) -- from the first page that holds a visible key of
+    any of its rows to its last token -- times Hkv * D * element size, for K
+    and for V. Masked keys inside those pages count; pages wholly outside every
+    row's window do not, and neither do the per-head re-reads the kernel
+    avoids (each kv head's K/V counts once for all of its q heads).
+  * per-(token, kv head) scales: 4 bytes per streamed token per kv head, for K
+    and for V; per-tensor scales: 8 bytes.
+  * Q read, out (bf16) and lse (fp32) written.
+  * page-table entries read (one int32 per streamed page per request) and the
+    int32 kv_indptr / kv_len / qo_indptr / window arrays.
+  * split scratch: for every request with more than one KV split, each split
+    writes and stage 2 reads (D + 1) fp32 per (row, q head).
+
+With the scratch, lse and index terms left out this is the accounting of
+"[Feature Request] Support q_len > 1 for FP8 decode" (hpc-ops issue #4): its
+FP8 decode benchmark (bs 128, 64/8 heads, D 128, ctx 2048) reports
+3672.1 GB/s at 6800 iter/s, which is (K+V at 1 B + Q at 1 B + O at 2 B) per
+iteration; the golden test pins that.
+
+Flops: 4 * D per (row, q head, visible key) -- QK^T and PV, two flops per
+multiply-add.
+"""
+from __future__ import annotations
+
+
+def _split_range(L, R, W, P, chunk_pages):
+    p0 = L - R
+    lo = max(0, p0 - W + 1) if W > 0 else 0
+    lo_page = lo // P
+    npages = -(-L // P)
+    span = npages - lo_page
+    nsplit = -(-span // chunk_pages) if span > 0 else 0
+    return lo, lo_page, npages, nsplit
+
+
+def call_bytes(wl, chunk_pages: int | None = None, include_scratch: bool = True) -> dict:
+    """Algorithmic bytes of one call on workload ``wl`` (a synth.Workload);
+    ``chunk_pages`` is the plan's chunk (None: treat as one split)."""
+    P, H, D, Hq = wl.page_size, wl.num_kv_heads, wl.head_dim, wl.num_qo_heads
+    kv_elt = 1 if wl.kv_e4m3 else 2
+    q_elt = 1 if wl.q_e4m3 else 2
+    lens = wl.kv_len.cpu().tolist()
+    qo = wl.qo_indptr.cpu().tolist()
+    wins = wl.window.cpu().tolist() if wl.window is not None else [0] * len(lens)
+    kv = scales = table = scratch = 0
+    rows_total = qo[-1]
+    for b, L in enumerate(lens):
+        R = qo[b + 1] - qo[b]
+        if R <= 0 or L < R:
+            continue
+        lo, lo_page, npages, nsplit = _split_range(L, R, wins[b], P, chunk_pages or 1 << 30)
+        tokens = L - lo_page * P
+        kv += 2 * tokens * H * D * kv_elt
+        if wl.scale_mode == 2:
+            scales += 2 * tokens * H * 4
+        table += (npages - lo_page) * 4
+        if include_scratch and nsplit > 1:
+            scratch += 2 * nsplit * R * Hq * (D + 1) * 4
+    if wl.scale_mode == 1:
+        scales += 8
+    q = rows_total * Hq * D * q_elt
+    out = rows_total * Hq * D * 2
+    lse = rows_total * Hq * 4
+    index = 4 * (3 * len(lens) + 2) + (4 * len(lens) if wl.window is not None else 0)
+    total = kv + scales + q + out + lse + table + index + scratch
+    return dict(kv=kv, scales=scales, q=q, out=out, lse=lse, page_table=table, index=index,
+                scratch=scratch, total=total)
+
+
+def call_flops(wl) -> int:
+    """4 * D per (row, q head, visible key)."""
+    D, Hq = wl.head_dim, wl.num_qo_heads
+    lens = wl.kv_len.cpu().tolist()
+    qo = wl.qo_indptr.cpu().tolist()
+    wins = wl.window.cpu().tolist() if wl.window is not None else [0] * len(lens)
+    visible = 0
+    for b, L in enumerate(lens):
+        R = qo[b + 1] - qo[b]
+        for i in range(R):
+            pos = L - R + i
+            lo = max(0, pos - wins[b] + 1) if wins[b] > 0 else 0
+            visible += pos - lo + 1
+    return 4 * D * Hq * visible

@@ -1,0 +1,82 @@
+"""Shared helpers of the GPU parity tests: run the CUDA library through its
+C ABI, run the fp64 oracle on the same arrays, compare with the stated
+tolerances.
+
+Tolerances (stated by the task's target and restated here): bf16 KV --
+max |err| <= 1e-2 and mean |err| <= 1e-3 over all output elements, lse
+|err| <= 1e-3; FP8 KV -- max |err| <= 3e-2 against the oracle on the
+dequantised values (mean <= 3e-3), lse |err| <= 1e-3.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from paged_split_kv_03_gb300 import binding as B
+
+TOL_BF16 = dict(max=1e-2, mean=1e-3, lse=1e-3)
+TOL_FP8 = dict(max=3e-2, mean=3e-3, lse=1e-3)
+
+
+def tol_for(wl):
+    return TOL_FP8 if wl.kv_e4m3 else TOL_BF16
+
+
+def run_decode(wl, *, chunk_pages=0, kernel=B.PDA_KERNEL_AUTO, max_q_len=None, max_batch=None,
+               max_kv_len=None, decoder=None, fill=float("nan")):
+    """Run pda_decode on a device-resident workload; returns (out fp32 CPU
+    [rows, Hq, D], lse CPU [rows, Hq], status bits, decoder)."""
+    dev = wl.q.device
+    assert dev.type == "cuda"
+    if decoder is None:
+        params = B.params_for(wl, chunk_pages=chunk_pages, kernel=kernel, max_q_len=max_q_len,
+                              max_batch=max_batch, max_kv_len=max_kv_len,
+                              device=dev.index or 0)
+        decoder = B.Decoder(params, device=dev)
+    rows = wl.total_rows
+    out = torch.full((rows, wl.num_qo_heads, wl.head_dim), fill, dtype=torch.bfloat16, device=dev)
+    lse = torch.full((rows, wl.num_qo_heads), fill, dtype=torch.float32, device=dev)
+    decoder.run(wl, out, lse, max_q_len=max_q_len)
+    torch.cuda.synchronize()
+    status = decoder.status()
+    return out.float().cpu(), lse.cpu(), status, decoder
+
+
+def oracle_ref(wl, items=None, num_threads=0):
+    """fp64 oracle on the workload's arrays (copied to the host)."""
+    host = wl.to("cpu")
+    out, lse, rc = oracle.attention_for(host, items=items, num_threads=num_threads)
+    assert rc == 0, f"oracle status {rc}"
+    if items is None:
+        out = out.reshape(wl.total_rows, wl.num_qo_heads, wl.head_dim)
+        lse = lse.reshape(wl.total_rows, wl.num_qo_heads)
+    return out, lse
+
+
+def assert_close(out, lse, ref_o, ref_l, tol, what=""):
+    out = np.asarray(out, dtype=np.float64)
+    lse = np.asarray(lse, dtype=np.float64)
+    assert np.all(np.isfinite(out)), f"{what}: non-finite output (stray read or unwritten row)"
+    assert np.all(np.isfinite(lse)), f"{what}: non-finite lse"
+    err = np.abs(out - ref_o)
+    lerr = np.abs(lse - ref_l)
+    assert err.max() <= tol["max"], f"{what}: max |err| {err.max():.3e} > {tol['max']}"
+    assert err.mean() <= tol["mean"], f"{what}: mean |err| {err.mean():.3e} > {tol['mean']}"
+    assert lerr.max() <= tol["lse"], f"{what}: lse |err| {lerr.max():.3e} > {tol['lse']}"
+    return float(err.max()), float(err.mean()), float(lerr.max())
+
+
+def sample_items(wl, n, seed=0, must=()):
+    """n flat (row, head) indices: spread over requests, rows and heads, plus
+    the first/last row of every ``must`` request."""
+    g = torch.Generator().manual_seed(seed)
+    total = wl.total_rows * wl.num_qo_heads
+    picks = set(torch.randint(0, total, (n,), generator=g).tolist())
+    qo = wl.qo_indptr.cpu().tolist()
+    for b in must:
+        for r in (qo[b], qo[b + 1] - 1):
+            if qo[b] <= r < qo[b + 1]:
+                picks.add(r * wl.num_qo_heads)
+                picks.add(r * wl.num_qo_heads + wl.num_qo_heads - 1)
+    return np.array(sorted(picks), dtype=np.int64)

@@ -1,0 +1,129 @@
+"""The C ABI on the CPU: the library builds and loads, exports every entry
+point include/pda.h declares, agrees with the binding's struct layouts, and
+its planner and host-side checks behave (no kernel is launched here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_split_kv_03_gb300 import binding as B
+from paged_split_kv_03_gb300 import build as build_mod
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "pda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return B.load_library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w[\w\s\*]*?\b(pda_\w+)\s*\(", src, re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"pda_plan", "pda_decode", "pda_get_status", "pda_reset_status",
+            "pda_strerror"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in pda.h but not exported"
+
+
+def test_struct_layouts_match(lib):
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.pda_struct_sizes(ctypes.byref(a), ctypes.byref(b)) == 0
+    assert a.value == ctypes.sizeof(B.PdaParams)
+    assert b.value == ctypes.sizeof(B.PdaPlan)
+
+
+def _params(**kw):
+    p = B.PdaParams()
+    base = dict(num_qo_heads=16, num_kv_heads=2, head_dim=256, page_size=16, q_dtype=0,
+                kv_dtype=0, scale_mode=0, max_batch=16, max_q_len=8, max_kv_len=32768,
+                num_pages=40000, kv_stride_page=16 * 2 * 256, kv_stride_token=2 * 256,
+                kv_stride_head=256, device=0, num_sms=152, batch=0, chunk_pages=0, kernel=0)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_plan_heads_divide_group(lib):
+    # 48 query / 2 kv heads: group 24; heads per CTA must divide 24 at every R
+    plan, nbytes, rc = B.pda_plan(_params(num_qo_heads=48, num_kv_heads=2, head_dim=128))
+    for R in range(1, 9):
+        h = plan.heads_per_cta[R]
+        assert 24 % h == 0 and R * h <= plan.rows_per_cta
+    assert plan.heads_per_cta[1] == 24 and plan.heads_per_cta[8] == 8
+    assert plan.head_blocks == 3
+
+
+def test_plan_splits_and_scratch(lib):
+    plan, nbytes, _ = B.pda_plan(_params(max_batch=1, max_kv_len=32768))
+    assert plan.max_splits > 1                      # bs 1: the KV split fills the GPU
+    assert plan.chunk_pages * 16 % 64 == 0          # whole 64-token tiles
+    assert plan.max_splits * plan.chunk_pages * 16 >= 32768
+    rows = 1 * 8
+    assert nbytes == plan.scratch_bytes >= 256 + plan.max_splits * rows * 16 * 257 * 4
+    plan2, nbytes2, _ = B.pda_plan(_params(num_qo_heads=64, num_kv_heads=8, head_dim=128,
+                                           page_size=64, q_dtype=1, kv_dtype=1, scale_mode=1,
+                                           max_batch=128, max_q_len=1, max_kv_len=2048,
+                                           kv_stride_page=64 * 8 * 128, kv_stride_token=8 * 128,
+                                           kv_stride_head=128))
+    assert plan2.grid_ctas >= 1024
+    forced, _, _ = B.pda_plan(_params(chunk_pages=5))
+    assert forced.chunk_pages == 8                  # rounded up to whole tiles
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(num_qo_heads=15), B.PDA_ERR_INVALID),
+    (dict(head_dim=96), B.PDA_ERR_UNSUPPORTED),
+    (dict(page_size=24), B.PDA_ERR_UNSUPPORTED),
+    (dict(max_q_len=9), B.PDA_ERR_INVALID),
+    (dict(max_q_len=0), B.PDA_ERR_INVALID),
+    (dict(q_dtype=1), B.PDA_ERR_UNSUPPORTED),          # e4m3 Q needs e4m3 KV
+    (dict(scale_mode=1), B.PDA_ERR_UNSUPPORTED),       # bf16 KV takes no scales
+    (dict(kv_dtype=1, scale_mode=0, kv_stride_page=16 * 2 * 256 // 2 * 2), B.PDA_ERR_UNSUPPORTED),
+    (dict(kv_stride_head=260), B.PDA_ERR_ALIGNMENT),   # 520 B: not a multiple of 16
+    (dict(batch=17), B.PDA_ERR_INVALID),
+    (dict(max_kv_len=0), B.PDA_ERR_INVALID),
+])
+def test_plan_rejects(lib, bad, code):
+    _, _, rc = B.pda_plan(_params(**bad), check=False)
+    assert rc == code, (bad, rc, B.pda_strerror(rc))
+
+
+def test_decode_host_checks_return_before_any_launch(lib):
+    plan, _, _ = B.pda_plan(_params())
+    fake = 1 << 20  # 16-byte aligned non-null address; never dereferenced on these paths
+    args = dict(q=fake, k_pages=fake, v_pages=fake, page_table=fake, kv_indptr=fake,
+                kv_len=fake, qo_indptr=fake, max_q_len=4, window=None, sm_scale=0.1,
+                k_scale=None, v_scale=None, out=fake, lse=fake, split_scratch=fake, stream=0)
+
+    def call(**over):
+        a = dict(args)
+        a.update(over)
+        return B.pda_decode(plan, check=False, **a)
+
+    assert call(q=None) == B.PDA_ERR_NULL
+    assert call(split_scratch=None) == B.PDA_ERR_SCRATCH
+    assert call(split_scratch=fake + 16) == B.PDA_ERR_SCRATCH
+    assert call(max_q_len=0) == B.PDA_ERR_INVALID
+    assert call(max_q_len=9) == B.PDA_ERR_INVALID
+    assert call(k_pages=fake + 8) == B.PDA_ERR_ALIGNMENT
+    assert call(out=fake + 2) == B.PDA_ERR_ALIGNMENT
+    bad = B.PdaPlan()
+    assert B.pda_decode(bad, check=False, **args) == B.PDA_ERR_PLAN
+    fplan, _, _ = B.pda_plan(_params(kv_dtype=1, scale_mode=2, kv_stride_page=16 * 2 * 256,
+                                     kv_stride_token=512, kv_stride_head=256))
+    assert B.pda_decode(fplan, check=False, **args) == B.PDA_ERR_NULL  # scales missing
+
+
+def test_strerror(lib):
+    for code in range(0, -8, -1):
+        assert B.pda_strerror(code)
+    assert "unknown" in B.pda_strerror(-99)

@@ -159,12 +159,13 @@ def setup_call(wl, dev):
                       device=dev)
     lse = torch.empty(wl.total_rows, wl.num_qo_heads, dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
+    mq = max(1, wl.max_q_len)
     with torch.cuda.stream(stream):
-        dec.run(wl, out, lse, stream=stream)
+        dec.run(wl, out, lse, max_q_len=mq, stream=stream)
     stream.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
-        dec.run(wl, out, lse, stream=stream)
+        dec.run(wl, out, lse, max_q_len=mq, stream=stream)
     return dec, out, lse, stream, graph
 
 

@@ -76,8 +76,12 @@ class Workload:
 
     @property
     def max_q_len(self) -> int:
-        r = self.qo_indptr[1:] - self.qo_indptr[:-1]
-        return int(r.max().item()) if r.numel() else 0
+        """Largest rows-per-request (read from host-side metadata when the
+        offsets live on a device, so that it never synchronises a stream)."""
+        if self.qo_indptr.device.type == "cpu" or "rows" not in self.meta:
+            r = self.qo_indptr[1:] - self.qo_indptr[:-1]
+            return int(r.max().item()) if r.numel() else 0
+        return max(self.meta["rows"]) if self.meta["rows"] else 0
 
     @property
     def group(self) -> int:

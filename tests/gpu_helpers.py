@@ -54,14 +54,29 @@ def oracle_ref(wl, items=None, num_threads=0):
     return out, lse
 
 
-def assert_close(out, lse, ref_o, ref_l, tol, what=""):
+def bf16_half_ulp(x):
+    """Half the bf16 spacing at |x|: the rounding error of a bf16 output alone."""
+    x = np.maximum(np.abs(np.asarray(x, dtype=np.float64)), 2.0 ** -126)
+    return 0.5 * 2.0 ** (np.floor(np.log2(x)) - 7)
+
+
+def assert_close(out, lse, ref_o, ref_l, tol, what="", output_rounding=False):
+    """Element-wise comparison. ``output_rounding`` adds the bf16 output's own
+    half-ulp to the max bound: used only for the peaked stress cases (Q x 4,
+    not one of the stated workloads), where one key dominates and |o| can
+    exceed 2, so that the bf16 result alone is off by up to 2^-8 |o|."""
     out = np.asarray(out, dtype=np.float64)
     lse = np.asarray(lse, dtype=np.float64)
     assert np.all(np.isfinite(out)), f"{what}: non-finite output (stray read or unwritten row)"
     assert np.all(np.isfinite(lse)), f"{what}: non-finite lse"
     err = np.abs(out - ref_o)
     lerr = np.abs(lse - ref_l)
-    assert err.max() <= tol["max"], f"{what}: max |err| {err.max():.3e} > {tol['max']}"
+    if output_rounding:
+        excess = err - bf16_half_ulp(ref_o)
+        assert excess.max() <= tol["max"], \
+            f"{what}: max |err| - half ulp {excess.max():.3e} > {tol['max']}"
+    else:
+        assert err.max() <= tol["max"], f"{what}: max |err| {err.max():.3e} > {tol['max']}"
     assert err.mean() <= tol["mean"], f"{what}: mean |err| {err.mean():.3e} > {tol['mean']}"
     assert lerr.max() <= tol["lse"], f"{what}: lse |err| {lerr.max():.3e} > {tol['lse']}"
     return float(err.max()), float(err.mean()), float(lerr.max())

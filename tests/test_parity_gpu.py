@@ -59,9 +59,10 @@ SMALL = {
                       head_dim=128, page_size=256, windows=[100, 0]),
     "bf16_p1": dict(batch=2, rows=2, kv_lens=[130, 3], num_qo_heads=4, num_kv_heads=2,
                     head_dim=64, page_size=1, chunk=64),
-    "bf16_peaked": dict(batch=2, rows=[4, 8], kv_lens=[2000, 900], num_qo_heads=16,
-                        num_kv_heads=2, head_dim=256, page_size=16, q_mult=4.0, chunk=16),
 }
+# peaked stress case (Q x 4): compared with the bf16 output's half-ulp added
+PEAKED_SMALL = dict(batch=2, rows=[4, 8], kv_lens=[2000, 900], num_qo_heads=16, num_kv_heads=2,
+                    head_dim=256, page_size=16, q_mult=4.0, chunk=16)
 
 
 def _make(name, args, seed=0):
@@ -78,6 +79,14 @@ def test_small_full_parity(name):
     assert status == 0
     ref_o, ref_l = oracle_ref(wl)
     assert_close(out, lse, ref_o, ref_l, tol_for(wl), what=name)
+
+
+def test_small_peaked_parity():
+    wl, chunk = _make("bf16_peaked", PEAKED_SMALL)
+    out, lse, status, dec = run_decode(wl, chunk_pages=chunk)
+    assert status == 0
+    ref_o, ref_l = oracle_ref(wl)
+    assert_close(out, lse, ref_o, ref_l, TOL_BF16, what="peaked", output_rounding=True)
 
 
 @pytest.mark.parametrize("chunk", [4, 16, 64, 0])
@@ -123,7 +132,7 @@ def test_config_parity(cfg, kw, n_sample, peaked):
     assert torch.isfinite(out).all() and torch.isfinite(lse).all()
     if n_sample is None:
         ref_o, ref_l = oracle_ref(wl)
-        assert_close(out, lse, ref_o, ref_l, tol_for(wl), what=cfg)
+        assert_close(out, lse, ref_o, ref_l, tol_for(wl), what=cfg, output_rounding=peaked)
     else:
         must = []
         if wl.window is not None:
@@ -134,7 +143,8 @@ def test_config_parity(cfg, kw, n_sample, peaked):
         hq = wl.num_qo_heads
         o = out.reshape(-1, wl.head_dim)[items]
         l_ = lse.reshape(-1)[items]
-        assert_close(o, l_, ref_o, ref_l, tol_for(wl), what=f"{cfg} sampled")
+        assert_close(o, l_, ref_o, ref_l, tol_for(wl), what=f"{cfg} sampled",
+                     output_rounding=peaked)
 
 
 # ------------------------------------------------ bit-exact gather and masks
@@ -154,9 +164,10 @@ def _index_code(L, H, D):
 @pytest.mark.parametrize("chunk", [0, 4])
 def test_causal_upper_bound_bit_exact(kind, chunk):
     """K channel 0 is 0 for old tokens and t+1 for the t-th new token; Q
-    channel 0 is 64, sm_scale 1. Row i's own token then outweighs every other
-    visible key by e^-64, so its output must be v_{p_i} bit for bit; a leaked
-    future key would outweigh it and show a different token's code."""
+    channel 0 is 128, sm_scale 1. Row i's own token then outweighs every other
+    visible key by e^-128 (below the smallest fp32), so its output must be
+    v_{p_i} bit for bit; a leaked future key would outweigh it and show a
+    different token's code."""
     R_list, L_list = [8, 1, 5, 3], [700, 90, 64, 5]
     H, G, D, P = 2, 4, 128, 16
 
@@ -171,7 +182,7 @@ def test_causal_upper_bound_bit_exact(kind, chunk):
     def value_fn(which, shape, gen):
         x = torch.zeros(shape)
         if which == "q":
-            x[..., 0] = 64.0
+            x[..., 0] = 128.0
         return x
 
     kv, qd, sm = {"bf16": ("bf16", "bf16", SCALE_NONE), "fp8_tensor": ("e4m3", "bf16", SCALE_TENSOR),
@@ -190,16 +201,17 @@ def test_causal_upper_bound_bit_exact(kind, chunk):
             pos = L - R + i
             for h in range(H * G):
                 assert torch.equal(out[r0 + i, h], code[pos, h // G]), (b, i, h)
-                assert math.isclose(float(lse[r0 + i, h]), 64.0 * (i + 1), rel_tol=1e-5)
+                assert math.isclose(float(lse[r0 + i, h]), 128.0 * (i + 1), rel_tol=1e-5)
         r0 += R
 
 
 @pytest.mark.parametrize("kind", ["bf16", "fp8_pth"])
 def test_window_lower_bound_bit_exact(kind):
     """K channel 0 falls by one per token (bf16: 256 - j; per-token-head
-    E4M3: code 1 with scale 256 - j), Q channel 0 is 64: the earliest visible
-    key of each row dominates, and the key just below the window would
-    dominate it if it were admitted. Output must be v at p_i - W + 1."""
+    E4M3: code 1 with scale 256 - j), Q channel 0 is 128: the earliest visible
+    key of each row outweighs the next by e^-128 (below the smallest fp32),
+    and the key just below the window would dominate it if it were admitted.
+    Output must be v at p_i - W + 1 bit for bit."""
     R_list, L_list, W_list = [8, 4, 2, 1], [200, 70, 33, 129], [1, 5, 64, 17]
     H, G, D, P = 2, 3, 64, 16
 
@@ -219,7 +231,7 @@ def test_window_lower_bound_bit_exact(kind):
     def value_fn(which, shape, gen):
         x = torch.zeros(shape)
         if which == "q":
-            x[..., 0] = 64.0
+            x[..., 0] = 128.0
         return x
 
     kv, sm = ("bf16", SCALE_NONE) if kind == "bf16" else ("e4m3", SCALE_TOKEN_HEAD)

@@ -51,11 +51,15 @@ def peaks():
     return 6800.0, "fallback"
 
 
-def source_sha() -> str:
-    """Hash of the CUDA sources: ncu traffic figures apply only to this code."""
+KERNEL_SOURCES = {"stage1": ("pda_mma.cu", "pda_internal.h")}
+
+
+def source_sha(kernel: str = "stage1") -> str:
+    """Hash of the sources a kernel is built from: ncu traffic figures apply
+    only to that code."""
     h = hashlib.sha256()
     cs = os.path.join(ROOT, "paged_split_kv_03_gb300", "csrc")
-    for f in sorted(os.listdir(cs)):
+    for f in KERNEL_SOURCES[kernel]:
         h.update(f.encode())
         h.update(open(os.path.join(cs, f), "rb").read())
     return h.hexdigest()[:12]
@@ -67,7 +71,7 @@ def recorded_traffic(kernel: str, workload: str):
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    sha = source_sha()
+    sha = source_sha(kernel)
     for line in open(path):
         m = re.match(r"\s*(\S+)\s+(\S+)\s+(\S+)\s+(\d+)", line)
         if m and m.group(1) == kernel and m.group(2) == workload and m.group(3) == sha:

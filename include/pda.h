@@ -67,6 +67,10 @@ enum { PDA_KERNEL_AUTO = 0, PDA_KERNEL_MMA = 1, PDA_KERNEL_TC = 2 };
 #define PDA_ERR_SCRATCH (-5)     /* split_scratch NULL or not 256-byte aligned */
 #define PDA_ERR_CUDA (-6)        /* a CUDA runtime call failed (launch, device query) */
 #define PDA_ERR_PLAN (-7)        /* plan not produced by pda_plan, or from another version */
+#define PDA_ERR_TOO_LARGE (-8)   /* plan needs more scratch than pda_decode_static's array */
+
+/* Size of the library's own split-scratch array used by pda_decode_static. */
+#define PDA_STATIC_SCRATCH_BYTES (32u << 20)
 
 /* Device status bits (sticky in the scratch header until pda_reset_status). */
 #define PDA_STATUS_KV_LEN_LT_ROWS 0x1u  /* kv_len[b] < rows of request b */
@@ -158,6 +162,27 @@ int pda_decode(const pda_plan_t* plan, const void* q, const void* k_pages, const
                const int32_t* qo_indptr, int32_t max_q_len, const int32_t* window,
                float sm_scale, const float* k_scale, const float* v_scale, void* out,
                float* lse, void* split_scratch, pda_stream_t stream);
+
+/* pda_decode without a caller-provided split_scratch (the pages have no
+ * counterpart: this serves callers that cannot allocate device memory, such
+ * as a plugin whose host framework owns every allocation and hands it only
+ * input and output pointers, or code that must not call cudaMalloc under its
+ * host's memory budget). The split scratch lives in a fixed
+ * PDA_STATIC_SCRATCH_BYTES array of the library's own device memory, which
+ * every GPU that loads the library holds until the process exits. Arguments
+ * are those of pda_decode minus split_scratch. Returns PDA_ERR_TOO_LARGE
+ * when plan->scratch_bytes exceeds the array. Allocates nothing. All calls
+ * share the array and it keeps the last call's contents; each call first
+ * clears the status word (an async memset on `stream`). Calls whose GPU
+ * work overlaps race on the array: serialise them (one stream). The first
+ * call on a device looks up the array's address with that device current;
+ * make it before any stream capture. The status bits are not readable by the
+ * caller through this entry point. */
+int pda_decode_static(const pda_plan_t* plan, const void* q, const void* k_pages,
+                      const void* v_pages, const int32_t* page_table, const int32_t* kv_indptr,
+                      const int32_t* kv_len, const int32_t* qo_indptr, int32_t max_q_len,
+                      const int32_t* window, float sm_scale, const float* k_scale,
+                      const float* v_scale, void* out, float* lse, pda_stream_t stream);
 
 /* Copy the device status word of `split_scratch` to *host_bits. Synchronises
  * `stream`. */

@@ -21,6 +21,8 @@ PDA_KERNEL_AUTO, PDA_KERNEL_MMA, PDA_KERNEL_TC = 0, 1, 2
 PDA_OK = 0
 PDA_ERR_NULL, PDA_ERR_INVALID, PDA_ERR_UNSUPPORTED = -1, -2, -3
 PDA_ERR_ALIGNMENT, PDA_ERR_SCRATCH, PDA_ERR_CUDA, PDA_ERR_PLAN = -4, -5, -6, -7
+PDA_ERR_TOO_LARGE = -8
+PDA_STATIC_SCRATCH_BYTES = 32 << 20
 PDA_STATUS_KV_LEN_LT_ROWS = 0x1
 PDA_STATUS_ROWS_GT_MAX = 0x2
 PDA_STATUS_KV_LEN_GT_MAX = 0x4
@@ -29,7 +31,7 @@ PDA_STATUS_ROWS_GT_CAP = 0x10
 PDA_PLAN_MAGIC = 0x50444131
 
 EXPORTED = ("pda_plan", "pda_decode", "pda_get_status", "pda_reset_status", "pda_strerror",
-            "pda_version", "pda_struct_sizes")
+            "pda_version", "pda_struct_sizes", "pda_decode_static")
 
 _i32, _i64, _u32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_void_p
 
@@ -83,6 +85,9 @@ def load_library(path: Optional[str] = None):
     lib.pda_decode.argtypes = [ctypes.POINTER(PdaPlan), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                _i32, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.pda_decode.restype = ctypes.c_int
+    lib.pda_decode_static.argtypes = [ctypes.POINTER(PdaPlan), _vp, _vp, _vp, _vp, _vp, _vp,
+                                      _vp, _i32, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp]
+    lib.pda_decode_static.restype = ctypes.c_int
     lib.pda_get_status.argtypes = [ctypes.POINTER(PdaPlan), _vp, ctypes.POINTER(_u32), _vp]
     lib.pda_get_status.restype = ctypes.c_int
     lib.pda_reset_status.argtypes = [ctypes.POINTER(PdaPlan), _vp, _vp]
@@ -139,6 +144,21 @@ def pda_decode(plan: PdaPlan, q, k_pages, v_pages, page_table, kv_indptr, kv_len
         _stream(stream))
     if check and rc != PDA_OK:
         raise PdaError(rc, "pda_decode")
+    return rc
+
+
+def pda_decode_static(plan: PdaPlan, q, k_pages, v_pages, page_table, kv_indptr, kv_len,
+                      qo_indptr, max_q_len: int, window, sm_scale: float, k_scale, v_scale, out,
+                      lse, stream=None, check: bool = True) -> int:
+    """pda_decode for callers that cannot allocate device memory: the split
+    scratch is the library's own fixed array (PDA_STATIC_SCRATCH_BYTES), so
+    nothing is allocated. Calls share that array: do not overlap them."""
+    rc = load_library().pda_decode_static(
+        ctypes.byref(plan), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+        _ptr(kv_indptr), _ptr(kv_len), _ptr(qo_indptr), int(max_q_len), _ptr(window),
+        float(sm_scale), _ptr(k_scale), _ptr(v_scale), _ptr(out), _ptr(lse), _stream(stream))
+    if check and rc != PDA_OK:
+        raise PdaError(rc, "pda_decode_static")
     return rc
 
 

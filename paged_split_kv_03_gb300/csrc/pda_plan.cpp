@@ -43,6 +43,8 @@ extern "C" const char* pda_strerror(int code) {
     case PDA_ERR_SCRATCH: return "split_scratch is NULL or not 256-byte aligned";
     case PDA_ERR_CUDA: return "a CUDA runtime call failed";
     case PDA_ERR_PLAN: return "plan was not produced by pda_plan of this library version";
+    case PDA_ERR_TOO_LARGE:
+      return "plan needs more split scratch than pda_decode_static's built-in array holds";
     default: return "unknown pda error code";
   }
 }

@@ -78,6 +78,7 @@ enum { PDA_KERNEL_AUTO = 0, PDA_KERNEL_MMA = 1, PDA_KERNEL_TC = 2 };
 #define PDA_STATUS_KV_LEN_GT_MAX 0x4u   /* kv_len[b] > plan max_kv_len */
 #define PDA_STATUS_PAGE_OOB 0x8u        /* a page id read from page_table outside [0, num_pages) */
 #define PDA_STATUS_ROWS_GT_CAP 0x10u    /* qo_indptr[batch] > max_batch * max_q_len */
+#define PDA_STATUS_WAIT_TIMEOUT 0x20u   /* a pipeline wait ran past its bound; the CTA gave up */
 
 /* Everything the planner needs; plain values, no device pointers. */
 typedef struct {

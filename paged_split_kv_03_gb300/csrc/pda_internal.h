@@ -4,6 +4,8 @@
 
 #include <stdint.h>
 
+#include <cuda_runtime.h>
+
 #include "pda.h"
 
 #ifdef __CUDACC__
@@ -17,7 +19,7 @@ namespace pda {
 constexpr int kStatusHeaderBytes = 256;  // status word + padding at the start of split_scratch
 constexpr int kMaxQLen = 8;              // rows per request ("up to 8 query rows")
 constexpr int kMmaRowsPerCta = 64;       // mma.sync path: 4 warps x m16 tiles
-constexpr int kTcRowsPerCta = 128;       // tcgen05 path: N of the swapped QK^T MMA
+constexpr int kTcRowsPerCta = 64;        // tcgen05 path: N of the swapped QK^T MMA
 
 // Arguments of both stage-1 variants and of stage 2 (passed by value).
 struct DecodeArgs {
@@ -42,6 +44,7 @@ struct DecodeArgs {
   int max_q_len, max_kv_len, max_splits, head_blocks, chunk_pages;
   int64_t rows_cap;
   int hpc[kMaxQLen + 1];  // q heads per CTA for R rows
+  int tma_slot_dim;       // tcgen05 path: tensor-map coordinate holding the slot (1 or 2)
 };
 
 // The KV range one (request, split) covers. Every kernel derives it from the
@@ -65,9 +68,14 @@ PDA_HD SplitRange split_range(int32_t L, int32_t R, int32_t W, int32_t P, int32_
   return s;
 }
 
-// Resolved launch choices (filled by the planner, read by the launcher).
-int launch_decode(const pda_plan_t* plan, const DecodeArgs& args, pda_stream_t stream);
-int stage1_smem_bytes(const pda_plan_t* plan);
-int stage1_ctas_per_sm(const pda_plan_t* plan);
+// Launchers and resource queries of the two stage-1 variants and stage 2.
+int mma_smem_bytes(const pda_plan_t* plan);
+int mma_ctas_per_sm(const pda_plan_t* plan);
+int launch_stage1_mma(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_t s);
+bool tc_supported(const pda_plan_t* plan);
+int tc_smem_bytes(const pda_plan_t* plan);
+int tc_ctas_per_sm(const pda_plan_t* plan);
+int launch_stage1_tc(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_t s);
+int launch_stage2(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_t s);
 
 }  // namespace pda

@@ -641,7 +641,7 @@ KernelFn stage2_for(const pda_plan_t* p) {
 
 }  // namespace
 
-int stage1_smem_bytes(const pda_plan_t* p) {
+int mma_smem_bytes(const pda_plan_t* p) {
   switch (p->head_dim) {
     case 64: return smem_of<64>(p->kv_dtype, p->q_dtype, p->scale_mode);
     case 128: return smem_of<128>(p->kv_dtype, p->q_dtype, p->scale_mode);
@@ -649,16 +649,15 @@ int stage1_smem_bytes(const pda_plan_t* p) {
   }
 }
 
-int stage1_ctas_per_sm(const pda_plan_t* p) {
+int mma_ctas_per_sm(const pda_plan_t* p) {
   // 228 KB of shared memory per SM, 1 KB reserved per CTA; the kernel is
   // built for at most 255 registers x 128 threads, so shared memory decides.
-  const int per = stage1_smem_bytes(p) + 1024;
+  const int per = mma_smem_bytes(p) + 1024;
   int n = (228 * 1024) / per;
   return n < 1 ? 1 : (n > 4 ? 4 : n);
 }
 
-int launch_decode(const pda_plan_t* plan, const DecodeArgs& args, pda_stream_t stream) {
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+int launch_stage1_mma(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_t s) {
   KernelFn k1 = stage1_for(plan);
   const int smem = plan->stage1_smem_bytes;
   if (cudaFuncSetAttribute(reinterpret_cast<const void*>(k1),
@@ -675,22 +674,24 @@ int launch_decode(const pda_plan_t* plan, const DecodeArgs& args, pda_stream_t s
     cudaGetLastError();
     return PDA_ERR_CUDA;
   }
-  if (plan->max_splits > 1) {
-    const int64_t items = (int64_t)plan->batch * args.max_q_len * plan->num_qo_heads;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t c2 = {};
-    c2.gridDim = dim3(static_cast<unsigned>((items + 3) / 4));
-    c2.blockDim = dim3(128);
-    c2.dynamicSmemBytes = 0;
-    c2.stream = s;
-    c2.attrs = attr;
-    c2.numAttrs = 1;
-    if (cudaLaunchKernelEx(&c2, stage2_for(plan), args) != cudaSuccess) {
-      cudaGetLastError();
-      return PDA_ERR_CUDA;
-    }
+  return PDA_OK;
+}
+
+int launch_stage2(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_t s) {
+  const int64_t items = (int64_t)plan->batch * args.max_q_len * plan->num_qo_heads;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t c2 = {};
+  c2.gridDim = dim3(static_cast<unsigned>((items + 3) / 4));
+  c2.blockDim = dim3(128);
+  c2.dynamicSmemBytes = 0;
+  c2.stream = s;
+  c2.attrs = attr;
+  c2.numAttrs = 1;
+  if (cudaLaunchKernelEx(&c2, stage2_for(plan), args) != cudaSuccess) {
+    cudaGetLastError();
+    return PDA_ERR_CUDA;
   }
   return PDA_OK;
 }

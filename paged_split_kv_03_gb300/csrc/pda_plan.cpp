@@ -106,9 +106,10 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
   pl.kv_stride_head = p->kv_stride_head;
   pl.group = p->num_qo_heads / p->num_kv_heads;
   pl.num_sms = num_sms;
+  if (p->kernel == PDA_KERNEL_TC && !pda::tc_supported(&pl)) return PDA_ERR_UNSUPPORTED;
+  // AUTO stays on the mma.sync path until the tcgen05 path is the validated default
   pl.kernel = p->kernel == PDA_KERNEL_AUTO ? PDA_KERNEL_MMA : p->kernel;
-  if (pl.kernel == PDA_KERNEL_TC) return PDA_ERR_UNSUPPORTED;  // not built yet
-  pl.rows_per_cta = pda::kMmaRowsPerCta;
+  pl.rows_per_cta = pl.kernel == PDA_KERNEL_TC ? pda::kTcRowsPerCta : pda::kMmaRowsPerCta;
 
   // Query heads per CTA for a request with R rows: the largest divisor of the
   // GQA group whose R x heads tile fits the CTA's rows.
@@ -133,8 +134,9 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
 
   // Split planning. A chunk is a whole number of 64-token tiles when pages
   // are smaller than a tile, so that only a request's last chunk is ragged.
-  pl.stage1_smem_bytes = pda::stage1_smem_bytes(&pl);
-  const int per_sm = std::max(1, pda::stage1_ctas_per_sm(&pl));
+  const bool tc = pl.kernel == PDA_KERNEL_TC;
+  pl.stage1_smem_bytes = tc ? pda::tc_smem_bytes(&pl) : pda::mma_smem_bytes(&pl);
+  const int per_sm = std::max(1, tc ? pda::tc_ctas_per_sm(&pl) : pda::mma_ctas_per_sm(&pl));
   const int64_t slots = (int64_t)num_sms * per_sm;
   const int64_t units = (int64_t)pl.batch * pl.num_kv_heads * pl.head_blocks;
   const int64_t tile_pages = std::max<int64_t>(1, 64 / p->page_size);
@@ -229,7 +231,11 @@ extern "C" int pda_decode(const pda_plan_t* plan, const void* q, const void* k_p
   a.chunk_pages = plan->chunk_pages;
   a.rows_cap = plan->rows_cap;
   for (int r = 0; r <= pda::kMaxQLen; ++r) a.hpc[r] = plan->heads_per_cta[r];
-  return pda::launch_decode(plan, a, stream);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int rc = plan->kernel == PDA_KERNEL_TC ? pda::launch_stage1_tc(plan, a, s)
+                                         : pda::launch_stage1_mma(plan, a, s);
+  if (rc == PDA_OK && plan->max_splits > 1) rc = pda::launch_stage2(plan, a, s);
+  return rc;
 }
 
 extern "C" int pda_get_status(const pda_plan_t* plan, const void* split_scratch,

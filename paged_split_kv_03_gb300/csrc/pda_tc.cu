@@ -1,0 +1,960 @@
+// pda_tc.cu -- stage 1 on the 5th-generation tensor cores (tcgen05, TMEM)
+// with TMA page gathers, for sm_103a.
+//
+// Method: "perf(attention): run up to 8 query rows per request in the triton
+// decode kernel" (FreeToken PR #900), "Changes" -- one CTA per (request,
+// kv head, head block, KV chunk); the request's R query rows x q heads share
+// every K/V byte; each row is masked at its own position and window; the
+// chunk's partial (o, lse) goes to stage 2. The orientation is the swap-AB of
+// "[Feature Request] Support q_len > 1 for FP8 decode" (hpc-ops issue #4):
+// S^T = K Q^T puts 128 KV tokens on the MMA M axis and the R x heads rows
+// (16..64) on N, so a decode tile fills the MMA. PV is O^T += V^T P^T with
+// head_dim on M. FP8 dequantisation folds into the logit scale and the
+// finalize ("Naive Support for Hopper FP8 Prefill Kernel with Per-Head
+// Quantization", item 3).
+//
+// Operands keep the cache's own type: bf16 caches run kind::f16 (bf16) MMAs;
+// OCP E4M3 caches run kind::f8f6f4 MMAs on the codes as they sit in shared
+// memory (no widening pass). For E4M3 the other operand is written as E4M3
+// terms: P = P1 + P2 (P2 the E4M3 residual of P1, about 8 significant bits
+// together), and a bf16 query as Q * 2^a = Q1 + Q2/16 + Q3/256 (stacked on N,
+// exact to ~2^-12 of the row's largest element). V is read MN-major straight
+// from its [token][d] tile, so no transpose is needed on this hardware. The
+// softmax denominator always sums the exact fp32 probabilities.
+//
+// Warp roles (192 threads): warp 0 issues the TMA page gathers (one 128-byte
+// swizzled box per page and 128-byte column of the head) into a ring of 16 KB
+// slots and owns the TMEM allocation; warp 1 issues the MMAs from one thread;
+// warps 2..5 run the online softmax out of TMEM (thread = token row of S^T),
+// write P to shared memory and finish the output (thread = head_dim row of
+// O^T). All hand-offs are mbarriers; every wait is bounded and a timeout sets
+// PDA_STATUS_WAIT_TIMEOUT and unwinds without hanging.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "pda_internal.h"
+
+namespace pda {
+namespace {
+
+constexpr int kTcThreads = 192;
+constexpr int kTok = 128;          // KV tokens per tile (MMA M of S^T)
+constexpr int kSlot = 16384;       // ring slot: [128 tokens x 128 bytes]
+constexpr int kNmax = 64;          // rows x q heads per CTA
+constexpr float kTh = 8.0f;        // lazy rescale threshold, log2 units (P <= 2^8)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr uint32_t kSpinLimit = 1u << 24;
+
+// ------------------------------------------------------------------ helpers
+__device__ __forceinline__ uint32_t su32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Byte offset of byte `b` (< 128) of row `r` inside a 128-byte-swizzled atom
+// (rows of 128 B, 16-byte chunks XORed with the row's low 3 bits).
+__device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t b) {
+  return r * 128u + ((((b >> 4) ^ r) & 7u) << 4) + (b & 15u);
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 family format).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor: f32 accumulate, A/B format `fmt` (kind::f16: 1 =
+// bf16; kind::f8f6f4: 0 = E4M3), A MN-major if `a_mn`, M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc(uint32_t fmt, uint32_t a_mn, uint32_t n) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | (a_mn << 15) | ((n >> 3) << 17) |
+         ((128u >> 4) << 24);
+}
+
+template <bool kF8>
+__device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  if constexpr (kF8)
+    asm volatile("{ .reg .pred p; setp.ne.b32 p, %4, 0;"
+                 " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p; }" ::"r"(d),
+                 "l"(a), "l"(b), "r"(id), "r"(acc));
+  else
+    asm volatile("{ .reg .pred p; setp.ne.b32 p, %4, 0;"
+                 " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d), "l"(a),
+                 "l"(b), "r"(id), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   su32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void bar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ void bar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint64_t* b, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(done)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Bounded wait: false if another role aborted or the limit ran out (which
+// records PDA_STATUS_WAIT_TIMEOUT and aborts the CTA).
+__device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag,
+                                         uint32_t* status) {
+  for (uint32_t it = 0;; ++it) {
+    if (bar_try(b, parity)) return true;
+    if ((it & 255u) == 255u) {
+      if (*abort_flag) return false;
+      if (it > kSpinLimit) {
+        *abort_flag = 1;
+        atomicOr(status, PDA_STATUS_WAIT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// 4-D tiled TMA load of one box into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                         int c2, int c3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(su32(bar))
+      : "memory");
+}
+
+// Two floats -> two E4M3 codes (RNE, saturating): low byte from `lo`.
+__device__ __forceinline__ uint16_t f2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two E4M3 codes -> two floats (exact): .x from the low byte.
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint16_t c) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(c));
+  return __half22float2(*reinterpret_cast<__half2*>(&h));
+}
+
+// Barrier of the 128 softmax threads (named barrier 1) that also ORs a predicate.
+__device__ __forceinline__ bool group_or(bool pred) {
+  uint32_t in = pred ? 1u : 0u, out;
+  asm volatile(
+      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; barrier.red.or.pred q, 1, 128, p; selp.u32 %0, 1, "
+      "0, q; }"
+      : "=r"(out)
+      : "r"(in)
+      : "memory");
+  return out != 0;
+}
+__device__ __forceinline__ void group_sync() { asm volatile("barrier.sync 1, 128;" ::: "memory"); }
+
+// ------------------------------------------------------------ configuration
+template <int D, int KVT, int QT, int SMODE>
+struct TcCfg {
+  static constexpr bool kF8 = KVT == PDA_E4M3;
+  static constexpr bool kQSplit = kF8 && QT == PDA_BF16;  // bf16 query as three E4M3 terms
+  static constexpr int kQTerms = kQSplit ? 3 : 1;
+  static constexpr int kElt = kF8 ? 1 : 2;
+  static constexpr int kAtom = 128 / kElt;           // elements per 128-byte row
+  static constexpr int kChunks = D / kAtom;          // ring slots per K (or V) tile
+  static constexpr int kTileSlots = 2 * kChunks;
+  static constexpr int kQRows = kNmax * kQTerms;
+  static constexpr int kQAtomBytes = kQRows * 128;
+  static constexpr int kQBytes = kChunks * kQAtomBytes;
+  static constexpr int kPAtomBytes = kNmax * 128;    // [64 rows x 128 B]
+  static constexpr int kPBytes = 2 * kPAtomBytes;    // bf16: 2 token halves; E4M3: 2 terms
+  static constexpr int kOBlocks = D / 128;
+  static constexpr int kSCols = kQRows;              // TMEM columns per S buffer
+  static constexpr int kTmemNeed = 2 * kSCols + kOBlocks * kNmax;
+  static constexpr int kTmemCols =
+      kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
+  static_assert(kTmemNeed <= 512, "TMEM budget");
+  static constexpr int kSmallBytes = 4096;
+  static constexpr int kAvail = 227 * 1024 - 1024 - kQBytes - kPBytes - kSmallBytes;
+  static constexpr int kRingRaw = kAvail / kSlot > 12 ? 12 : kAvail / kSlot;
+  // bf16 V blocks span two adjacent slots: keep the ring even so pairs never wrap
+  static constexpr int kRing = kF8 ? kRingRaw : (kRingRaw & ~1);
+  static_assert(kRing >= kTileSlots, "ring must hold one tile");
+  static constexpr int kSmem = 1024 + kQBytes + kPBytes + kRing * kSlot + kSmallBytes;
+};
+
+// ---------------------------------------------------------------- the kernel
+template <int D, int KVT, int QT, int SMODE>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    stage1_tc(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
+              const __grid_constant__ CUtensorMap tmv) {
+  using C = TcCfg<D, KVT, QT, SMODE>;
+  constexpr bool kF8 = C::kF8;
+  constexpr int R_ = C::kRing;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* q_s = smem;
+  uint8_t* p_s = q_s + C::kQBytes;
+  uint8_t* ring = p_s + C::kPBytes;
+  uint8_t* small = ring + R_ * kSlot;
+  uint64_t* full = reinterpret_cast<uint64_t*>(small);
+  uint64_t* empty = full + R_;
+  uint64_t* s_full = empty + R_;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* p_full = s_free + 2;
+  uint64_t* pv_done = p_full + 1;
+  uint64_t* q_ready = pv_done + 1;
+  uint64_t* drain = q_ready + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* m_used = reinterpret_cast<float*>(small + 512);
+  float* alpha = m_used + kNmax;
+  float* colscale = alpha + kNmax;
+  float* red = colscale + kNmax;  // [4][kNmax]
+  float* linv = red + 4 * kNmax;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- which work item (uniform per CTA; exits before any barrier)
+  int64_t bid = blockIdx.x;
+  const int hb = static_cast<int>(bid % a.head_blocks);
+  bid /= a.head_blocks;
+  const int split = static_cast<int>(bid % a.max_splits);
+  bid /= a.max_splits;
+  const int hkv = static_cast<int>(bid % a.hkv);
+  const int b = static_cast<int>(bid / a.hkv);
+  if (b >= a.batch) return;
+  const int q0 = a.qo_indptr[b];
+  const int R = a.qo_indptr[b + 1] - q0;
+  const int L = a.kv_len[b];
+  if (R <= 0 || R > a.max_q_len || L < R || L > a.max_kv_len || q0 + R > a.rows_cap) {
+    if (tid == 0 && split == 0 && hb == 0 && hkv == 0) {
+      uint32_t bits = 0;
+      if (R < 0 || R > a.max_q_len) bits |= PDA_STATUS_ROWS_GT_MAX;
+      else if (R > 0 && L < R) bits |= PDA_STATUS_KV_LEN_LT_ROWS;
+      else if (R > 0 && L > a.max_kv_len) bits |= PDA_STATUS_KV_LEN_GT_MAX;
+      else if (R > 0 && q0 + R > a.rows_cap) bits |= PDA_STATUS_ROWS_GT_CAP;
+      if (bits) atomicOr(a.status, bits);
+    }
+    return;
+  }
+  const int hpc = a.hpc[R];
+  if (hb >= a.group / hpc) return;
+  const int W = a.window ? a.window[b] : 0;
+  const int P = a.page_size;
+  const SplitRange sr = split_range(L, R, W, P, a.chunk_pages);
+  if (split >= sr.num_splits) return;
+  const int page_begin = sr.lo_page + split * a.chunk_pages;
+  const int page_end = min(page_begin + a.chunk_pages, sr.num_pages);
+  const int t_begin = page_begin * P;
+  const int t_end = min(page_end * P, L);
+  const int ntiles = (t_end - t_begin + kTok - 1) / kTok;
+  const int M = R * hpc;
+  const int N = (M + 15) & ~15;   // MMA N of PV (and of each Q term)
+  const int Nq = N * C::kQTerms;  // MMA N of S^T
+  const int head0 = hkv * a.group + hb * hpc;
+  const int32_t* ptab = a.page_table + a.kv_indptr[b];
+
+  // ---- setup: barriers, TMEM, running maxima
+  if (tid == 0) {
+    for (int s = 0; s < R_; ++s) {
+      bar_init(full + s, 1);
+      bar_init(empty + s, 1);
+    }
+    bar_init(s_full, 1);
+    bar_init(s_full + 1, 1);
+    bar_init(s_free, 128);
+    bar_init(s_free + 1, 128);
+    bar_init(p_full, 128);
+    bar_init(pv_done, 1);
+    bar_init(q_ready, 128);
+    bar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (tid < kNmax) {
+    m_used[tid] = -INFINITY;
+    colscale[tid] = 1.f;
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     su32(tmem_slot)),
+                 "r"(C::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem_o = tmem + 2 * C::kSCols;
+
+  if (warp == 0) {
+    // ================================================= TMA producer warp
+    const int box_rows = P < kTok ? P : kTok;
+    const int nbox = kTok / box_rows;  // <= 16 (P >= 8)
+    const uint32_t box_bytes = static_cast<uint32_t>(box_rows) * 128u;
+    const CUtensorMap* maps[2] = {&tmk, &tmv};
+    auto page_of = [&](int j, int& page, int& slot0) -> bool {
+      const int tb = t_begin + j * kTok + lane * box_rows;
+      if (lane >= nbox || tb >= t_end) return false;
+      page = __ldg(ptab + tb / P);
+      slot0 = tb % P;
+      if (page < 0 || page >= a.num_pages) {
+        atomicOr(a.status, PDA_STATUS_PAGE_OOB);
+        return false;
+      }
+      return true;
+    };
+    int pg = 0, s0 = 0, pg_n = 0, s0_n = 0;
+    bool ok = page_of(0, pg, s0), ok_n = false;
+    uint32_t g = 0;
+    bool alive = true;
+    for (int j = 0; j < ntiles && alive; ++j) {
+      if (j + 1 < ntiles) ok_n = page_of(j + 1, pg_n, s0_n);
+      const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, ok));
+      for (int kind = 0; kind < 2 && alive; ++kind) {
+        for (int c = 0; c < C::kChunks; ++c, ++g) {
+          const uint32_t slot = g % R_, round = g / R_;
+          int good = 1;
+          if (lane == 0) {
+            good = bar_wait(empty + slot, (round & 1u) ^ 1u, abort_flag, a.status);
+            if (good) bar_expect_tx(full + slot, nvalid * box_bytes);
+          }
+          good = __shfl_sync(0xffffffffu, good, 0);
+          if (!good) {
+            alive = false;
+            break;
+          }
+          if (ok) {
+            const uint32_t dst = su32(ring + slot * kSlot) + lane * box_bytes;
+            const int c1 = a.tma_slot_dim == 1 ? s0 : hkv;
+            const int c2 = a.tma_slot_dim == 1 ? hkv : s0;
+            tma_load(dst, maps[kind], c * C::kAtom, c1, c2, pg, full + slot);
+          }
+        }
+      }
+      pg = pg_n;
+      s0 = s0_n;
+      ok = ok_n;
+    }
+    // drain: every box issued must have landed before the CTA can exit
+    if (lane == 0) {
+      const uint32_t first = g > (uint32_t)R_ ? g - R_ : 0u;
+      for (uint32_t h = first; h < g; ++h) {
+        for (uint32_t it = 0; it < kSpinLimit && !bar_try(full + h % R_, (h / R_) & 1u); ++it) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ===================================================== MMA issuer warp
+    if (lane == 0) {
+      bool alive = bar_wait(q_ready, 0, abort_flag, a.status);
+      fence_after();
+      const uint32_t fmt = kF8 ? 0u : 1u;
+      const uint32_t id_s = idesc(fmt, 0, static_cast<uint32_t>(Nq));
+      const uint32_t id_p = idesc(fmt, 1, static_cast<uint32_t>(N));
+      const uint32_t q_addr = su32(q_s), p_addr = su32(p_s), ring_addr = su32(ring);
+      for (int j = 0; j <= ntiles && alive; ++j) {
+        if (j < ntiles) {
+          const int sb = j & 1;
+          if (j >= 2) alive = bar_wait(s_free + sb, ((j >> 1) - 1) & 1, abort_flag, a.status);
+          fence_after();
+          const uint32_t gk = static_cast<uint32_t>(j) * C::kTileSlots;
+          for (int c = 0; c < C::kChunks && alive; ++c) {
+            const uint32_t slot = (gk + c) % R_;
+            alive = bar_wait(full + slot, ((gk + c) / R_) & 1u, abort_flag, a.status);
+            fence_after();
+            if (!alive) break;
+            const uint32_t abase = ring_addr + slot * kSlot;
+            const uint32_t bbase = q_addr + c * C::kQAtomBytes;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma<kF8>(tmem + sb * C::kSCols, sdesc(abase + kk * 32, 16, 1024),
+                       sdesc(bbase + kk * 32, 16, 1024), id_s, (c | kk) != 0);
+          }
+          if (!alive) break;
+          mma_commit(s_full + sb);
+          for (int c = 0; c < C::kChunks; ++c) mma_commit(empty + (gk + c) % R_);
+        }
+        if (j >= 1) {
+          const int jp = j - 1;
+          alive = bar_wait(p_full, jp & 1, abort_flag, a.status);
+          fence_after();
+          if (!alive) break;
+          const uint32_t gv = static_cast<uint32_t>(jp) * C::kTileSlots + C::kChunks;
+          for (int c = 0; c < C::kChunks && alive; ++c) {
+            alive = bar_wait(full + (gv + c) % R_, ((gv + c) / R_) & 1u, abort_flag, a.status);
+          }
+          fence_after();
+          if (!alive) break;
+#pragma unroll
+          for (int blk = 0; blk < C::kOBlocks; ++blk) {
+            if constexpr (kF8) {
+              // V block = one slot (128 d); P as two E4M3 terms, K = 32 tokens per MMA
+              const uint32_t vbase = ring_addr + ((gv + blk) % R_) * kSlot;
+#pragma unroll
+              for (int t = 0; t < 2; ++t)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  mma<true>(tmem_o + blk * kNmax, sdesc(vbase + kk * 4096, kSlot, 1024),
+                            sdesc(p_addr + t * C::kPAtomBytes + kk * 32, 16, 1024), id_p,
+                            !(jp == 0 && t == 0 && kk == 0));
+            } else {
+              // V block = two adjacent slots (2 x 64 d); K = 16 tokens per MMA
+              const uint32_t vbase = ring_addr + ((gv + 2 * blk) % R_) * kSlot;
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                mma<false>(tmem_o + blk * kNmax, sdesc(vbase + kk * 2048, kSlot, 1024),
+                           sdesc(p_addr + (kk >> 2) * C::kPAtomBytes + (kk & 3) * 32, 16, 1024),
+                           id_p, !(jp == 0 && kk == 0));
+            }
+          }
+          mma_commit(pv_done);
+          for (int c = 0; c < C::kChunks; ++c) mma_commit(empty + (gv + c) % R_);
+        }
+      }
+      // make sure nothing issued is still running before TMEM is released
+      mma_commit(drain);
+      for (uint32_t it = 0; it < kSpinLimit && !bar_try(drain, 0); ++it) {
+      }
+    }
+  } else {
+    // ========================================= softmax / epilogue warps
+    const int st = tid - 64;       // 0..127
+    const int qd = warp & 3;       // TMEM lane quadrant of this warp
+    const int r = qd * 32 + lane;  // token row of S^T / d row of O^T
+    const uint32_t tl = tmem + (static_cast<uint32_t>(qd * 32) << 16);
+    const int sw = warp - 2;       // 0..3 softmax warp index
+
+    // ---- query operand Q^T (K-major, 128-byte swizzle), rows n < N (zero past M)
+    if constexpr (!C::kQSplit) {
+      constexpr int kRowChunks = D * C::kElt / 16;  // 16-byte pieces of one query row
+      for (int idx = st; idx < N * kRowChunks; idx += 128) {
+        const int n = idx / kRowChunks, cch = idx % kRowChunks;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (n < M) {
+          const uint8_t* src = static_cast<const uint8_t*>(a.q) +
+                               (((int64_t)(q0 + n / hpc) * a.hq + head0 + n % hpc) * D) * C::kElt +
+                               cch * 16;
+          v = __ldg(reinterpret_cast<const uint4*>(src));
+        }
+        const int byte = cch * 16;
+        *reinterpret_cast<uint4*>(q_s + (byte / 128) * C::kQAtomBytes + sw128(n, byte % 128)) = v;
+      }
+    } else {
+      // bf16 query row -> Q * 2^a = Q1 + Q2/16 + Q3/256 in E4M3, rows n, N + n, 2N + n
+      constexpr int kPer = D / 32;  // elements per lane (8 or 4)
+      for (int n = sw; n < N; n += 4) {
+        float x[kPer];
+        if (n < M) {
+          const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(a.q) +
+                                     ((int64_t)(q0 + n / hpc) * a.hq + head0 + n % hpc) * D +
+                                     lane * kPer;
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) x[e] = __bfloat162float(src[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) x[e] = 0.f;
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+        for (int off = 16; off; off >>= 1)
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        int ex = 0;
+        if (amax > 0.f) ex = static_cast<int>(floorf(__log2f(448.f / amax)));
+        ex = ex > 126 ? 126 : ex;
+        // keep the scaled maximum inside E4M3's finite range despite log2 rounding
+        while (ex > -126 && amax * exp2f(static_cast<float>(ex)) > 448.f) --ex;
+        const float up = exp2f(static_cast<float>(ex));
+        if (lane == 0) colscale[n] = 1.f / up;
+        uint8_t codes[3][kPer];
+#pragma unroll
+        for (int e = 0; e < kPer; e += 2) {
+          float v0 = x[e] * up, v1 = x[e + 1] * up;
+#pragma unroll
+          for (int t = 0; t < 3; ++t) {
+            const uint16_t c2 = f2_to_e4m3x2(v0, v1);
+            const float2 back = e4m3x2_to_f2(c2);
+            codes[t][e] = static_cast<uint8_t>(c2 & 0xFF);
+            codes[t][e + 1] = static_cast<uint8_t>(c2 >> 8);
+            v0 = (v0 - back.x) * 16.f;
+            v1 = (v1 - back.y) * 16.f;
+          }
+        }
+        const int byte = lane * kPer;  // d of this lane's first element (1 byte each)
+#pragma unroll
+        for (int t = 0; t < 3; ++t) {
+          uint8_t* dst = q_s + (byte / 128) * C::kQAtomBytes + sw128(t * N + n, byte % 128);
+          if constexpr (kPer == 8) {
+            uint2 w;
+            w.x = codes[t][0] | (codes[t][1] << 8) | (codes[t][2] << 16) |
+                  ((uint32_t)codes[t][3] << 24);
+            w.y = codes[t][4] | (codes[t][5] << 8) | (codes[t][6] << 16) |
+                  ((uint32_t)codes[t][7] << 24);
+            *reinterpret_cast<uint2*>(dst) = w;
+          } else {
+            *reinterpret_cast<uint32_t*>(dst) = codes[t][0] | (codes[t][1] << 8) |
+                                                (codes[t][2] << 16) | ((uint32_t)codes[t][3] << 24);
+          }
+        }
+      }
+    }
+    fence_async_smem();
+    bar_arrive(q_ready);
+    group_sync();  // colscale visible to the whole group
+
+    // ---- per-CTA scalars
+    float qk_scale = a.sm_scale * kLog2e;  // logits in log2 units
+    float v_final = 1.f;
+    if constexpr (SMODE == PDA_SCALE_TENSOR) {
+      qk_scale *= __ldg(a.k_scale);
+      v_final = __ldg(a.v_scale);
+    }
+    const int p_first = L - R;                   // position of row 0
+    const int all_hi = min(p_first, t_end - 1);  // every real row sees keys <= all_hi
+    const int all_lo = W > 0 ? L - W : 0;        // ... and >= all_lo
+
+    float lsum[kNmax];
+#pragma unroll
+    for (int n = 0; n < kNmax; ++n) lsum[n] = 0.f;
+    bool alive = true;
+
+    for (int j = 0; j < ntiles; ++j) {
+      const int tok = t_begin + j * kTok + r;
+      // per-token scales of this thread's key (loaded before waiting on S)
+      float row_scale = qk_scale, log2_vs = 0.f, inv_vs = 1.f;
+      if constexpr (SMODE == PDA_SCALE_TOKEN_HEAD) {
+        float ks = 0.f, vs = 1.f;
+        if (tok < t_end) {
+          const int page = __ldg(ptab + tok / P);
+          if (page >= 0 && page < a.num_pages) {
+            const int64_t sidx = ((int64_t)page * P + tok % P) * a.hkv + hkv;
+            ks = __ldg(a.k_scale + sidx);
+            vs = __ldg(a.v_scale + sidx);
+          }
+        }
+        row_scale *= ks;
+        vs = vs > 0.f ? vs : 1.f;
+        log2_vs = __log2f(vs);
+        inv_vs = 1.f / vs;
+      }
+      // columns this key is visible to: rows i with lo_i <= tok <= pos_i
+      int n_lo = M, n_hi = 0;  // empty
+      if (tok < t_end) {
+        const int i_lo = max(0, tok - p_first);
+        const int i_hi = W > 0 ? min(R - 1, tok + W - 1 - p_first) : R - 1;
+        if (i_lo <= i_hi) {
+          n_lo = i_lo * hpc;
+          n_hi = (i_hi + 1) * hpc;
+        }
+      }
+      const int tile0 = t_begin + j * kTok;
+      const bool full_tile = tile0 >= all_lo && tile0 + kTok - 1 <= all_hi;
+
+      if (alive) alive = bar_wait(s_full + (j & 1), (j >> 1) & 1, abort_flag, a.status);
+      alive = __all_sync(0xffffffffu, alive);
+      fence_after();
+      float s[kNmax];
+      if (alive) {
+        const uint32_t scol = tl + (j & 1) * C::kSCols;
+#pragma unroll
+        for (int ch = 0; ch < kNmax / 16; ++ch) {
+          if (ch * 16 < N) {
+            float v[16];
+            tmem_ld16(scol + ch * 16, v);
+            if constexpr (C::kQSplit) {
+              float v2[16], v3[16];
+              tmem_ld16(scol + N + ch * 16, v2);
+              tmem_ld16(scol + 2 * N + ch * 16, v3);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                s[ch * 16 + e] =
+                    (v[e] + v2[e] * 0.0625f + v3[e] * 0.00390625f) * colscale[ch * 16 + e];
+            } else {
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) s[ch * 16 + e] = v[e];
+            }
+          }
+        }
+      }
+      fence_before();
+      bar_arrive(s_free + (j & 1));
+
+      // scale, mask, and the lazy-rescale vote
+      bool trig = false;
+#pragma unroll
+      for (int n = 0; n < kNmax; ++n) {
+        if (n < N) {
+          float x = s[n] * row_scale + log2_vs;
+          const bool vis = full_tile ? (n < M && tok < t_end) : (n >= n_lo && n < n_hi);
+          x = vis ? x : -INFINITY;
+          s[n] = x;
+          trig |= x > m_used[n] + kTh;
+        }
+      }
+      // leave together: the failure test is a barrier reduction, so every
+      // softmax thread takes the same branch
+      if (group_or(!alive || *abort_flag != 0)) {
+        alive = false;
+        break;
+      }
+      const bool any = group_or(trig);
+      if (any) {
+        // exact column maxima over the tile's 128 keys
+#pragma unroll
+        for (int n = 0; n < kNmax; ++n) {
+          if (n < N) {
+            float x = s[n];
+#pragma unroll
+            for (int off = 16; off; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+            if (lane == 0) red[sw * kNmax + n] = x;
+          }
+        }
+        group_sync();
+        if (st < N) {
+          const float mx = fmaxf(fmaxf(red[st], red[kNmax + st]),
+                                 fmaxf(red[2 * kNmax + st], red[3 * kNmax + st]));
+          const float mo = m_used[st];
+          const float mn = fmaxf(mo, mx);
+          alpha[st] = mn == -INFINITY ? 1.f : exp2f(mo - mn);
+          m_used[st] = mn;
+        }
+        group_sync();
+#pragma unroll
+        for (int n = 0; n < kNmax; ++n)
+          if (n < N) lsum[n] *= alpha[n];
+      }
+      // probabilities (<= 2^kTh)
+#pragma unroll
+      for (int n = 0; n < kNmax; ++n) {
+        if (n < N) {
+          float mu = m_used[n];
+          mu = mu == -INFINITY ? 0.f : mu;
+          s[n] = exp2f(s[n] - mu);
+        }
+      }
+      // P buffer and O are free once the previous tile's PV has finished
+      if (j >= 1) alive = bar_wait(pv_done, (j - 1) & 1, abort_flag, a.status);
+      alive = __all_sync(0xffffffffu, alive);
+      fence_after();
+      if (alive && any && j >= 1) {
+        // rescale O^T (this thread's d row) by alpha per column
+#pragma unroll
+        for (int blk = 0; blk < C::kOBlocks; ++blk) {
+#pragma unroll
+          for (int ch = 0; ch < kNmax / 16; ++ch) {
+            if (ch * 16 < N) {
+              float v[16];
+              tmem_ld16(tl + 2 * C::kSCols + blk * kNmax + ch * 16, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) v[e] *= alpha[ch * 16 + e];
+              tmem_st16(tl + 2 * C::kSCols + blk * kNmax + ch * 16, v);
+            }
+          }
+        }
+        tmem_wait_st();
+      }
+      // last tile: rows past the chunk's end may hold stale or poisoned V
+      if (alive && tile0 + kTok > t_end && tok >= t_end) {
+        const uint32_t gv = static_cast<uint32_t>(j) * C::kTileSlots + C::kChunks;
+        for (int c = 0; c < C::kChunks && alive; ++c) {
+          const uint32_t slot = (gv + c) % R_;
+          alive = bar_wait(full + slot, ((gv + c) / R_) & 1u, abort_flag, a.status);
+          uint4* row = reinterpret_cast<uint4*>(ring + slot * kSlot + r * 128);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) row[e] = make_uint4(0, 0, 0, 0);
+        }
+      }
+      // write P^T (K-major, 128-byte swizzle); the denominator sums exact p
+      if constexpr (kF8) {
+#pragma unroll
+        for (int n = 0; n < kNmax; n += 2) {
+          if (n < N) {
+            const uint16_t c1 = f2_to_e4m3x2(s[n], s[n + 1]);
+            const float2 f1 = e4m3x2_to_f2(c1);
+            const uint16_t c2 = f2_to_e4m3x2(s[n] - f1.x, s[n + 1] - f1.y);
+            lsum[n] += s[n] * inv_vs;
+            lsum[n + 1] += s[n + 1] * inv_vs;
+            p_s[sw128(n, r)] = static_cast<uint8_t>(c1 & 0xFF);
+            p_s[sw128(n + 1, r)] = static_cast<uint8_t>(c1 >> 8);
+            p_s[C::kPAtomBytes + sw128(n, r)] = static_cast<uint8_t>(c2 & 0xFF);
+            p_s[C::kPAtomBytes + sw128(n + 1, r)] = static_cast<uint8_t>(c2 >> 8);
+          }
+        }
+      } else {
+        uint8_t* pbase = p_s + (r >> 6) * C::kPAtomBytes;
+        const uint32_t byte = static_cast<uint32_t>(r & 63) * 2u;
+#pragma unroll
+        for (int n = 0; n < kNmax; ++n) {
+          if (n < N) {
+            lsum[n] += s[n];
+            *reinterpret_cast<__nv_bfloat16*>(pbase + sw128(n, byte)) = __float2bfloat16_rn(s[n]);
+          }
+        }
+      }
+      fence_async_smem();
+      fence_before();
+      bar_arrive(p_full);
+    }
+    // ---------------------------------------------------------- epilogue
+    if (alive && ntiles > 0) alive = bar_wait(pv_done, (ntiles - 1) & 1, abort_flag, a.status);
+    fence_after();
+    const bool ok = !group_or(!alive);
+    if (ok) {
+      // column sums of the per-token partial denominators
+#pragma unroll
+      for (int n = 0; n < kNmax; ++n) {
+        if (n < N) {
+          float x = lsum[n];
+#pragma unroll
+          for (int off = 16; off; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+          if (lane == 0) red[sw * kNmax + n] = x;
+        }
+      }
+      group_sync();
+      const bool single = sr.num_splits == 1;
+      if (st < M) {
+        const float lt = red[st] + red[kNmax + st] + red[2 * kNmax + st] + red[3 * kNmax + st];
+        linv[st] = lt > 0.f ? v_final / lt : 0.f;
+        const float lse2 = lt > 0.f ? m_used[st] + __log2f(lt) : -INFINITY;
+        const int64_t row = q0 + st / hpc;
+        const int head = head0 + st % hpc;
+        if (single) {
+          if (a.lse) a.lse[row * a.hq + head] = lse2 * kLn2;
+        } else {
+          a.part_lse[((int64_t)split * a.rows_cap + row) * a.hq + head] = lse2;
+        }
+      }
+      group_sync();
+#pragma unroll
+      for (int blk = 0; blk < C::kOBlocks; ++blk) {
+        const int d = blk * 128 + r;
+#pragma unroll
+        for (int ch = 0; ch < kNmax / 16; ++ch) {
+          if (ch * 16 < N) {
+            float v[16];
+            tmem_ld16(tl + 2 * C::kSCols + blk * kNmax + ch * 16, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int n = ch * 16 + e;
+              if (n < M) {
+                const float o = v[e] * linv[n];
+                const int64_t row = q0 + n / hpc;
+                const int head = head0 + n % hpc;
+                if (single) {
+                  static_cast<__nv_bfloat16*>(a.out)[(row * a.hq + head) * D + d] =
+                      __float2bfloat16_rn(o);
+                } else {
+                  a.part_o[(((int64_t)split * a.rows_cap + row) * a.hq + head) * D + d] = o;
+                }
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // ---- teardown: everyone done with TMEM and shared memory
+  __syncwarp();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(C::kTmemCols)
+                 : "memory");
+}
+
+// -------------------------------------------------------------- dispatch
+using TcFn = void (*)(DecodeArgs, CUtensorMap, CUtensorMap);
+
+template <int D>
+TcFn pick_tc(int kv, int qd, int sm) {
+  if (kv == PDA_BF16) return stage1_tc<D, PDA_BF16, PDA_BF16, PDA_SCALE_NONE>;
+  if (qd == PDA_BF16) {
+    if (sm == PDA_SCALE_TENSOR) return stage1_tc<D, PDA_E4M3, PDA_BF16, PDA_SCALE_TENSOR>;
+    return stage1_tc<D, PDA_E4M3, PDA_BF16, PDA_SCALE_TOKEN_HEAD>;
+  }
+  if (sm == PDA_SCALE_TENSOR) return stage1_tc<D, PDA_E4M3, PDA_E4M3, PDA_SCALE_TENSOR>;
+  return stage1_tc<D, PDA_E4M3, PDA_E4M3, PDA_SCALE_TOKEN_HEAD>;
+}
+
+template <int D>
+int tc_smem_of(int kv, int qd, int sm) {
+  if (kv == PDA_BF16) return TcCfg<D, PDA_BF16, PDA_BF16, PDA_SCALE_NONE>::kSmem;
+  if (qd == PDA_BF16) {
+    if (sm == PDA_SCALE_TENSOR) return TcCfg<D, PDA_E4M3, PDA_BF16, PDA_SCALE_TENSOR>::kSmem;
+    return TcCfg<D, PDA_E4M3, PDA_BF16, PDA_SCALE_TOKEN_HEAD>::kSmem;
+  }
+  if (sm == PDA_SCALE_TENSOR) return TcCfg<D, PDA_E4M3, PDA_E4M3, PDA_SCALE_TENSOR>::kSmem;
+  return TcCfg<D, PDA_E4M3, PDA_E4M3, PDA_SCALE_TOKEN_HEAD>::kSmem;
+}
+
+// cuTensorMapEncodeTiled, fetched once from the driver through the runtime.
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encoder() {
+  static std::once_flag once;
+  static EncodeFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+// Tensor map over the paged cache: dims (c, slot, head, page) or
+// (c, head, slot, page), ordered by stride; one box = one page's (<= 128)
+// tokens x 128 bytes of one head.
+bool make_map(CUtensorMap* m, const void* base, const pda_plan_t* p, int* slot_dim) {
+  EncodeFn enc = encoder();
+  if (!enc) return false;
+  const int eb = p->kv_dtype == PDA_E4M3 ? 1 : 2;
+  const bool slot_first = p->kv_stride_token <= p->kv_stride_head;
+  *slot_dim = slot_first ? 1 : 2;
+  const cuuint32_t rows = static_cast<cuuint32_t>(p->page_size < kTok ? p->page_size : kTok);
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
+  dims[0] = static_cast<cuuint64_t>(p->head_dim);
+  box[0] = static_cast<cuuint32_t>(128 / eb);
+  if (slot_first) {
+    dims[1] = p->page_size;
+    dims[2] = p->num_kv_heads;
+    strides[0] = static_cast<cuuint64_t>(p->kv_stride_token) * eb;
+    strides[1] = static_cast<cuuint64_t>(p->kv_stride_head) * eb;
+    box[1] = rows;
+    box[2] = 1;
+  } else {
+    dims[1] = p->num_kv_heads;
+    dims[2] = p->page_size;
+    strides[0] = static_cast<cuuint64_t>(p->kv_stride_head) * eb;
+    strides[1] = static_cast<cuuint64_t>(p->kv_stride_token) * eb;
+    box[1] = 1;
+    box[2] = rows;
+  }
+  dims[3] = static_cast<cuuint64_t>(p->num_pages);
+  strides[2] = static_cast<cuuint64_t>(p->kv_stride_page) * eb;
+  box[3] = 1;
+  const CUtensorMapDataType dt =
+      p->kv_dtype == PDA_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool tc_supported(const pda_plan_t* p) {
+  return (p->head_dim == 128 || p->head_dim == 256) && p->page_size >= 8 && p->page_size <= 256;
+}
+
+int tc_smem_bytes(const pda_plan_t* p) {
+  return p->head_dim == 128 ? tc_smem_of<128>(p->kv_dtype, p->q_dtype, p->scale_mode)
+                            : tc_smem_of<256>(p->kv_dtype, p->q_dtype, p->scale_mode);
+}
+
+int tc_ctas_per_sm(const pda_plan_t* p) {
+  const int per = tc_smem_bytes(p) + 1024;
+  const int n = (228 * 1024) / per;
+  return n < 1 ? 1 : n;
+}
+
+int launch_stage1_tc(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_t s) {
+  DecodeArgs a = args;
+  CUtensorMap mk, mv;
+  int slot_dim = 1;
+  if (!make_map(&mk, args.k, plan, &slot_dim) || !make_map(&mv, args.v, plan, &slot_dim))
+    return PDA_ERR_CUDA;
+  a.tma_slot_dim = slot_dim;
+  TcFn k1 = plan->head_dim == 128 ? pick_tc<128>(plan->kv_dtype, plan->q_dtype, plan->scale_mode)
+                                  : pick_tc<256>(plan->kv_dtype, plan->q_dtype, plan->scale_mode);
+  const int smem = plan->stage1_smem_bytes;
+  if (cudaFuncSetAttribute(reinterpret_cast<const void*>(k1),
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return PDA_ERR_CUDA;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(plan->grid_ctas));
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  if (cudaLaunchKernelEx(&cfg, k1, a, mk, mv) != cudaSuccess) {
+    cudaGetLastError();
+    return PDA_ERR_CUDA;
+  }
+  return PDA_OK;
+}
+
+}  // namespace pda

@@ -72,30 +72,43 @@ def _make(name, args, seed=0):
     return wl, chunk
 
 
+KERNELS = {"mma": B.PDA_KERNEL_MMA, "tc": B.PDA_KERNEL_TC}
+
+
+def _tc_ok(wl):
+    """Shapes the tcgen05 path is built for (head_dim 128/256, pages of >= 8)."""
+    return wl.head_dim in (128, 256) and wl.page_size >= 8
+
+
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
 @pytest.mark.parametrize("name", sorted(SMALL))
-def test_small_full_parity(name):
+def test_small_full_parity(name, kernel):
     wl, chunk = _make(name, SMALL[name])
-    out, lse, status, dec = run_decode(wl, chunk_pages=chunk)
+    if kernel == "tc" and not _tc_ok(wl):
+        pytest.skip("shape served by the mma.sync path only")
+    out, lse, status, dec = run_decode(wl, chunk_pages=chunk, kernel=KERNELS[kernel])
     assert status == 0
     ref_o, ref_l = oracle_ref(wl)
-    assert_close(out, lse, ref_o, ref_l, tol_for(wl), what=name)
+    assert_close(out, lse, ref_o, ref_l, tol_for(wl), what=f"{name}/{kernel}")
 
 
-def test_small_peaked_parity():
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
+def test_small_peaked_parity(kernel):
     wl, chunk = _make("bf16_peaked", PEAKED_SMALL)
-    out, lse, status, dec = run_decode(wl, chunk_pages=chunk)
+    out, lse, status, dec = run_decode(wl, chunk_pages=chunk, kernel=KERNELS[kernel])
     assert status == 0
     ref_o, ref_l = oracle_ref(wl)
     assert_close(out, lse, ref_o, ref_l, TOL_BF16, what="peaked", output_rounding=True)
 
 
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
 @pytest.mark.parametrize("chunk", [4, 16, 64, 0])
-def test_split_count_invariance(chunk):
+def test_split_count_invariance(chunk, kernel):
     """Different KV chunkings (1..many splits per request) all match the
     oracle, and match one another within the same tolerance."""
     wl, _ = _make("split", dict(batch=2, rows=[3, 8], kv_lens=[4096, 1111], num_qo_heads=16,
                                 num_kv_heads=2, head_dim=128, page_size=16, windows=[0, 300]))
-    out, lse, status, dec = run_decode(wl, chunk_pages=chunk)
+    out, lse, status, dec = run_decode(wl, chunk_pages=chunk, kernel=KERNELS[kernel])
     assert status == 0
     ref_o, ref_l = oracle_ref(wl)
     assert_close(out, lse, ref_o, ref_l, TOL_BF16, what=f"chunk {chunk} ({dec.plan.max_splits})")
@@ -160,9 +173,10 @@ def _index_code(L, H, D):
     return (digit * sign).expand(L, H, D).clone()
 
 
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
 @pytest.mark.parametrize("kind", ["bf16", "fp8_tensor", "fp8_pth", "fp8_qfp8"])
 @pytest.mark.parametrize("chunk", [0, 4])
-def test_causal_upper_bound_bit_exact(kind, chunk):
+def test_causal_upper_bound_bit_exact(kind, chunk, kernel):
     """K channel 0 is 0 for old tokens and t+1 for the t-th new token; Q
     channel 0 is 128, sm_scale 1. Row i's own token then outweighs every other
     visible key by e^-128 (below the smallest fp32), so its output must be
@@ -192,7 +206,7 @@ def test_causal_upper_bound_bit_exact(kind, chunk):
                        head_dim=D, page_size=P, kv_dtype=kv, q_dtype=qd, scale_mode=sm,
                        sm_scale=1.0, value_fn=value_fn, token_fn=token_fn, unit_scale=True,
                        seed=5, device=DEV)
-    out, lse, status, _ = run_decode(wl, chunk_pages=chunk)
+    out, lse, status, _ = run_decode(wl, chunk_pages=chunk, kernel=KERNELS[kernel])
     assert status == 0
     r0 = 0
     for b, (R, L) in enumerate(zip(R_list, L_list)):
@@ -205,15 +219,16 @@ def test_causal_upper_bound_bit_exact(kind, chunk):
         r0 += R
 
 
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
 @pytest.mark.parametrize("kind", ["bf16", "fp8_pth"])
-def test_window_lower_bound_bit_exact(kind):
+def test_window_lower_bound_bit_exact(kind, kernel):
     """K channel 0 falls by one per token (bf16: 256 - j; per-token-head
     E4M3: code 1 with scale 256 - j), Q channel 0 is 128: the earliest visible
     key of each row outweighs the next by e^-128 (below the smallest fp32),
     and the key just below the window would dominate it if it were admitted.
     Output must be v at p_i - W + 1 bit for bit."""
     R_list, L_list, W_list = [8, 4, 2, 1], [200, 70, 33, 129], [1, 5, 64, 17]
-    H, G, D, P = 2, 3, 64, 16
+    H, G, D, P = 2, 3, 128, 16
 
     def token_fn(which, b, L):
         if which == "v":
@@ -240,7 +255,7 @@ def test_window_lower_bound_bit_exact(kind):
                        scale_mode=sm, sm_scale=1.0, value_fn=value_fn, token_fn=token_fn,
                        scale_fn=scale_fn if kind != "bf16" else None, unit_scale=True, seed=9,
                        device=DEV)
-    out, lse, status, _ = run_decode(wl, chunk_pages=4)
+    out, lse, status, _ = run_decode(wl, chunk_pages=4, kernel=KERNELS[kernel])
     assert status == 0
     r0 = 0
     for b, (R, L, W) in enumerate(zip(R_list, L_list, W_list)):

@@ -50,7 +50,6 @@ constexpr int kNmax = 64;          // rows x q heads per CTA
 constexpr float kTh = 8.0f;        // lazy rescale threshold, log2 units (P <= 2^8)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr uint32_t kSpinLimit = 1u << 24;
 
 // ------------------------------------------------------------------ helpers
 __device__ __forceinline__ uint32_t su32(const void* p) {
@@ -153,20 +152,44 @@ __device__ __forceinline__ bool bar_try(uint64_t* b, uint32_t parity) {
       : "memory");
   return done != 0;
 }
+// try_wait that lets the hardware suspend the thread (up to `ns`) until the
+// phase completes, so waiting warps stop competing for issue slots.
+__device__ __forceinline__ bool bar_try_sleep(uint64_t* b, uint32_t parity, uint32_t ns) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, "
+      "0, p; }"
+      : "=r"(done)
+      : "r"(su32(b)), "r"(parity), "r"(ns)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s of wall time per wait
 // Bounded wait: false if another role aborted or the limit ran out (which
 // records PDA_STATUS_WAIT_TIMEOUT and aborts the CTA).
 __device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag,
                                          uint32_t* status) {
-  for (uint32_t it = 0;; ++it) {
-    if (bar_try(b, parity)) return true;
-    if ((it & 255u) == 255u) {
-      if (*abort_flag) return false;
-      if (it > kSpinLimit) {
-        *abort_flag = 1;
-        atomicOr(status, PDA_STATUS_WAIT_TIMEOUT);
-        return false;
-      }
+  if (bar_try(b, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (bar_try_sleep(b, parity, 20000u)) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicOr(status, PDA_STATUS_WAIT_TIMEOUT);
+      return false;
     }
+  }
+}
+// Bounded wait that ignores the abort flag (draining work already issued).
+__device__ __forceinline__ void bar_drain(uint64_t* b, uint32_t parity) {
+  const uint64_t t0 = global_ns();
+  while (!bar_try_sleep(b, parity, 20000u) && global_ns() - t0 < kWaitLimitNs) {
   }
 }
 
@@ -209,6 +232,7 @@ __device__ __forceinline__ void group_sync() { asm volatile("barrier.sync 1, 128
 // ------------------------------------------------------------ configuration
 template <int D, int KVT, int QT, int SMODE>
 struct TcCfg {
+  static constexpr int kD = D;
   static constexpr bool kF8 = KVT == PDA_E4M3;
   static constexpr bool kQSplit = kF8 && QT == PDA_BF16;  // bf16 query as three E4M3 terms
   static constexpr int kQTerms = kQSplit ? 3 : 1;
@@ -236,7 +260,284 @@ struct TcCfg {
   static constexpr int kSmem = 1024 + kQBytes + kPBytes + kRing * kSlot + kSmallBytes;
 };
 
-// ---------------------------------------------------------------- the kernel
+// Position of a tile's K or V unit (kChunks ring slots each) in the order
+// the MMA issuer consumes them: K0, K1, then V_j followed by K_{j+2} for
+// j = 0, 1, ... -- S^T runs two tiles ahead of PV. The producer loads in the
+// same order, so the ring is a plain FIFO.
+__device__ __forceinline__ int unit_pos_k(int j) { return j < 2 ? j : 2 * j - 1; }
+__device__ __forceinline__ int unit_pos_v(int j, int n) { return j <= n - 2 ? 2 + 2 * j : 2 * n - 1; }
+
+// Everything the softmax / epilogue warps need from the CTA prologue.
+struct SoftmaxCtx {
+  uint8_t* p_s;
+  uint8_t* ring;
+  uint64_t* full;
+  uint64_t* s_full;
+  uint64_t* s_free;
+  uint64_t* p_full;
+  uint64_t* pv_done;
+  volatile int* abort_flag;
+  float* m_used;
+  float* alpha;
+  float* colscale;
+  float* red;
+  float* linv;
+  const int32_t* ptab;
+  uint32_t tmem;
+  int q0, R, L, W, P, hpc, M, head0, hkv, split, t_begin, t_end, ntiles;
+  bool single;
+};
+
+// Online softmax over S^T in TMEM (thread = one KV token of the tile), P^T
+// to shared memory, then the epilogue (thread = one head_dim row of O^T).
+// NCH = N / 16 is a compile-time constant so that every per-column loop has
+// an exact trip count.
+template <class C, int SMODE, int NCH>
+__device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxCtx& x, int warp,
+                                             int lane, int tid) {
+  constexpr int N = NCH * 16;
+  constexpr int R_ = C::kRing;
+  constexpr bool kF8 = C::kF8;
+  constexpr int D = C::kD;
+  const int st = tid - 64;       // 0..127
+  const int qd = warp & 3;       // TMEM lane quadrant of this warp
+  const int r = qd * 32 + lane;  // token row of S^T / d row of O^T
+  const uint32_t tl = x.tmem + (static_cast<uint32_t>(qd * 32) << 16);
+  const uint32_t tl_o = tl + 2 * C::kSCols;
+  const int sw = warp - 2;       // 0..3 softmax warp index
+  const int M = x.M, hpc = x.hpc, R = x.R;
+
+  float qk_scale = a.sm_scale * kLog2e;  // logits in log2 units
+  float v_final = 1.f;
+  if constexpr (SMODE == PDA_SCALE_TENSOR) {
+    qk_scale *= __ldg(a.k_scale);
+    v_final = __ldg(a.v_scale);
+  }
+  const int p_first = x.L - R;                   // position of row 0
+  const int all_hi = min(p_first, x.t_end - 1);  // every real row sees keys <= all_hi
+  const int all_lo = x.W > 0 ? x.L - x.W : 0;    // ... and >= all_lo
+
+  float lsum[N];
+#pragma unroll
+  for (int n = 0; n < N; ++n) lsum[n] = 0.f;
+  bool alive = true;
+
+  for (int j = 0; j < x.ntiles; ++j) {
+    const int tok = x.t_begin + j * kTok + r;
+    // per-token scales of this thread's key (loaded before waiting on S)
+    float row_scale = qk_scale, log2_vs = 0.f, inv_vs = 1.f;
+    if constexpr (SMODE == PDA_SCALE_TOKEN_HEAD) {
+      float ks = 0.f, vs = 1.f;
+      if (tok < x.t_end) {
+        const int page = __ldg(x.ptab + tok / x.P);
+        if (page >= 0 && page < a.num_pages) {
+          const int64_t sidx = ((int64_t)page * x.P + tok % x.P) * a.hkv + x.hkv;
+          ks = __ldg(a.k_scale + sidx);
+          vs = __ldg(a.v_scale + sidx);
+        }
+      }
+      row_scale *= ks;
+      vs = vs > 0.f ? vs : 1.f;
+      log2_vs = __log2f(vs);
+      inv_vs = 1.f / vs;
+    }
+    // columns this key is visible to: rows i with lo_i <= tok <= pos_i
+    int n_lo = M, n_hi = 0;  // empty
+    if (tok < x.t_end) {
+      const int i_lo = max(0, tok - p_first);
+      const int i_hi = x.W > 0 ? min(R - 1, tok + x.W - 1 - p_first) : R - 1;
+      if (i_lo <= i_hi) {
+        n_lo = i_lo * hpc;
+        n_hi = (i_hi + 1) * hpc;
+      }
+    }
+    const int tile0 = x.t_begin + j * kTok;
+    if (tile0 >= all_lo && tile0 + kTok - 1 <= all_hi) {
+      n_lo = 0;
+      n_hi = M;
+    }
+
+    if (alive) alive = bar_wait(x.s_full + (j & 1), (j >> 1) & 1, x.abort_flag, a.status);
+    alive = __all_sync(0xffffffffu, alive);
+    fence_after();
+    float s[N];
+    if (alive) {
+      const uint32_t scol = tl + (j & 1) * C::kSCols;
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) {
+        float v[16];
+        tmem_ld16(scol + ch * 16, v);
+        if constexpr (C::kQSplit) {
+          float v2[16], v3[16];
+          tmem_ld16(scol + N + ch * 16, v2);
+          tmem_ld16(scol + 2 * N + ch * 16, v3);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            s[ch * 16 + e] = (v[e] + v2[e] * 0.0625f + v3[e] * 0.00390625f) * x.colscale[ch * 16 + e];
+        } else {
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) s[ch * 16 + e] = v[e];
+        }
+      }
+    }
+    fence_before();
+    bar_arrive(x.s_free + (j & 1));
+
+    // scale, mask, and the lazy-rescale vote
+    bool trig = false;
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+      float v = s[n] * row_scale + log2_vs;
+      v = (n >= n_lo && n < n_hi) ? v : -INFINITY;
+      s[n] = v;
+      trig |= v > x.m_used[n] + kTh;
+    }
+    // One barrier reduction per tile: the vote also carries failures, and a
+    // second reduction (only when the first fired) tells them apart, so
+    // every softmax thread takes the same branch.
+    const bool fired = group_or(trig || !alive || *x.abort_flag != 0);
+    if (fired && group_or(!alive || *x.abort_flag != 0)) {
+      alive = false;
+      break;
+    }
+    if (fired) {
+      // exact column maxima over the tile's 128 keys
+#pragma unroll
+      for (int n = 0; n < N; ++n) {
+        float v = s[n];
+#pragma unroll
+        for (int off = 16; off; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+        if (lane == 0) x.red[sw * kNmax + n] = v;
+      }
+      group_sync();
+      if (st < N) {
+        const float mx = fmaxf(fmaxf(x.red[st], x.red[kNmax + st]),
+                               fmaxf(x.red[2 * kNmax + st], x.red[3 * kNmax + st]));
+        const float mo = x.m_used[st];
+        const float mn = fmaxf(mo, mx);
+        x.alpha[st] = mn == -INFINITY ? 1.f : exp2f(mo - mn);
+        x.m_used[st] = mn;
+      }
+      group_sync();
+#pragma unroll
+      for (int n = 0; n < N; ++n) lsum[n] *= x.alpha[n];
+    }
+    // probabilities (<= 2^kTh); the denominator sums them exactly
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+      float mu = x.m_used[n];
+      mu = mu == -INFINITY ? 0.f : mu;
+      s[n] = exp2f(s[n] - mu);
+      lsum[n] += s[n] * inv_vs;
+    }
+    // P buffer and O are free once the previous tile's PV has finished
+    if (j >= 1) alive = bar_wait(x.pv_done, (j - 1) & 1, x.abort_flag, a.status);
+    alive = __all_sync(0xffffffffu, alive);
+    fence_after();
+    if (alive && fired && j >= 1) {
+      // rescale O^T (this thread's d row) by alpha per column
+#pragma unroll
+      for (int blk = 0; blk < C::kOBlocks; ++blk) {
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+          float v[16];
+          tmem_ld16(tl_o + blk * kNmax + ch * 16, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] *= x.alpha[ch * 16 + e];
+          tmem_st16(tl_o + blk * kNmax + ch * 16, v);
+        }
+      }
+      tmem_wait_st();
+    }
+    // last tile: rows past the chunk's end may hold stale or poisoned V
+    if (alive && tile0 + kTok > x.t_end && tok >= x.t_end) {
+      const uint32_t gv = static_cast<uint32_t>(unit_pos_v(j, x.ntiles)) * C::kChunks;
+      for (int c = 0; c < C::kChunks && alive; ++c) {
+        const uint32_t slot = (gv + c) % R_;
+        alive = bar_wait(x.full + slot, ((gv + c) / R_) & 1u, x.abort_flag, a.status);
+        uint4* row = reinterpret_cast<uint4*>(x.ring + slot * kSlot + r * 128);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) row[e] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    // write P^T (K-major, 128-byte swizzle)
+    if constexpr (kF8) {
+#pragma unroll
+      for (int n = 0; n < N; n += 2) {
+        const uint16_t c1 = f2_to_e4m3x2(s[n], s[n + 1]);
+        const float2 f1 = e4m3x2_to_f2(c1);
+        const uint16_t c2 = f2_to_e4m3x2(s[n] - f1.x, s[n + 1] - f1.y);
+        x.p_s[sw128(n, r)] = static_cast<uint8_t>(c1 & 0xFF);
+        x.p_s[sw128(n + 1, r)] = static_cast<uint8_t>(c1 >> 8);
+        x.p_s[C::kPAtomBytes + sw128(n, r)] = static_cast<uint8_t>(c2 & 0xFF);
+        x.p_s[C::kPAtomBytes + sw128(n + 1, r)] = static_cast<uint8_t>(c2 >> 8);
+      }
+    } else {
+      uint8_t* pbase = x.p_s + (r >> 6) * C::kPAtomBytes;
+      const uint32_t byte = static_cast<uint32_t>(r & 63) * 2u;
+#pragma unroll
+      for (int n = 0; n < N; ++n)
+        *reinterpret_cast<__nv_bfloat16*>(pbase + sw128(n, byte)) = __float2bfloat16_rn(s[n]);
+    }
+    fence_async_smem();
+    fence_before();
+    bar_arrive(x.p_full);
+  }
+  // ---------------------------------------------------------- epilogue
+  if (alive && x.ntiles > 0) alive = bar_wait(x.pv_done, (x.ntiles - 1) & 1, x.abort_flag, a.status);
+  fence_after();
+  if (group_or(!alive)) return;
+  // column sums of the per-token partial denominators
+#pragma unroll
+  for (int n = 0; n < N; ++n) {
+    float v = lsum[n];
+#pragma unroll
+    for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0) x.red[sw * kNmax + n] = v;
+  }
+  group_sync();
+  if (st < M) {
+    const float lt = x.red[st] + x.red[kNmax + st] + x.red[2 * kNmax + st] + x.red[3 * kNmax + st];
+    x.linv[st] = lt > 0.f ? v_final / lt : 0.f;
+    const float lse2 = lt > 0.f ? x.m_used[st] + __log2f(lt) : -INFINITY;
+    const int64_t row = x.q0 + st / hpc;
+    const int head = x.head0 + st % hpc;
+    if (x.single) {
+      if (a.lse) a.lse[row * a.hq + head] = lse2 * kLn2;
+    } else {
+      a.part_lse[((int64_t)x.split * a.rows_cap + row) * a.hq + head] = lse2;
+    }
+  }
+  group_sync();
+#pragma unroll
+  for (int blk = 0; blk < C::kOBlocks; ++blk) {
+    const int d = blk * 128 + r;
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) {
+      float v[16];
+      tmem_ld16(tl_o + blk * kNmax + ch * 16, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int n = ch * 16 + e;
+        if (n < M) {
+          const float o = v[e] * x.linv[n];
+          const int64_t row = x.q0 + n / hpc;
+          const int head = x.head0 + n % hpc;
+          if (x.single) {
+            static_cast<__nv_bfloat16*>(a.out)[(row * a.hq + head) * D + d] = __float2bfloat16_rn(o);
+          } else {
+            a.part_o[(((int64_t)x.split * a.rows_cap + row) * a.hq + head) * D + d] = o;
+          }
+        }
+      }
+    }
+  }
+}
+
 template <int D, int KVT, int QT, int SMODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
     stage1_tc(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
@@ -349,9 +650,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int nbox = kTok / box_rows;  // <= 16 (P >= 8)
     const uint32_t box_bytes = static_cast<uint32_t>(box_rows) * 128u;
     const CUtensorMap* maps[2] = {&tmk, &tmv};
+    // this lane's box of tile j: page id and first slot (false: nothing to load)
     auto page_of = [&](int j, int& page, int& slot0) -> bool {
       const int tb = t_begin + j * kTok + lane * box_rows;
-      if (lane >= nbox || tb >= t_end) return false;
+      if (j >= ntiles || lane >= nbox || tb >= t_end) return false;
       page = __ldg(ptab + tb / P);
       slot0 = tb % P;
       if (page < 0 || page >= a.num_pages) {
@@ -360,45 +662,46 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       return true;
     };
-    int pg = 0, s0 = 0, pg_n = 0, s0_n = 0;
-    bool ok = page_of(0, pg, s0), ok_n = false;
+    // page ids of tiles j, j+1, j+2 (rotated as V_j and K_{j+2} are emitted)
+    int pg0 = 0, s00 = 0, pg1 = 0, s01 = 0, pg2 = 0, s02 = 0;
+    bool ok0 = page_of(0, pg0, s00), ok1 = page_of(1, pg1, s01), ok2 = page_of(2, pg2, s02);
     uint32_t g = 0;
     bool alive = true;
-    for (int j = 0; j < ntiles && alive; ++j) {
-      if (j + 1 < ntiles) ok_n = page_of(j + 1, pg_n, s0_n);
+    auto emit = [&](int kind, bool ok, int pg, int s0) {
       const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, ok));
-      for (int kind = 0; kind < 2 && alive; ++kind) {
-        for (int c = 0; c < C::kChunks; ++c, ++g) {
-          const uint32_t slot = g % R_, round = g / R_;
-          int good = 1;
-          if (lane == 0) {
-            good = bar_wait(empty + slot, (round & 1u) ^ 1u, abort_flag, a.status);
-            if (good) bar_expect_tx(full + slot, nvalid * box_bytes);
-          }
-          good = __shfl_sync(0xffffffffu, good, 0);
-          if (!good) {
-            alive = false;
-            break;
-          }
-          if (ok) {
-            const uint32_t dst = su32(ring + slot * kSlot) + lane * box_bytes;
-            const int c1 = a.tma_slot_dim == 1 ? s0 : hkv;
-            const int c2 = a.tma_slot_dim == 1 ? hkv : s0;
-            tma_load(dst, maps[kind], c * C::kAtom, c1, c2, pg, full + slot);
-          }
+      for (int c = 0; c < C::kChunks && alive; ++c, ++g) {
+        const uint32_t slot = g % R_, round = g / R_;
+        int good = 1;
+        if (lane == 0) {
+          good = bar_wait(empty + slot, (round & 1u) ^ 1u, abort_flag, a.status);
+          if (good) bar_expect_tx(full + slot, nvalid * box_bytes);
+        }
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) {
+          alive = false;
+          break;
+        }
+        if (ok) {
+          const uint32_t dst = su32(ring + slot * kSlot) + lane * box_bytes;
+          const int c1 = a.tma_slot_dim == 1 ? s0 : hkv;
+          const int c2 = a.tma_slot_dim == 1 ? hkv : s0;
+          tma_load(dst, maps[kind], c * C::kAtom, c1, c2, pg, full + slot);
         }
       }
-      pg = pg_n;
-      s0 = s0_n;
-      ok = ok_n;
+    };
+    emit(0, ok0, pg0, s00);
+    if (ntiles > 1) emit(0, ok1, pg1, s01);
+    for (int j = 0; j < ntiles && alive; ++j) {
+      emit(1, ok0, pg0, s00);                       // V_j
+      if (j + 2 < ntiles) emit(0, ok2, pg2, s02);   // K_{j+2}
+      pg0 = pg1; s00 = s01; ok0 = ok1;
+      pg1 = pg2; s01 = s02; ok1 = ok2;
+      ok2 = page_of(j + 3, pg2, s02);
     }
     // drain: every box issued must have landed before the CTA can exit
     if (lane == 0) {
       const uint32_t first = g > (uint32_t)R_ ? g - R_ : 0u;
-      for (uint32_t h = first; h < g; ++h) {
-        for (uint32_t it = 0; it < kSpinLimit && !bar_try(full + h % R_, (h / R_) & 1u); ++it) {
-        }
-      }
+      for (uint32_t h = first; h < g; ++h) bar_drain(full + h % R_, (h / R_) & 1u);
     }
   } else if (warp == 1) {
     // ===================================================== MMA issuer warp
@@ -409,78 +712,74 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t id_s = idesc(fmt, 0, static_cast<uint32_t>(Nq));
       const uint32_t id_p = idesc(fmt, 1, static_cast<uint32_t>(N));
       const uint32_t q_addr = su32(q_s), p_addr = su32(p_s), ring_addr = su32(ring);
-      for (int j = 0; j <= ntiles && alive; ++j) {
-        if (j < ntiles) {
-          const int sb = j & 1;
-          if (j >= 2) alive = bar_wait(s_free + sb, ((j >> 1) - 1) & 1, abort_flag, a.status);
+      // S^T of tile j into TMEM buffer j & 1 (the softmax has freed it)
+      auto issue_s = [&](int j) -> bool {
+        const int sb = j & 1;
+        if (j >= 2 && !bar_wait(s_free + sb, ((j >> 1) - 1) & 1, abort_flag, a.status)) return false;
+        fence_after();
+        const uint32_t gk = static_cast<uint32_t>(unit_pos_k(j)) * C::kChunks;
+        for (int c = 0; c < C::kChunks; ++c) {
+          const uint32_t slot = (gk + c) % R_;
+          if (!bar_wait(full + slot, ((gk + c) / R_) & 1u, abort_flag, a.status)) return false;
           fence_after();
-          const uint32_t gk = static_cast<uint32_t>(j) * C::kTileSlots;
-          for (int c = 0; c < C::kChunks && alive; ++c) {
-            const uint32_t slot = (gk + c) % R_;
-            alive = bar_wait(full + slot, ((gk + c) / R_) & 1u, abort_flag, a.status);
-            fence_after();
-            if (!alive) break;
-            const uint32_t abase = ring_addr + slot * kSlot;
-            const uint32_t bbase = q_addr + c * C::kQAtomBytes;
+          const uint32_t abase = ring_addr + slot * kSlot;
+          const uint32_t bbase = q_addr + c * C::kQAtomBytes;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma<kF8>(tmem + sb * C::kSCols, sdesc(abase + kk * 32, 16, 1024),
-                       sdesc(bbase + kk * 32, 16, 1024), id_s, (c | kk) != 0);
-          }
-          if (!alive) break;
-          mma_commit(s_full + sb);
-          for (int c = 0; c < C::kChunks; ++c) mma_commit(empty + (gk + c) % R_);
+          for (int kk = 0; kk < 4; ++kk)
+            mma<kF8>(tmem + sb * C::kSCols, sdesc(abase + kk * 32, 16, 1024),
+                     sdesc(bbase + kk * 32, 16, 1024), id_s, (c | kk) != 0);
         }
-        if (j >= 1) {
-          const int jp = j - 1;
-          alive = bar_wait(p_full, jp & 1, abort_flag, a.status);
-          fence_after();
-          if (!alive) break;
-          const uint32_t gv = static_cast<uint32_t>(jp) * C::kTileSlots + C::kChunks;
-          for (int c = 0; c < C::kChunks && alive; ++c) {
-            alive = bar_wait(full + (gv + c) % R_, ((gv + c) / R_) & 1u, abort_flag, a.status);
+        mma_commit(s_full + sb);
+        for (int c = 0; c < C::kChunks; ++c) mma_commit(empty + (gk + c) % R_);
+        return true;
+      };
+      if (alive) alive = issue_s(0);
+      if (alive && ntiles > 1) alive = issue_s(1);
+      for (int j = 0; j < ntiles && alive; ++j) {
+        // O^T += V_j^T P_j^T as soon as the softmax has written P_j
+        alive = bar_wait(p_full, j & 1, abort_flag, a.status);
+        fence_after();
+        if (!alive) break;
+        const uint32_t gv = static_cast<uint32_t>(unit_pos_v(j, ntiles)) * C::kChunks;
+        for (int c = 0; c < C::kChunks && alive; ++c)
+          alive = bar_wait(full + (gv + c) % R_, ((gv + c) / R_) & 1u, abort_flag, a.status);
+        fence_after();
+        if (!alive) break;
+#pragma unroll
+        for (int blk = 0; blk < C::kOBlocks; ++blk) {
+          if constexpr (kF8) {
+            // V block = one slot (128 d); P as two E4M3 terms, K = 32 tokens per MMA
+            const uint32_t vbase = ring_addr + ((gv + blk) % R_) * kSlot;
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma<true>(tmem_o + blk * kNmax, sdesc(vbase + kk * 4096, kSlot, 1024),
+                          sdesc(p_addr + t * C::kPAtomBytes + kk * 32, 16, 1024), id_p,
+                          !(j == 0 && t == 0 && kk == 0));
+          } else {
+            // V block = two adjacent slots (2 x 64 d); K = 16 tokens per MMA
+            const uint32_t vbase = ring_addr + ((gv + 2 * blk) % R_) * kSlot;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma<false>(tmem_o + blk * kNmax, sdesc(vbase + kk * 2048, kSlot, 1024),
+                         sdesc(p_addr + (kk >> 2) * C::kPAtomBytes + (kk & 3) * 32, 16, 1024),
+                         id_p, !(j == 0 && kk == 0));
           }
-          fence_after();
-          if (!alive) break;
-#pragma unroll
-          for (int blk = 0; blk < C::kOBlocks; ++blk) {
-            if constexpr (kF8) {
-              // V block = one slot (128 d); P as two E4M3 terms, K = 32 tokens per MMA
-              const uint32_t vbase = ring_addr + ((gv + blk) % R_) * kSlot;
-#pragma unroll
-              for (int t = 0; t < 2; ++t)
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                  mma<true>(tmem_o + blk * kNmax, sdesc(vbase + kk * 4096, kSlot, 1024),
-                            sdesc(p_addr + t * C::kPAtomBytes + kk * 32, 16, 1024), id_p,
-                            !(jp == 0 && t == 0 && kk == 0));
-            } else {
-              // V block = two adjacent slots (2 x 64 d); K = 16 tokens per MMA
-              const uint32_t vbase = ring_addr + ((gv + 2 * blk) % R_) * kSlot;
-#pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                mma<false>(tmem_o + blk * kNmax, sdesc(vbase + kk * 2048, kSlot, 1024),
-                           sdesc(p_addr + (kk >> 2) * C::kPAtomBytes + (kk & 3) * 32, 16, 1024),
-                           id_p, !(jp == 0 && kk == 0));
-            }
-          }
-          mma_commit(pv_done);
-          for (int c = 0; c < C::kChunks; ++c) mma_commit(empty + (gv + c) % R_);
         }
+        mma_commit(pv_done);
+        for (int c = 0; c < C::kChunks; ++c) mma_commit(empty + (gv + c) % R_);
+        // keep S two tiles ahead of the softmax
+        if (j + 2 < ntiles) alive = issue_s(j + 2);
       }
       // make sure nothing issued is still running before TMEM is released
       mma_commit(drain);
-      for (uint32_t it = 0; it < kSpinLimit && !bar_try(drain, 0); ++it) {
-      }
+      bar_drain(drain, 0);
     }
   } else {
     // ========================================= softmax / epilogue warps
-    const int st = tid - 64;       // 0..127
-    const int qd = warp & 3;       // TMEM lane quadrant of this warp
-    const int r = qd * 32 + lane;  // token row of S^T / d row of O^T
-    const uint32_t tl = tmem + (static_cast<uint32_t>(qd * 32) << 16);
-    const int sw = warp - 2;       // 0..3 softmax warp index
-
+    const int st = tid - 64;  // 0..127
+    const int sw = warp - 2;  // 0..3 softmax warp index
     // ---- query operand Q^T (K-major, 128-byte swizzle), rows n < N (zero past M)
     if constexpr (!C::kQSplit) {
       constexpr int kRowChunks = D * C::kElt / 16;  // 16-byte pieces of one query row
@@ -500,20 +799,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // bf16 query row -> Q * 2^a = Q1 + Q2/16 + Q3/256 in E4M3, rows n, N + n, 2N + n
       constexpr int kPer = D / 32;  // elements per lane (8 or 4)
       for (int n = sw; n < N; n += 4) {
-        float x[kPer];
+        float xv[kPer];
         if (n < M) {
           const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(a.q) +
                                      ((int64_t)(q0 + n / hpc) * a.hq + head0 + n % hpc) * D +
                                      lane * kPer;
 #pragma unroll
-          for (int e = 0; e < kPer; ++e) x[e] = __bfloat162float(src[e]);
+          for (int e = 0; e < kPer; ++e) xv[e] = __bfloat162float(src[e]);
         } else {
 #pragma unroll
-          for (int e = 0; e < kPer; ++e) x[e] = 0.f;
+          for (int e = 0; e < kPer; ++e) xv[e] = 0.f;
         }
         float amax = 0.f;
 #pragma unroll
-        for (int e = 0; e < kPer; ++e) amax = fmaxf(amax, fabsf(x[e]));
+        for (int e = 0; e < kPer; ++e) amax = fmaxf(amax, fabsf(xv[e]));
 #pragma unroll
         for (int off = 16; off; off >>= 1)
           amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
@@ -527,7 +826,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint8_t codes[3][kPer];
 #pragma unroll
         for (int e = 0; e < kPer; e += 2) {
-          float v0 = x[e] * up, v1 = x[e + 1] * up;
+          float v0 = xv[e] * up, v1 = xv[e + 1] * up;
 #pragma unroll
           for (int t = 0; t < 3; ++t) {
             const uint16_t c2 = f2_to_e4m3x2(v0, v1);
@@ -560,259 +859,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bar_arrive(q_ready);
     group_sync();  // colscale visible to the whole group
 
-    // ---- per-CTA scalars
-    float qk_scale = a.sm_scale * kLog2e;  // logits in log2 units
-    float v_final = 1.f;
-    if constexpr (SMODE == PDA_SCALE_TENSOR) {
-      qk_scale *= __ldg(a.k_scale);
-      v_final = __ldg(a.v_scale);
-    }
-    const int p_first = L - R;                   // position of row 0
-    const int all_hi = min(p_first, t_end - 1);  // every real row sees keys <= all_hi
-    const int all_lo = W > 0 ? L - W : 0;        // ... and >= all_lo
-
-    float lsum[kNmax];
-#pragma unroll
-    for (int n = 0; n < kNmax; ++n) lsum[n] = 0.f;
-    bool alive = true;
-
-    for (int j = 0; j < ntiles; ++j) {
-      const int tok = t_begin + j * kTok + r;
-      // per-token scales of this thread's key (loaded before waiting on S)
-      float row_scale = qk_scale, log2_vs = 0.f, inv_vs = 1.f;
-      if constexpr (SMODE == PDA_SCALE_TOKEN_HEAD) {
-        float ks = 0.f, vs = 1.f;
-        if (tok < t_end) {
-          const int page = __ldg(ptab + tok / P);
-          if (page >= 0 && page < a.num_pages) {
-            const int64_t sidx = ((int64_t)page * P + tok % P) * a.hkv + hkv;
-            ks = __ldg(a.k_scale + sidx);
-            vs = __ldg(a.v_scale + sidx);
-          }
-        }
-        row_scale *= ks;
-        vs = vs > 0.f ? vs : 1.f;
-        log2_vs = __log2f(vs);
-        inv_vs = 1.f / vs;
-      }
-      // columns this key is visible to: rows i with lo_i <= tok <= pos_i
-      int n_lo = M, n_hi = 0;  // empty
-      if (tok < t_end) {
-        const int i_lo = max(0, tok - p_first);
-        const int i_hi = W > 0 ? min(R - 1, tok + W - 1 - p_first) : R - 1;
-        if (i_lo <= i_hi) {
-          n_lo = i_lo * hpc;
-          n_hi = (i_hi + 1) * hpc;
-        }
-      }
-      const int tile0 = t_begin + j * kTok;
-      const bool full_tile = tile0 >= all_lo && tile0 + kTok - 1 <= all_hi;
-
-      if (alive) alive = bar_wait(s_full + (j & 1), (j >> 1) & 1, abort_flag, a.status);
-      alive = __all_sync(0xffffffffu, alive);
-      fence_after();
-      float s[kNmax];
-      if (alive) {
-        const uint32_t scol = tl + (j & 1) * C::kSCols;
-#pragma unroll
-        for (int ch = 0; ch < kNmax / 16; ++ch) {
-          if (ch * 16 < N) {
-            float v[16];
-            tmem_ld16(scol + ch * 16, v);
-            if constexpr (C::kQSplit) {
-              float v2[16], v3[16];
-              tmem_ld16(scol + N + ch * 16, v2);
-              tmem_ld16(scol + 2 * N + ch * 16, v3);
-              tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 16; ++e)
-                s[ch * 16 + e] =
-                    (v[e] + v2[e] * 0.0625f + v3[e] * 0.00390625f) * colscale[ch * 16 + e];
-            } else {
-              tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 16; ++e) s[ch * 16 + e] = v[e];
-            }
-          }
-        }
-      }
-      fence_before();
-      bar_arrive(s_free + (j & 1));
-
-      // scale, mask, and the lazy-rescale vote
-      bool trig = false;
-#pragma unroll
-      for (int n = 0; n < kNmax; ++n) {
-        if (n < N) {
-          float x = s[n] * row_scale + log2_vs;
-          const bool vis = full_tile ? (n < M && tok < t_end) : (n >= n_lo && n < n_hi);
-          x = vis ? x : -INFINITY;
-          s[n] = x;
-          trig |= x > m_used[n] + kTh;
-        }
-      }
-      // leave together: the failure test is a barrier reduction, so every
-      // softmax thread takes the same branch
-      if (group_or(!alive || *abort_flag != 0)) {
-        alive = false;
-        break;
-      }
-      const bool any = group_or(trig);
-      if (any) {
-        // exact column maxima over the tile's 128 keys
-#pragma unroll
-        for (int n = 0; n < kNmax; ++n) {
-          if (n < N) {
-            float x = s[n];
-#pragma unroll
-            for (int off = 16; off; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
-            if (lane == 0) red[sw * kNmax + n] = x;
-          }
-        }
-        group_sync();
-        if (st < N) {
-          const float mx = fmaxf(fmaxf(red[st], red[kNmax + st]),
-                                 fmaxf(red[2 * kNmax + st], red[3 * kNmax + st]));
-          const float mo = m_used[st];
-          const float mn = fmaxf(mo, mx);
-          alpha[st] = mn == -INFINITY ? 1.f : exp2f(mo - mn);
-          m_used[st] = mn;
-        }
-        group_sync();
-#pragma unroll
-        for (int n = 0; n < kNmax; ++n)
-          if (n < N) lsum[n] *= alpha[n];
-      }
-      // probabilities (<= 2^kTh)
-#pragma unroll
-      for (int n = 0; n < kNmax; ++n) {
-        if (n < N) {
-          float mu = m_used[n];
-          mu = mu == -INFINITY ? 0.f : mu;
-          s[n] = exp2f(s[n] - mu);
-        }
-      }
-      // P buffer and O are free once the previous tile's PV has finished
-      if (j >= 1) alive = bar_wait(pv_done, (j - 1) & 1, abort_flag, a.status);
-      alive = __all_sync(0xffffffffu, alive);
-      fence_after();
-      if (alive && any && j >= 1) {
-        // rescale O^T (this thread's d row) by alpha per column
-#pragma unroll
-        for (int blk = 0; blk < C::kOBlocks; ++blk) {
-#pragma unroll
-          for (int ch = 0; ch < kNmax / 16; ++ch) {
-            if (ch * 16 < N) {
-              float v[16];
-              tmem_ld16(tl + 2 * C::kSCols + blk * kNmax + ch * 16, v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 16; ++e) v[e] *= alpha[ch * 16 + e];
-              tmem_st16(tl + 2 * C::kSCols + blk * kNmax + ch * 16, v);
-            }
-          }
-        }
-        tmem_wait_st();
-      }
-      // last tile: rows past the chunk's end may hold stale or poisoned V
-      if (alive && tile0 + kTok > t_end && tok >= t_end) {
-        const uint32_t gv = static_cast<uint32_t>(j) * C::kTileSlots + C::kChunks;
-        for (int c = 0; c < C::kChunks && alive; ++c) {
-          const uint32_t slot = (gv + c) % R_;
-          alive = bar_wait(full + slot, ((gv + c) / R_) & 1u, abort_flag, a.status);
-          uint4* row = reinterpret_cast<uint4*>(ring + slot * kSlot + r * 128);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) row[e] = make_uint4(0, 0, 0, 0);
-        }
-      }
-      // write P^T (K-major, 128-byte swizzle); the denominator sums exact p
-      if constexpr (kF8) {
-#pragma unroll
-        for (int n = 0; n < kNmax; n += 2) {
-          if (n < N) {
-            const uint16_t c1 = f2_to_e4m3x2(s[n], s[n + 1]);
-            const float2 f1 = e4m3x2_to_f2(c1);
-            const uint16_t c2 = f2_to_e4m3x2(s[n] - f1.x, s[n + 1] - f1.y);
-            lsum[n] += s[n] * inv_vs;
-            lsum[n + 1] += s[n + 1] * inv_vs;
-            p_s[sw128(n, r)] = static_cast<uint8_t>(c1 & 0xFF);
-            p_s[sw128(n + 1, r)] = static_cast<uint8_t>(c1 >> 8);
-            p_s[C::kPAtomBytes + sw128(n, r)] = static_cast<uint8_t>(c2 & 0xFF);
-            p_s[C::kPAtomBytes + sw128(n + 1, r)] = static_cast<uint8_t>(c2 >> 8);
-          }
-        }
-      } else {
-        uint8_t* pbase = p_s + (r >> 6) * C::kPAtomBytes;
-        const uint32_t byte = static_cast<uint32_t>(r & 63) * 2u;
-#pragma unroll
-        for (int n = 0; n < kNmax; ++n) {
-          if (n < N) {
-            lsum[n] += s[n];
-            *reinterpret_cast<__nv_bfloat16*>(pbase + sw128(n, byte)) = __float2bfloat16_rn(s[n]);
-          }
-        }
-      }
-      fence_async_smem();
-      fence_before();
-      bar_arrive(p_full);
-    }
-    // ---------------------------------------------------------- epilogue
-    if (alive && ntiles > 0) alive = bar_wait(pv_done, (ntiles - 1) & 1, abort_flag, a.status);
-    fence_after();
-    const bool ok = !group_or(!alive);
-    if (ok) {
-      // column sums of the per-token partial denominators
-#pragma unroll
-      for (int n = 0; n < kNmax; ++n) {
-        if (n < N) {
-          float x = lsum[n];
-#pragma unroll
-          for (int off = 16; off; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-          if (lane == 0) red[sw * kNmax + n] = x;
-        }
-      }
-      group_sync();
-      const bool single = sr.num_splits == 1;
-      if (st < M) {
-        const float lt = red[st] + red[kNmax + st] + red[2 * kNmax + st] + red[3 * kNmax + st];
-        linv[st] = lt > 0.f ? v_final / lt : 0.f;
-        const float lse2 = lt > 0.f ? m_used[st] + __log2f(lt) : -INFINITY;
-        const int64_t row = q0 + st / hpc;
-        const int head = head0 + st % hpc;
-        if (single) {
-          if (a.lse) a.lse[row * a.hq + head] = lse2 * kLn2;
-        } else {
-          a.part_lse[((int64_t)split * a.rows_cap + row) * a.hq + head] = lse2;
-        }
-      }
-      group_sync();
-#pragma unroll
-      for (int blk = 0; blk < C::kOBlocks; ++blk) {
-        const int d = blk * 128 + r;
-#pragma unroll
-        for (int ch = 0; ch < kNmax / 16; ++ch) {
-          if (ch * 16 < N) {
-            float v[16];
-            tmem_ld16(tl + 2 * C::kSCols + blk * kNmax + ch * 16, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int n = ch * 16 + e;
-              if (n < M) {
-                const float o = v[e] * linv[n];
-                const int64_t row = q0 + n / hpc;
-                const int head = head0 + n % hpc;
-                if (single) {
-                  static_cast<__nv_bfloat16*>(a.out)[(row * a.hq + head) * D + d] =
-                      __float2bfloat16_rn(o);
-                } else {
-                  a.part_o[(((int64_t)split * a.rows_cap + row) * a.hq + head) * D + d] = o;
-                }
-              }
-            }
-          }
-        }
-      }
+    SoftmaxCtx x;
+    x.p_s = p_s;
+    x.ring = ring;
+    x.full = full;
+    x.s_full = s_full;
+    x.s_free = s_free;
+    x.p_full = p_full;
+    x.pv_done = pv_done;
+    x.abort_flag = abort_flag;
+    x.m_used = m_used;
+    x.alpha = alpha;
+    x.colscale = colscale;
+    x.red = red;
+    x.linv = linv;
+    x.ptab = ptab;
+    x.tmem = tmem;
+    x.q0 = q0;
+    x.R = R;
+    x.L = L;
+    x.W = W;
+    x.P = P;
+    x.hpc = hpc;
+    x.M = M;
+    x.head0 = head0;
+    x.hkv = hkv;
+    x.split = split;
+    x.t_begin = t_begin;
+    x.t_end = t_end;
+    x.ntiles = ntiles;
+    x.single = sr.num_splits == 1;
+    switch (N >> 4) {
+      case 1: softmax_role<C, SMODE, 1>(a, x, warp, lane, tid); break;
+      case 2: softmax_role<C, SMODE, 2>(a, x, warp, lane, tid); break;
+      case 3: softmax_role<C, SMODE, 3>(a, x, warp, lane, tid); break;
+      default: softmax_role<C, SMODE, 4>(a, x, warp, lane, tid); break;
     }
   }
 

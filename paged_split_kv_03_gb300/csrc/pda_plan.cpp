@@ -107,8 +107,11 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
   pl.group = p->num_qo_heads / p->num_kv_heads;
   pl.num_sms = num_sms;
   if (p->kernel == PDA_KERNEL_TC && !pda::tc_supported(&pl)) return PDA_ERR_UNSUPPORTED;
-  // AUTO stays on the mma.sync path until the tcgen05 path is the validated default
-  pl.kernel = p->kernel == PDA_KERNEL_AUTO ? PDA_KERNEL_MMA : p->kernel;
+  // AUTO takes the tcgen05 path wherever it is built (head_dim 128/256, pages >= 8)
+  if (p->kernel == PDA_KERNEL_AUTO)
+    pl.kernel = pda::tc_supported(&pl) ? PDA_KERNEL_TC : PDA_KERNEL_MMA;
+  else
+    pl.kernel = p->kernel;
   pl.rows_per_cta = pl.kernel == PDA_KERNEL_TC ? pda::kTcRowsPerCta : pda::kMmaRowsPerCta;
 
   // Query heads per CTA for a request with R rows: the largest divisor of the
@@ -132,26 +135,63 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
   }
   const int64_t pages_max = ceil_div(max_len, p->page_size);
 
-  // Split planning. A chunk is a whole number of 64-token tiles when pages
-  // are smaller than a tile, so that only a request's last chunk is ragged.
+  // Split planning: pick the KV chunk (pages per CTA) that minimises a small
+  // cost model of stage 1 + stage 2 on this GPU. A CTA costs a fixed
+  // overhead (prologue, pipeline fill, epilogue) plus its K/V bytes at the
+  // SM's share of HBM bandwidth; CTAs run in waves of `slots`; more than one
+  // split adds the merge (stage 2 launch plus partials written and read).
+  // With host lengths, per-request work replaces the uniform worst case.
   const bool tc = pl.kernel == PDA_KERNEL_TC;
   pl.stage1_smem_bytes = tc ? pda::tc_smem_bytes(&pl) : pda::mma_smem_bytes(&pl);
   const int per_sm = std::max(1, tc ? pda::tc_ctas_per_sm(&pl) : pda::mma_ctas_per_sm(&pl));
   const int64_t slots = (int64_t)num_sms * per_sm;
-  const int64_t units = (int64_t)pl.batch * pl.num_kv_heads * pl.head_blocks;
-  const int64_t tile_pages = std::max<int64_t>(1, 64 / p->page_size);
-  const int64_t min_chunk = std::max<int64_t>(tile_pages, ceil_div(256, p->page_size));
+  const int64_t hb_units = (int64_t)pl.num_kv_heads * pl.head_blocks;  // CTAs per (request, split)
+  const int64_t units = (int64_t)pl.batch * hb_units;
+  const double page_kv_bytes = 2.0 * p->page_size * p->head_dim * eb;  // K+V of one head, one page
+  const double sm_bytes_per_us = 44000.0 / per_sm;                       // ~6.7 TB/s over 152 SMs
+  const double cta_overhead_us = 4.0;
+  const double merge_us = 3.0;
+  const double rows_heads = (double)pl.batch * pl.max_q_len * pl.num_qo_heads;
+  auto cost = [&](int64_t chunk) -> double {
+    const int64_t nsplit = ceil_div(pages_max, chunk);
+    double t;
+    if (p->host_kv_len) {
+      double total = 0.0, longest = 0.0;
+      for (int b = 0; b < pl.batch; ++b) {
+        const int64_t pages = std::max<int64_t>(1, ceil_div(p->host_kv_len[b], p->page_size));
+        for (int64_t s0 = 0; s0 < pages; s0 += chunk) {
+          const double w = cta_overhead_us + std::min<int64_t>(chunk, pages - s0) * page_kv_bytes /
+                                                 sm_bytes_per_us;
+          total += w * hb_units;
+          longest = std::max(longest, w);
+        }
+      }
+      t = std::max(total / slots, longest);
+    } else {
+      const double w = cta_overhead_us + chunk * page_kv_bytes / sm_bytes_per_us;
+      t = (double)ceil_div(units * nsplit, slots) * w;
+    }
+    if (nsplit > 1) t += merge_us + 2.0 * nsplit * rows_heads * (p->head_dim + 1) * 4 / 6.0e6;
+    return t;
+  };
   int64_t chunk;
   if (p->chunk_pages > 0) {
-    chunk = ceil_div(p->chunk_pages, tile_pages) * tile_pages;
+    chunk = p->chunk_pages;
   } else {
-    const int64_t want_splits = std::max<int64_t>(1, ceil_div(2 * slots, units));
-    chunk = ceil_div(pages_max, want_splits);
-    chunk = ceil_div(chunk, tile_pages) * tile_pages;
-    chunk = std::max(chunk, min_chunk);
+    chunk = std::max<int64_t>(pages_max, 1);
+    double best = cost(chunk);
+    const int64_t max_split = std::min<int64_t>(pages_max, 8 * slots);
+    for (int64_t n = 2; n <= max_split; ++n) {
+      const int64_t c = ceil_div(pages_max, n);
+      if (ceil_div(pages_max, c) != n) continue;  // same chunk as a smaller n
+      const double t = cost(c);
+      if (t < best * 0.999) {
+        best = t;
+        chunk = c;
+      }
+    }
   }
-  chunk = std::min<int64_t>(chunk, std::max<int64_t>(pages_max, 1));
-  chunk = ceil_div(chunk, tile_pages) * tile_pages;
+  chunk = std::min<int64_t>(std::max<int64_t>(chunk, 1), std::max<int64_t>(pages_max, 1));
   pl.chunk_pages = (int32_t)chunk;
   pl.max_splits = (int32_t)ceil_div(pages_max, chunk);
   pl.grid_ctas = units * pl.max_splits;

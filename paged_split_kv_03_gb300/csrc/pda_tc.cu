@@ -43,7 +43,8 @@
 namespace pda {
 namespace {
 
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 320;  // producer, MMA issuer, 8 softmax warps
+constexpr int kSmThreads = 256;  // softmax / epilogue threads (two per TMEM lane)
 constexpr int kTok = 128;          // KV tokens per tile (MMA M of S^T)
 constexpr int kSlot = 16384;       // ring slot: [128 tokens x 128 bytes]
 constexpr int kNmax = 64;          // rows x q heads per CTA
@@ -125,6 +126,22 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
       "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
       "r"(__float_as_uint(v[15]))
       : "memory");
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+               "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+               "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+               : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -216,18 +233,18 @@ __device__ __forceinline__ float2 e4m3x2_to_f2(uint16_t c) {
   return __half22float2(*reinterpret_cast<__half2*>(&h));
 }
 
-// Barrier of the 128 softmax threads (named barrier 1) that also ORs a predicate.
+// Barrier of the 256 softmax threads (named barrier 1) that also ORs a predicate.
 __device__ __forceinline__ bool group_or(bool pred) {
   uint32_t in = pred ? 1u : 0u, out;
   asm volatile(
-      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; barrier.red.or.pred q, 1, 128, p; selp.u32 %0, 1, "
+      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; barrier.red.or.pred q, 1, 256, p; selp.u32 %0, 1, "
       "0, q; }"
       : "=r"(out)
       : "r"(in)
       : "memory");
   return out != 0;
 }
-__device__ __forceinline__ void group_sync() { asm volatile("barrier.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void group_sync() { asm volatile("barrier.sync 1, 256;" ::: "memory"); }
 
 // ------------------------------------------------------------ configuration
 template <int D, int KVT, int QT, int SMODE>
@@ -288,23 +305,26 @@ struct SoftmaxCtx {
   bool single;
 };
 
-// Online softmax over S^T in TMEM (thread = one KV token of the tile), P^T
-// to shared memory, then the epilogue (thread = one head_dim row of O^T).
-// NCH = N / 16 is a compile-time constant so that every per-column loop has
-// an exact trip count.
+// Online softmax over S^T in TMEM, P^T to shared memory, then the epilogue.
+// Two warps share each TMEM lane quadrant: a thread owns one KV token of the
+// tile (one head_dim row of O^T in the epilogue) and one half of the N
+// columns. NCH = N / 16 is a compile-time constant so that every
+// per-column loop has an exact trip count.
 template <class C, int SMODE, int NCH>
 __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxCtx& x, int warp,
                                              int lane, int tid) {
   constexpr int N = NCH * 16;
+  constexpr int NH = NCH * 8;    // columns of this thread
   constexpr int R_ = C::kRing;
   constexpr bool kF8 = C::kF8;
   constexpr int D = C::kD;
-  const int st = tid - 64;       // 0..127
+  const int st = tid - 64;       // 0..255
   const int qd = warp & 3;       // TMEM lane quadrant of this warp
   const int r = qd * 32 + lane;  // token row of S^T / d row of O^T
+  const int sw = (warp - 2) & 3; // warp index within the column half
+  const int c0 = ((warp - 2) >> 2) * NH;  // first column of this thread
   const uint32_t tl = x.tmem + (static_cast<uint32_t>(qd * 32) << 16);
   const uint32_t tl_o = tl + 2 * C::kSCols;
-  const int sw = warp - 2;       // 0..3 softmax warp index
   const int M = x.M, hpc = x.hpc, R = x.R;
 
   float qk_scale = a.sm_scale * kLog2e;  // logits in log2 units
@@ -317,9 +337,9 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
   const int all_hi = min(p_first, x.t_end - 1);  // every real row sees keys <= all_hi
   const int all_lo = x.W > 0 ? x.L - x.W : 0;    // ... and >= all_lo
 
-  float lsum[N];
+  float lsum[NH];
 #pragma unroll
-  for (int n = 0; n < N; ++n) lsum[n] = 0.f;
+  for (int i = 0; i < NH; ++i) lsum[i] = 0.f;
   bool alive = true;
 
   for (int j = 0; j < x.ntiles; ++j) {
@@ -360,25 +380,26 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
     if (alive) alive = bar_wait(x.s_full + (j & 1), (j >> 1) & 1, x.abort_flag, a.status);
     alive = __all_sync(0xffffffffu, alive);
     fence_after();
-    float s[N];
+    float s[NH];
     if (alive) {
-      const uint32_t scol = tl + (j & 1) * C::kSCols;
+      const uint32_t scol = tl + (j & 1) * C::kSCols + c0;
 #pragma unroll
       for (int ch = 0; ch < NCH; ++ch) {
-        float v[16];
-        tmem_ld16(scol + ch * 16, v);
+        float v[8];
+        tmem_ld8(scol + ch * 8, v);
         if constexpr (C::kQSplit) {
-          float v2[16], v3[16];
-          tmem_ld16(scol + N + ch * 16, v2);
-          tmem_ld16(scol + 2 * N + ch * 16, v3);
+          float v2[8], v3[8];
+          tmem_ld8(scol + N + ch * 8, v2);
+          tmem_ld8(scol + 2 * N + ch * 8, v3);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            s[ch * 16 + e] = (v[e] + v2[e] * 0.0625f + v3[e] * 0.00390625f) * x.colscale[ch * 16 + e];
+          for (int e = 0; e < 8; ++e)
+            s[ch * 8 + e] =
+                (v[e] + v2[e] * 0.0625f + v3[e] * 0.00390625f) * x.colscale[c0 + ch * 8 + e];
         } else {
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) s[ch * 16 + e] = v[e];
+          for (int e = 0; e < 8; ++e) s[ch * 8 + e] = v[e];
         }
       }
     }
@@ -388,10 +409,11 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
     // scale, mask, and the lazy-rescale vote
     bool trig = false;
 #pragma unroll
-    for (int n = 0; n < N; ++n) {
-      float v = s[n] * row_scale + log2_vs;
+    for (int i = 0; i < NH; ++i) {
+      const int n = c0 + i;
+      float v = s[i] * row_scale + log2_vs;
       v = (n >= n_lo && n < n_hi) ? v : -INFINITY;
-      s[n] = v;
+      s[i] = v;
       trig |= v > x.m_used[n] + kTh;
     }
     // One barrier reduction per tile: the vote also carries failures, and a
@@ -405,11 +427,11 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
     if (fired) {
       // exact column maxima over the tile's 128 keys
 #pragma unroll
-      for (int n = 0; n < N; ++n) {
-        float v = s[n];
+      for (int i = 0; i < NH; ++i) {
+        float v = s[i];
 #pragma unroll
         for (int off = 16; off; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-        if (lane == 0) x.red[sw * kNmax + n] = v;
+        if (lane == 0) x.red[sw * kNmax + c0 + i] = v;
       }
       group_sync();
       if (st < N) {
@@ -422,15 +444,15 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
       }
       group_sync();
 #pragma unroll
-      for (int n = 0; n < N; ++n) lsum[n] *= x.alpha[n];
+      for (int i = 0; i < NH; ++i) lsum[i] *= x.alpha[c0 + i];
     }
     // probabilities (<= 2^kTh); the denominator sums them exactly
 #pragma unroll
-    for (int n = 0; n < N; ++n) {
-      float mu = x.m_used[n];
+    for (int i = 0; i < NH; ++i) {
+      float mu = x.m_used[c0 + i];
       mu = mu == -INFINITY ? 0.f : mu;
-      s[n] = exp2f(s[n] - mu);
-      lsum[n] += s[n] * inv_vs;
+      s[i] = exp2f(s[i] - mu);
+      lsum[i] += s[i] * inv_vs;
     }
     // P buffer and O are free once the previous tile's PV has finished
     if (j >= 1) alive = bar_wait(x.pv_done, (j - 1) & 1, x.abort_flag, a.status);
@@ -442,18 +464,18 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
       for (int blk = 0; blk < C::kOBlocks; ++blk) {
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
-          float v[16];
-          tmem_ld16(tl_o + blk * kNmax + ch * 16, v);
+          float v[8];
+          tmem_ld8(tl_o + blk * kNmax + c0 + ch * 8, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] *= x.alpha[ch * 16 + e];
-          tmem_st16(tl_o + blk * kNmax + ch * 16, v);
+          for (int e = 0; e < 8; ++e) v[e] *= x.alpha[c0 + ch * 8 + e];
+          tmem_st8(tl_o + blk * kNmax + c0 + ch * 8, v);
         }
       }
       tmem_wait_st();
     }
     // last tile: rows past the chunk's end may hold stale or poisoned V
-    if (alive && tile0 + kTok > x.t_end && tok >= x.t_end) {
+    if (alive && c0 == 0 && tile0 + kTok > x.t_end && tok >= x.t_end) {
       const uint32_t gv = static_cast<uint32_t>(unit_pos_v(j, x.ntiles)) * C::kChunks;
       for (int c = 0; c < C::kChunks && alive; ++c) {
         const uint32_t slot = (gv + c) % R_;
@@ -466,10 +488,11 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
     // write P^T (K-major, 128-byte swizzle)
     if constexpr (kF8) {
 #pragma unroll
-      for (int n = 0; n < N; n += 2) {
-        const uint16_t c1 = f2_to_e4m3x2(s[n], s[n + 1]);
+      for (int i = 0; i < NH; i += 2) {
+        const int n = c0 + i;
+        const uint16_t c1 = f2_to_e4m3x2(s[i], s[i + 1]);
         const float2 f1 = e4m3x2_to_f2(c1);
-        const uint16_t c2 = f2_to_e4m3x2(s[n] - f1.x, s[n + 1] - f1.y);
+        const uint16_t c2 = f2_to_e4m3x2(s[i] - f1.x, s[i + 1] - f1.y);
         x.p_s[sw128(n, r)] = static_cast<uint8_t>(c1 & 0xFF);
         x.p_s[sw128(n + 1, r)] = static_cast<uint8_t>(c1 >> 8);
         x.p_s[C::kPAtomBytes + sw128(n, r)] = static_cast<uint8_t>(c2 & 0xFF);
@@ -479,8 +502,8 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
       uint8_t* pbase = x.p_s + (r >> 6) * C::kPAtomBytes;
       const uint32_t byte = static_cast<uint32_t>(r & 63) * 2u;
 #pragma unroll
-      for (int n = 0; n < N; ++n)
-        *reinterpret_cast<__nv_bfloat16*>(pbase + sw128(n, byte)) = __float2bfloat16_rn(s[n]);
+      for (int i = 0; i < NH; ++i)
+        *reinterpret_cast<__nv_bfloat16*>(pbase + sw128(c0 + i, byte)) = __float2bfloat16_rn(s[i]);
     }
     fence_async_smem();
     fence_before();
@@ -492,11 +515,11 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
   if (group_or(!alive)) return;
   // column sums of the per-token partial denominators
 #pragma unroll
-  for (int n = 0; n < N; ++n) {
-    float v = lsum[n];
+  for (int i = 0; i < NH; ++i) {
+    float v = lsum[i];
 #pragma unroll
     for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    if (lane == 0) x.red[sw * kNmax + n] = v;
+    if (lane == 0) x.red[sw * kNmax + c0 + i] = v;
   }
   group_sync();
   if (st < M) {
@@ -517,12 +540,12 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
     const int d = blk * 128 + r;
 #pragma unroll
     for (int ch = 0; ch < NCH; ++ch) {
-      float v[16];
-      tmem_ld16(tl_o + blk * kNmax + ch * 16, v);
+      float v[8];
+      tmem_ld8(tl_o + blk * kNmax + c0 + ch * 8, v);
       tmem_wait_ld();
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int n = ch * 16 + e;
+      for (int e = 0; e < 8; ++e) {
+        const int n = c0 + ch * 8 + e;
         if (n < M) {
           const float o = v[e] * x.linv[n];
           const int64_t row = x.q0 + n / hpc;
@@ -618,11 +641,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     bar_init(s_full, 1);
     bar_init(s_full + 1, 1);
-    bar_init(s_free, 128);
-    bar_init(s_free + 1, 128);
-    bar_init(p_full, 128);
+    bar_init(s_free, kSmThreads);
+    bar_init(s_free + 1, kSmThreads);
+    bar_init(p_full, kSmThreads);
     bar_init(pv_done, 1);
-    bar_init(q_ready, 128);
+    bar_init(q_ready, kSmThreads);
     bar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -778,12 +801,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // ========================================= softmax / epilogue warps
-    const int st = tid - 64;  // 0..127
-    const int sw = warp - 2;  // 0..3 softmax warp index
+    const int st = tid - 64;  // 0..255
+    const int sw = warp - 2;  // 0..7 softmax warp index
     // ---- query operand Q^T (K-major, 128-byte swizzle), rows n < N (zero past M)
     if constexpr (!C::kQSplit) {
       constexpr int kRowChunks = D * C::kElt / 16;  // 16-byte pieces of one query row
-      for (int idx = st; idx < N * kRowChunks; idx += 128) {
+      for (int idx = st; idx < N * kRowChunks; idx += kSmThreads) {
         const int n = idx / kRowChunks, cch = idx % kRowChunks;
         uint4 v = make_uint4(0, 0, 0, 0);
         if (n < M) {
@@ -798,7 +821,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else {
       // bf16 query row -> Q * 2^a = Q1 + Q2/16 + Q3/256 in E4M3, rows n, N + n, 2N + n
       constexpr int kPer = D / 32;  // elements per lane (8 or 4)
-      for (int n = sw; n < N; n += 4) {
+      for (int n = sw; n < N; n += 8) {
         float xv[kPer];
         if (n < M) {
           const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(a.q) +

@@ -51,7 +51,7 @@ def peaks():
     return 6800.0, "fallback"
 
 
-KERNEL_SOURCES = {"stage1": ("pda_mma.cu", "pda_internal.h")}
+KERNEL_SOURCES = {"stage1": ("pda_tc.cu", "pda_internal.h")}
 
 
 def source_sha(kernel: str = "stage1") -> str:

@@ -125,6 +125,8 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
   pl.heads_per_cta[0] = pl.heads_per_cta[1];
   pl.head_blocks = pl.group / pl.heads_per_cta[pl.max_q_len];
 
+  if (pl.kernel == PDA_KERNEL_TC) pl.rows_per_cta = pda::tc_variant_rows(&pl);
+
   // Context to plan for: the maximum, or the exact host lengths when given.
   int64_t max_len = p->max_kv_len;
   if (p->host_kv_len) {

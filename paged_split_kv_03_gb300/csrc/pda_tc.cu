@@ -47,7 +47,6 @@ constexpr int kTcThreads = 320;  // producer, MMA issuer, 8 softmax warps
 constexpr int kSmThreads = 256;  // softmax / epilogue threads (two per TMEM lane)
 constexpr int kTok = 128;          // KV tokens per tile (MMA M of S^T)
 constexpr int kSlot = 16384;       // ring slot: [128 tokens x 128 bytes]
-constexpr int kNmax = 64;          // rows x q heads per CTA
 constexpr float kTh = 8.0f;        // lazy rescale threshold, log2 units (P <= 2^8)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -220,6 +219,13 @@ __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// 2^x by the SFU (ex2.approx.ftz): about 2 ulp, -inf -> 0.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Two floats -> two E4M3 codes (RNE, saturating): low byte from `lo`.
 __device__ __forceinline__ uint16_t f2_to_e4m3x2(float lo, float hi) {
   uint16_t r;
@@ -247,9 +253,12 @@ __device__ __forceinline__ bool group_or(bool pred) {
 __device__ __forceinline__ void group_sync() { asm volatile("barrier.sync 1, 256;" ::: "memory"); }
 
 // ------------------------------------------------------------ configuration
-template <int D, int KVT, int QT, int SMODE>
+// NMAX: rows x q heads one CTA holds (16: two CTAs per SM; 64: one).
+template <int D, int KVT, int QT, int SMODE, int NMAX>
 struct TcCfg {
   static constexpr int kD = D;
+  static constexpr int kNmax = NMAX;
+  static constexpr int kCtasPerSm = NMAX <= 16 ? 2 : 1;
   static constexpr bool kF8 = KVT == PDA_E4M3;
   static constexpr bool kQSplit = kF8 && QT == PDA_BF16;  // bf16 query as three E4M3 terms
   static constexpr int kQTerms = kQSplit ? 3 : 1;
@@ -269,11 +278,12 @@ struct TcCfg {
       kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
   static_assert(kTmemNeed <= 512, "TMEM budget");
   static constexpr int kSmallBytes = 4096;
-  static constexpr int kAvail = 227 * 1024 - 1024 - kQBytes - kPBytes - kSmallBytes;
+  static constexpr int kBudget = kCtasPerSm == 2 ? 228 * 1024 / 2 - 1024 : 227 * 1024;
+  static constexpr int kAvail = kBudget - 1024 - kQBytes - kPBytes - kSmallBytes;
   static constexpr int kRingRaw = kAvail / kSlot > 12 ? 12 : kAvail / kSlot;
   // bf16 V blocks span two adjacent slots: keep the ring even so pairs never wrap
   static constexpr int kRing = kF8 ? kRingRaw : (kRingRaw & ~1);
-  static_assert(kRing >= kTileSlots, "ring must hold one tile");
+  static constexpr bool kBuildable = kRing >= kTileSlots;
   static constexpr int kSmem = 1024 + kQBytes + kPBytes + kRing * kSlot + kSmallBytes;
 };
 
@@ -431,15 +441,15 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
         float v = s[i];
 #pragma unroll
         for (int off = 16; off; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-        if (lane == 0) x.red[sw * kNmax + c0 + i] = v;
+        if (lane == 0) x.red[sw * C::kNmax + c0 + i] = v;
       }
       group_sync();
       if (st < N) {
-        const float mx = fmaxf(fmaxf(x.red[st], x.red[kNmax + st]),
-                               fmaxf(x.red[2 * kNmax + st], x.red[3 * kNmax + st]));
+        const float mx = fmaxf(fmaxf(x.red[st], x.red[C::kNmax + st]),
+                               fmaxf(x.red[2 * C::kNmax + st], x.red[3 * C::kNmax + st]));
         const float mo = x.m_used[st];
         const float mn = fmaxf(mo, mx);
-        x.alpha[st] = mn == -INFINITY ? 1.f : exp2f(mo - mn);
+        x.alpha[st] = mn == -INFINITY ? 1.f : ex2(mo - mn);
         x.m_used[st] = mn;
       }
       group_sync();
@@ -451,7 +461,7 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
     for (int i = 0; i < NH; ++i) {
       float mu = x.m_used[c0 + i];
       mu = mu == -INFINITY ? 0.f : mu;
-      s[i] = exp2f(s[i] - mu);
+      s[i] = ex2(s[i] - mu);
       lsum[i] += s[i] * inv_vs;
     }
     // P buffer and O are free once the previous tile's PV has finished
@@ -465,11 +475,11 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
           float v[8];
-          tmem_ld8(tl_o + blk * kNmax + c0 + ch * 8, v);
+          tmem_ld8(tl_o + blk * C::kNmax + c0 + ch * 8, v);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 8; ++e) v[e] *= x.alpha[c0 + ch * 8 + e];
-          tmem_st8(tl_o + blk * kNmax + c0 + ch * 8, v);
+          tmem_st8(tl_o + blk * C::kNmax + c0 + ch * 8, v);
         }
       }
       tmem_wait_st();
@@ -519,11 +529,11 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
     float v = lsum[i];
 #pragma unroll
     for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    if (lane == 0) x.red[sw * kNmax + c0 + i] = v;
+    if (lane == 0) x.red[sw * C::kNmax + c0 + i] = v;
   }
   group_sync();
   if (st < M) {
-    const float lt = x.red[st] + x.red[kNmax + st] + x.red[2 * kNmax + st] + x.red[3 * kNmax + st];
+    const float lt = x.red[st] + x.red[C::kNmax + st] + x.red[2 * C::kNmax + st] + x.red[3 * C::kNmax + st];
     x.linv[st] = lt > 0.f ? v_final / lt : 0.f;
     const float lse2 = lt > 0.f ? x.m_used[st] + __log2f(lt) : -INFINITY;
     const int64_t row = x.q0 + st / hpc;
@@ -541,7 +551,7 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
 #pragma unroll
     for (int ch = 0; ch < NCH; ++ch) {
       float v[8];
-      tmem_ld8(tl_o + blk * kNmax + c0 + ch * 8, v);
+      tmem_ld8(tl_o + blk * C::kNmax + c0 + ch * 8, v);
       tmem_wait_ld();
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -561,11 +571,11 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
   }
 }
 
-template <int D, int KVT, int QT, int SMODE>
-__global__ void __launch_bounds__(kTcThreads, 1)
+template <int D, int KVT, int QT, int SMODE, int NMAX>
+__global__ void __launch_bounds__(kTcThreads, (NMAX <= 16 ? 2 : 1))
     stage1_tc(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
               const __grid_constant__ CUtensorMap tmv) {
-  using C = TcCfg<D, KVT, QT, SMODE>;
+  using C = TcCfg<D, KVT, QT, SMODE, NMAX>;
   constexpr bool kF8 = C::kF8;
   constexpr int R_ = C::kRing;
   extern __shared__ uint8_t smem_raw[];
@@ -586,10 +596,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* m_used = reinterpret_cast<float*>(small + 512);
-  float* alpha = m_used + kNmax;
-  float* colscale = alpha + kNmax;
-  float* red = colscale + kNmax;  // [4][kNmax]
-  float* linv = red + 4 * kNmax;
+  float* alpha = m_used + C::kNmax;
+  float* colscale = alpha + C::kNmax;
+  float* red = colscale + C::kNmax;  // [4][C::kNmax]
+  float* linv = red + 4 * C::kNmax;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -650,7 +660,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (tid < kNmax) {
+  if (tid < C::kNmax) {
     m_used[tid] = -INFINITY;
     colscale[tid] = 1.f;
   }
@@ -777,7 +787,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int t = 0; t < 2; ++t)
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                mma<true>(tmem_o + blk * kNmax, sdesc(vbase + kk * 4096, kSlot, 1024),
+                mma<true>(tmem_o + blk * C::kNmax, sdesc(vbase + kk * 4096, kSlot, 1024),
                           sdesc(p_addr + t * C::kPAtomBytes + kk * 32, 16, 1024), id_p,
                           !(j == 0 && t == 0 && kk == 0));
           } else {
@@ -785,7 +795,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t vbase = ring_addr + ((gv + 2 * blk) % R_) * kSlot;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma<false>(tmem_o + blk * kNmax, sdesc(vbase + kk * 2048, kSlot, 1024),
+              mma<false>(tmem_o + blk * C::kNmax, sdesc(vbase + kk * 2048, kSlot, 1024),
                          sdesc(p_addr + (kk >> 2) * C::kPAtomBytes + (kk & 3) * 32, 16, 1024),
                          id_p, !(j == 0 && kk == 0));
           }
@@ -912,11 +922,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     x.t_end = t_end;
     x.ntiles = ntiles;
     x.single = sr.num_splits == 1;
-    switch (N >> 4) {
-      case 1: softmax_role<C, SMODE, 1>(a, x, warp, lane, tid); break;
-      case 2: softmax_role<C, SMODE, 2>(a, x, warp, lane, tid); break;
-      case 3: softmax_role<C, SMODE, 3>(a, x, warp, lane, tid); break;
-      default: softmax_role<C, SMODE, 4>(a, x, warp, lane, tid); break;
+    if constexpr (NMAX <= 16) {
+      softmax_role<C, SMODE, 1>(a, x, warp, lane, tid);
+    } else {
+      switch (N >> 4) {
+        case 1: softmax_role<C, SMODE, 1>(a, x, warp, lane, tid); break;
+        case 2: softmax_role<C, SMODE, 2>(a, x, warp, lane, tid); break;
+        case 3: softmax_role<C, SMODE, 3>(a, x, warp, lane, tid); break;
+        default: softmax_role<C, SMODE, 4>(a, x, warp, lane, tid); break;
+      }
     }
   }
 
@@ -935,27 +949,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // -------------------------------------------------------------- dispatch
 using TcFn = void (*)(DecodeArgs, CUtensorMap, CUtensorMap);
 
-template <int D>
-TcFn pick_tc(int kv, int qd, int sm) {
-  if (kv == PDA_BF16) return stage1_tc<D, PDA_BF16, PDA_BF16, PDA_SCALE_NONE>;
-  if (qd == PDA_BF16) {
-    if (sm == PDA_SCALE_TENSOR) return stage1_tc<D, PDA_E4M3, PDA_BF16, PDA_SCALE_TENSOR>;
-    return stage1_tc<D, PDA_E4M3, PDA_BF16, PDA_SCALE_TOKEN_HEAD>;
-  }
-  if (sm == PDA_SCALE_TENSOR) return stage1_tc<D, PDA_E4M3, PDA_E4M3, PDA_SCALE_TENSOR>;
-  return stage1_tc<D, PDA_E4M3, PDA_E4M3, PDA_SCALE_TOKEN_HEAD>;
+template <int D, int KVT, int QT, int SMODE, int NMAX>
+TcFn tc_fn() {
+  if constexpr (TcCfg<D, KVT, QT, SMODE, NMAX>::kBuildable)
+    return stage1_tc<D, KVT, QT, SMODE, NMAX>;
+  else
+    return nullptr;
+}
+template <int D, int KVT, int QT, int SMODE, int NMAX>
+int tc_smem() {
+  using C = TcCfg<D, KVT, QT, SMODE, NMAX>;
+  return C::kBuildable ? C::kSmem : -1;
 }
 
-template <int D>
-int tc_smem_of(int kv, int qd, int sm) {
-  if (kv == PDA_BF16) return TcCfg<D, PDA_BF16, PDA_BF16, PDA_SCALE_NONE>::kSmem;
-  if (qd == PDA_BF16) {
-    if (sm == PDA_SCALE_TENSOR) return TcCfg<D, PDA_E4M3, PDA_BF16, PDA_SCALE_TENSOR>::kSmem;
-    return TcCfg<D, PDA_E4M3, PDA_BF16, PDA_SCALE_TOKEN_HEAD>::kSmem;
+// Kernel (or shared-memory size) for the plan's dtypes, head_dim and NMAX.
+template <class F>
+auto tc_select(const pda_plan_t* p, int nmax, F f) {
+  const int kv = p->kv_dtype, qd = p->q_dtype, sm = p->scale_mode;
+#define PDA_TC_CASES(DD, NN)                                                              \
+  if (kv == PDA_BF16) return f.template get<DD, PDA_BF16, PDA_BF16, PDA_SCALE_NONE, NN>(); \
+  if (qd == PDA_BF16) {                                                                   \
+    if (sm == PDA_SCALE_TENSOR)                                                           \
+      return f.template get<DD, PDA_E4M3, PDA_BF16, PDA_SCALE_TENSOR, NN>();              \
+    return f.template get<DD, PDA_E4M3, PDA_BF16, PDA_SCALE_TOKEN_HEAD, NN>();            \
+  }                                                                                       \
+  if (sm == PDA_SCALE_TENSOR) return f.template get<DD, PDA_E4M3, PDA_E4M3, PDA_SCALE_TENSOR, NN>(); \
+  return f.template get<DD, PDA_E4M3, PDA_E4M3, PDA_SCALE_TOKEN_HEAD, NN>();
+  if (p->head_dim == 128) {
+    if (nmax <= 16) { PDA_TC_CASES(128, 16) }
+    PDA_TC_CASES(128, 64)
   }
-  if (sm == PDA_SCALE_TENSOR) return TcCfg<D, PDA_E4M3, PDA_E4M3, PDA_SCALE_TENSOR>::kSmem;
-  return TcCfg<D, PDA_E4M3, PDA_E4M3, PDA_SCALE_TOKEN_HEAD>::kSmem;
+  if (nmax <= 16) { PDA_TC_CASES(256, 16) }
+  PDA_TC_CASES(256, 64)
+#undef PDA_TC_CASES
 }
+struct GetFn {
+  template <int D, int KVT, int QT, int SMODE, int NMAX>
+  TcFn get() { return tc_fn<D, KVT, QT, SMODE, NMAX>(); }
+};
+struct GetSmem {
+  template <int D, int KVT, int QT, int SMODE, int NMAX>
+  int get() { return tc_smem<D, KVT, QT, SMODE, NMAX>(); }
+};
 
 // cuTensorMapEncodeTiled, fetched once from the driver through the runtime.
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -1023,16 +1058,25 @@ bool tc_supported(const pda_plan_t* p) {
   return (p->head_dim == 128 || p->head_dim == 256) && p->page_size >= 8 && p->page_size <= 256;
 }
 
-int tc_smem_bytes(const pda_plan_t* p) {
-  return p->head_dim == 128 ? tc_smem_of<128>(p->kv_dtype, p->q_dtype, p->scale_mode)
-                            : tc_smem_of<256>(p->kv_dtype, p->q_dtype, p->scale_mode);
+// Largest N (rows x heads, rounded up to 16) a CTA of this plan can hold.
+static int plan_nmax(const pda_plan_t* p) {
+  int n = 16;
+  for (int r = 1; r <= p->max_q_len; ++r) {
+    const int m = ((r * p->heads_per_cta[r] + 15) / 16) * 16;
+    n = m > n ? m : n;
+  }
+  return n;
 }
 
-int tc_ctas_per_sm(const pda_plan_t* p) {
-  const int per = tc_smem_bytes(p) + 1024;
-  const int n = (228 * 1024) / per;
-  return n < 1 ? 1 : n;
+int tc_variant_rows(const pda_plan_t* p) {
+  // the two-CTAs-per-SM build when every CTA fits 16 columns and it exists
+  if (plan_nmax(p) <= 16 && tc_select(p, 16, GetSmem()) > 0) return 16;
+  return 64;
 }
+
+int tc_smem_bytes(const pda_plan_t* p) { return tc_select(p, p->rows_per_cta, GetSmem()); }
+
+int tc_ctas_per_sm(const pda_plan_t* p) { return p->rows_per_cta <= 16 ? 2 : 1; }
 
 int launch_stage1_tc(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_t s) {
   DecodeArgs a = args;
@@ -1041,8 +1085,8 @@ int launch_stage1_tc(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_
   if (!make_map(&mk, args.k, plan, &slot_dim) || !make_map(&mv, args.v, plan, &slot_dim))
     return PDA_ERR_CUDA;
   a.tma_slot_dim = slot_dim;
-  TcFn k1 = plan->head_dim == 128 ? pick_tc<128>(plan->kv_dtype, plan->q_dtype, plan->scale_mode)
-                                  : pick_tc<256>(plan->kv_dtype, plan->q_dtype, plan->scale_mode);
+  TcFn k1 = tc_select(plan, plan->rows_per_cta, GetFn());
+  if (!k1) return PDA_ERR_UNSUPPORTED;
   const int smem = plan->stage1_smem_bytes;
   if (cudaFuncSetAttribute(reinterpret_cast<const void*>(k1),
                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {

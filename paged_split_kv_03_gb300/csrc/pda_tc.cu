@@ -43,8 +43,7 @@
 namespace pda {
 namespace {
 
-constexpr int kTcThreads = 320;  // producer, MMA issuer, 8 softmax warps
-constexpr int kSmThreads = 256;  // softmax / epilogue threads (two per TMEM lane)
+
 constexpr int kTok = 128;          // KV tokens per tile (MMA M of S^T)
 constexpr int kSlot = 16384;       // ring slot: [128 tokens x 128 bytes]
 constexpr float kTh = 8.0f;        // lazy rescale threshold, log2 units (P <= 2^8)
@@ -141,6 +140,30 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const float* v) {
                "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
                "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
                : "memory");
+}
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float* v) {
+  uint32_t r[4];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const float* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr),
+               "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+               "r"(__float_as_uint(v[3]))
+               : "memory");
+}
+template <int K>
+__device__ __forceinline__ void tmem_ldk(uint32_t taddr, float* v) {
+  if constexpr (K == 8) tmem_ld8(taddr, v);
+  else tmem_ld4(taddr, v);
+}
+template <int K>
+__device__ __forceinline__ void tmem_stk(uint32_t taddr, const float* v) {
+  if constexpr (K == 8) tmem_st8(taddr, v);
+  else tmem_st4(taddr, v);
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -239,18 +262,22 @@ __device__ __forceinline__ float2 e4m3x2_to_f2(uint16_t c) {
   return __half22float2(*reinterpret_cast<__half2*>(&h));
 }
 
-// Barrier of the 256 softmax threads (named barrier 1) that also ORs a predicate.
+// Barrier of the NT softmax threads (named barrier 1) that also ORs a predicate.
+template <int NT>
 __device__ __forceinline__ bool group_or(bool pred) {
   uint32_t in = pred ? 1u : 0u, out;
   asm volatile(
-      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; barrier.red.or.pred q, 1, 256, p; selp.u32 %0, 1, "
+      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; barrier.red.or.pred q, 1, %2, p; selp.u32 %0, 1, "
       "0, q; }"
       : "=r"(out)
-      : "r"(in)
+      : "r"(in), "n"(NT)
       : "memory");
   return out != 0;
 }
-__device__ __forceinline__ void group_sync() { asm volatile("barrier.sync 1, 256;" ::: "memory"); }
+template <int NT>
+__device__ __forceinline__ void group_sync() {
+  asm volatile("barrier.sync 1, %0;" ::"n"(NT) : "memory");
+}
 
 // ------------------------------------------------------------ configuration
 // NMAX: rows x q heads one CTA holds (16: two CTAs per SM; 64: one).
@@ -259,6 +286,11 @@ struct TcCfg {
   static constexpr int kD = D;
   static constexpr int kNmax = NMAX;
   static constexpr int kCtasPerSm = NMAX <= 16 ? 2 : 1;
+  // softmax warps: 4 per TMEM lane quadrant when a CTA holds up to 64 columns, else 2
+  static constexpr int kSmWarps = NMAX <= 16 ? 8 : 16;
+  static constexpr int kSmThreads = 32 * kSmWarps;
+  static constexpr int kThreads = 64 + kSmThreads;
+  static constexpr int kColGroups = kSmWarps / 4;   // warps sharing a lane quadrant
   static constexpr bool kF8 = KVT == PDA_E4M3;
   static constexpr bool kQSplit = kF8 && QT == PDA_BF16;  // bf16 query as three E4M3 terms
   static constexpr int kQTerms = kQSplit ? 3 : 1;
@@ -324,14 +356,17 @@ template <class C, int SMODE, int NCH>
 __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxCtx& x, int warp,
                                              int lane, int tid) {
   constexpr int N = NCH * 16;
-  constexpr int NH = NCH * 8;    // columns of this thread
+  constexpr int NT = C::kSmThreads;
+  constexpr int NH = N / C::kColGroups;  // columns of this thread
+  constexpr int KC = NH % 8 == 0 ? 8 : 4; // TMEM load width
+  constexpr int NCK = NH / KC;
   constexpr int R_ = C::kRing;
   constexpr bool kF8 = C::kF8;
   constexpr int D = C::kD;
-  const int st = tid - 64;       // 0..255
+  const int st = tid - 64;       // 0..NT-1
   const int qd = warp & 3;       // TMEM lane quadrant of this warp
   const int r = qd * 32 + lane;  // token row of S^T / d row of O^T
-  const int sw = (warp - 2) & 3; // warp index within the column half
+  const int sw = (warp - 2) & 3; // warp index within the column group
   const int c0 = ((warp - 2) >> 2) * NH;  // first column of this thread
   const uint32_t tl = x.tmem + (static_cast<uint32_t>(qd * 32) << 16);
   const uint32_t tl_o = tl + 2 * C::kSCols;
@@ -394,22 +429,22 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
     if (alive) {
       const uint32_t scol = tl + (j & 1) * C::kSCols + c0;
 #pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) {
-        float v[8];
-        tmem_ld8(scol + ch * 8, v);
+      for (int ch = 0; ch < NCK; ++ch) {
+        float v[KC];
+        tmem_ldk<KC>(scol + ch * KC, v);
         if constexpr (C::kQSplit) {
-          float v2[8], v3[8];
-          tmem_ld8(scol + N + ch * 8, v2);
-          tmem_ld8(scol + 2 * N + ch * 8, v3);
+          float v2[KC], v3[KC];
+          tmem_ldk<KC>(scol + N + ch * KC, v2);
+          tmem_ldk<KC>(scol + 2 * N + ch * KC, v3);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            s[ch * 8 + e] =
-                (v[e] + v2[e] * 0.0625f + v3[e] * 0.00390625f) * x.colscale[c0 + ch * 8 + e];
+          for (int e = 0; e < KC; ++e)
+            s[ch * KC + e] =
+                (v[e] + v2[e] * 0.0625f + v3[e] * 0.00390625f) * x.colscale[c0 + ch * KC + e];
         } else {
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 8; ++e) s[ch * 8 + e] = v[e];
+          for (int e = 0; e < KC; ++e) s[ch * KC + e] = v[e];
         }
       }
     }
@@ -429,8 +464,8 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
     // One barrier reduction per tile: the vote also carries failures, and a
     // second reduction (only when the first fired) tells them apart, so
     // every softmax thread takes the same branch.
-    const bool fired = group_or(trig || !alive || *x.abort_flag != 0);
-    if (fired && group_or(!alive || *x.abort_flag != 0)) {
+    const bool fired = group_or<NT>(trig || !alive || *x.abort_flag != 0);
+    if (fired && group_or<NT>(!alive || *x.abort_flag != 0)) {
       alive = false;
       break;
     }
@@ -443,7 +478,7 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
         for (int off = 16; off; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
         if (lane == 0) x.red[sw * C::kNmax + c0 + i] = v;
       }
-      group_sync();
+      group_sync<NT>();
       if (st < N) {
         const float mx = fmaxf(fmaxf(x.red[st], x.red[C::kNmax + st]),
                                fmaxf(x.red[2 * C::kNmax + st], x.red[3 * C::kNmax + st]));
@@ -452,7 +487,7 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
         x.alpha[st] = mn == -INFINITY ? 1.f : ex2(mo - mn);
         x.m_used[st] = mn;
       }
-      group_sync();
+      group_sync<NT>();
 #pragma unroll
       for (int i = 0; i < NH; ++i) lsum[i] *= x.alpha[c0 + i];
     }
@@ -473,13 +508,13 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
 #pragma unroll
       for (int blk = 0; blk < C::kOBlocks; ++blk) {
 #pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) {
-          float v[8];
-          tmem_ld8(tl_o + blk * C::kNmax + c0 + ch * 8, v);
+        for (int ch = 0; ch < NCK; ++ch) {
+          float v[KC];
+          tmem_ldk<KC>(tl_o + blk * C::kNmax + c0 + ch * KC, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 8; ++e) v[e] *= x.alpha[c0 + ch * 8 + e];
-          tmem_st8(tl_o + blk * C::kNmax + c0 + ch * 8, v);
+          for (int e = 0; e < KC; ++e) v[e] *= x.alpha[c0 + ch * KC + e];
+          tmem_stk<KC>(tl_o + blk * C::kNmax + c0 + ch * KC, v);
         }
       }
       tmem_wait_st();
@@ -522,7 +557,7 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
   // ---------------------------------------------------------- epilogue
   if (alive && x.ntiles > 0) alive = bar_wait(x.pv_done, (x.ntiles - 1) & 1, x.abort_flag, a.status);
   fence_after();
-  if (group_or(!alive)) return;
+  if (group_or<NT>(!alive)) return;
   // column sums of the per-token partial denominators
 #pragma unroll
   for (int i = 0; i < NH; ++i) {
@@ -531,7 +566,7 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
     for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
     if (lane == 0) x.red[sw * C::kNmax + c0 + i] = v;
   }
-  group_sync();
+  group_sync<NT>();
   if (st < M) {
     const float lt = x.red[st] + x.red[C::kNmax + st] + x.red[2 * C::kNmax + st] + x.red[3 * C::kNmax + st];
     x.linv[st] = lt > 0.f ? v_final / lt : 0.f;
@@ -544,18 +579,18 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
       a.part_lse[((int64_t)x.split * a.rows_cap + row) * a.hq + head] = lse2;
     }
   }
-  group_sync();
+  group_sync<NT>();
 #pragma unroll
   for (int blk = 0; blk < C::kOBlocks; ++blk) {
     const int d = blk * 128 + r;
 #pragma unroll
-    for (int ch = 0; ch < NCH; ++ch) {
-      float v[8];
-      tmem_ld8(tl_o + blk * C::kNmax + c0 + ch * 8, v);
+    for (int ch = 0; ch < NCK; ++ch) {
+      float v[KC];
+      tmem_ldk<KC>(tl_o + blk * C::kNmax + c0 + ch * KC, v);
       tmem_wait_ld();
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int n = c0 + ch * 8 + e;
+      for (int e = 0; e < KC; ++e) {
+        const int n = c0 + ch * KC + e;
         if (n < M) {
           const float o = v[e] * x.linv[n];
           const int64_t row = x.q0 + n / hpc;
@@ -572,7 +607,7 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
 }
 
 template <int D, int KVT, int QT, int SMODE, int NMAX>
-__global__ void __launch_bounds__(kTcThreads, (NMAX <= 16 ? 2 : 1))
+__global__ void __launch_bounds__(64 + 32 * (NMAX <= 16 ? 8 : 16), (NMAX <= 16 ? 2 : 1))
     stage1_tc(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
               const __grid_constant__ CUtensorMap tmv) {
   using C = TcCfg<D, KVT, QT, SMODE, NMAX>;
@@ -651,11 +686,11 @@ __global__ void __launch_bounds__(kTcThreads, (NMAX <= 16 ? 2 : 1))
     }
     bar_init(s_full, 1);
     bar_init(s_full + 1, 1);
-    bar_init(s_free, kSmThreads);
-    bar_init(s_free + 1, kSmThreads);
-    bar_init(p_full, kSmThreads);
+    bar_init(s_free, C::kSmThreads);
+    bar_init(s_free + 1, C::kSmThreads);
+    bar_init(p_full, C::kSmThreads);
     bar_init(pv_done, 1);
-    bar_init(q_ready, kSmThreads);
+    bar_init(q_ready, C::kSmThreads);
     bar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -811,12 +846,12 @@ __global__ void __launch_bounds__(kTcThreads, (NMAX <= 16 ? 2 : 1))
     }
   } else {
     // ========================================= softmax / epilogue warps
-    const int st = tid - 64;  // 0..255
-    const int sw = warp - 2;  // 0..7 softmax warp index
+    const int st = tid - 64;  // 0..kSmThreads-1
+    const int sw = warp - 2;  // softmax warp index
     // ---- query operand Q^T (K-major, 128-byte swizzle), rows n < N (zero past M)
     if constexpr (!C::kQSplit) {
       constexpr int kRowChunks = D * C::kElt / 16;  // 16-byte pieces of one query row
-      for (int idx = st; idx < N * kRowChunks; idx += kSmThreads) {
+      for (int idx = st; idx < N * kRowChunks; idx += C::kSmThreads) {
         const int n = idx / kRowChunks, cch = idx % kRowChunks;
         uint4 v = make_uint4(0, 0, 0, 0);
         if (n < M) {
@@ -831,7 +866,7 @@ __global__ void __launch_bounds__(kTcThreads, (NMAX <= 16 ? 2 : 1))
     } else {
       // bf16 query row -> Q * 2^a = Q1 + Q2/16 + Q3/256 in E4M3, rows n, N + n, 2N + n
       constexpr int kPer = D / 32;  // elements per lane (8 or 4)
-      for (int n = sw; n < N; n += 8) {
+      for (int n = sw; n < N; n += C::kSmWarps) {
         float xv[kPer];
         if (n < M) {
           const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(a.q) +
@@ -890,7 +925,7 @@ __global__ void __launch_bounds__(kTcThreads, (NMAX <= 16 ? 2 : 1))
     }
     fence_async_smem();
     bar_arrive(q_ready);
-    group_sync();  // colscale visible to the whole group
+    group_sync<C::kSmThreads>();  // colscale visible to the whole group
 
     SoftmaxCtx x;
     x.p_s = p_s;
@@ -1078,6 +1113,8 @@ int tc_smem_bytes(const pda_plan_t* p) { return tc_select(p, p->rows_per_cta, Ge
 
 int tc_ctas_per_sm(const pda_plan_t* p) { return p->rows_per_cta <= 16 ? 2 : 1; }
 
+static unsigned tc_threads(const pda_plan_t* p) { return p->rows_per_cta <= 16 ? 64 + 256 : 64 + 512; }
+
 int launch_stage1_tc(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_t s) {
   DecodeArgs a = args;
   CUtensorMap mk, mv;
@@ -1095,7 +1132,7 @@ int launch_stage1_tc(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(plan->grid_ctas));
-  cfg.blockDim = dim3(kTcThreads);
+  cfg.blockDim = dim3(tc_threads(plan));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   if (cudaLaunchKernelEx(&cfg, k1, a, mk, mv) != cudaSuccess) {

@@ -17,8 +17,10 @@
 // OCP E4M3 caches run kind::f8f6f4 MMAs on the codes as they sit in shared
 // memory (no widening pass). For E4M3 the other operand is written as E4M3
 // terms: P = P1 + P2 (P2 the E4M3 residual of P1, about 8 significant bits
-// together), and a bf16 query as Q * 2^a = Q1 + Q2/16 + Q3/256 (stacked on N,
-// exact to ~2^-12 of the row's largest element). V is read MN-major straight
+// together), and a bf16 query as Q * 2^a = Q1 + Q2/16 (stacked on N): a bf16
+// value has 8 significant bits, Q1 holds 4 and the residual the other 4, so
+// the split is exact except for residuals below E4M3's normal range (an
+// absolute error under 2^-22 of the row's largest element). V is read MN-major straight
 // from its [token][d] tile, so no transpose is needed on this hardware. The
 // softmax denominator always sums the exact fp32 probabilities.
 //
@@ -292,8 +294,8 @@ struct TcCfg {
   static constexpr int kThreads = 64 + kSmThreads;
   static constexpr int kColGroups = kSmWarps / 4;   // warps sharing a lane quadrant
   static constexpr bool kF8 = KVT == PDA_E4M3;
-  static constexpr bool kQSplit = kF8 && QT == PDA_BF16;  // bf16 query as three E4M3 terms
-  static constexpr int kQTerms = kQSplit ? 3 : 1;
+  static constexpr bool kQSplit = kF8 && QT == PDA_BF16;  // bf16 query as two E4M3 terms
+  static constexpr int kQTerms = kQSplit ? 2 : 1;
   static constexpr int kElt = kF8 ? 1 : 2;
   static constexpr int kAtom = 128 / kElt;           // elements per 128-byte row
   static constexpr int kChunks = D / kAtom;          // ring slots per K (or V) tile
@@ -387,20 +389,30 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
   for (int i = 0; i < NH; ++i) lsum[i] = 0.f;
   bool alive = true;
 
+  // per-token scales of this thread's key, fetched one tile ahead
+  float ks_next = 0.f, vs_next = 1.f;
+  auto fetch_scales = [&](int j, float& ks, float& vs) {
+    ks = 0.f;
+    vs = 1.f;
+    const int tok = x.t_begin + j * kTok + r;
+    if (j < x.ntiles && tok < x.t_end) {
+      const int page = __ldg(x.ptab + tok / x.P);
+      if (page >= 0 && page < a.num_pages) {
+        const int64_t sidx = ((int64_t)page * x.P + tok % x.P) * a.hkv + x.hkv;
+        ks = __ldg(a.k_scale + sidx);
+        vs = __ldg(a.v_scale + sidx);
+      }
+    }
+  };
+  if constexpr (SMODE == PDA_SCALE_TOKEN_HEAD) fetch_scales(0, ks_next, vs_next);
+
   for (int j = 0; j < x.ntiles; ++j) {
     const int tok = x.t_begin + j * kTok + r;
-    // per-token scales of this thread's key (loaded before waiting on S)
     float row_scale = qk_scale, log2_vs = 0.f, inv_vs = 1.f;
     if constexpr (SMODE == PDA_SCALE_TOKEN_HEAD) {
-      float ks = 0.f, vs = 1.f;
-      if (tok < x.t_end) {
-        const int page = __ldg(x.ptab + tok / x.P);
-        if (page >= 0 && page < a.num_pages) {
-          const int64_t sidx = ((int64_t)page * x.P + tok % x.P) * a.hkv + x.hkv;
-          ks = __ldg(a.k_scale + sidx);
-          vs = __ldg(a.v_scale + sidx);
-        }
-      }
+      const float ks = ks_next;
+      float vs = vs_next;
+      fetch_scales(j + 1, ks_next, vs_next);
       row_scale *= ks;
       vs = vs > 0.f ? vs : 1.f;
       log2_vs = __log2f(vs);
@@ -433,14 +445,12 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
         float v[KC];
         tmem_ldk<KC>(scol + ch * KC, v);
         if constexpr (C::kQSplit) {
-          float v2[KC], v3[KC];
+          float v2[KC];
           tmem_ldk<KC>(scol + N + ch * KC, v2);
-          tmem_ldk<KC>(scol + 2 * N + ch * KC, v3);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < KC; ++e)
-            s[ch * KC + e] =
-                (v[e] + v2[e] * 0.0625f + v3[e] * 0.00390625f) * x.colscale[c0 + ch * KC + e];
+            s[ch * KC + e] = fmaf(v2[e], 0.0625f, v[e]) * x.colscale[c0 + ch * KC + e];
         } else {
           tmem_wait_ld();
 #pragma unroll
@@ -864,7 +874,7 @@ __global__ void __launch_bounds__(64 + 32 * (NMAX <= 16 ? 8 : 16), (NMAX <= 16 ?
         *reinterpret_cast<uint4*>(q_s + (byte / 128) * C::kQAtomBytes + sw128(n, byte % 128)) = v;
       }
     } else {
-      // bf16 query row -> Q * 2^a = Q1 + Q2/16 + Q3/256 in E4M3, rows n, N + n, 2N + n
+      // bf16 query row -> Q * 2^a = Q1 + Q2/16 in E4M3, rows n and N + n
       constexpr int kPer = D / 32;  // elements per lane (8 or 4)
       for (int n = sw; n < N; n += C::kSmWarps) {
         float xv[kPer];
@@ -891,12 +901,12 @@ __global__ void __launch_bounds__(64 + 32 * (NMAX <= 16 ? 8 : 16), (NMAX <= 16 ?
         while (ex > -126 && amax * exp2f(static_cast<float>(ex)) > 448.f) --ex;
         const float up = exp2f(static_cast<float>(ex));
         if (lane == 0) colscale[n] = 1.f / up;
-        uint8_t codes[3][kPer];
+        uint8_t codes[2][kPer];
 #pragma unroll
         for (int e = 0; e < kPer; e += 2) {
           float v0 = xv[e] * up, v1 = xv[e + 1] * up;
 #pragma unroll
-          for (int t = 0; t < 3; ++t) {
+          for (int t = 0; t < 2; ++t) {
             const uint16_t c2 = f2_to_e4m3x2(v0, v1);
             const float2 back = e4m3x2_to_f2(c2);
             codes[t][e] = static_cast<uint8_t>(c2 & 0xFF);
@@ -907,7 +917,7 @@ __global__ void __launch_bounds__(64 + 32 * (NMAX <= 16 ? 8 : 16), (NMAX <= 16 ?
         }
         const int byte = lane * kPer;  // d of this lane's first element (1 byte each)
 #pragma unroll
-        for (int t = 0; t < 3; ++t) {
+        for (int t = 0; t < 2; ++t) {
           uint8_t* dst = q_s + (byte / 128) * C::kQAtomBytes + sw128(t * N + n, byte % 128);
           if constexpr (kPer == 8) {
             uint2 w;

@@ -63,6 +63,26 @@ __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t b) {
   return r * 128u + ((((b >> 4) ^ r) & 7u) << 4) + (b & 15u);
 }
 
+// NB bytes (a multiple of 4, packed little-endian in `w`) at byte b0 of row
+// r of a 128-byte-swizzled buffer; b0 is a multiple of NB's alignment (16,
+// 8 or 4), so no store crosses a 16-byte chunk.
+template <int NB>
+__device__ __forceinline__ void store_row(uint8_t* base, int r, int b0, const uint32_t* w) {
+  if constexpr (NB % 16 == 0) {
+#pragma unroll
+    for (int q = 0; q < NB / 16; ++q)
+      *reinterpret_cast<uint4*>(base + sw128(r, b0 + 16 * q)) =
+          make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  } else if constexpr (NB % 8 == 0) {
+#pragma unroll
+    for (int q = 0; q < NB / 8; ++q)
+      *reinterpret_cast<uint2*>(base + sw128(r, b0 + 8 * q)) = make_uint2(w[2 * q], w[2 * q + 1]);
+  } else {
+#pragma unroll
+    for (int q = 0; q < NB / 4; ++q) *reinterpret_cast<uint32_t*>(base + sw128(r, b0 + 4 * q)) = w[q];
+  }
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (sm_100 family format).
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
@@ -70,9 +90,11 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
 }
 
 // Instruction descriptor: f32 accumulate, A/B format `fmt` (kind::f16: 1 =
-// bf16; kind::f8f6f4: 0 = E4M3), A MN-major if `a_mn`, M = 128, N = n.
-__device__ __forceinline__ uint32_t idesc(uint32_t fmt, uint32_t a_mn, uint32_t n) {
-  return (1u << 4) | (fmt << 7) | (fmt << 10) | (a_mn << 15) | ((n >> 3) << 17) |
+// bf16; kind::f8f6f4: 0 = E4M3), A (B) MN-major if `a_mn` (`b_mn`), M = 128,
+// N = n.
+__device__ __forceinline__ uint32_t idesc(uint32_t fmt, uint32_t a_mn, uint32_t n,
+                                          uint32_t b_mn = 0) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | (a_mn << 15) | (b_mn << 16) | ((n >> 3) << 17) |
          ((128u >> 4) << 24);
 }
 
@@ -291,7 +313,13 @@ struct TcCfg {
   // softmax warps: 4 per TMEM lane quadrant when a CTA holds up to 64 columns, else 2
   static constexpr int kSmWarps = NMAX <= 16 ? 8 : 16;
   static constexpr int kSmThreads = 32 * kSmWarps;
-  static constexpr int kThreads = 64 + kSmThreads;
+  // TMA producer warps (warp 0, then warps after the softmax warps): one warp
+  // issues a 16-row page box about every 130 cycles, too few for one CTA
+  // per SM on small pages, so the 64-column build splits each chunk's
+  // boxes over two warps
+  static constexpr int kProducers = NMAX > 16 ? 2 : 1;
+  static constexpr int kProdWarp1 = 2 + kSmWarps;
+  static constexpr int kThreads = 64 + kSmThreads + 32 * (kProducers - 1);
   static constexpr int kColGroups = kSmWarps / 4;   // warps sharing a lane quadrant
   static constexpr bool kF8 = KVT == PDA_E4M3;
   static constexpr bool kQSplit = kF8 && QT == PDA_BF16;  // bf16 query as two E4M3 terms
@@ -303,11 +331,21 @@ struct TcCfg {
   static constexpr int kQRows = kNmax * kQTerms;
   static constexpr int kQAtomBytes = kQRows * 128;
   static constexpr int kQBytes = kChunks * kQAtomBytes;
-  static constexpr int kPAtomBytes = kNmax * 128;    // [64 rows x 128 B]
-  static constexpr int kPBytes = 2 * kPAtomBytes;    // bf16: 2 token halves; E4M3: 2 terms
+  // P^T operand of PV. K-major: rows n (bf16: two 64-token halves; E4M3: the
+  // two terms' rows stacked, 16 + 16). MN-major (E4M3, up to 64 columns):
+  // one 128-byte row per token holding term 1 then term 2 of every column,
+  // so a thread stores its columns with wide stores. One buffer: the PV
+  // issuer starts as soon as P is written, long before the next P is due.
+  static constexpr bool kPMn = kF8 && NMAX > 16;
+  static constexpr int kPBufs = 1;
+  static constexpr int kPAtomBytes = kNmax * 128;    // [kNmax rows x 128 B]
+  static constexpr int kPBufBytes = kPMn ? kTok * 128 : 2 * kPAtomBytes;
+  static constexpr int kPBytes = kPBufs * kPBufBytes;
   static constexpr int kOBlocks = D / 128;
+  // E4M3: one PV MMA of N = 2 x columns yields both terms' sums side by side
+  static constexpr int kOCols = kF8 ? 2 * kNmax : kNmax;  // TMEM columns per O block
   static constexpr int kSCols = kQRows;              // TMEM columns per S buffer
-  static constexpr int kTmemNeed = 2 * kSCols + kOBlocks * kNmax;
+  static constexpr int kTmemNeed = 2 * kSCols + kOBlocks * kOCols;
   static constexpr int kTmemCols =
       kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
   static_assert(kTmemNeed <= 512, "TMEM budget");
@@ -322,11 +360,12 @@ struct TcCfg {
 };
 
 // Position of a tile's K or V unit (kChunks ring slots each) in the order
-// the MMA issuer consumes them: K0, K1, then V_j followed by K_{j+2} for
-// j = 0, 1, ... -- S^T runs two tiles ahead of PV. The producer loads in the
-// same order, so the ring is a plain FIFO.
-__device__ __forceinline__ int unit_pos_k(int j) { return j < 2 ? j : 2 * j - 1; }
-__device__ __forceinline__ int unit_pos_v(int j, int n) { return j <= n - 2 ? 2 + 2 * j : 2 * n - 1; }
+// the MMA issuer consumes them: K0, K1, then K_{j+2} followed by V_j for
+// j = 0, 1, ... -- S^T of tile j + 2 is issued as soon as the softmax has
+// read S^T of tile j, before PV of tile j, so the softmax never waits on a
+// PV. The producer loads in the same order, so the ring is a plain FIFO.
+__device__ __forceinline__ int unit_pos_k(int j) { return j < 2 ? j : 2 * j - 2; }
+__device__ __forceinline__ int unit_pos_v(int j, int n) { return min(j + 3, n) + j; }
 
 // Everything the softmax / epilogue warps need from the CTA prologue.
 struct SoftmaxCtx {
@@ -389,22 +428,30 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
   for (int i = 0; i < NH; ++i) lsum[i] = 0.f;
   bool alive = true;
 
-  // per-token scales of this thread's key, fetched one tile ahead
-  float ks_next = 0.f, vs_next = 1.f;
-  auto fetch_scales = [&](int j, float& ks, float& vs) {
+  // per-token scales of this thread's key: the page id is loaded two tiles
+  // ahead and the scales one tile ahead, so the loop never waits on a load
+  // whose address depends on another load
+  auto page_for = [&](int jj) -> int {
+    const int tok = x.t_begin + jj * kTok + r;
+    return (jj < x.ntiles && tok < x.t_end) ? __ldg(x.ptab + tok / x.P) : -1;
+  };
+  auto scales_for = [&](int jj, int page, float& ks, float& vs) {
     ks = 0.f;
     vs = 1.f;
-    const int tok = x.t_begin + j * kTok + r;
-    if (j < x.ntiles && tok < x.t_end) {
-      const int page = __ldg(x.ptab + tok / x.P);
-      if (page >= 0 && page < a.num_pages) {
-        const int64_t sidx = ((int64_t)page * x.P + tok % x.P) * a.hkv + x.hkv;
-        ks = __ldg(a.k_scale + sidx);
-        vs = __ldg(a.v_scale + sidx);
-      }
+    const int tok = x.t_begin + jj * kTok + r;
+    if (page >= 0 && page < a.num_pages && jj < x.ntiles && tok < x.t_end) {
+      const int64_t sidx = ((int64_t)page * x.P + tok % x.P) * a.hkv + x.hkv;
+      ks = __ldg(a.k_scale + sidx);
+      vs = __ldg(a.v_scale + sidx);
     }
   };
-  if constexpr (SMODE == PDA_SCALE_TOKEN_HEAD) fetch_scales(0, ks_next, vs_next);
+  float ks_next = 0.f, vs_next = 1.f;  // scales of the tile about to start
+  int pg_ahead = -1;                   // page of the tile after it
+  if constexpr (SMODE == PDA_SCALE_TOKEN_HEAD) {
+    const int pg0 = page_for(0);
+    pg_ahead = page_for(1);
+    scales_for(0, pg0, ks_next, vs_next);
+  }
 
   for (int j = 0; j < x.ntiles; ++j) {
     const int tok = x.t_begin + j * kTok + r;
@@ -412,7 +459,8 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
     if constexpr (SMODE == PDA_SCALE_TOKEN_HEAD) {
       const float ks = ks_next;
       float vs = vs_next;
-      fetch_scales(j + 1, ks_next, vs_next);
+      scales_for(j + 1, pg_ahead, ks_next, vs_next);
+      pg_ahead = page_for(j + 2);
       row_scale *= ks;
       vs = vs > 0.f ? vs : 1.f;
       log2_vs = __log2f(vs);
@@ -509,22 +557,33 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
       s[i] = ex2(s[i] - mu);
       lsum[i] += s[i] * inv_vs;
     }
-    // P buffer and O are free once the previous tile's PV has finished
-    if (j >= 1) alive = bar_wait(x.pv_done, (j - 1) & 1, x.abort_flag, a.status);
+    // this tile's P buffer is free once PV of tile j - kPBufs has finished;
+    // O (rescaled when the vote fired) once PV of tile j - 1 has. A commit
+    // covers every earlier MMA, and no barrier can run a phase ahead: the
+    // next PV on it needs the P this thread has not written yet.
+    {
+      const int need = fired ? j - 1 : j - C::kPBufs;
+      if (need >= 0)
+        alive = bar_wait(x.pv_done + (need & 1), (need >> 1) & 1, x.abort_flag, a.status);
+    }
     alive = __all_sync(0xffffffffu, alive);
     fence_after();
     if (alive && fired && j >= 1) {
-      // rescale O^T (this thread's d row) by alpha per column
+      // rescale O^T (this thread's d row) by alpha per column (E4M3: both terms)
 #pragma unroll
       for (int blk = 0; blk < C::kOBlocks; ++blk) {
 #pragma unroll
-        for (int ch = 0; ch < NCK; ++ch) {
-          float v[KC];
-          tmem_ldk<KC>(tl_o + blk * C::kNmax + c0 + ch * KC, v);
-          tmem_wait_ld();
+        for (int half = 0; half < (kF8 ? 2 : 1); ++half) {
 #pragma unroll
-          for (int e = 0; e < KC; ++e) v[e] *= x.alpha[c0 + ch * KC + e];
-          tmem_stk<KC>(tl_o + blk * C::kNmax + c0 + ch * KC, v);
+          for (int ch = 0; ch < NCK; ++ch) {
+            const uint32_t col = tl_o + blk * C::kOCols + half * N + c0 + ch * KC;
+            float v[KC];
+            tmem_ldk<KC>(col, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < KC; ++e) v[e] *= x.alpha[c0 + ch * KC + e];
+            tmem_stk<KC>(col, v);
+          }
         }
       }
       tmem_wait_st();
@@ -540,21 +599,40 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
         for (int e = 0; e < 8; ++e) row[e] = make_uint4(0, 0, 0, 0);
       }
     }
-    // write P^T (K-major, 128-byte swizzle)
+    // write P^T (128-byte swizzle)
+    uint8_t* pb = x.p_s + (j % C::kPBufs) * C::kPBufBytes;
     if constexpr (kF8) {
+      // P = P1 + P2 in E4M3 (P2 the rounding residual of P1)
+      uint32_t w1[NH / 4], w2[NH / 4];
 #pragma unroll
       for (int i = 0; i < NH; i += 2) {
-        const int n = c0 + i;
         const uint16_t c1 = f2_to_e4m3x2(s[i], s[i + 1]);
         const float2 f1 = e4m3x2_to_f2(c1);
         const uint16_t c2 = f2_to_e4m3x2(s[i] - f1.x, s[i + 1] - f1.y);
-        x.p_s[sw128(n, r)] = static_cast<uint8_t>(c1 & 0xFF);
-        x.p_s[sw128(n + 1, r)] = static_cast<uint8_t>(c1 >> 8);
-        x.p_s[C::kPAtomBytes + sw128(n, r)] = static_cast<uint8_t>(c2 & 0xFF);
-        x.p_s[C::kPAtomBytes + sw128(n + 1, r)] = static_cast<uint8_t>(c2 >> 8);
+        if constexpr (C::kPMn) {
+          if ((i & 2) == 0) {
+            w1[i >> 2] = c1;
+            w2[i >> 2] = c2;
+          } else {
+            w1[i >> 2] |= static_cast<uint32_t>(c1) << 16;
+            w2[i >> 2] |= static_cast<uint32_t>(c2) << 16;
+          }
+        } else {
+          // K-major: term t of column n in row t * N + n, this token's byte
+          const int n = c0 + i;
+          pb[sw128(n, r)] = static_cast<uint8_t>(c1 & 0xFF);
+          pb[sw128(n + 1, r)] = static_cast<uint8_t>(c1 >> 8);
+          pb[N * 128 + sw128(n, r)] = static_cast<uint8_t>(c2 & 0xFF);
+          pb[N * 128 + sw128(n + 1, r)] = static_cast<uint8_t>(c2 >> 8);
+        }
+      }
+      if constexpr (C::kPMn) {
+        // MN-major: this token's row, term 1 at byte c0, term 2 at byte N + c0
+        store_row<NH>(pb, r, c0, w1);
+        store_row<NH>(pb, r, N + c0, w2);
       }
     } else {
-      uint8_t* pbase = x.p_s + (r >> 6) * C::kPAtomBytes;
+      uint8_t* pbase = pb + (r >> 6) * C::kPAtomBytes;
       const uint32_t byte = static_cast<uint32_t>(r & 63) * 2u;
 #pragma unroll
       for (int i = 0; i < NH; ++i)
@@ -562,10 +640,12 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
     }
     fence_async_smem();
     fence_before();
-    bar_arrive(x.p_full);
+    bar_arrive(x.p_full + (j & 1));
   }
   // ---------------------------------------------------------- epilogue
-  if (alive && x.ntiles > 0) alive = bar_wait(x.pv_done, (x.ntiles - 1) & 1, x.abort_flag, a.status);
+  if (alive && x.ntiles > 0)
+    alive = bar_wait(x.pv_done + ((x.ntiles - 1) & 1), ((x.ntiles - 1) >> 1) & 1, x.abort_flag,
+                     a.status);
   fence_after();
   if (group_or<NT>(!alive)) return;
   // column sums of the per-token partial denominators
@@ -596,8 +676,16 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
 #pragma unroll
     for (int ch = 0; ch < NCK; ++ch) {
       float v[KC];
-      tmem_ldk<KC>(tl_o + blk * C::kNmax + c0 + ch * KC, v);
-      tmem_wait_ld();
+      tmem_ldk<KC>(tl_o + blk * C::kOCols + c0 + ch * KC, v);
+      if constexpr (kF8) {
+        float v2[KC];
+        tmem_ldk<KC>(tl_o + blk * C::kOCols + N + c0 + ch * KC, v2);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < KC; ++e) v[e] += v2[e];
+      } else {
+        tmem_wait_ld();
+      }
 #pragma unroll
       for (int e = 0; e < KC; ++e) {
         const int n = c0 + ch * KC + e;
@@ -617,7 +705,8 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
 }
 
 template <int D, int KVT, int QT, int SMODE, int NMAX>
-__global__ void __launch_bounds__(64 + 32 * (NMAX <= 16 ? 8 : 16), (NMAX <= 16 ? 2 : 1))
+__global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
+                                  TcCfg<D, KVT, QT, SMODE, NMAX>::kCtasPerSm)
     stage1_tc(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
               const __grid_constant__ CUtensorMap tmv) {
   using C = TcCfg<D, KVT, QT, SMODE, NMAX>;
@@ -634,9 +723,9 @@ __global__ void __launch_bounds__(64 + 32 * (NMAX <= 16 ? 8 : 16), (NMAX <= 16 ?
   uint64_t* empty = full + R_;
   uint64_t* s_full = empty + R_;
   uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_free + 2;
-  uint64_t* pv_done = p_full + 1;
-  uint64_t* q_ready = pv_done + 1;
+  uint64_t* p_full = s_free + 2;   // [2]: P of tile j complete, by j & 1
+  uint64_t* pv_done = p_full + 2;  // [2]: PV of tile j complete, by j & 1
+  uint64_t* q_ready = pv_done + 2;
   uint64_t* drain = q_ready + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -691,7 +780,7 @@ __global__ void __launch_bounds__(64 + 32 * (NMAX <= 16 ? 8 : 16), (NMAX <= 16 ?
   // ---- setup: barriers, TMEM, running maxima
   if (tid == 0) {
     for (int s = 0; s < R_; ++s) {
-      bar_init(full + s, 1);
+      bar_init(full + s, C::kProducers);
       bar_init(empty + s, 1);
     }
     bar_init(s_full, 1);
@@ -699,7 +788,9 @@ __global__ void __launch_bounds__(64 + 32 * (NMAX <= 16 ? 8 : 16), (NMAX <= 16 ?
     bar_init(s_free, C::kSmThreads);
     bar_init(s_free + 1, C::kSmThreads);
     bar_init(p_full, C::kSmThreads);
+    bar_init(p_full + 1, C::kSmThreads);
     bar_init(pv_done, 1);
+    bar_init(pv_done + 1, 1);
     bar_init(q_ready, C::kSmThreads);
     bar_init(drain, 1);
     *abort_flag = 0;
@@ -722,27 +813,39 @@ __global__ void __launch_bounds__(64 + 32 * (NMAX <= 16 ? 8 : 16), (NMAX <= 16 ?
   const uint32_t tmem = *tmem_slot;
   const uint32_t tmem_o = tmem + 2 * C::kSCols;
 
-  if (warp == 0) {
-    // ================================================= TMA producer warp
+  if (warp == 0 || (warp >= C::kProdWarp1 && warp < C::kProdWarp1 + C::kProducers - 1)) {
+    // ================================================ TMA producer warps
+    // producer pw issues boxes pw, pw + kProducers, ... of every chunk and
+    // arrives on the chunk's full barrier with its own byte count
+    const int pw = warp == 0 ? 0 : warp - C::kProdWarp1 + 1;
     const int box_rows = P < kTok ? P : kTok;
     const int nbox = kTok / box_rows;  // <= 16 (P >= 8)
+    const int bx = pw + lane * C::kProducers;  // this lane's box within a chunk
     const uint32_t box_bytes = static_cast<uint32_t>(box_rows) * 128u;
     const CUtensorMap* maps[2] = {&tmk, &tmv};
-    // this lane's box of tile j: page id and first slot (false: nothing to load)
+    // this lane's box of tile j: page id (loaded now, checked when used, so
+    // the warp never waits on the load) and first slot; false: no box
     auto page_of = [&](int j, int& page, int& slot0) -> bool {
-      const int tb = t_begin + j * kTok + lane * box_rows;
-      if (j >= ntiles || lane >= nbox || tb >= t_end) return false;
+      const int tb = t_begin + j * kTok + bx * box_rows;
+      if (j >= ntiles || bx >= nbox || tb >= t_end) return false;
       page = __ldg(ptab + tb / P);
       slot0 = tb % P;
-      if (page < 0 || page >= a.num_pages) {
+      return true;
+    };
+    auto checked = [&](bool want, int page) -> bool {
+      if (want && (page < 0 || page >= a.num_pages)) {
         atomicOr(a.status, PDA_STATUS_PAGE_OOB);
         return false;
       }
-      return true;
+      return want;
     };
-    // page ids of tiles j, j+1, j+2 (rotated as V_j and K_{j+2} are emitted)
-    int pg0 = 0, s00 = 0, pg1 = 0, s01 = 0, pg2 = 0, s02 = 0;
-    bool ok0 = page_of(0, pg0, s00), ok1 = page_of(1, pg1, s01), ok2 = page_of(2, pg2, s02);
+    // page ids of tiles j .. j+3 (rotated as K_{j+2} and V_j are emitted);
+    // tile j+4's is loaded two tiles before its check
+    int pg0 = 0, s00 = 0, pg1 = 0, s01 = 0, pg2 = 0, s02 = 0, pg3 = 0, s03 = 0;
+    bool ok0 = page_of(0, pg0, s00), ok1 = page_of(1, pg1, s01), ok2 = page_of(2, pg2, s02),
+         ok3 = page_of(3, pg3, s03);
+    ok0 = checked(ok0, pg0);
+    ok1 = checked(ok1, pg1);
     uint32_t g = 0;
     bool alive = true;
     auto emit = [&](int kind, bool ok, int pg, int s0) {
@@ -760,7 +863,7 @@ __global__ void __launch_bounds__(64 + 32 * (NMAX <= 16 ? 8 : 16), (NMAX <= 16 ?
           break;
         }
         if (ok) {
-          const uint32_t dst = su32(ring + slot * kSlot) + lane * box_bytes;
+          const uint32_t dst = su32(ring + slot * kSlot) + bx * box_bytes;
           const int c1 = a.tma_slot_dim == 1 ? s0 : hkv;
           const int c2 = a.tma_slot_dim == 1 ? hkv : s0;
           tma_load(dst, maps[kind], c * C::kAtom, c1, c2, pg, full + slot);
@@ -770,11 +873,15 @@ __global__ void __launch_bounds__(64 + 32 * (NMAX <= 16 ? 8 : 16), (NMAX <= 16 ?
     emit(0, ok0, pg0, s00);
     if (ntiles > 1) emit(0, ok1, pg1, s01);
     for (int j = 0; j < ntiles && alive; ++j) {
+      if (j + 2 < ntiles) {
+        ok2 = checked(ok2, pg2);
+        emit(0, ok2, pg2, s02);                     // K_{j+2}
+      }
       emit(1, ok0, pg0, s00);                       // V_j
-      if (j + 2 < ntiles) emit(0, ok2, pg2, s02);   // K_{j+2}
       pg0 = pg1; s00 = s01; ok0 = ok1;
       pg1 = pg2; s01 = s02; ok1 = ok2;
-      ok2 = page_of(j + 3, pg2, s02);
+      pg2 = pg3; s02 = s03; ok2 = ok3;
+      ok3 = page_of(j + 4, pg3, s03);
     }
     // drain: every box issued must have landed before the CTA can exit
     if (lane == 0) {
@@ -788,7 +895,8 @@ __global__ void __launch_bounds__(64 + 32 * (NMAX <= 16 ? 8 : 16), (NMAX <= 16 ?
       fence_after();
       const uint32_t fmt = kF8 ? 0u : 1u;
       const uint32_t id_s = idesc(fmt, 0, static_cast<uint32_t>(Nq));
-      const uint32_t id_p = idesc(fmt, 1, static_cast<uint32_t>(N));
+      // E4M3: N = both P terms' columns; bf16: N columns
+      const uint32_t id_p = idesc(fmt, 1, static_cast<uint32_t>(kF8 ? 2 * N : N), C::kPMn ? 1u : 0u);
       const uint32_t q_addr = su32(q_s), p_addr = su32(p_s), ring_addr = su32(ring);
       // S^T of tile j into TMEM buffer j & 1 (the softmax has freed it)
       auto issue_s = [&](int j) -> bool {
@@ -811,44 +919,48 @@ __global__ void __launch_bounds__(64 + 32 * (NMAX <= 16 ? 8 : 16), (NMAX <= 16 ?
         for (int c = 0; c < C::kChunks; ++c) mma_commit(empty + (gk + c) % R_);
         return true;
       };
-      if (alive) alive = issue_s(0);
-      if (alive && ntiles > 1) alive = issue_s(1);
-      for (int j = 0; j < ntiles && alive; ++j) {
-        // O^T += V_j^T P_j^T as soon as the softmax has written P_j
-        alive = bar_wait(p_full, j & 1, abort_flag, a.status);
-        fence_after();
-        if (!alive) break;
+      // O^T += V_j^T P_j^T as soon as the softmax has written P_j
+      auto issue_pv = [&](int j) -> bool {
+        if (!bar_wait(p_full + (j & 1), (j >> 1) & 1, abort_flag, a.status)) return false;
         const uint32_t gv = static_cast<uint32_t>(unit_pos_v(j, ntiles)) * C::kChunks;
-        for (int c = 0; c < C::kChunks && alive; ++c)
-          alive = bar_wait(full + (gv + c) % R_, ((gv + c) / R_) & 1u, abort_flag, a.status);
+        for (int c = 0; c < C::kChunks; ++c)
+          if (!bar_wait(full + (gv + c) % R_, ((gv + c) / R_) & 1u, abort_flag, a.status))
+            return false;
         fence_after();
-        if (!alive) break;
+        const uint32_t pbuf = p_addr + static_cast<uint32_t>(j % C::kPBufs) * C::kPBufBytes;
 #pragma unroll
         for (int blk = 0; blk < C::kOBlocks; ++blk) {
           if constexpr (kF8) {
-            // V block = one slot (128 d); P as two E4M3 terms, K = 32 tokens per MMA
+            // V block = one slot (128 d); K = 32 tokens per MMA; both P terms
+            // in one MMA (B rows 0..N-1 term 1, N..2N-1 term 2)
             const uint32_t vbase = ring_addr + ((gv + blk) % R_) * kSlot;
 #pragma unroll
-            for (int t = 0; t < 2; ++t)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma<true>(tmem_o + blk * C::kNmax, sdesc(vbase + kk * 4096, kSlot, 1024),
-                          sdesc(p_addr + t * C::kPAtomBytes + kk * 32, 16, 1024), id_p,
-                          !(j == 0 && t == 0 && kk == 0));
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bd = C::kPMn ? sdesc(pbuf + kk * 4096, 16384, 1024)
+                                          : sdesc(pbuf + kk * 32, 16, 1024);
+              mma<true>(tmem_o + blk * C::kOCols, sdesc(vbase + kk * 4096, kSlot, 1024), bd,
+                        id_p, !(j == 0 && kk == 0));
+            }
           } else {
             // V block = two adjacent slots (2 x 64 d); K = 16 tokens per MMA
             const uint32_t vbase = ring_addr + ((gv + 2 * blk) % R_) * kSlot;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma<false>(tmem_o + blk * C::kNmax, sdesc(vbase + kk * 2048, kSlot, 1024),
-                         sdesc(p_addr + (kk >> 2) * C::kPAtomBytes + (kk & 3) * 32, 16, 1024),
+              mma<false>(tmem_o + blk * C::kOCols, sdesc(vbase + kk * 2048, kSlot, 1024),
+                         sdesc(pbuf + (kk >> 2) * C::kPAtomBytes + (kk & 3) * 32, 16, 1024),
                          id_p, !(j == 0 && kk == 0));
           }
         }
-        mma_commit(pv_done);
+        mma_commit(pv_done + (j & 1));
         for (int c = 0; c < C::kChunks; ++c) mma_commit(empty + (gv + c) % R_);
-        // keep S two tiles ahead of the softmax
+        return true;
+      };
+      if (alive) alive = issue_s(0);
+      if (alive && ntiles > 1) alive = issue_s(1);
+      for (int j = 0; j < ntiles && alive; ++j) {
+        // S^T of tile j + 2 once the softmax has read tile j's buffer
         if (j + 2 < ntiles) alive = issue_s(j + 2);
+        if (alive) alive = issue_pv(j);
       }
       // make sure nothing issued is still running before TMEM is released
       mma_commit(drain);
@@ -1123,7 +1235,13 @@ int tc_smem_bytes(const pda_plan_t* p) { return tc_select(p, p->rows_per_cta, Ge
 
 int tc_ctas_per_sm(const pda_plan_t* p) { return p->rows_per_cta <= 16 ? 2 : 1; }
 
-static unsigned tc_threads(const pda_plan_t* p) { return p->rows_per_cta <= 16 ? 64 + 256 : 64 + 512; }
+struct GetThreads {
+  template <int D, int KVT, int QT, int SMODE, int NMAX>
+  int get() { return TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads; }
+};
+static unsigned tc_threads(const pda_plan_t* p) {
+  return static_cast<unsigned>(tc_select(p, p->rows_per_cta, GetThreads()));
+}
 
 int launch_stage1_tc(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_t s) {
   DecodeArgs a = args;

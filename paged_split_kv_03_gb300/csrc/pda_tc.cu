@@ -50,6 +50,9 @@ constexpr int kTok = 128;          // KV tokens per tile (MMA M of S^T)
 constexpr int kSlot = 16384;       // ring slot: [128 tokens x 128 bytes]
 constexpr float kTh = 8.0f;        // lazy rescale threshold, log2 units (P <= 2^8)
 constexpr float kLog2e = 1.4426950408889634f;
+// running maximum before any key: finite, so a column with no visible key
+// so far gives ex2(-inf - kMInit) = 0 rather than NaN
+constexpr float kMInit = -1.0e30f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // ------------------------------------------------------------------ helpers
@@ -316,8 +319,8 @@ struct TcCfg {
   // TMA producer warps (warp 0, then warps after the softmax warps): one warp
   // issues a 16-row page box about every 130 cycles, too few for one CTA
   // per SM on small pages, so the 64-column build splits each chunk's
-  // boxes over two warps
-  static constexpr int kProducers = NMAX > 16 ? 2 : 1;
+  // boxes over three warps
+  static constexpr int kProducers = NMAX > 16 ? 3 : 1;
   static constexpr int kProdWarp1 = 2 + kSmWarps;
   static constexpr int kThreads = 64 + kSmThreads + 32 * (kProducers - 1);
   static constexpr int kColGroups = kSmWarps / 4;   // warps sharing a lane quadrant
@@ -414,6 +417,7 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
   const int M = x.M, hpc = x.hpc, R = x.R;
 
   float qk_scale = a.sm_scale * kLog2e;  // logits in log2 units
+  if constexpr (C::kQSplit) qk_scale *= x.colscale[0];  // the query's 2^-a
   float v_final = 1.f;
   if constexpr (SMODE == PDA_SCALE_TENSOR) {
     qk_scale *= __ldg(a.k_scale);
@@ -477,10 +481,9 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
       }
     }
     const int tile0 = x.t_begin + j * kTok;
-    if (tile0 >= all_lo && tile0 + kTok - 1 <= all_hi) {
-      n_lo = 0;
-      n_hi = M;
-    }
+    // every real row sees every key of the tile: no mask (padding columns
+    // past M then hold finite values that are never written out)
+    const bool full = tile0 >= all_lo && tile0 + kTok - 1 <= all_hi;
 
     if (alive) alive = bar_wait(x.s_full + (j & 1), (j >> 1) & 1, x.abort_flag, a.status);
     alive = __all_sync(0xffffffffu, alive);
@@ -497,8 +500,7 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
           tmem_ldk<KC>(scol + N + ch * KC, v2);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < KC; ++e)
-            s[ch * KC + e] = fmaf(v2[e], 0.0625f, v[e]) * x.colscale[c0 + ch * KC + e];
+          for (int e = 0; e < KC; ++e) s[ch * KC + e] = fmaf(v2[e], 0.0625f, v[e]);
         } else {
           tmem_wait_ld();
 #pragma unroll
@@ -509,16 +511,39 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
     fence_before();
     bar_arrive(x.s_free + (j & 1));
 
-    // scale, mask, and the lazy-rescale vote
-    bool trig = false;
+    // scale, mask, and the lazy-rescale vote against this thread's running
+    // maxima (vector loads; they change only when a vote fires)
+    auto load_mu = [&](float* mu) {
 #pragma unroll
-    for (int i = 0; i < NH; ++i) {
-      const int n = c0 + i;
-      float v = s[i] * row_scale + log2_vs;
-      v = (n >= n_lo && n < n_hi) ? v : -INFINITY;
-      s[i] = v;
-      trig |= v > x.m_used[n] + kTh;
+      for (int i = 0; i < NH; i += 4) {
+        const float4 m4 = *reinterpret_cast<const float4*>(x.m_used + c0 + i);
+        mu[i] = m4.x;
+        mu[i + 1] = m4.y;
+        mu[i + 2] = m4.z;
+        mu[i + 3] = m4.w;
+      }
+    };
+    float dmax = -INFINITY;
+    {
+      float mu[NH];
+      load_mu(mu);
+      if (full) {
+#pragma unroll
+        for (int i = 0; i < NH; ++i) {
+          s[i] = fmaf(s[i], row_scale, log2_vs);
+          dmax = fmaxf(dmax, s[i] - mu[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < NH; ++i) {
+          const int n = c0 + i;
+          const float v = fmaf(s[i], row_scale, log2_vs);
+          s[i] = (n >= n_lo && n < n_hi) ? v : -INFINITY;
+          dmax = fmaxf(dmax, s[i] - mu[i]);
+        }
+      }
     }
+    const bool trig = dmax > kTh;
     // One barrier reduction per tile: the vote also carries failures, and a
     // second reduction (only when the first fired) tells them apart, so
     // every softmax thread takes the same branch.
@@ -541,21 +566,23 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
         const float mx = fmaxf(fmaxf(x.red[st], x.red[C::kNmax + st]),
                                fmaxf(x.red[2 * C::kNmax + st], x.red[3 * C::kNmax + st]));
         const float mo = x.m_used[st];
-        const float mn = fmaxf(mo, mx);
-        x.alpha[st] = mn == -INFINITY ? 1.f : ex2(mo - mn);
+        const float mn = fmaxf(mo, mx);  // finite: kMInit bounds it below
+        x.alpha[st] = ex2(mo - mn);
         x.m_used[st] = mn;
       }
       group_sync<NT>();
 #pragma unroll
       for (int i = 0; i < NH; ++i) lsum[i] *= x.alpha[c0 + i];
     }
-    // probabilities (<= 2^kTh); the denominator sums them exactly
+    // probabilities (<= 2^kTh; masked keys -> 0); the denominator sums them exactly
+    {
+      float mu[NH];
+      load_mu(mu);
 #pragma unroll
-    for (int i = 0; i < NH; ++i) {
-      float mu = x.m_used[c0 + i];
-      mu = mu == -INFINITY ? 0.f : mu;
-      s[i] = ex2(s[i] - mu);
-      lsum[i] += s[i] * inv_vs;
+      for (int i = 0; i < NH; ++i) {
+        s[i] = ex2(s[i] - mu[i]);
+        lsum[i] += s[i] * inv_vs;
+      }
     }
     // this tile's P buffer is free once PV of tile j - kPBufs has finished;
     // O (rescaled when the vote fired) once PV of tile j - 1 has. A commit
@@ -797,7 +824,7 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (tid < C::kNmax) {
-    m_used[tid] = -INFINITY;
+    m_used[tid] = kMInit;
     colscale[tid] = 1.f;
   }
   if (warp == 0) {
@@ -986,10 +1013,10 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
         *reinterpret_cast<uint4*>(q_s + (byte / 128) * C::kQAtomBytes + sw128(n, byte % 128)) = v;
       }
     } else {
-      // bf16 query row -> Q * 2^a = Q1 + Q2/16 in E4M3, rows n and N + n
+      // bf16 query -> Q * 2^a = Q1 + Q2/16 in E4M3 (rows n and N + n), with
+      // one exponent a for the CTA, from its largest |Q|
       constexpr int kPer = D / 32;  // elements per lane (8 or 4)
-      for (int n = sw; n < N; n += C::kSmWarps) {
-        float xv[kPer];
+      auto load_row = [&](int n, float* xv) {
         if (n < M) {
           const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(a.q) +
                                      ((int64_t)(q0 + n / hpc) * a.hq + head0 + n % hpc) * D +
@@ -1000,19 +1027,30 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
 #pragma unroll
           for (int e = 0; e < kPer; ++e) xv[e] = 0.f;
         }
-        float amax = 0.f;
+      };
+      float amax = 0.f;
+      for (int n = sw; n < M; n += C::kSmWarps) {
+        float xv[kPer];
+        load_row(n, xv);
 #pragma unroll
         for (int e = 0; e < kPer; ++e) amax = fmaxf(amax, fabsf(xv[e]));
+      }
 #pragma unroll
-        for (int off = 16; off; off >>= 1)
-          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        int ex = 0;
-        if (amax > 0.f) ex = static_cast<int>(floorf(__log2f(448.f / amax)));
-        ex = ex > 126 ? 126 : ex;
-        // keep the scaled maximum inside E4M3's finite range despite log2 rounding
-        while (ex > -126 && amax * exp2f(static_cast<float>(ex)) > 448.f) --ex;
-        const float up = exp2f(static_cast<float>(ex));
-        if (lane == 0) colscale[n] = 1.f / up;
+      for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      if (lane == 0) red[sw] = amax;
+      group_sync<C::kSmThreads>();
+      amax = 0.f;
+      for (int w = 0; w < C::kSmWarps; ++w) amax = fmaxf(amax, red[w]);
+      int ex = 0;
+      if (amax > 0.f) ex = static_cast<int>(floorf(__log2f(448.f / amax)));
+      ex = ex > 126 ? 126 : ex;
+      // keep the scaled maximum inside E4M3's finite range despite log2 rounding
+      while (ex > -126 && amax * exp2f(static_cast<float>(ex)) > 448.f) --ex;
+      const float up = exp2f(static_cast<float>(ex));
+      if (st == 0) colscale[0] = 1.f / up;
+      for (int n = sw; n < N; n += C::kSmWarps) {
+        float xv[kPer];
+        load_row(n, xv);
         uint8_t codes[2][kPer];
 #pragma unroll
         for (int e = 0; e < kPer; e += 2) {
@@ -1047,7 +1085,7 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
     }
     fence_async_smem();
     bar_arrive(q_ready);
-    group_sync<C::kSmThreads>();  // colscale visible to the whole group
+    group_sync<C::kSmThreads>();  // the query scale visible to the whole group
 
     SoftmaxCtx x;
     x.p_s = p_s;

@@ -536,58 +536,80 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_mma(const __grid_constant_
 }
 
 // ------------------------------------------------------------------ stage 2
-// One warp per (request, row, q head): log-sum-exp merge of the chunk
-// partials ("Stage 2 merges per row").
-template <int D>
-__global__ void __launch_bounds__(128) stage2_merge(const __grid_constant__ DecodeArgs a) {
+// Log-sum-exp merge of the chunk partials, one output row per (request, row,
+// q head) ("Stage 2 merges per row"). WPI warps share one row's splits
+// (WPI grows with the split count), each keeping four partials in flight,
+// and combine through shared memory; 256 threads per CTA.
+template <int D, int WPI>
+__global__ void __launch_bounds__(256) stage2_merge(const __grid_constant__ DecodeArgs a) {
+  constexpr int kItems = 8 / WPI;  // rows per CTA
+  constexpr int kPer = D / 32;     // floats per lane
+  __shared__ float sh_acc[8][D];
+  __shared__ float sh_w[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t item = (int64_t)blockIdx.x * 4 + warp;
+  const int sub = warp % WPI;
+  const int64_t item = (int64_t)blockIdx.x * kItems + warp / WPI;
   const int64_t per_b = (int64_t)a.max_q_len * a.hq;
+  bool valid = false;
+  int n = 0;
+  int64_t base = 0;
   const int b = static_cast<int>(item / per_b);
-  if (b >= a.batch) return;
-  const int rem = static_cast<int>(item % per_b);
-  const int i = rem / a.hq, head = rem % a.hq;
-  const int q0 = a.qo_indptr[b];
-  const int R = a.qo_indptr[b + 1] - q0;
-  const int L = a.kv_len[b];
-  if (i >= R || R > a.max_q_len || L < R || L > a.max_kv_len || q0 + R > a.rows_cap) return;
-  const int W = a.window ? a.window[b] : 0;
-  const SplitRange sr = split_range(L, R, W, a.page_size, a.chunk_pages);
-  if (sr.num_splits <= 1) return;  // stage 1 wrote the final result
-  const int64_t row = q0 + i;
-  const int n = sr.num_splits;
+  if (b < a.batch) {
+    const int rem = static_cast<int>(item % per_b);
+    const int i = rem / a.hq, head = rem % a.hq;
+    const int q0 = a.qo_indptr[b];
+    const int R = a.qo_indptr[b + 1] - q0;
+    const int L = a.kv_len[b];
+    if (i < R && R <= a.max_q_len && L >= R && L <= a.max_kv_len && q0 + R <= a.rows_cap) {
+      const int W = a.window ? a.window[b] : 0;
+      const SplitRange sr = split_range(L, R, W, a.page_size, a.chunk_pages);
+      n = sr.num_splits;
+      valid = n > 1;  // one split: stage 1 wrote the final result
+      base = (int64_t)(q0 + i) * a.hq + head;
+    }
+  }
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
   const int64_t stride = a.rows_cap * a.hq;  // partial rows per split
-  const int64_t base = row * a.hq + head;
   float mx = -INFINITY;
-  for (int s = lane; s < n; s += 32) mx = fmaxf(mx, a.part_lse[s * stride + base]);
-#pragma unroll
-  for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  constexpr int kPer = D / 32;  // floats per lane
   float acc[kPer];
 #pragma unroll
   for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
   float wsum = 0.f;
-  if (mx != -INFINITY) {
-    for (int s = 0; s < n; ++s) {
-      const float ls = a.part_lse[s * stride + base];
-      if (ls == -INFINITY) continue;
-      const float w = exp2f(ls - mx);
-      wsum += w;
-      const float* src = a.part_o + (s * stride + base) * D + lane * kPer;
+  if (valid) {
+    for (int s = lane; s < n; s += 32) mx = fmaxf(mx, a.part_lse[s * stride + base]);
 #pragma unroll
-      for (int e = 0; e < kPer; e += 4) {
-        if constexpr (kPer >= 4) {
-          const float4 x = *reinterpret_cast<const float4*>(src + e);
-          acc[e] += w * x.x; acc[e + 1] += w * x.y; acc[e + 2] += w * x.z; acc[e + 3] += w * x.w;
+    for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (mx != -INFINITY) {
+#pragma unroll 4
+      for (int s = sub; s < n; s += WPI) {
+        const float ls = a.part_lse[s * stride + base];
+        const float w = ls == -INFINITY ? 0.f : exp2f(ls - mx);
+        wsum += w;
+        const float* src = a.part_o + (s * stride + base) * D + lane * kPer;
+        // an empty split's partial may hold anything: select, do not scale
+#pragma unroll
+        for (int e = 0; e < kPer; e += 2) {
+          const float2 x = *reinterpret_cast<const float2*>(src + e);
+          acc[e] = w > 0.f ? fmaf(w, x.x, acc[e]) : acc[e];
+          acc[e + 1] = w > 0.f ? fmaf(w, x.y, acc[e + 1]) : acc[e + 1];
         }
-      }
-      if constexpr (kPer == 2) {
-        const float2 x = *reinterpret_cast<const float2*>(src);
-        acc[0] += w * x.x; acc[1] += w * x.y;
       }
     }
   }
+  if constexpr (WPI > 1) {
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) sh_acc[warp][lane * kPer + e] = acc[e];
+    if (lane == 0) sh_w[warp] = wsum;
+    __syncthreads();
+    if (sub == 0) {
+      for (int k = 1; k < WPI; ++k) {
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) acc[e] += sh_acc[warp + k][lane * kPer + e];
+        wsum += sh_w[warp + k];
+      }
+    }
+  }
+  if (!valid || sub != 0) return;
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + base * D + lane * kPer;
 #pragma unroll
@@ -631,11 +653,25 @@ KernelFn stage1_for(const pda_plan_t* p) {
   }
 }
 
+// warps per merged row: one up to 8 splits, then up to 8 splits a warp
+static int stage2_wpi(const pda_plan_t* p) {
+  return p->max_splits <= 8 ? 1 : p->max_splits <= 16 ? 2 : p->max_splits <= 32 ? 4 : 8;
+}
+template <int D>
+KernelFn stage2_pick(int wpi) {
+  switch (wpi) {
+    case 1: return stage2_merge<D, 1>;
+    case 2: return stage2_merge<D, 2>;
+    case 4: return stage2_merge<D, 4>;
+    default: return stage2_merge<D, 8>;
+  }
+}
 KernelFn stage2_for(const pda_plan_t* p) {
+  const int wpi = stage2_wpi(p);
   switch (p->head_dim) {
-    case 64: return stage2_merge<64>;
-    case 128: return stage2_merge<128>;
-    default: return stage2_merge<256>;
+    case 64: return stage2_pick<64>(wpi);
+    case 128: return stage2_pick<128>(wpi);
+    default: return stage2_pick<256>(wpi);
   }
 }
 
@@ -683,8 +719,9 @@ int launch_stage2(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_t s
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t c2 = {};
-  c2.gridDim = dim3(static_cast<unsigned>((items + 3) / 4));
-  c2.blockDim = dim3(128);
+  const int per_cta = 8 / stage2_wpi(plan);
+  c2.gridDim = dim3(static_cast<unsigned>((items + per_cta - 1) / per_cta));
+  c2.blockDim = dim3(256);
   c2.dynamicSmemBytes = 0;
   c2.stream = s;
   c2.attrs = attr;

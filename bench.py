@@ -6,7 +6,9 @@ One step is one pda_decode call (all of stage 1 and stage 2) over the
 fp8_decode workload: bs 128, R 1, 64 query / 8 kv heads, head_dim 128,
 ctx 2048, page 64, Q/K/V E4M3 with per-tensor scales, bf16 output. The call is
 captured once in a CUDA graph and replayed; before every step L2 is flushed by
-a memset of twice its size, outside the CUDA events that time the step.
+a memset of twice its size followed by a read of another buffer of twice its
+size (which writes the memset's dirty lines back), both outside the CUDA
+events that time the step, so each step starts from a cold, clean L2.
 `value` is the algorithmic HBM bytes of the call (paged_split_kv_03_gb300.
 traffic) over its measured time, summed over ranks; the line also carries the
 R = 1 / 4 / 8 sweep of the two bs-16 workloads at 16 query / 2 kv heads and
@@ -134,6 +136,23 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ GPU arm
+def make_flush(dev):
+    """L2 flush for timing: a memset of 2x L2, then a read of another 2x L2
+    buffer, so the timed step neither hits in L2 nor pays for write-backs of
+    the memset's dirty lines."""
+    import torch
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n = max(2 * l2, 256 << 20)
+    wbuf = torch.empty(n, dtype=torch.uint8, device=dev)
+    rbuf = torch.zeros(n // 8, dtype=torch.int64, device=dev)
+
+    def flush():
+        wbuf.zero_()
+        rbuf.max()
+
+    return flush
+
+
 def time_graph(fn, steps, warmup, flush, stream):
     """Per-step CUDA-event times (ms) of ``fn`` replayed on ``stream``, with an
     L2 flush enqueued before every step outside the events."""
@@ -252,11 +271,7 @@ def run_ours(args, rank, world, dev):
     from paged_split_kv_03_gb300.traffic import call_bytes, call_flops
     torch.cuda.set_device(dev)
     peak, peak_kind = peaks()
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
-
-    def flush():
-        flush_buf.zero_()
+    flush = make_flush(dev)
 
     wl = config_workload(HEADLINE, device=dev)
     dec, out, lse, stream, graph = setup_call(wl, dev)
@@ -336,7 +351,7 @@ def run_ours(args, rank, world, dev):
         "vs_baseline_ref": PAGES_NUMBER, "dtype": "e4m3 codes, f16 MMA, fp32 accumulate",
         "data": "synthetic (seeded N(0,1), e4m3 per-tensor)",
         "config": {"workload": HEADLINE_DESC, "parallelism": f"replicas x{world}",
-                   "l2": "flushed before every step (memset of 2x L2), outside the events",
+                   "l2": "flushed before every step (memset of 2x L2, then a read of 2x L2), outside the events",
                    "graph": "stage 1 + stage 2 captured in one CUDA graph",
                    "splits": dec.plan.max_splits, "chunk_pages": dec.plan.chunk_pages,
                    "grid_ctas": dec.plan.grid_ctas, "bytes_per_call": nbytes,

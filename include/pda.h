@@ -79,6 +79,8 @@ enum { PDA_KERNEL_AUTO = 0, PDA_KERNEL_MMA = 1, PDA_KERNEL_TC = 2 };
 #define PDA_STATUS_PAGE_OOB 0x8u        /* a page id read from page_table outside [0, num_pages) */
 #define PDA_STATUS_ROWS_GT_CAP 0x10u    /* qo_indptr[batch] > max_batch * max_q_len */
 #define PDA_STATUS_WAIT_TIMEOUT 0x20u   /* a pipeline wait ran past its bound; the CTA gave up */
+#define PDA_STATUS_SMEM_MISALIGNED 0x40u /* a stage-1 CTA's shared-memory window was not 1024-byte
+                                            aligned; that CTA wrote nothing */
 
 /* Everything the planner needs; plain values, no device pointers. */
 typedef struct {

@@ -29,6 +29,7 @@ PDA_STATUS_KV_LEN_GT_MAX = 0x4
 PDA_STATUS_PAGE_OOB = 0x8
 PDA_STATUS_ROWS_GT_CAP = 0x10
 PDA_STATUS_WAIT_TIMEOUT = 0x20
+PDA_STATUS_SMEM_MISALIGNED = 0x40
 PDA_PLAN_MAGIC = 0x50444131
 
 EXPORTED = ("pda_plan", "pda_decode", "pda_get_status", "pda_reset_status", "pda_strerror",

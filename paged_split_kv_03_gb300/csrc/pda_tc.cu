@@ -352,14 +352,16 @@ struct TcCfg {
   static constexpr int kTmemCols =
       kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
   static_assert(kTmemNeed <= 512, "TMEM budget");
-  static constexpr int kSmallBytes = 4096;
+  // barriers (512 B), then m_used, alpha, colscale, red[4], linv (kNmax floats each)
+  static constexpr int kSmallBytes = 512 + 8 * kNmax * 4;
   static constexpr int kBudget = kCtasPerSm == 2 ? 228 * 1024 / 2 - 1024 : 227 * 1024;
-  static constexpr int kAvail = kBudget - 1024 - kQBytes - kPBytes - kSmallBytes;
+  // the dynamic window starts 1024-byte aligned (checked at run time)
+  static constexpr int kAvail = kBudget - kQBytes - kPBytes - kSmallBytes;
   static constexpr int kRingRaw = kAvail / kSlot > 12 ? 12 : kAvail / kSlot;
   // bf16 V blocks span two adjacent slots: keep the ring even so pairs never wrap
   static constexpr int kRing = kF8 ? kRingRaw : (kRingRaw & ~1);
   static constexpr bool kBuildable = kRing >= kTileSlots;
-  static constexpr int kSmem = 1024 + kQBytes + kPBytes + kRing * kSlot + kSmallBytes;
+  static constexpr int kSmem = kQBytes + kPBytes + kRing * kSlot + kSmallBytes;
 };
 
 // Position of a tile's K or V unit (kChunks ring slots each) in the order
@@ -432,9 +434,9 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
   for (int i = 0; i < NH; ++i) lsum[i] = 0.f;
   bool alive = true;
 
-  // per-token scales of this thread's key: the page id is loaded two tiles
-  // ahead and the scales one tile ahead, so the loop never waits on a load
-  // whose address depends on another load
+  // per-token scales of this thread's key: the page id is loaded three tiles
+  // ahead and the scales two tiles ahead (a tile takes about one loaded HBM
+  // latency), so the loop never waits on a load
   auto page_for = [&](int jj) -> int {
     const int tok = x.t_begin + jj * kTok + r;
     return (jj < x.ntiles && tok < x.t_end) ? __ldg(x.ptab + tok / x.P) : -1;
@@ -449,22 +451,25 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
       vs = __ldg(a.v_scale + sidx);
     }
   };
-  float ks_next = 0.f, vs_next = 1.f;  // scales of the tile about to start
-  int pg_ahead = -1;                   // page of the tile after it
+  float ks_a = 0.f, vs_a = 1.f, ks_b = 0.f, vs_b = 1.f;  // scales of tiles j and j + 1
+  int pg_c = -1;                                         // page of tile j + 2
   if constexpr (SMODE == PDA_SCALE_TOKEN_HEAD) {
-    const int pg0 = page_for(0);
-    pg_ahead = page_for(1);
-    scales_for(0, pg0, ks_next, vs_next);
+    const int pg0 = page_for(0), pg1 = page_for(1);
+    pg_c = page_for(2);
+    scales_for(0, pg0, ks_a, vs_a);
+    scales_for(1, pg1, ks_b, vs_b);
   }
 
   for (int j = 0; j < x.ntiles; ++j) {
     const int tok = x.t_begin + j * kTok + r;
     float row_scale = qk_scale, log2_vs = 0.f, inv_vs = 1.f;
     if constexpr (SMODE == PDA_SCALE_TOKEN_HEAD) {
-      const float ks = ks_next;
-      float vs = vs_next;
-      scales_for(j + 1, pg_ahead, ks_next, vs_next);
-      pg_ahead = page_for(j + 2);
+      const float ks = ks_a;
+      float vs = vs_a;
+      ks_a = ks_b;
+      vs_a = vs_b;
+      scales_for(j + 2, pg_c, ks_b, vs_b);
+      pg_c = page_for(j + 3);
       row_scale *= ks;
       vs = vs > 0.f ? vs : 1.f;
       log2_vs = __log2f(vs);
@@ -739,9 +744,14 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
   using C = TcCfg<D, KVT, QT, SMODE, NMAX>;
   constexpr bool kF8 = C::kF8;
   constexpr int R_ = C::kRing;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // swizzled TMA boxes and MMA operands need 1024-byte alignment; the sizes
+  // above assume the window provides it, so a CTA without it does nothing
+  if ((su32(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicOr(a.status, PDA_STATUS_SMEM_MISALIGNED);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   uint8_t* q_s = smem;
   uint8_t* p_s = q_s + C::kQBytes;
   uint8_t* ring = p_s + C::kPBytes;

@@ -305,6 +305,21 @@ template <int NT>
 __device__ __forceinline__ void group_sync() {
   asm volatile("barrier.sync 1, %0;" ::"n"(NT) : "memory");
 }
+// The same over the 128 threads (4 warps) of one column group, on named
+// barrier `id` (2 + the group's index).
+__device__ __forceinline__ bool colgroup_or(bool pred, uint32_t id) {
+  uint32_t in = pred ? 1u : 0u, out;
+  asm volatile(
+      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; barrier.red.or.pred q, %2, 128, p; selp.u32 %0, "
+      "1, 0, q; }"
+      : "=r"(out)
+      : "r"(in), "r"(id)
+      : "memory");
+  return out != 0;
+}
+__device__ __forceinline__ void colgroup_sync(uint32_t id) {
+  asm volatile("barrier.sync %0, 128;" ::"r"(id) : "memory");
+}
 
 // ------------------------------------------------------------ configuration
 // NMAX: rows x q heads one CTA holds (16: two CTAs per SM; 64: one).
@@ -414,6 +429,8 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
   const int r = qd * 32 + lane;  // token row of S^T / d row of O^T
   const int sw = (warp - 2) & 3; // warp index within the column group
   const int c0 = ((warp - 2) >> 2) * NH;  // first column of this thread
+  const uint32_t bar_id = 2u + static_cast<uint32_t>((warp - 2) >> 2);  // column group's barrier
+  const int gi = sw * 32 + lane;          // thread index within the column group
   const uint32_t tl = x.tmem + (static_cast<uint32_t>(qd * 32) << 16);
   const uint32_t tl_o = tl + 2 * C::kSCols;
   const int M = x.M, hpc = x.hpc, R = x.R;
@@ -549,11 +566,14 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
       }
     }
     const bool trig = dmax > kTh;
-    // One barrier reduction per tile: the vote also carries failures, and a
-    // second reduction (only when the first fired) tells them apart, so
-    // every softmax thread takes the same branch.
-    const bool fired = group_or<NT>(trig || !alive || *x.abort_flag != 0);
-    if (fired && group_or<NT>(!alive || *x.abort_flag != 0)) {
+    // One barrier reduction per tile among the 4 warps that share these
+    // columns (their maxima and O columns are theirs alone): the vote also
+    // carries failures, and a second reduction (only when the first fired)
+    // tells them apart, so the group takes one branch. Groups meet again
+    // on p_full and in the epilogue; a group that aborts is followed by the
+    // others at their next vote (the abort flag is shared).
+    const bool fired = colgroup_or(trig || !alive || *x.abort_flag != 0, bar_id);
+    if (fired && colgroup_or(!alive || *x.abort_flag != 0, bar_id)) {
       alive = false;
       break;
     }
@@ -566,16 +586,17 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
         for (int off = 16; off; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
         if (lane == 0) x.red[sw * C::kNmax + c0 + i] = v;
       }
-      group_sync<NT>();
-      if (st < N) {
-        const float mx = fmaxf(fmaxf(x.red[st], x.red[C::kNmax + st]),
-                               fmaxf(x.red[2 * C::kNmax + st], x.red[3 * C::kNmax + st]));
-        const float mo = x.m_used[st];
+      colgroup_sync(bar_id);
+      if (gi < NH) {
+        const int c = c0 + gi;
+        const float mx = fmaxf(fmaxf(x.red[c], x.red[C::kNmax + c]),
+                               fmaxf(x.red[2 * C::kNmax + c], x.red[3 * C::kNmax + c]));
+        const float mo = x.m_used[c];
         const float mn = fmaxf(mo, mx);  // finite: kMInit bounds it below
-        x.alpha[st] = ex2(mo - mn);
-        x.m_used[st] = mn;
+        x.alpha[c] = ex2(mo - mn);
+        x.m_used[c] = mn;
       }
-      group_sync<NT>();
+      colgroup_sync(bar_id);
 #pragma unroll
       for (int i = 0; i < NH; ++i) lsum[i] *= x.alpha[c0 + i];
     }

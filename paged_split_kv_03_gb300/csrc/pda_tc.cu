@@ -453,30 +453,44 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
 
   // per-token scales of this thread's key: the page id is loaded three tiles
   // ahead and the scales two tiles ahead (a tile takes about one loaded HBM
-  // latency), so the loop never waits on a load
-  auto page_for = [&](int jj) -> int {
-    const int tok = x.t_begin + jj * kTok + r;
-    return (jj < x.ntiles && tok < x.t_end) ? __ldg(x.ptab + tok / x.P) : -1;
+  // latency), so the loop never waits on a load. The key's page index and
+  // slot advance by (kTok / P, kTok % P) per tile: no division in the loop.
+  const int sP = x.P;
+  const int dq = kTok / sP, dr = kTok % sP;
+  const int64_t s_page = static_cast<int64_t>(sP) * a.hkv;  // scales per page
+  int cur_pi = (x.t_begin + r) / sP, cur_ps = (x.t_begin + r) % sP, cur_j = 0;
+  // page id of tile cur_j (-1: past the chunk), then the cursor moves on
+  auto next_page = [&](int& slot) -> int {
+    const int tok = x.t_begin + cur_j * kTok + r;
+    const int pg = (cur_j < x.ntiles && tok < x.t_end) ? __ldg(x.ptab + cur_pi) : -1;
+    slot = cur_ps;
+    ++cur_j;
+    cur_pi += dq;
+    cur_ps += dr;
+    if (cur_ps >= sP) {
+      cur_ps -= sP;
+      ++cur_pi;
+    }
+    return pg;
   };
-  auto scales_for = [&](int jj, int page, float& ks, float& vs) {
+  auto scales_for = [&](int page, int slot, float& ks, float& vs) {
     ks = 0.f;
     vs = 1.f;
-    const int tok = x.t_begin + jj * kTok + r;
-    if (page >= 0 && page < a.num_pages && jj < x.ntiles && tok < x.t_end) {
-      const int64_t sidx = ((int64_t)page * x.P + tok % x.P) * a.hkv + x.hkv;
+    if (page >= 0 && page < a.num_pages) {
+      const int64_t sidx = page * s_page + slot * a.hkv + x.hkv;
       ks = __ldg(a.k_scale + sidx);
       vs = __ldg(a.v_scale + sidx);
     }
   };
   float ks_a = 0.f, vs_a = 1.f, ks_b = 0.f, vs_b = 1.f;  // scales of tiles j and j + 1
-  int pg_c = -1;                                         // page of tile j + 2
+  int pg_c = -1, sl_c = 0;                               // page and slot of tile j + 2
   if constexpr (SMODE == PDA_SCALE_TOKEN_HEAD) {
-    const int pg0 = page_for(0), pg1 = page_for(1);
-    pg_c = page_for(2);
-    scales_for(0, pg0, ks_a, vs_a);
-    scales_for(1, pg1, ks_b, vs_b);
+    int sl0, sl1;
+    const int pg0 = next_page(sl0), pg1 = next_page(sl1);
+    pg_c = next_page(sl_c);
+    scales_for(pg0, sl0, ks_a, vs_a);
+    scales_for(pg1, sl1, ks_b, vs_b);
   }
-
   for (int j = 0; j < x.ntiles; ++j) {
     const int tok = x.t_begin + j * kTok + r;
     float row_scale = qk_scale, log2_vs = 0.f, inv_vs = 1.f;
@@ -485,12 +499,12 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
       float vs = vs_a;
       ks_a = ks_b;
       vs_a = vs_b;
-      scales_for(j + 2, pg_c, ks_b, vs_b);
-      pg_c = page_for(j + 3);
+      scales_for(pg_c, sl_c, ks_b, vs_b);
+      pg_c = next_page(sl_c);
       row_scale *= ks;
       vs = vs > 0.f ? vs : 1.f;
       log2_vs = __log2f(vs);
-      inv_vs = 1.f / vs;
+      inv_vs = __frcp_rn(vs);
     }
     // columns this key is visible to: rows i with lo_i <= tok <= pos_i
     int n_lo = M, n_hi = 0;  // empty

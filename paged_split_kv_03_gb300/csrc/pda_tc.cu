@@ -282,6 +282,17 @@ __device__ __forceinline__ uint16_t f2_to_e4m3x2(float lo, float hi) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// P of two columns as two E4M3 terms each, P = P1 + P2 (low bytes: `lo`),
+// through f16x2: P <= 2^8 rounds to f16 (11 bits), P1 = E4M3(P) and the
+// residual P - P1 (exact in f16) gives P2 = E4M3(P - P1).
+__device__ __forceinline__ void p_terms(float lo, float hi, uint16_t& c1, uint16_t& c2) {
+  uint32_t h, b, r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(hi), "f"(lo));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(c1) : "r"(h));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(b) : "h"(c1));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(b));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(c2) : "r"(r));
+}
 // Two E4M3 codes -> two floats (exact): .x from the low byte.
 __device__ __forceinline__ float2 e4m3x2_to_f2(uint16_t c) {
   uint32_t h;
@@ -352,10 +363,10 @@ struct TcCfg {
   // P^T operand of PV. K-major: rows n (bf16: two 64-token halves; E4M3: the
   // two terms' rows stacked, 16 + 16). MN-major (E4M3, up to 64 columns):
   // one 128-byte row per token holding term 1 then term 2 of every column,
-  // so a thread stores its columns with wide stores. One buffer: the PV
-  // issuer starts as soon as P is written, long before the next P is due.
+  // so a thread stores its columns with wide stores, in two buffers so that
+  // P of tile j + 1 need not wait for PV of tile j.
   static constexpr bool kPMn = kF8 && NMAX > 16;
-  static constexpr int kPBufs = 1;
+  static constexpr int kPBufs = kPMn ? 2 : 1;
   static constexpr int kPAtomBytes = kNmax * 128;    // [kNmax rows x 128 B]
   static constexpr int kPBufBytes = kPMn ? kTok * 128 : 2 * kPAtomBytes;
   static constexpr int kPBytes = kPBufs * kPBufBytes;
@@ -673,9 +684,8 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
       uint32_t w1[NH / 4], w2[NH / 4];
 #pragma unroll
       for (int i = 0; i < NH; i += 2) {
-        const uint16_t c1 = f2_to_e4m3x2(s[i], s[i + 1]);
-        const float2 f1 = e4m3x2_to_f2(c1);
-        const uint16_t c2 = f2_to_e4m3x2(s[i] - f1.x, s[i + 1] - f1.y);
+        uint16_t c1, c2;
+        p_terms(s[i], s[i + 1], c1, c2);
         if constexpr (C::kPMn) {
           if ((i & 2) == 0) {
             w1[i >> 2] = c1;

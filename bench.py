@@ -275,7 +275,7 @@ def run_ours(args, rank, world, dev):
 
     wl = config_workload(HEADLINE, device=dev)
     dec, out, lse, stream, graph = setup_call(wl, dev)
-    nbytes = call_bytes(wl, dec.plan.chunk_pages)
+    nbytes = call_bytes(wl, plan=dec.plan)
     flops = call_flops(wl)
     launches_per_step = 1 + (1 if dec.plan.max_splits > 1 else 0)
 
@@ -314,7 +314,7 @@ def run_ours(args, rank, world, dev):
             w2 = config_workload(name, R=R, bs=bs, device=dev)
             d2, o2, l2_, s2, g2 = setup_call(w2, dev)
             t2 = time_graph(g2.replay, max(10, args.steps), 3, flush, s2)
-            b2 = call_bytes(w2, d2.plan.chunk_pages)["total"]
+            b2 = call_bytes(w2, plan=d2.plan)["total"]
             med = statistics.median(t2)
             sweep.append({"workload": f"{name} bs{bs} R{R}", "us_per_call": med * 1e3,
                           "GB_s": b2 / (med * 1e-3) / 1e9,

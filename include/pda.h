@@ -128,7 +128,15 @@ typedef struct {
   int64_t scratch_lse_offset; /* byte offsets inside split_scratch */
   int64_t scratch_o_offset;
   int32_t stage1_smem_bytes;
-  int32_t reserved[15];
+  /* Requests [tail_from, batch) use chunks of tail_chunk_pages (and up to
+   * tail_splits splits) instead of chunk_pages (head_splits): the planner
+   * cuts the requests that would run in a last, partial wave of CTAs into
+   * shorter chunks, laid out last in the grid. tail_from = batch: none. */
+  int32_t tail_from;
+  int32_t tail_chunk_pages;
+  int32_t head_splits;
+  int32_t tail_splits;
+  int32_t reserved[11];
 } pda_plan_t;
 
 #define PDA_PLAN_MAGIC 0x50444131u /* "PDA1" */

@@ -59,7 +59,8 @@ class PdaPlan(ctypes.Structure):
                 ("max_splits", _i32), ("num_sms", _i32), ("grid_ctas", _i64),
                 ("rows_cap", _i64), ("scratch_bytes", _i64), ("scratch_lse_offset", _i64),
                 ("scratch_o_offset", _i64), ("stage1_smem_bytes", _i32),
-                ("reserved", _i32 * 15)]
+                ("tail_from", _i32), ("tail_chunk_pages", _i32), ("head_splits", _i32),
+                ("tail_splits", _i32), ("reserved", _i32 * 11)]
 
 
 class PdaError(RuntimeError):

@@ -42,6 +42,7 @@ struct DecodeArgs {
   int64_t sp, st, sh; // cache strides (elements)
   int batch, hq, hkv, group, head_dim, page_size, num_pages;
   int max_q_len, max_kv_len, max_splits, head_blocks, chunk_pages;
+  int tail_from, tail_chunk_pages, head_splits, tail_splits;  // see pda_plan_t
   int64_t rows_cap;
   int hpc[kMaxQLen + 1];  // q heads per CTA for R rows
   int tma_slot_dim;       // tcgen05 path: tensor-map coordinate holding the slot (1 or 2)
@@ -66,6 +67,35 @@ PDA_HD SplitRange split_range(int32_t L, int32_t R, int32_t W, int32_t P, int32_
   int32_t span = s.num_pages - s.lo_page;
   s.num_splits = span > 0 ? (span + chunk_pages - 1) / chunk_pages : 0;
   return s;
+}
+
+// KV chunk (pages per split) of request b.
+PDA_HD int32_t chunk_for(const DecodeArgs& a, int b) {
+  return b >= a.tail_from ? a.tail_chunk_pages : a.chunk_pages;
+}
+
+// Stage-1 work item of a CTA: requests [0, tail_from) with head_splits
+// splits each come first, then the tail requests with tail_splits; inside
+// each part the order is (request, kv head, split, head block), head block
+// fastest. False past the last request.
+struct WorkItem {
+  int b, hkv, split, hb;
+};
+PDA_HD bool work_item(const DecodeArgs& a, int64_t bid, WorkItem& w) {
+  const int64_t head_ctas = (int64_t)a.tail_from * a.hkv * a.head_splits * a.head_blocks;
+  int splits = a.head_splits, b0 = 0;
+  if (bid >= head_ctas) {
+    bid -= head_ctas;
+    splits = a.tail_splits;
+    b0 = a.tail_from;
+  }
+  w.hb = static_cast<int>(bid % a.head_blocks);
+  bid /= a.head_blocks;
+  w.split = static_cast<int>(bid % splits);
+  bid /= splits;
+  w.hkv = static_cast<int>(bid % a.hkv);
+  w.b = b0 + static_cast<int>(bid / a.hkv);
+  return w.b < a.batch;
 }
 
 // Launchers and resource queries of the two stage-1 variants and stage 2.

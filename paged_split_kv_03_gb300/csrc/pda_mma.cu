@@ -162,14 +162,9 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_mma(const __grid_constant_
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // ---- which work item
-  int64_t bid = blockIdx.x;
-  const int hb = static_cast<int>(bid % a.head_blocks);
-  bid /= a.head_blocks;
-  const int split = static_cast<int>(bid % a.max_splits);
-  bid /= a.max_splits;
-  const int hkv = static_cast<int>(bid % a.hkv);
-  const int b = static_cast<int>(bid / a.hkv);
-  if (b >= a.batch) return;
+  WorkItem wi;
+  if (!work_item(a, blockIdx.x, wi)) return;
+  const int hb = wi.hb, split = wi.split, hkv = wi.hkv, b = wi.b;
   const int q0 = a.qo_indptr[b];
   const int R = a.qo_indptr[b + 1] - q0;
   const int L = a.kv_len[b];
@@ -188,10 +183,11 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_mma(const __grid_constant_
   if (hb >= a.group / hpc) return;  // fewer head blocks are needed for fewer rows
   const int W = a.window ? a.window[b] : 0;
   const int P = a.page_size;
-  const SplitRange sr = split_range(L, R, W, P, a.chunk_pages);
+  const SplitRange sr = split_range(L, R, W, P, chunk_for(a, b));
   if (split >= sr.num_splits) return;
-  const int page_begin = sr.lo_page + split * a.chunk_pages;
-  const int page_end = min(page_begin + a.chunk_pages, sr.num_pages);
+  const int chunk = chunk_for(a, b);
+  const int page_begin = sr.lo_page + split * chunk;
+  const int page_end = min(page_begin + chunk, sr.num_pages);
   const int t_begin = page_begin * P;              // first token of the chunk (tile origin)
   const int t_end = min(page_end * P, L);          // one past the chunk's last real token
   const int ntiles = (t_end - t_begin + kT - 1) / kT;
@@ -562,7 +558,7 @@ __global__ void __launch_bounds__(256) stage2_merge(const __grid_constant__ Deco
     const int L = a.kv_len[b];
     if (i < R && R <= a.max_q_len && L >= R && L <= a.max_kv_len && q0 + R <= a.rows_cap) {
       const int W = a.window ? a.window[b] : 0;
-      const SplitRange sr = split_range(L, R, W, a.page_size, a.chunk_pages);
+      const SplitRange sr = split_range(L, R, W, a.page_size, chunk_for(a, b));
       n = sr.num_splits;
       valid = n > 1;  // one split: stage 1 wrote the final result
       base = (int64_t)(q0 + i) * a.hq + head;

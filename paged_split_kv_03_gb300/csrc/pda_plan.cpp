@@ -12,6 +12,8 @@
 
 #include <algorithm>
 #include <cstring>
+#include <queue>
+#include <vector>
 
 #include "pda_internal.h"
 
@@ -195,8 +197,66 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
   }
   chunk = std::min<int64_t>(std::max<int64_t>(chunk, 1), std::max<int64_t>(pages_max, 1));
   pl.chunk_pages = (int32_t)chunk;
-  pl.max_splits = (int32_t)ceil_div(pages_max, chunk);
-  pl.grid_ctas = units * pl.max_splits;
+  pl.head_splits = (int32_t)ceil_div(pages_max, chunk);
+  pl.tail_from = pl.batch;
+  pl.tail_chunk_pages = pl.chunk_pages;
+  pl.tail_splits = pl.head_splits;
+
+  // Tail split: CTAs of equal length run in waves of `slots`, so a last,
+  // partial wave leaves SMs idle. When the planner chose the chunk, the
+  // requests whose CTAs would form that wave get chunks k times shorter
+  // (k ~ slots / their CTAs) and run last, if a greedy schedule of the CTAs
+  // (each SM slot takes the next CTA when free) finishes sooner, merge
+  // included.
+  if (p->chunk_pages == 0 && pl.batch > 0) {
+    const int64_t per_req = hb_units * pl.head_splits;  // CTAs of one request
+    const int64_t total = (int64_t)pl.batch * per_req;
+    const int64_t rem = total % slots;
+    auto cta_us = [&](int64_t c) {
+      return cta_overhead_us + std::min<int64_t>(c, pages_max) * page_kv_bytes / sm_bytes_per_us;
+    };
+    // makespan of n1 CTAs of t1 then n2 of t2 when each of `slots` slots
+    // takes the next CTA as soon as it is free
+    auto makespan = [&](int64_t n1, double t1, int64_t n2, double t2) {
+      std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+      for (int64_t i = 0; i < slots; ++i) free_at.push(0.0);
+      double end = 0.0;
+      auto run = [&](int64_t n, double t) {
+        for (int64_t i = 0; i < n; ++i) {
+          const double s0 = free_at.top();
+          free_at.pop();
+          free_at.push(s0 + t);
+          end = std::max(end, s0 + t);
+        }
+      };
+      run(n1, t1);
+      run(n2, t2);
+      return end;
+    };
+    if (total > slots && rem > 0 && total <= 64 * slots) {
+      const int64_t nt = std::min<int64_t>(ceil_div(rem, per_req), pl.batch);
+      const int64_t k = slots / (nt * per_req);
+      if (k >= 2) {
+        const int64_t tchunk = std::max<int64_t>(1, ceil_div(chunk, k));
+        const int64_t tsplits = ceil_div(pages_max, tchunk);
+        const int64_t head = (int64_t)(pl.batch - nt) * per_req;
+        const int64_t tail = nt * hb_units * tsplits;
+        const double merge_rows = (double)nt * pl.max_q_len * pl.num_qo_heads;
+        double t_with = makespan(head, cta_us(chunk), tail, cta_us(tchunk)) +
+                        2.0 * tsplits * merge_rows * (p->head_dim + 1) * 4 / 6.0e6;
+        if (pl.head_splits == 1) t_with += merge_us;  // stage 2 was not needed before
+        const double t_without = makespan(total, cta_us(chunk), 0, 0.0);
+        if (t_with < 0.97 * t_without) {
+          pl.tail_from = (int32_t)(pl.batch - nt);
+          pl.tail_chunk_pages = (int32_t)tchunk;
+          pl.tail_splits = (int32_t)tsplits;
+        }
+      }
+    }
+  }
+  pl.max_splits = std::max(pl.head_splits, pl.tail_splits);
+  pl.grid_ctas = (int64_t)pl.tail_from * hb_units * pl.head_splits +
+                 (int64_t)(pl.batch - pl.tail_from) * hb_units * pl.tail_splits;
   if (pl.grid_ctas > 0x7fffffffLL) return PDA_ERR_INVALID;
 
   pl.rows_cap = (int64_t)pl.max_batch * pl.max_q_len;
@@ -271,6 +331,10 @@ extern "C" int pda_decode(const pda_plan_t* plan, const void* q, const void* k_p
   a.max_splits = plan->max_splits;
   a.head_blocks = plan->head_blocks;
   a.chunk_pages = plan->chunk_pages;
+  a.tail_from = plan->tail_from;
+  a.tail_chunk_pages = plan->tail_chunk_pages;
+  a.head_splits = plan->head_splits;
+  a.tail_splits = plan->tail_splits;
   a.rows_cap = plan->rows_cap;
   for (int r = 0; r <= pda::kMaxQLen; ++r) a.hpc[r] = plan->heads_per_cta[r];
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -820,14 +820,9 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // ---- which work item (uniform per CTA; exits before any barrier)
-  int64_t bid = blockIdx.x;
-  const int hb = static_cast<int>(bid % a.head_blocks);
-  bid /= a.head_blocks;
-  const int split = static_cast<int>(bid % a.max_splits);
-  bid /= a.max_splits;
-  const int hkv = static_cast<int>(bid % a.hkv);
-  const int b = static_cast<int>(bid / a.hkv);
-  if (b >= a.batch) return;
+  WorkItem wi;
+  if (!work_item(a, blockIdx.x, wi)) return;
+  const int hb = wi.hb, split = wi.split, hkv = wi.hkv, b = wi.b;
   const int q0 = a.qo_indptr[b];
   const int R = a.qo_indptr[b + 1] - q0;
   const int L = a.kv_len[b];
@@ -846,10 +841,11 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
   if (hb >= a.group / hpc) return;
   const int W = a.window ? a.window[b] : 0;
   const int P = a.page_size;
-  const SplitRange sr = split_range(L, R, W, P, a.chunk_pages);
+  const SplitRange sr = split_range(L, R, W, P, chunk_for(a, b));
   if (split >= sr.num_splits) return;
-  const int page_begin = sr.lo_page + split * a.chunk_pages;
-  const int page_end = min(page_begin + a.chunk_pages, sr.num_pages);
+  const int chunk = chunk_for(a, b);
+  const int page_begin = sr.lo_page + split * chunk;
+  const int page_end = min(page_begin + chunk, sr.num_pages);
   const int t_begin = page_begin * P;
   const int t_end = min(page_end * P, L);
   const int ntiles = (t_end - t_begin + kTok - 1) / kTok;
@@ -878,16 +874,140 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (tid < C::kNmax) {
-    m_used[tid] = kMInit;
-    colscale[tid] = 1.f;
-  }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      su32(tmem_slot)),
                  "r"(C::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // Before the CTA-wide sync, so that their latency overlaps the setup:
+  // producer warps prefetch the tensor maps and load the first page ids;
+  // softmax warps reset the running maxima and build the query tile.
+  const bool producer = warp == 0 || (warp >= C::kProdWarp1 && warp < C::kProdWarp1 + C::kProducers - 1);
+  const int pw = warp == 0 ? 0 : warp - C::kProdWarp1 + 1;  // producer index
+  const int box_rows = P < kTok ? P : kTok;
+  const int nbox = kTok / box_rows;  // <= 16 (P >= 8)
+  const int bx = pw + lane * C::kProducers;  // this lane's box within a chunk
+  const uint32_t box_bytes = static_cast<uint32_t>(box_rows) * 128u;
+  const CUtensorMap* maps[2] = {&tmk, &tmv};
+  // this lane's box of tile j: page id (loaded now, checked when used, so
+  // the warp never waits on the load) and first slot; false: no box
+  auto page_of = [&](int j, int& page, int& slot0) -> bool {
+    const int tb = t_begin + j * kTok + bx * box_rows;
+    if (j >= ntiles || bx >= nbox || tb >= t_end) return false;
+    page = __ldg(ptab + tb / P);
+    slot0 = tb % P;
+    return true;
+  };
+  // page ids of tiles j .. j+3 (rotated as K_{j+2} and V_j are emitted);
+  // tile j+4's is loaded two tiles before its check
+  int pg0 = 0, s00 = 0, pg1 = 0, s01 = 0, pg2 = 0, s02 = 0, pg3 = 0, s03 = 0;
+  bool ok0 = false, ok1 = false, ok2 = false, ok3 = false;
+  if (producer) {
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+    }
+    ok0 = page_of(0, pg0, s00);
+    ok1 = page_of(1, pg1, s01);
+    ok2 = page_of(2, pg2, s02);
+    ok3 = page_of(3, pg3, s03);
+  } else if (warp >= 2 && warp < 2 + C::kSmWarps) {
+    const int st = tid - 64;  // 0..kSmThreads-1
+    const int sw = warp - 2;  // softmax warp index
+    if (st < C::kNmax) {
+      m_used[st] = kMInit;
+      colscale[st] = 1.f;
+    }
+    // ---- query operand Q^T (K-major, 128-byte swizzle), rows n < N (zero past M)
+    if constexpr (!C::kQSplit) {
+      constexpr int kRowChunks = D * C::kElt / 16;  // 16-byte pieces of one query row
+      for (int idx = st; idx < N * kRowChunks; idx += C::kSmThreads) {
+        const int n = idx / kRowChunks, cch = idx % kRowChunks;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (n < M) {
+          const uint8_t* src = static_cast<const uint8_t*>(a.q) +
+                               (((int64_t)(q0 + n / hpc) * a.hq + head0 + n % hpc) * D) * C::kElt +
+                               cch * 16;
+          v = __ldg(reinterpret_cast<const uint4*>(src));
+        }
+        const int byte = cch * 16;
+        *reinterpret_cast<uint4*>(q_s + (byte / 128) * C::kQAtomBytes + sw128(n, byte % 128)) = v;
+      }
+    } else {
+      // bf16 query -> Q * 2^a = Q1 + Q2/16 in E4M3 (rows n and N + n), with
+      // one exponent a for the CTA, from its largest |Q|
+      constexpr int kPer = D / 32;  // elements per lane (8 or 4)
+      auto load_row = [&](int n, float* xv) {
+        if (n < M) {
+          const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(a.q) +
+                                     ((int64_t)(q0 + n / hpc) * a.hq + head0 + n % hpc) * D +
+                                     lane * kPer;
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) xv[e] = __bfloat162float(src[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) xv[e] = 0.f;
+        }
+      };
+      float amax = 0.f;
+      for (int n = sw; n < M; n += C::kSmWarps) {
+        float xv[kPer];
+        load_row(n, xv);
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) amax = fmaxf(amax, fabsf(xv[e]));
+      }
+#pragma unroll
+      for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      if (lane == 0) red[sw] = amax;
+      group_sync<C::kSmThreads>();
+      amax = 0.f;
+      for (int w = 0; w < C::kSmWarps; ++w) amax = fmaxf(amax, red[w]);
+      int ex = 0;
+      if (amax > 0.f) ex = static_cast<int>(floorf(__log2f(448.f / amax)));
+      ex = ex > 126 ? 126 : ex;
+      // keep the scaled maximum inside E4M3's finite range despite log2 rounding
+      while (ex > -126 && amax * exp2f(static_cast<float>(ex)) > 448.f) --ex;
+      const float up = exp2f(static_cast<float>(ex));
+      if (st == 0) colscale[0] = 1.f / up;
+      for (int n = sw; n < N; n += C::kSmWarps) {
+        float xv[kPer];
+        load_row(n, xv);
+        uint8_t codes[2][kPer];
+#pragma unroll
+        for (int e = 0; e < kPer; e += 2) {
+          float v0 = xv[e] * up, v1 = xv[e + 1] * up;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const uint16_t c2 = f2_to_e4m3x2(v0, v1);
+            const float2 back = e4m3x2_to_f2(c2);
+            codes[t][e] = static_cast<uint8_t>(c2 & 0xFF);
+            codes[t][e + 1] = static_cast<uint8_t>(c2 >> 8);
+            v0 = (v0 - back.x) * 16.f;
+            v1 = (v1 - back.y) * 16.f;
+          }
+        }
+        const int byte = lane * kPer;  // d of this lane's first element (1 byte each)
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          uint8_t* dst = q_s + (byte / 128) * C::kQAtomBytes + sw128(t * N + n, byte % 128);
+          if constexpr (kPer == 8) {
+            uint2 w;
+            w.x = codes[t][0] | (codes[t][1] << 8) | (codes[t][2] << 16) |
+                  ((uint32_t)codes[t][3] << 24);
+            w.y = codes[t][4] | (codes[t][5] << 8) | (codes[t][6] << 16) |
+                  ((uint32_t)codes[t][7] << 24);
+            *reinterpret_cast<uint2*>(dst) = w;
+          } else {
+            *reinterpret_cast<uint32_t*>(dst) = codes[t][0] | (codes[t][1] << 8) |
+                                                (codes[t][2] << 16) | ((uint32_t)codes[t][3] << 24);
+          }
+        }
+      }
+    }
+    fence_async_smem();
+    group_sync<C::kSmThreads>();  // the query scale visible to the whole group
   }
   fence_before();
   __syncthreads();
@@ -899,21 +1019,6 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
     // ================================================ TMA producer warps
     // producer pw issues boxes pw, pw + kProducers, ... of every chunk and
     // arrives on the chunk's full barrier with its own byte count
-    const int pw = warp == 0 ? 0 : warp - C::kProdWarp1 + 1;
-    const int box_rows = P < kTok ? P : kTok;
-    const int nbox = kTok / box_rows;  // <= 16 (P >= 8)
-    const int bx = pw + lane * C::kProducers;  // this lane's box within a chunk
-    const uint32_t box_bytes = static_cast<uint32_t>(box_rows) * 128u;
-    const CUtensorMap* maps[2] = {&tmk, &tmv};
-    // this lane's box of tile j: page id (loaded now, checked when used, so
-    // the warp never waits on the load) and first slot; false: no box
-    auto page_of = [&](int j, int& page, int& slot0) -> bool {
-      const int tb = t_begin + j * kTok + bx * box_rows;
-      if (j >= ntiles || bx >= nbox || tb >= t_end) return false;
-      page = __ldg(ptab + tb / P);
-      slot0 = tb % P;
-      return true;
-    };
     auto checked = [&](bool want, int page) -> bool {
       if (want && (page < 0 || page >= a.num_pages)) {
         atomicOr(a.status, PDA_STATUS_PAGE_OOB);
@@ -921,11 +1026,6 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
       }
       return want;
     };
-    // page ids of tiles j .. j+3 (rotated as K_{j+2} and V_j are emitted);
-    // tile j+4's is loaded two tiles before its check
-    int pg0 = 0, s00 = 0, pg1 = 0, s01 = 0, pg2 = 0, s02 = 0, pg3 = 0, s03 = 0;
-    bool ok0 = page_of(0, pg0, s00), ok1 = page_of(1, pg1, s01), ok2 = page_of(2, pg2, s02),
-         ok3 = page_of(3, pg3, s03);
     ok0 = checked(ok0, pg0);
     ok1 = checked(ok1, pg1);
     uint32_t g = 0;
@@ -1052,95 +1152,7 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
     // ========================================= softmax / epilogue warps
     const int st = tid - 64;  // 0..kSmThreads-1
     const int sw = warp - 2;  // softmax warp index
-    // ---- query operand Q^T (K-major, 128-byte swizzle), rows n < N (zero past M)
-    if constexpr (!C::kQSplit) {
-      constexpr int kRowChunks = D * C::kElt / 16;  // 16-byte pieces of one query row
-      for (int idx = st; idx < N * kRowChunks; idx += C::kSmThreads) {
-        const int n = idx / kRowChunks, cch = idx % kRowChunks;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (n < M) {
-          const uint8_t* src = static_cast<const uint8_t*>(a.q) +
-                               (((int64_t)(q0 + n / hpc) * a.hq + head0 + n % hpc) * D) * C::kElt +
-                               cch * 16;
-          v = __ldg(reinterpret_cast<const uint4*>(src));
-        }
-        const int byte = cch * 16;
-        *reinterpret_cast<uint4*>(q_s + (byte / 128) * C::kQAtomBytes + sw128(n, byte % 128)) = v;
-      }
-    } else {
-      // bf16 query -> Q * 2^a = Q1 + Q2/16 in E4M3 (rows n and N + n), with
-      // one exponent a for the CTA, from its largest |Q|
-      constexpr int kPer = D / 32;  // elements per lane (8 or 4)
-      auto load_row = [&](int n, float* xv) {
-        if (n < M) {
-          const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(a.q) +
-                                     ((int64_t)(q0 + n / hpc) * a.hq + head0 + n % hpc) * D +
-                                     lane * kPer;
-#pragma unroll
-          for (int e = 0; e < kPer; ++e) xv[e] = __bfloat162float(src[e]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < kPer; ++e) xv[e] = 0.f;
-        }
-      };
-      float amax = 0.f;
-      for (int n = sw; n < M; n += C::kSmWarps) {
-        float xv[kPer];
-        load_row(n, xv);
-#pragma unroll
-        for (int e = 0; e < kPer; ++e) amax = fmaxf(amax, fabsf(xv[e]));
-      }
-#pragma unroll
-      for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      if (lane == 0) red[sw] = amax;
-      group_sync<C::kSmThreads>();
-      amax = 0.f;
-      for (int w = 0; w < C::kSmWarps; ++w) amax = fmaxf(amax, red[w]);
-      int ex = 0;
-      if (amax > 0.f) ex = static_cast<int>(floorf(__log2f(448.f / amax)));
-      ex = ex > 126 ? 126 : ex;
-      // keep the scaled maximum inside E4M3's finite range despite log2 rounding
-      while (ex > -126 && amax * exp2f(static_cast<float>(ex)) > 448.f) --ex;
-      const float up = exp2f(static_cast<float>(ex));
-      if (st == 0) colscale[0] = 1.f / up;
-      for (int n = sw; n < N; n += C::kSmWarps) {
-        float xv[kPer];
-        load_row(n, xv);
-        uint8_t codes[2][kPer];
-#pragma unroll
-        for (int e = 0; e < kPer; e += 2) {
-          float v0 = xv[e] * up, v1 = xv[e + 1] * up;
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const uint16_t c2 = f2_to_e4m3x2(v0, v1);
-            const float2 back = e4m3x2_to_f2(c2);
-            codes[t][e] = static_cast<uint8_t>(c2 & 0xFF);
-            codes[t][e + 1] = static_cast<uint8_t>(c2 >> 8);
-            v0 = (v0 - back.x) * 16.f;
-            v1 = (v1 - back.y) * 16.f;
-          }
-        }
-        const int byte = lane * kPer;  // d of this lane's first element (1 byte each)
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          uint8_t* dst = q_s + (byte / 128) * C::kQAtomBytes + sw128(t * N + n, byte % 128);
-          if constexpr (kPer == 8) {
-            uint2 w;
-            w.x = codes[t][0] | (codes[t][1] << 8) | (codes[t][2] << 16) |
-                  ((uint32_t)codes[t][3] << 24);
-            w.y = codes[t][4] | (codes[t][5] << 8) | (codes[t][6] << 16) |
-                  ((uint32_t)codes[t][7] << 24);
-            *reinterpret_cast<uint2*>(dst) = w;
-          } else {
-            *reinterpret_cast<uint32_t*>(dst) = codes[t][0] | (codes[t][1] << 8) |
-                                                (codes[t][2] << 16) | ((uint32_t)codes[t][3] << 24);
-          }
-        }
-      }
-    }
-    fence_async_smem();
-    bar_arrive(q_ready);
-    group_sync<C::kSmThreads>();  // the query scale visible to the whole group
+    bar_arrive(q_ready);  // the query tile was built before the CTA-wide sync
 
     SoftmaxCtx x;
     x.p_s = p_s;

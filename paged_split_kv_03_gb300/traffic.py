@@ -38,9 +38,15 @@ def _split_range(L, R, W, P, chunk_pages):
     return lo, lo_page, npages, nsplit
 
 
-def call_bytes(wl, chunk_pages: int | None = None, include_scratch: bool = True) -> dict:
+def call_bytes(wl, chunk_pages: int | None = None, include_scratch: bool = True,
+               plan=None) -> dict:
     """Algorithmic bytes of one call on workload ``wl`` (a synth.Workload);
-    ``chunk_pages`` is the plan's chunk (None: treat as one split)."""
+    ``chunk_pages`` is the plan's chunk (None: treat as one split). With a
+    ``plan`` (a pda_plan_t), its chunk and its tail requests' shorter chunk
+    are used instead."""
+    tail_from, tail_chunk = None, None
+    if plan is not None:
+        chunk_pages, tail_from, tail_chunk = plan.chunk_pages, plan.tail_from, plan.tail_chunk_pages
     P, H, D, Hq = wl.page_size, wl.num_kv_heads, wl.head_dim, wl.num_qo_heads
     kv_elt = 1 if wl.kv_e4m3 else 2
     q_elt = 1 if wl.q_e4m3 else 2
@@ -53,7 +59,8 @@ def call_bytes(wl, chunk_pages: int | None = None, include_scratch: bool = True)
         R = qo[b + 1] - qo[b]
         if R <= 0 or L < R:
             continue
-        lo, lo_page, npages, nsplit = _split_range(L, R, wins[b], P, chunk_pages or 1 << 30)
+        cp = tail_chunk if tail_from is not None and b >= tail_from else chunk_pages
+        lo, lo_page, npages, nsplit = _split_range(L, R, wins[b], P, cp or 1 << 30)
         tokens = L - lo_page * P
         kv += 2 * tokens * H * D * kv_elt
         if wl.scale_mode == 2:

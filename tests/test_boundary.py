@@ -79,6 +79,30 @@ def test_plan_splits_and_scratch(lib):
     assert forced.chunk_pages == 5 and forced.max_splits == 32768 // (5 * 16) + 1
 
 
+FP8_DECODE = dict(num_qo_heads=64, num_kv_heads=8, head_dim=128, page_size=64, q_dtype=1,
+                  kv_dtype=1, scale_mode=1, max_batch=128, max_q_len=1, max_kv_len=2048,
+                  kv_stride_page=64 * 8 * 128, kv_stride_token=8 * 128, kv_stride_head=128)
+
+
+def test_plan_tail_split(lib):
+    # 1024 one-split CTAs at 2 per SM are 3.37 waves of 304: the 14 requests
+    # of the partial wave are cut into 2 chunks each and laid out last
+    plan, _, rc = B.pda_plan(_params(**FP8_DECODE))
+    assert rc == 0 and plan.kernel == B.PDA_KERNEL_TC
+    assert plan.chunk_pages == 32 and plan.head_splits == 1
+    assert (plan.tail_from, plan.tail_chunk_pages, plan.tail_splits) == (114, 16, 2)
+    assert plan.max_splits == 2
+    assert plan.grid_ctas == 114 * 8 + 14 * 8 * 2
+    assert plan.scratch_bytes >= 256 + 2 * 128 * 64 * 129 * 4  # partials for max_splits
+    # a forced chunk is used as it is, for every request
+    forced, _, _ = B.pda_plan(_params(chunk_pages=8, **FP8_DECODE))
+    assert forced.tail_from == forced.batch and forced.tail_chunk_pages == 8
+    assert forced.grid_ctas == 128 * 8 * 4
+    # a whole number of waves has no tail
+    even, _, _ = B.pda_plan(_params(**dict(FP8_DECODE, max_batch=76)))
+    assert even.tail_from == even.batch and even.grid_ctas == 76 * 8
+
+
 @pytest.mark.parametrize("bad,code", [
     (dict(num_qo_heads=15), B.PDA_ERR_INVALID),
     (dict(head_dim=96), B.PDA_ERR_UNSUPPORTED),

@@ -173,6 +173,17 @@ def test_config_parity(cfg, kw, n_sample, peaked):
                      output_rounding=peaked)
 
 
+def test_tail_split_parity():
+    """A plan whose last requests run with shorter chunks than the rest (the
+    partial last wave cut finer) matches the oracle everywhere."""
+    wl = config_workload("fp8_decode", device=DEV, batch=40)
+    out, lse, status, dec = run_decode(wl)
+    assert status == 0
+    assert dec.plan.tail_from < wl.batch and dec.plan.tail_chunk_pages < dec.plan.chunk_pages
+    ref_o, ref_l = oracle_ref(wl)
+    assert_close(out, lse, ref_o, ref_l, tol_for(wl), what="tail split")
+
+
 # ------------------------------------------------ bit-exact gather and masks
 def _index_code(L, H, D):
     """v_j[c]: hex digit (c mod 4) of token j, negated for kv head 1 --

@@ -174,6 +174,35 @@ int pda_decode(const pda_plan_t* plan, const void* q, const void* k_pages, const
                float sm_scale, const float* k_scale, const float* v_scale, void* out,
                float* lse, void* split_scratch, pda_stream_t stream);
 
+/* Quantise-on-append: write the R_b new tokens of every request into the
+ * paged cache, the step before decode reads them ("perf(attention): run up
+ * to 8 query rows per request in the triton decode kernel", End-to-end A/B:
+ * the fp8_per_token_head cache; "fp8 support", Functionality: symmetric
+ * per-tensor FP8). Row i < R_b of request b is token L_b - R_b + i; it lands
+ * in page page_table[kv_indptr[b] + t / P], slot t % P, kv head h, with the
+ * plan's strides. Per kv dtype and scale mode of the plan:
+ *   bf16 cache             the bf16 values, copied;
+ *   E4M3, per tensor       codes = RNE(sat(x / s)) with s = k_scale[0] (v_scale[0]), read;
+ *   E4M3, per token-head   s = amax / 448 over the D values of (token, kv head)
+ *                          (1 if amax = 0), written to k_scale / v_scale
+ *                          [num_pages, P, Hkv], and codes = RNE(sat(x / s)).
+ * x / s is one fp32 division; sat clamps to +-448 (E4M3, OCP e4m3fn).
+ *   k_new, v_new  bf16 [qo_indptr[batch], Hkv, D], rows in qo_indptr order
+ *   k_pages, v_pages  the cache (written), layout and strides as planned
+ *   page_table, kv_indptr, kv_len, qo_indptr  as for pda_decode (kv_len
+ *                 counts the new tokens)
+ *   k_scale, v_scale  NULL for bf16; fp32 [1] read (per tensor) or fp32
+ *                 [num_pages, P, Hkv] written (per token-head)
+ *   split_scratch only its status word is used: page ids outside
+ *                 [0, num_pages), kv_len < rows and rows > max_q_len set the
+ *                 pda_decode status bits and skip that request
+ * Returns PDA_OK or a negative code from the host checks (nothing launched).
+ * All device pointers; nothing is allocated or synchronised. */
+int pda_append_kv(const pda_plan_t* plan, const void* k_new, const void* v_new,
+                  const int32_t* page_table, const int32_t* kv_indptr, const int32_t* kv_len,
+                  const int32_t* qo_indptr, int32_t max_q_len, void* k_pages, void* v_pages,
+                  float* k_scale, float* v_scale, void* split_scratch, pda_stream_t stream);
+
 /* pda_decode without a caller-provided split_scratch (the pages have no
  * counterpart: this serves callers that cannot allocate device memory, such
  * as a plugin whose host framework owns every allocation and hands it only

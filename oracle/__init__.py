@@ -34,6 +34,7 @@ _LIBS: dict = {}
 PDO_OK = 0
 PDO_ERR_ARG = -1
 PDO_ERR_KVLEN = -2
+PDO_ERR_PAGE = -3
 
 
 def lib_path(mutation: int = 0) -> str:
@@ -75,6 +76,11 @@ def _load(mutation: int = 0):
     lib.pdo_e4m3_to_double.argtypes = [ctypes.c_uint8]
     lib.pdo_e4m3_to_double.restype = dbl
     lib.pdo_max_threads.restype = i32
+    lib.pdo_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.pdo_e4m3_encode.restype = ctypes.c_uint8
+    lib.pdo_append.argtypes = [i32, i32, i32, i32, i32, i64, i64, i64, i64, vp, vp, vp, vp, vp,
+                               vp, vp, vp, vp, vp]
+    lib.pdo_append.restype = i32
     _LIBS[mutation] = lib
     return lib
 
@@ -162,3 +168,42 @@ def attention_for(wl, items=None, split_tokens=0, num_threads=0, mutation=0, **o
     args.update(overrides)
     return attention(items=items, split_tokens=split_tokens, num_threads=num_threads,
                      mutation=mutation, **args)
+
+
+def e4m3_encode(y: float, mutation: int = 0) -> int:
+    """Nearest E4M3 code to the fp32 value y (ties to even, saturating)."""
+    return int(_load(mutation).pdo_e4m3_encode(float(y)))
+
+
+APPEND_BF16, APPEND_TENSOR, APPEND_TOKEN_HEAD = 0, 1, 2
+
+
+def append_kv(*, k_new, v_new, page_table, kv_indptr, kv_len, qo_indptr, k_pages, v_pages,
+              k_scale, v_scale, num_kv_heads, head_dim, page_size, mode, strides, num_pages,
+              mutation=0):
+    """Quantise-on-append into copies of the given caches.
+
+    ``k_new`` / ``v_new``: bf16 [rows, Hkv, D] (CPU tensors or 16-bit words);
+    ``k_pages`` / ``v_pages``: the caches before the append (bytes, or bf16
+    words for mode 0); ``k_scale`` / ``v_scale``: fp32 arrays (read for
+    mode 1, written for mode 2, None for mode 0). Returns (k_pages, v_pages,
+    k_scale, v_scale, status) as numpy arrays (caches as raw bytes).
+    """
+    lib = _load(mutation)
+    kn = _np(k_new).view(np.uint16)
+    vn = _np(v_new).view(np.uint16)
+    kc = np.array(_np(k_pages), copy=True).view(np.uint8)
+    vc = np.array(_np(v_pages), copy=True).view(np.uint8)
+    ks = None if k_scale is None else np.array(_np(k_scale, np.float32), copy=True)
+    vs = None if v_scale is None else np.array(_np(v_scale, np.float32), copy=True)
+    pt = _np(page_table, np.int32)
+    ki = _np(kv_indptr, np.int32)
+    kl = _np(kv_len, np.int32)
+    qi = _np(qo_indptr, np.int32)
+    sp, st, sh = (int(s) for s in strides)
+    rc = lib.pdo_append(int(kl.shape[0]), num_kv_heads, head_dim, page_size, int(mode), sp, st, sh,
+                        int(num_pages), _ptr(kn), _ptr(vn), _ptr(pt), _ptr(ki), _ptr(kl), _ptr(qi),
+                        _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs))
+    if rc == PDO_ERR_ARG:
+        raise ValueError("oracle rejected its arguments")
+    return kc, vc, ks, vs, rc

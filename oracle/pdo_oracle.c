@@ -55,6 +55,7 @@
 #define PDO_OK 0
 #define PDO_ERR_ARG (-1)
 #define PDO_ERR_KVLEN (-2) /* a request has kv_len < rows: its outputs are NaN */
+#define PDO_ERR_PAGE (-3)  /* append: a page id outside [0, num_pages) */
 
 /* bf16 is the upper half of an IEEE binary32 word. */
 static double pdo_bf16_to_double(uint16_t bits) {
@@ -242,6 +243,106 @@ int pdo_attention(int batch, int hq, int hkv, int d, int page_size, int q_e4m3, 
     }
     free(s);
     free(oc);
+  }
+  return status;
+}
+
+/* ------------------------------------------------------------------------
+ * Quantise-on-append (the step before decode reads the cache): FreeToken PR
+ * #900, "End-to-end A/B" (the fp8_per_token_head cache: one fp32 scale per
+ * token and kv head) and FlashMLA PR #54, "Functionality" (symmetric
+ * per-tensor FP8). The code decision is taken in fp32, the precision the
+ * kernel takes it in (the pages fix none): s = fp32(amax / 448) (1 if amax
+ * is 0), y = fp32(x / s), code = the E4M3 value nearest to y, ties to the
+ * even code, |y| above 448 saturating to 448.
+ * ------------------------------------------------------------------------ */
+
+/* Nearest E4M3 code to y (OCP e4m3fn), ties to the even code, saturating to
+ * +-448; NaN -> 0x7F. By exhaustive comparison with every finite code. */
+uint8_t pdo_e4m3_encode(float y) {
+  if (isnan(y)) return 0x7F;
+  uint8_t sign = (signbit(y) && !MUT(19)) ? 0x80 : 0x00;
+  double a = fabs((double)y);
+  if (a > 448.0) return (uint8_t)(sign | 0x7E);
+  uint8_t best = 0;
+  double best_d = INFINITY;
+  for (int c = 0; c <= 0x7E; ++c) {
+    double dist = fabs(pdo_e4m3_to_double((uint8_t)c) - a);
+    /* strictly nearer wins; on a tie the even code wins */
+    if (dist < best_d || (dist == best_d && (c & 1) == MUT(17))) {
+      best = (uint8_t)c;
+      best_d = dist;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
+/*
+ * pdo_append: writes row i < R_b of every request b (token t = L_b - R_b + i)
+ * into page page_table[kv_indptr[b] + t / P], slot t % P, kv head h.
+ *   mode 0: bf16 cache, the bf16 bits copied
+ *   mode 1: E4M3 cache, s = k_scale[0] / v_scale[0] (read)
+ *   mode 2: E4M3 cache, s per (token, kv head) from the row's amax, written
+ *           to k_scale / v_scale [num_pages, page_size, hkv]
+ *   k_new, v_new  bf16 bits [total_rows, hkv, d]
+ *   k, v          caches (bytes; bf16 cache: 2 bytes per element), strides in elements
+ * Returns PDO_OK, PDO_ERR_ARG, PDO_ERR_KVLEN (a request with L < R, skipped)
+ * or PDO_ERR_PAGE (a page id outside [0, num_pages), that row skipped).
+ */
+int pdo_append(int batch, int hkv, int d, int page_size, int mode, int64_t sp, int64_t st,
+               int64_t sh, int64_t num_pages, const uint16_t* k_new, const uint16_t* v_new,
+               const int32_t* page_table, const int32_t* kv_indptr, const int32_t* kv_len,
+               const int32_t* qo_indptr, uint8_t* k, uint8_t* v, float* k_scale,
+               float* v_scale) {
+  if (batch < 0 || hkv <= 0 || d <= 0 || page_size <= 0 || mode < 0 || mode > 2) return PDO_ERR_ARG;
+  int status = PDO_OK;
+  for (int b = 0; b < batch; ++b) {
+    int R = qo_indptr[b + 1] - qo_indptr[b];
+    int L = kv_len[b];
+    if (R <= 0) continue;
+    if (L < R) {
+      status = PDO_ERR_KVLEN;
+      continue;
+    }
+    for (int i = 0; i < R; ++i) {
+      int64_t t = (int64_t)L - R + i - MUT(18);
+      int32_t page = page_table[kv_indptr[b] + t / page_size];
+      int64_t slot = t % page_size;
+      if (page < 0 || page >= num_pages) {
+        status = PDO_ERR_PAGE;
+        continue;
+      }
+      for (int h = 0; h < hkv; ++h) {
+        int64_t row = ((int64_t)(qo_indptr[b] + i) * hkv + h) * d;
+        int64_t base = (int64_t)page * sp + slot * st + (int64_t)h * sh;
+        int64_t sidx = ((int64_t)page * page_size + slot) * hkv + h;
+        for (int kv = 0; kv < 2; ++kv) {
+          const uint16_t* src = (kv ? v_new : k_new) + row;
+          uint8_t* cache = kv ? v : k;
+          float* scale = kv ? v_scale : k_scale;
+          if (mode == 0) {
+            for (int c = 0; c < d; ++c) memcpy(cache + (base + c) * 2, src + c, 2);
+            continue;
+          }
+          float amax = 0.0f;
+          for (int c = 0; c < d; ++c) {
+            float x = (float)pdo_bf16_to_double(src[c]);
+            if (fabsf(x) > amax) amax = fabsf(x);
+          }
+          float s;
+          if (mode == 1) {
+            s = scale[0];
+          } else {
+            s = amax > 0.0f ? amax / (MUT(16) ? 256.0f : 448.0f) : 1.0f;
+            scale[sidx] = s;
+          }
+          for (int c = 0; c < d; ++c) {
+            float y = (float)pdo_bf16_to_double(src[c]) / s;
+            cache[base + c] = pdo_e4m3_encode(y);
+          }
+        }
+      }
+    }
   }
   return status;
 }

@@ -91,6 +91,9 @@ def load_library(path: Optional[str] = None):
     lib.pda_decode_static.argtypes = [ctypes.POINTER(PdaPlan), _vp, _vp, _vp, _vp, _vp, _vp,
                                       _vp, _i32, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp]
     lib.pda_decode_static.restype = ctypes.c_int
+    lib.pda_append_kv.argtypes = [ctypes.POINTER(PdaPlan), _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                                  _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.pda_append_kv.restype = ctypes.c_int
     lib.pda_get_status.argtypes = [ctypes.POINTER(PdaPlan), _vp, ctypes.POINTER(_u32), _vp]
     lib.pda_get_status.restype = ctypes.c_int
     lib.pda_reset_status.argtypes = [ctypes.POINTER(PdaPlan), _vp, _vp]
@@ -162,6 +165,20 @@ def pda_decode_static(plan: PdaPlan, q, k_pages, v_pages, page_table, kv_indptr,
         float(sm_scale), _ptr(k_scale), _ptr(v_scale), _ptr(out), _ptr(lse), _stream(stream))
     if check and rc != PDA_OK:
         raise PdaError(rc, "pda_decode_static")
+    return rc
+
+
+def pda_append_kv(plan: PdaPlan, k_new, v_new, page_table, kv_indptr, kv_len, qo_indptr,
+                  max_q_len: int, k_pages, v_pages, k_scale, v_scale, split_scratch,
+                  stream=None, check: bool = True) -> int:
+    """Quantise-on-append of the new rows' K/V (bf16 [rows, Hkv, D]) into the
+    paged cache of the plan's dtype and scale mode (see include/pda.h)."""
+    rc = load_library().pda_append_kv(
+        ctypes.byref(plan), _ptr(k_new), _ptr(v_new), _ptr(page_table), _ptr(kv_indptr),
+        _ptr(kv_len), _ptr(qo_indptr), int(max_q_len), _ptr(k_pages), _ptr(v_pages),
+        _ptr(k_scale), _ptr(v_scale), _ptr(split_scratch), _stream(stream))
+    if check and rc != PDA_OK:
+        raise PdaError(rc, "pda_append_kv")
     return rc
 
 

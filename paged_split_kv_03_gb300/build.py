@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIBDIR, "libpda.so")
 
-SOURCES = ["pda_plan.cpp", "pda_mma.cu", "pda_tc.cu", "pda_noalloc.cu"]
+SOURCES = ["pda_plan.cpp", "pda_mma.cu", "pda_tc.cu", "pda_noalloc.cu", "pda_append.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

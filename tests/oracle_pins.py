@@ -14,6 +14,13 @@ copy built with one planted mistake, ``mutation`` > 0) disagrees with:
 The semantics pinned are those of "perf(attention): run up to 8 query rows
 per request in the triton decode kernel", section "Changes" (per-row causal
 limit and window, per-row merge of the KV split, GQA groups).
+
+The quantise-on-append oracle (the fp8_per_token_head cache of the same
+page's "End-to-end A/B", per-tensor FP8 of "fp8 support") is pinned to
+torch's float8_e4m3fn cast (codes within +-448, ties to even), to the
+saturation of the format's largest finite value, to closed forms of the
+scale (amax / 448, 1 for a zero row) and to the page-table placement of
+token L - R + i read independently here.
 """
 from __future__ import annotations
 
@@ -245,8 +252,144 @@ def pin_rows_vs_single(mutation=0):
         _close(lse1, lse, what=f"rows vs single lse W={W}")
 
 
+# ------------------------------------------------------------ append pins
+def _e4m3_torch(y: torch.Tensor) -> torch.Tensor:
+    return y.to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def pin_e4m3_encode_vs_torch(mutation=0):
+    # every finite code's value, every midpoint between neighbours (a tie:
+    # the even code), and random fp32 values, both signs, all within +-448
+    codes = torch.arange(0, 0x7F, dtype=torch.uint8)
+    vals = codes.view(torch.float8_e4m3fn).float()
+    mids = (vals[:-1] + vals[1:]) / 2
+    g = torch.Generator().manual_seed(5)
+    rnd = (torch.rand(4000, generator=g) * 2 - 1) * 448
+    tiny = (torch.rand(1000, generator=g) * 2 - 1) * 2.0 ** -6
+    ys = torch.cat([vals, mids, rnd, tiny]).float()
+    ys = torch.cat([ys, -ys])
+    got = torch.tensor([oracle.e4m3_encode(float(y), mutation) for y in ys], dtype=torch.uint8)
+    ref = _e4m3_torch(ys)
+    bad = (got != ref).nonzero()
+    assert bad.numel() == 0, f"E4M3 encode differs from torch at {ys[bad[0]].item()!r}"
+
+
+def pin_e4m3_encode_saturates(mutation=0):
+    # the largest finite E4M3 value is 448 (S.1111.110); beyond it the code
+    # saturates; S.1111.111 is NaN
+    for y, code in [(448.0, 0x7E), (449.0, 0x7E), (1e30, 0x7E), (float("inf"), 0x7E),
+                    (-449.0, 0xFE), (-float("inf"), 0xFE)]:
+        assert oracle.e4m3_encode(y, mutation) == code, (y, code)
+    assert oracle.e4m3_encode(float("nan"), mutation) == 0x7F
+
+
+def _append_case(mode, D=8, P=4, H=2, lens=(9, 5), rows=(3, 2), seed=0):
+    """Tiny cache with a shuffled page table; returns the pieces by name."""
+    g = torch.Generator().manual_seed(seed)
+    B = len(lens)
+    pages_per = [math.ceil(L / P) for L in lens]
+    num_pages = sum(pages_per) + 2
+    perm = torch.randperm(num_pages, generator=g)[:sum(pages_per)].to(torch.int32)
+    kv_indptr = torch.tensor([0] + list(np.cumsum(pages_per)), dtype=torch.int32)
+    qo = torch.tensor([0] + list(np.cumsum(rows)), dtype=torch.int32)
+    n = int(qo[-1])
+    k_new = (torch.randn(n, H, D, generator=g) * 3).to(torch.bfloat16)
+    v_new = (torch.randn(n, H, D, generator=g) * 3).to(torch.bfloat16)
+    elt = 2 if mode == oracle.APPEND_BF16 else 1
+    shape = (num_pages, P, H, D)
+    fill = torch.randint(0, 256, (num_pages * P * H * D * elt,), generator=g, dtype=torch.uint8)
+    k_pages = fill.clone().numpy()
+    v_pages = fill.flip(0).clone().numpy()
+    ks = vs = None
+    if mode == oracle.APPEND_TENSOR:
+        ks, vs = np.array([0.0125], np.float32), np.array([0.02], np.float32)
+    elif mode == oracle.APPEND_TOKEN_HEAD:
+        ks = np.full(num_pages * P * H, -1.0, np.float32)
+        vs = np.full(num_pages * P * H, -2.0, np.float32)
+    return dict(k_new=k_new, v_new=v_new, page_table=perm, kv_indptr=kv_indptr,
+                kv_len=torch.tensor(lens, dtype=torch.int32), qo_indptr=qo, k_pages=k_pages,
+                v_pages=v_pages, k_scale=ks, v_scale=vs, num_kv_heads=H, head_dim=D,
+                page_size=P, mode=mode, strides=(P * H * D, H * D, D), num_pages=num_pages)
+
+
+def _slots(case):
+    """(row, page, slot) of every new row, from the page table, read here."""
+    P = case["page_size"]
+    out = []
+    qo = case["qo_indptr"].tolist()
+    for b, L in enumerate(case["kv_len"].tolist()):
+        R = qo[b + 1] - qo[b]
+        for i in range(R):
+            t = L - R + i
+            page = int(case["page_table"][int(case["kv_indptr"][b]) + t // P])
+            out.append((qo[b] + i, page, t % P))
+    return out
+
+
+def pin_append_token_head(mutation=0):
+    case = _append_case(oracle.APPEND_TOKEN_HEAD)
+    # closed forms: a row with one nonzero value, a zero row, a negative peak
+    kn = case["k_new"].float()
+    kn[0, 0] = 0
+    kn[0, 0, 3] = 3.0
+    kn[1, 1] = 0
+    kn[2, 0] = torch.linspace(-5, 1, 8)
+    case["k_new"] = kn.to(torch.bfloat16)
+    kc, vc, ks, vs, rc = oracle.append_kv(**case, mutation=mutation)
+    assert rc == 0
+    P, H, D = case["page_size"], case["num_kv_heads"], case["head_dim"]
+    kcache = kc.reshape(-1, P, H, D)
+    touched = np.zeros((case["num_pages"], P), bool)
+    for row, page, slot in _slots(case):
+        touched[page, slot] = True
+        for h in range(H):
+            for new, cache, scales in ((case["k_new"], kcache, ks),
+                                       (case["v_new"], vc.reshape(-1, P, H, D), vs)):
+                x = new[row, h].float()
+                amax = float(x.abs().max())
+                s = np.float32(np.float32(amax) / np.float32(448.0)) if amax > 0 else np.float32(1.0)
+                assert scales[(page * P + slot) * H + h] == s, (row, h)
+                ref = _e4m3_torch((x / torch.tensor(float(s))).float()).numpy()
+                assert np.array_equal(cache[page, slot, h], ref), (row, h)
+    assert kcache[_slots(case)[0][1], _slots(case)[0][2], 0, 3] == 0x7E
+    assert np.all(kcache[_slots(case)[1][1], _slots(case)[1][2], 1] == 0)
+    assert ks[(_slots(case)[1][1] * P + _slots(case)[1][2]) * H + 1] == 1.0
+    assert kcache[_slots(case)[2][1], _slots(case)[2][2], 0, 0] == 0xFE
+    # nothing else changed
+    before = case["k_pages"].reshape(-1, P, H, D)
+    assert np.array_equal(kcache[~touched], before[~touched])
+    assert np.all(ks.reshape(-1, P, H)[~touched] == -1.0)
+
+
+def pin_append_per_tensor(mutation=0):
+    case = _append_case(oracle.APPEND_TENSOR, seed=1)
+    kc, vc, ks, vs, rc = oracle.append_kv(**case, mutation=mutation)
+    assert rc == 0
+    P, H, D = case["page_size"], case["num_kv_heads"], case["head_dim"]
+    for row, page, slot in _slots(case):
+        for new, cache, s in ((case["k_new"], kc, 0.0125), (case["v_new"], vc, 0.02)):
+            y = new[row].float() / torch.tensor(s, dtype=torch.float32)
+            ref = _e4m3_torch(y.clamp(-448, 448)).numpy()
+            got = cache.reshape(-1, P, H, D)[page, slot]
+            assert np.array_equal(got, ref), row
+
+
+def pin_append_bf16_copy(mutation=0):
+    case = _append_case(oracle.APPEND_BF16, seed=2)
+    kc, vc, _, _, rc = oracle.append_kv(**case, mutation=mutation)
+    assert rc == 0
+    P, H, D = case["page_size"], case["num_kv_heads"], case["head_dim"]
+    k16 = kc.view(np.uint16).reshape(-1, P, H, D)
+    v16 = vc.view(np.uint16).reshape(-1, P, H, D)
+    for row, page, slot in _slots(case):
+        assert np.array_equal(k16[page, slot], case["k_new"][row].view(torch.int16).numpy().view(np.uint16))
+        assert np.array_equal(v16[page, slot], case["v_new"][row].view(torch.int16).numpy().view(np.uint16))
+
+
 ALL_PINS = [pin_e4m3_all_codes, pin_bruteforce, pin_q_zero_closed_form, pin_single_visible_key,
-            pin_constant_v, pin_page_permutation, pin_split_merge, pin_rows_vs_single]
+            pin_constant_v, pin_page_permutation, pin_split_merge, pin_rows_vs_single,
+            pin_e4m3_encode_vs_torch, pin_e4m3_encode_saturates, pin_append_token_head,
+            pin_append_per_tensor, pin_append_bf16_copy]
 
 # Planted mistakes compiled into copies of the oracle (see MUT(k) in pdo_oracle.c).
 MUTATIONS = {
@@ -265,4 +408,8 @@ MUTATIONS = {
     13: "page table read one entry late",
     14: "query row read from the previous row",
     15: "softmax output not divided by its denominator",
+    16: "append: per-token scale amax / 256",
+    17: "append: E4M3 ties go to the odd code",
+    18: "append: new row written one token early",
+    19: "append: E4M3 sign dropped",
 }

@@ -153,6 +153,55 @@ def make_flush(dev):
     return flush
 
 
+# Quantise-on-append of one decode step's new rows, timed like a call:
+# (workload, sizes) -- per-tensor E4M3 (bs 128, R 1, 8 kv heads, D 128),
+# per-(token, head) E4M3 (bs 16, R 8, 2 kv heads, D 256), bf16 (same shape).
+APPEND_SWEEP = [("fp8_decode", {}), ("longctx_fp8_pth", dict(bs=16, R=8)),
+                ("mtp_verify_bf16", dict(bs=16, R=8))]
+
+
+def append_time(name, kw, dev, steps, flush, peak):
+    """Median time of one pda_append_kv (graph-replayed, L2 flushed) and its
+    algorithmic bytes: the new rows' bf16 K and V read, their cache bytes and
+    per-(token, head) scales written, one page-table entry per row and the
+    index arrays."""
+    import torch
+    from paged_split_kv_03_gb300 import binding as B
+    from paged_split_kv_03_gb300.synth import config_workload
+    wl = config_workload(name, device=dev, **kw)
+    dec = B.Decoder(B.params_for(wl, device=dev.index or 0), device=dev)
+    rows, H, D = wl.total_rows, wl.num_kv_heads, wl.head_dim
+    g = torch.Generator(device=dev).manual_seed(11)
+    k_new = torch.randn(rows, H, D, generator=g, device=dev).to(torch.bfloat16)
+    v_new = torch.randn(rows, H, D, generator=g, device=dev).to(torch.bfloat16)
+    mq = max(1, wl.max_q_len)
+    s = torch.cuda.Stream(device=dev)
+
+    def call():
+        B.pda_append_kv(dec.plan, k_new, v_new, wl.page_table, wl.kv_indptr, wl.kv_len,
+                        wl.qo_indptr, mq, wl.k_pages, wl.v_pages, wl.k_scale, wl.v_scale,
+                        dec.scratch, stream=s)
+
+    with torch.cuda.stream(s):
+        call()
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        call()
+    med = statistics.median(time_graph(graph.replay, steps, 3, flush, s))
+    elt = 1 if wl.kv_e4m3 else 2
+    nbytes = 2 * rows * H * D * (2 + elt) + rows * 4 + 4 * (3 * wl.batch + 2)
+    if wl.scale_mode == 2:
+        nbytes += 2 * rows * H * 4
+    elif wl.scale_mode == 1:
+        nbytes += 8
+    status = dec.status()
+    del graph, dec, k_new, v_new, wl
+    return {"workload": f"{name} {kw}".strip(), "us_per_call": med * 1e3,
+            "GB_s": nbytes / (med * 1e-3) / 1e9, "frac_of_peak": nbytes / (med * 1e-3) / 1e9 / peak,
+            "bytes": nbytes, "status": status}
+
+
 def time_graph(fn, steps, warmup, flush, stream):
     """Per-step CUDA-event times (ms) of ``fn`` replayed on ``stream``, with an
     L2 flush enqueued before every step outside the events."""
@@ -328,6 +377,12 @@ def run_ours(args, rank, world, dev):
             if r1 and r8:
                 sweep.append({"workload": f"{name} bs16", "R8_over_R1": r8 / r1})
 
+    append = []
+    if rank == 0 and not args.no_sweep:
+        for name, kw in APPEND_SWEEP:
+            append.append(append_time(name, kw, dev, max(10, args.steps), flush, peak))
+            torch.cuda.empty_cache()
+
     e2e = None
     if rank == 0:
         e_ms, h2d, d2h = e2e_time(wl, dec, max(5, args.steps // 2), 2, dev)
@@ -348,7 +403,7 @@ def run_ours(args, rank, world, dev):
         "warmup": args.warmup, "ms_per_step": ms, "us_per_call": ms * 1e3,
         "frac_of_peak": value / world / peak, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": value / world / PAGES_NUMBER["value"],
-        "vs_baseline_ref": PAGES_NUMBER, "dtype": "e4m3 codes, f16 MMA, fp32 accumulate",
+        "vs_baseline_ref": PAGES_NUMBER, "dtype": "e4m3 (tcgen05 e4m3 x e4m3 MMAs, fp32 accumulate)",
         "data": "synthetic (seeded N(0,1), e4m3 per-tensor)",
         "config": {"workload": HEADLINE_DESC, "parallelism": f"replicas x{world}",
                    "l2": "flushed before every step (memset of 2x L2, then a read of 2x L2), outside the events",
@@ -358,7 +413,7 @@ def run_ours(args, rank, world, dev):
                    "flops_per_call": flops, "tflops": flops / (ms * 1e-3) / 1e12},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "clocks": clk.summary(),
-        "r_sweep": sweep, "source_sha": source_sha(),
+        "r_sweep": sweep, "append": append, "source_sha": source_sha(),
     }
 
 

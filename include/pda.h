@@ -86,7 +86,7 @@ enum { PDA_KERNEL_AUTO = 0, PDA_KERNEL_MMA = 1, PDA_KERNEL_TC = 2 };
 typedef struct {
   int32_t num_qo_heads;    /* Hq, a multiple of num_kv_heads */
   int32_t num_kv_heads;    /* Hkv >= 1 */
-  int32_t head_dim;        /* D: 64, 128 or 256 */
+  int32_t head_dim;        /* D: 64, 128, 256 or 512 (512: tcgen05 path, pages >= 8) */
   int32_t page_size;       /* P: power of two in [1, 256] */
   int32_t q_dtype;         /* PDA_BF16, or PDA_E4M3 (then kv_dtype must be PDA_E4M3) */
   int32_t kv_dtype;        /* PDA_BF16 or PDA_E4M3 */

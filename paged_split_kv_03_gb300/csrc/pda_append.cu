@@ -87,9 +87,14 @@ __device__ __forceinline__ void put_row(const __nv_bfloat16* src, uint8_t* pages
       *reinterpret_cast<uint16_t*>(dst) = c[0];
     } else if constexpr (kPer == 4) {
       *reinterpret_cast<uint32_t*>(dst) = c[0] | (static_cast<uint32_t>(c[1]) << 16);
-    } else {
+    } else if constexpr (kPer == 8) {
       *reinterpret_cast<uint2*>(dst) = make_uint2(c[0] | (static_cast<uint32_t>(c[1]) << 16),
                                                   c[2] | (static_cast<uint32_t>(c[3]) << 16));
+    } else {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(c[0] | (static_cast<uint32_t>(c[1]) << 16),
+                                                  c[2] | (static_cast<uint32_t>(c[3]) << 16),
+                                                  c[4] | (static_cast<uint32_t>(c[5]) << 16),
+                                                  c[6] | (static_cast<uint32_t>(c[7]) << 16));
     }
   }
 }
@@ -168,7 +173,7 @@ extern "C" int pda_append_kv(const pda_plan_t* plan, const void* k_new, const vo
   if (fp8 && (reinterpret_cast<uintptr_t>(k_scale) % 4 || reinterpret_cast<uintptr_t>(v_scale) % 4))
     return PDA_ERR_ALIGNMENT;
   const int D = plan->head_dim;
-  if (D != 64 && D != 128 && D != 256) return PDA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256 && D != 512) return PDA_ERR_UNSUPPORTED;
   if (plan->batch == 0) return PDA_OK;
 
   pda::AppendArgs a;
@@ -195,7 +200,8 @@ extern "C" int pda_append_kv(const pda_plan_t* plan, const void* k_new, const vo
   const int mode = !fp8 ? 0 : plan->scale_mode == PDA_SCALE_TENSOR ? 1 : 2;
   pda::AppendFn fn = D == 64 ? pda::pick_mode<64>(mode)
                      : D == 128 ? pda::pick_mode<128>(mode)
-                                : pda::pick_mode<256>(mode);
+                     : D == 256 ? pda::pick_mode<256>(mode)
+                                : pda::pick_mode<512>(mode);
   const int64_t warps = (int64_t)plan->batch * max_q_len * plan->num_kv_heads;
   const int64_t blocks = (warps + 7) / 8;
   if (blocks > 0x7fffffffLL) return PDA_ERR_INVALID;

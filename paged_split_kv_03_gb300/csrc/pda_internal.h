@@ -103,6 +103,7 @@ int mma_smem_bytes(const pda_plan_t* plan);
 int mma_ctas_per_sm(const pda_plan_t* plan);
 int launch_stage1_mma(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_t s);
 bool tc_supported(const pda_plan_t* plan);
+int tc_rows_limit(const pda_plan_t* plan);
 int tc_variant_rows(const pda_plan_t* plan);
 int tc_smem_bytes(const pda_plan_t* plan);
 int tc_ctas_per_sm(const pda_plan_t* plan);

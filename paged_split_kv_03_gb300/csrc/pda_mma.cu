@@ -533,18 +533,32 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_mma(const __grid_constant_
 
 // ------------------------------------------------------------------ stage 2
 // Log-sum-exp merge of the chunk partials, one output row per (request, row,
-// q head) ("Stage 2 merges per row"). WPI warps share one row's splits
-// (WPI grows with the split count), each keeping four partials in flight,
-// and combine through shared memory; 256 threads per CTA.
+// q head) ("Stage 2 merges per row"). A warp owns a slice of 32 x VW
+// consecutive floats of the row (VW = 4, or 2 at head_dim 64), so each
+// partial is one coalesced vector load per lane; WPI warps per slice share
+// the row's splits (WPI grows with the split count), each keeping eight
+// partials in flight, and combine through shared memory.
 template <int D, int WPI>
-__global__ void __launch_bounds__(256) stage2_merge(const __grid_constant__ DecodeArgs a) {
-  constexpr int kItems = 8 / WPI;  // rows per CTA
-  constexpr int kPer = D / 32;     // floats per lane
-  __shared__ float sh_acc[8][D];
-  __shared__ float sh_w[8];
+struct MergeCfg {
+  static constexpr int kVW = D >= 128 ? 4 : 2;                  // floats per lane
+  static constexpr int kSlices = D / (32 * kVW);                // warps across the row
+  static constexpr int kWarpsPerItem = kSlices * WPI;           // <= 32
+  static constexpr int kItems = kWarpsPerItem >= 8 ? 1 : 8 / kWarpsPerItem;  // rows per CTA
+  static constexpr int kThreads = kItems * kWarpsPerItem * 32;
+  static constexpr int kBatch = 8;                              // partials in flight
+};
+
+template <int D, int WPI>
+__global__ void __launch_bounds__(MergeCfg<D, WPI>::kThreads)
+    stage2_merge(const __grid_constant__ DecodeArgs a) {
+  using M = MergeCfg<D, WPI>;
+  constexpr int kVW = M::kVW;
+  __shared__ __align__(16) float sh_acc[M::kThreads / 32][32 * kVW];
+  __shared__ float sh_w[M::kThreads / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int sub = warp % WPI;
-  const int64_t item = (int64_t)blockIdx.x * kItems + warp / WPI;
+  const int wi = warp % M::kWarpsPerItem;
+  const int slice = wi % M::kSlices, sub = wi / M::kSlices;
+  const int64_t item = (int64_t)blockIdx.x * M::kItems + warp / M::kWarpsPerItem;
   const int64_t per_b = (int64_t)a.max_q_len * a.hq;
   bool valid = false;
   int n = 0;
@@ -566,54 +580,79 @@ __global__ void __launch_bounds__(256) stage2_merge(const __grid_constant__ Deco
   }
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
   const int64_t stride = a.rows_cap * a.hq;  // partial rows per split
+  const int col = slice * 32 * kVW + lane * kVW;
   float mx = -INFINITY;
-  float acc[kPer];
+  float acc[kVW];
 #pragma unroll
-  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  for (int e = 0; e < kVW; ++e) acc[e] = 0.f;
   float wsum = 0.f;
   if (valid) {
     for (int s = lane; s < n; s += 32) mx = fmaxf(mx, a.part_lse[s * stride + base]);
 #pragma unroll
     for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     if (mx != -INFINITY) {
-#pragma unroll 4
-      for (int s = sub; s < n; s += WPI) {
-        const float ls = a.part_lse[s * stride + base];
-        const float w = ls == -INFINITY ? 0.f : exp2f(ls - mx);
-        wsum += w;
-        const float* src = a.part_o + (s * stride + base) * D + lane * kPer;
-        // an empty split's partial may hold anything: select, do not scale
+      for (int s0 = sub; s0 < n; s0 += M::kBatch * WPI) {
+        float ls[M::kBatch];
+        float x[M::kBatch][kVW];
+        // issue the batch's loads first, then combine
 #pragma unroll
-        for (int e = 0; e < kPer; e += 2) {
-          const float2 x = *reinterpret_cast<const float2*>(src + e);
-          acc[e] = w > 0.f ? fmaf(w, x.x, acc[e]) : acc[e];
-          acc[e + 1] = w > 0.f ? fmaf(w, x.y, acc[e + 1]) : acc[e + 1];
+        for (int u = 0; u < M::kBatch; ++u) {
+          const int s = s0 + u * WPI;
+          ls[u] = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < kVW; ++e) x[u][e] = 0.f;
+          if (s < n) {
+            ls[u] = a.part_lse[s * stride + base];
+            const float* src = a.part_o + (s * stride + base) * D + col;
+            if constexpr (kVW == 4) {
+              const float4 v = *reinterpret_cast<const float4*>(src);
+              x[u][0] = v.x; x[u][1] = v.y; x[u][2] = v.z; x[u][3] = v.w;
+            } else {
+              const float2 v = *reinterpret_cast<const float2*>(src);
+              x[u][0] = v.x; x[u][1] = v.y;
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < M::kBatch; ++u) {
+          const float w = ls[u] == -INFINITY ? 0.f : exp2f(ls[u] - mx);
+          wsum += w;
+          // an empty split's partial may hold anything: select, do not scale
+#pragma unroll
+          for (int e = 0; e < kVW; ++e) acc[e] = w > 0.f ? fmaf(w, x[u][e], acc[e]) : acc[e];
         }
       }
     }
   }
   if constexpr (WPI > 1) {
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) sh_acc[warp][lane * kPer + e] = acc[e];
+    for (int e = 0; e < kVW; ++e) sh_acc[warp][lane * kVW + e] = acc[e];
     if (lane == 0) sh_w[warp] = wsum;
     __syncthreads();
     if (sub == 0) {
       for (int k = 1; k < WPI; ++k) {
+        const int w2 = warp + k * M::kSlices;  // same slice, split group k
 #pragma unroll
-        for (int e = 0; e < kPer; ++e) acc[e] += sh_acc[warp + k][lane * kPer + e];
-        wsum += sh_w[warp + k];
+        for (int e = 0; e < kVW; ++e) acc[e] += sh_acc[w2][lane * kVW + e];
+        wsum += sh_w[w2];
       }
     }
   }
   if (!valid || sub != 0) return;
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + base * D + lane * kPer;
-#pragma unroll
-  for (int e = 0; e < kPer; e += 2) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
-    *reinterpret_cast<__nv_bfloat162*>(dst + e) = v;
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + base * D + col;
+  if constexpr (kVW == 4) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(dst) = pk;
+  } else {
+    *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
   }
-  if (lane == 0 && a.lse) a.lse[base] = wsum > 0.f ? (mx + __log2f(wsum)) * kLn2 : -INFINITY;
+  if (slice == 0 && lane == 0 && a.lse)
+    a.lse[base] = wsum > 0.f ? (mx + __log2f(wsum)) * kLn2 : -INFINITY;
 }
 
 // ---------------------------------------------------------------- dispatch
@@ -645,29 +684,42 @@ KernelFn stage1_for(const pda_plan_t* p) {
   switch (p->head_dim) {
     case 64: return pick_stage1<64>(p->kv_dtype, p->q_dtype, p->scale_mode);
     case 128: return pick_stage1<128>(p->kv_dtype, p->q_dtype, p->scale_mode);
-    default: return pick_stage1<256>(p->kv_dtype, p->q_dtype, p->scale_mode);
+    case 256: return pick_stage1<256>(p->kv_dtype, p->q_dtype, p->scale_mode);
+    default: return nullptr;  // head_dim 512: tcgen05 path only
   }
 }
 
-// warps per merged row: one up to 8 splits, then up to 8 splits a warp
+// Warps per slice of a merged row: one up to 8 splits, then up to 8 splits
+// a warp, with at most 16 warps per row (head_dim 512: 4 slices x 4).
 static int stage2_wpi(const pda_plan_t* p) {
-  return p->max_splits <= 8 ? 1 : p->max_splits <= 16 ? 2 : p->max_splits <= 32 ? 4 : 8;
+  const int w = p->max_splits <= 8 ? 1 : p->max_splits <= 16 ? 2 : p->max_splits <= 32 ? 4 : 8;
+  return p->head_dim == 512 && w > 4 ? 4 : w;
+}
+struct Stage2Launch {
+  KernelFn fn;
+  int items_per_cta, threads;
+};
+template <int D, int WPI>
+Stage2Launch stage2_entry() {
+  using M = MergeCfg<D, WPI>;
+  return {stage2_merge<D, WPI>, M::kItems, M::kThreads};
 }
 template <int D>
-KernelFn stage2_pick(int wpi) {
+Stage2Launch stage2_pick(int wpi) {
   switch (wpi) {
-    case 1: return stage2_merge<D, 1>;
-    case 2: return stage2_merge<D, 2>;
-    case 4: return stage2_merge<D, 4>;
-    default: return stage2_merge<D, 8>;
+    case 1: return stage2_entry<D, 1>();
+    case 2: return stage2_entry<D, 2>();
+    case 4: return stage2_entry<D, 4>();
+    default: return stage2_entry<D, (D == 512 ? 4 : 8)>();
   }
 }
-KernelFn stage2_for(const pda_plan_t* p) {
+Stage2Launch stage2_for(const pda_plan_t* p) {
   const int wpi = stage2_wpi(p);
   switch (p->head_dim) {
     case 64: return stage2_pick<64>(wpi);
     case 128: return stage2_pick<128>(wpi);
-    default: return stage2_pick<256>(wpi);
+    case 256: return stage2_pick<256>(wpi);
+    default: return stage2_pick<512>(wpi);
   }
 }
 
@@ -677,7 +729,8 @@ int mma_smem_bytes(const pda_plan_t* p) {
   switch (p->head_dim) {
     case 64: return smem_of<64>(p->kv_dtype, p->q_dtype, p->scale_mode);
     case 128: return smem_of<128>(p->kv_dtype, p->q_dtype, p->scale_mode);
-    default: return smem_of<256>(p->kv_dtype, p->q_dtype, p->scale_mode);
+    case 256: return smem_of<256>(p->kv_dtype, p->q_dtype, p->scale_mode);
+    default: return -1;  // head_dim 512: no mma.sync build
   }
 }
 
@@ -691,6 +744,7 @@ int mma_ctas_per_sm(const pda_plan_t* p) {
 
 int launch_stage1_mma(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_t s) {
   KernelFn k1 = stage1_for(plan);
+  if (!k1) return PDA_ERR_UNSUPPORTED;
   const int smem = plan->stage1_smem_bytes;
   if (cudaFuncSetAttribute(reinterpret_cast<const void*>(k1),
                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
@@ -715,14 +769,15 @@ int launch_stage2(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_t s
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t c2 = {};
-  const int per_cta = 8 / stage2_wpi(plan);
+  const Stage2Launch l2 = stage2_for(plan);
+  const int per_cta = l2.items_per_cta;
   c2.gridDim = dim3(static_cast<unsigned>((items + per_cta - 1) / per_cta));
-  c2.blockDim = dim3(256);
+  c2.blockDim = dim3(static_cast<unsigned>(l2.threads));
   c2.dynamicSmemBytes = 0;
   c2.stream = s;
   c2.attrs = attr;
   c2.numAttrs = 1;
-  if (cudaLaunchKernelEx(&c2, stage2_for(plan), args) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&c2, l2.fn, args) != cudaSuccess) {
     cudaGetLastError();
     return PDA_ERR_CUDA;
   }

@@ -58,7 +58,8 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
   // ---- shape checks
   if (p->num_qo_heads <= 0 || p->num_kv_heads <= 0 || p->num_qo_heads % p->num_kv_heads)
     return PDA_ERR_INVALID;
-  if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256) return PDA_ERR_UNSUPPORTED;
+  if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256 && p->head_dim != 512)
+    return PDA_ERR_UNSUPPORTED;
   if (!is_pow2(p->page_size) || p->page_size > 256) return PDA_ERR_UNSUPPORTED;
   if (p->kv_dtype != PDA_BF16 && p->kv_dtype != PDA_E4M3) return PDA_ERR_UNSUPPORTED;
   if (p->q_dtype != PDA_BF16 && p->q_dtype != PDA_E4M3) return PDA_ERR_UNSUPPORTED;
@@ -109,12 +110,15 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
   pl.group = p->num_qo_heads / p->num_kv_heads;
   pl.num_sms = num_sms;
   if (p->kernel == PDA_KERNEL_TC && !pda::tc_supported(&pl)) return PDA_ERR_UNSUPPORTED;
-  // AUTO takes the tcgen05 path wherever it is built (head_dim 128/256, pages >= 8)
+  // AUTO takes the tcgen05 path wherever it is built (head_dim 128/256/512,
+  // pages >= 8); head_dim 512 has no mma.sync build (its O tile would not fit
+  // the registers)
   if (p->kernel == PDA_KERNEL_AUTO)
     pl.kernel = pda::tc_supported(&pl) ? PDA_KERNEL_TC : PDA_KERNEL_MMA;
   else
     pl.kernel = p->kernel;
-  pl.rows_per_cta = pl.kernel == PDA_KERNEL_TC ? pda::kTcRowsPerCta : pda::kMmaRowsPerCta;
+  if (pl.kernel == PDA_KERNEL_MMA && p->head_dim == 512) return PDA_ERR_UNSUPPORTED;
+  pl.rows_per_cta = pl.kernel == PDA_KERNEL_TC ? pda::tc_rows_limit(&pl) : pda::kMmaRowsPerCta;
 
   // Query heads per CTA for a request with R rows: the largest divisor of the
   // GQA group whose R x heads tile fits the CTA's rows.

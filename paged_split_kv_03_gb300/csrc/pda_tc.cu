@@ -338,7 +338,8 @@ template <int D, int KVT, int QT, int SMODE, int NMAX>
 struct TcCfg {
   static constexpr int kD = D;
   static constexpr int kNmax = NMAX;
-  static constexpr int kCtasPerSm = NMAX <= 16 ? 2 : 1;
+  // head_dim 512: a K (or V) tile alone is 64-128 KB, one CTA per SM
+  static constexpr int kCtasPerSm = NMAX <= 16 && D <= 256 ? 2 : 1;
   // softmax warps: 4 per TMEM lane quadrant when a CTA holds up to 64 columns, else 2
   static constexpr int kSmWarps = NMAX <= 16 ? 8 : 16;
   static constexpr int kSmThreads = 32 * kSmWarps;
@@ -346,7 +347,7 @@ struct TcCfg {
   // issues a 16-row page box about every 130 cycles, too few for one CTA
   // per SM on small pages, so the 64-column build splits each chunk's
   // boxes over three warps
-  static constexpr int kProducers = NMAX > 16 ? 3 : 1;
+  static constexpr int kProducers = NMAX > 16 || kCtasPerSm == 1 ? 3 : 1;
   static constexpr int kProdWarp1 = 2 + kSmWarps;
   static constexpr int kThreads = 64 + kSmThreads + 32 * (kProducers - 1);
   static constexpr int kColGroups = kSmWarps / 4;   // warps sharing a lane quadrant
@@ -377,7 +378,7 @@ struct TcCfg {
   static constexpr int kTmemNeed = 2 * kSCols + kOBlocks * kOCols;
   static constexpr int kTmemCols =
       kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
-  static_assert(kTmemNeed <= 512, "TMEM budget");
+  // two CTAs of an SM share its 512 columns
   // barriers (512 B), then m_used, alpha, colscale, red[4], linv (kNmax floats each)
   static constexpr int kSmallBytes = 512 + 8 * kNmax * 4;
   static constexpr int kBudget = kCtasPerSm == 2 ? 228 * 1024 / 2 - 1024 : 227 * 1024;
@@ -386,7 +387,12 @@ struct TcCfg {
   static constexpr int kRingRaw = kAvail / kSlot > 12 ? 12 : kAvail / kSlot;
   // bf16 V blocks span two adjacent slots: keep the ring even so pairs never wrap
   static constexpr int kRing = kF8 ? kRingRaw : (kRingRaw & ~1);
-  static constexpr bool kBuildable = kRing >= kTileSlots;
+  // The MMA issuer frees each slot as soon as its MMAs finish, so the ring
+  // must hold one whole K (or V) tile (the softmax zeroes the tail rows of
+  // the last V tile before its PV); head_dim <= 256 builds keep two tiles
+  // in flight, head_dim 512 (a tile of 8 or 4 slots) as many as fit.
+  static constexpr bool kBuildable = kRing >= (D > 256 ? kChunks : kTileSlots) &&
+                                     kTmemNeed <= 512 && kTmemCols * kCtasPerSm <= 512;
   static constexpr int kSmem = kQBytes + kPBytes + kRing * kSlot + kSmallBytes;
 };
 
@@ -938,7 +944,7 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
     } else {
       // bf16 query -> Q * 2^a = Q1 + Q2/16 in E4M3 (rows n and N + n), with
       // one exponent a for the CTA, from its largest |Q|
-      constexpr int kPer = D / 32;  // elements per lane (8 or 4)
+      constexpr int kPer = D / 32;  // elements per lane (16, 8 or 4)
       auto load_row = [&](int n, float* xv) {
         if (n < M) {
           const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(a.q) +
@@ -992,16 +998,17 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           uint8_t* dst = q_s + (byte / 128) * C::kQAtomBytes + sw128(t * N + n, byte % 128);
-          if constexpr (kPer == 8) {
-            uint2 w;
-            w.x = codes[t][0] | (codes[t][1] << 8) | (codes[t][2] << 16) |
-                  ((uint32_t)codes[t][3] << 24);
-            w.y = codes[t][4] | (codes[t][5] << 8) | (codes[t][6] << 16) |
-                  ((uint32_t)codes[t][7] << 24);
-            *reinterpret_cast<uint2*>(dst) = w;
+          uint32_t w[kPer / 4];
+#pragma unroll
+          for (int e = 0; e < kPer / 4; ++e)
+            w[e] = codes[t][4 * e] | (codes[t][4 * e + 1] << 8) | (codes[t][4 * e + 2] << 16) |
+                   ((uint32_t)codes[t][4 * e + 3] << 24);
+          if constexpr (kPer == 16) {
+            *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+          } else if constexpr (kPer == 8) {
+            *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
           } else {
-            *reinterpret_cast<uint32_t*>(dst) = codes[t][0] | (codes[t][1] << 8) |
-                                                (codes[t][2] << 16) | ((uint32_t)codes[t][3] << 24);
+            *reinterpret_cast<uint32_t*>(dst) = w[0];
           }
         }
       }
@@ -1096,22 +1103,23 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
           for (int kk = 0; kk < 4; ++kk)
             mma<kF8>(tmem + sb * C::kSCols, sdesc(abase + kk * 32, 16, 1024),
                      sdesc(bbase + kk * 32, 16, 1024), id_s, (c | kk) != 0);
+          mma_commit(empty + slot);  // the slot is free once these MMAs finish
         }
         mma_commit(s_full + sb);
-        for (int c = 0; c < C::kChunks; ++c) mma_commit(empty + (gk + c) % R_);
         return true;
       };
       // O^T += V_j^T P_j^T as soon as the softmax has written P_j
       auto issue_pv = [&](int j) -> bool {
         if (!bar_wait(p_full + (j & 1), (j >> 1) & 1, abort_flag, a.status)) return false;
         const uint32_t gv = static_cast<uint32_t>(unit_pos_v(j, ntiles)) * C::kChunks;
-        for (int c = 0; c < C::kChunks; ++c)
-          if (!bar_wait(full + (gv + c) % R_, ((gv + c) / R_) & 1u, abort_flag, a.status))
-            return false;
-        fence_after();
+        constexpr int kBlkSlots = kF8 ? 1 : 2;  // ring slots of one 128-d V block
         const uint32_t pbuf = p_addr + static_cast<uint32_t>(j % C::kPBufs) * C::kPBufBytes;
 #pragma unroll
         for (int blk = 0; blk < C::kOBlocks; ++blk) {
+          for (int c = blk * kBlkSlots; c < (blk + 1) * kBlkSlots; ++c)
+            if (!bar_wait(full + (gv + c) % R_, ((gv + c) / R_) & 1u, abort_flag, a.status))
+              return false;
+          fence_after();
           if constexpr (kF8) {
             // V block = one slot (128 d); K = 32 tokens per MMA; both P terms
             // in one MMA (B rows 0..N-1 term 1, N..2N-1 term 2)
@@ -1132,9 +1140,10 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
                          sdesc(pbuf + (kk >> 2) * C::kPAtomBytes + (kk & 3) * 32, 16, 1024),
                          id_p, !(j == 0 && kk == 0));
           }
+          for (int c = blk * kBlkSlots; c < (blk + 1) * kBlkSlots; ++c)
+            mma_commit(empty + (gv + c) % R_);
         }
         mma_commit(pv_done + (j & 1));
-        for (int c = 0; c < C::kChunks; ++c) mma_commit(empty + (gv + c) % R_);
         return true;
       };
       if (alive) alive = issue_s(0);
@@ -1241,6 +1250,10 @@ auto tc_select(const pda_plan_t* p, int nmax, F f) {
     if (nmax <= 16) { PDA_TC_CASES(128, 16) }
     PDA_TC_CASES(128, 64)
   }
+  if (p->head_dim == 512) {
+    if (nmax <= 16) { PDA_TC_CASES(512, 16) }
+    PDA_TC_CASES(512, 64)
+  }
   if (nmax <= 16) { PDA_TC_CASES(256, 16) }
   PDA_TC_CASES(256, 64)
 #undef PDA_TC_CASES
@@ -1317,7 +1330,16 @@ bool make_map(CUtensorMap* m, const void* base, const pda_plan_t* p, int* slot_d
 }  // namespace
 
 bool tc_supported(const pda_plan_t* p) {
-  return (p->head_dim == 128 || p->head_dim == 256) && p->page_size >= 8 && p->page_size <= 256;
+  return (p->head_dim == 128 || p->head_dim == 256 || p->head_dim == 512) && p->page_size >= 8 &&
+         p->page_size <= 256;
+}
+
+// Rows x heads a CTA may hold: 64, except head_dim 512 over an E4M3 cache,
+// whose two-term O accumulator (4 blocks x 2N columns) leaves TMEM room for
+// 16 ("quantized head_dim 512 takes 16 rows x heads", "perf(attention): run
+// up to 8 query rows per request in the triton decode kernel").
+int tc_rows_limit(const pda_plan_t* p) {
+  return p->head_dim == 512 && p->kv_dtype == PDA_E4M3 ? 16 : kTcRowsPerCta;
 }
 
 // Largest N (rows x heads, rounded up to 16) a CTA of this plan can hold.
@@ -1338,7 +1360,11 @@ int tc_variant_rows(const pda_plan_t* p) {
 
 int tc_smem_bytes(const pda_plan_t* p) { return tc_select(p, p->rows_per_cta, GetSmem()); }
 
-int tc_ctas_per_sm(const pda_plan_t* p) { return p->rows_per_cta <= 16 ? 2 : 1; }
+struct GetCtasPerSm {
+  template <int D, int KVT, int QT, int SMODE, int NMAX>
+  int get() { return TcCfg<D, KVT, QT, SMODE, NMAX>::kCtasPerSm; }
+};
+int tc_ctas_per_sm(const pda_plan_t* p) { return tc_select(p, p->rows_per_cta, GetCtasPerSm()); }
 
 struct GetThreads {
   template <int D, int KVT, int QT, int SMODE, int NMAX>

@@ -303,6 +303,11 @@ def make_workload(*, name: str = "custom", batch: int, rows: Union[int, Sequence
 # The five workloads the benchmark and the parity tests use.
 
 CONFIG_NAMES = ("tiny", "fp8_decode", "mtp_verify_bf16", "longctx_fp8_pth", "mixed")
+# head_dim 512 with one kv head: the full-attention layers of the Gemma-4
+# MTP runs ("perf(attention): run up to 8 query rows per request in the
+# triton decode kernel", "Gemma-4 MTP at long context"); 16 query heads
+# (the page gives no count), bs 1, R 1 / 4 / 8 (no spec, k = 3, k = 7)
+D512_NAMES = ("d512_mtp_bf16", "d512_mtp_fp8")
 
 
 def config_workload(name: str, *, R: Optional[int] = None, bs: Optional[int] = None,
@@ -317,7 +322,18 @@ def config_workload(name: str, *, R: Optional[int] = None, bs: Optional[int] = N
                     e4m3 K/V with a scale per (token, kv head), 1% K channels x20, Q bf16
     mixed           bs 64, 48/2 heads, D 128, R_b ~ U{1..8}, ctx_b ~ U[1024, 65536],
                     window 64 on half the requests, page 32, bf16
+    d512_mtp_bf16   bs 1 (16), R 4 (1, 8), 16/1 heads, D 512, ctx 32768, page 16, bf16
+    d512_mtp_fp8    bs 1 (16), R 4 (1, 8), 16/1 heads, D 512, ctx 32768, page 16, e4m3
+                    K/V with a scale per (token, kv head), Q bf16 (seeds 1100 + index)
     """
+    if name in D512_NAMES:
+        seed = 1100 + D512_NAMES.index(name) if seed is None else seed
+        args = dict(batch=bs or 1, rows=R or 4, kv_lens=32768, num_qo_heads=16, num_kv_heads=1,
+                    head_dim=512, page_size=16)
+        if name == "d512_mtp_fp8":
+            args.update(kv_dtype="e4m3", q_dtype="bf16", scale_mode=SCALE_TOKEN_HEAD)
+        args.update(kw)
+        return make_workload(name=name, seed=seed, device=device, **args)
     idx = CONFIG_NAMES.index(name)
     seed = 1000 + idx if seed is None else seed
     if name == "tiny":

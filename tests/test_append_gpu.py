@@ -1,7 +1,7 @@
 """GPU parity of quantise-on-append (pda_append_kv) against the oracle:
 every byte of both caches and every scale must match exactly, for the three
 cache kinds (bf16 copy, E4M3 per tensor, E4M3 per token and kv head), head
-dims 64 / 128 / 256, both cache layouts, ragged rows per request, and the
+dims 64 / 128 / 256 / 512, both cache layouts, ragged rows per request, and the
 status bits of requests the kernel must skip."""
 from __future__ import annotations
 
@@ -30,6 +30,12 @@ CASES = {
                             num_kv_heads=8),
     "bf16_d256_p16": dict(kv_dtype="bf16", scale_mode=SCALE_NONE, head_dim=256, page_size=16,
                           rows=[4, 1], kv_lens=[33, 16], num_qo_heads=16, num_kv_heads=2),
+    "pth_d512_p16": dict(kv_dtype="e4m3", scale_mode=SCALE_TOKEN_HEAD, head_dim=512,
+                         page_size=16, rows=[2, 8], kv_lens=[40, 300], num_qo_heads=16,
+                         num_kv_heads=1),
+    "bf16_d512_p64_hnd": dict(kv_dtype="bf16", scale_mode=SCALE_NONE, head_dim=512,
+                              page_size=64, rows=[3], kv_lens=[70], num_qo_heads=4,
+                              num_kv_heads=2, layout="HND"),
 }
 
 

@@ -103,6 +103,29 @@ def test_plan_tail_split(lib):
     assert even.tail_from == even.batch and even.grid_ctas == 76 * 8
 
 
+D512 = dict(num_qo_heads=16, num_kv_heads=1, head_dim=512, page_size=16, max_batch=1,
+            max_kv_len=131072, kv_stride_page=16 * 512, kv_stride_token=512, kv_stride_head=512)
+
+
+def test_plan_head_dim_512(lib):
+    # bf16: up to 64 rows x heads per CTA (R 8 -> 8 heads, 2 head blocks)
+    plan, _, rc = B.pda_plan(_params(**D512))
+    assert rc == 0 and plan.kernel == B.PDA_KERNEL_TC and plan.rows_per_cta == 64
+    assert plan.heads_per_cta[1] == 16 and plan.heads_per_cta[8] == 8 and plan.head_blocks == 2
+    assert plan.stage1_smem_bytes <= 227 * 1024
+    # E4M3: 16 rows x heads (the two-term O accumulator's TMEM share)
+    for sm in (1, 2):
+        q, _, rc = B.pda_plan(_params(kv_dtype=1, scale_mode=sm, **D512))
+        assert rc == 0 and q.rows_per_cta == 16
+        assert [q.heads_per_cta[r] for r in (1, 2, 4, 8)] == [16, 8, 4, 2] and q.head_blocks == 8
+    # R 1 over bf16 fits 16 columns: the 16-column build, still one CTA per SM
+    one, _, _ = B.pda_plan(_params(**dict(D512, max_q_len=1)))
+    assert one.rows_per_cta == 16 and one.head_blocks == 1
+    # no mma.sync build for head_dim 512
+    _, _, rc = B.pda_plan(_params(kernel=B.PDA_KERNEL_MMA, **D512), check=False)
+    assert rc == B.PDA_ERR_UNSUPPORTED
+
+
 @pytest.mark.parametrize("bad,code", [
     (dict(num_qo_heads=15), B.PDA_ERR_INVALID),
     (dict(head_dim=96), B.PDA_ERR_UNSUPPORTED),

@@ -65,6 +65,18 @@ SMALL = {
                       head_dim=128, page_size=256, windows=[100, 0]),
     "bf16_p1": dict(batch=2, rows=2, kv_lens=[130, 3], num_qo_heads=4, num_kv_heads=2,
                     head_dim=64, page_size=1, chunk=64),
+    # head_dim 512 (tcgen05 path only): one kv head, G = 16 / 8 / 2
+    "bf16_d512_g16_r148": dict(batch=3, rows=[1, 4, 8], kv_lens=[700, 1500, 33],
+                               windows=[0, 64, 0], num_qo_heads=16, num_kv_heads=1,
+                               head_dim=512, page_size=16, chunk=4),
+    "bf16_d512_g2_p64": dict(batch=2, rows=[8, 2], kv_lens=[900, 130], num_qo_heads=4,
+                             num_kv_heads=2, head_dim=512, page_size=64, layout="HND"),
+    "fp8pth_d512_g16": dict(batch=2, rows=[8, 3], kv_lens=[1300, 260], num_qo_heads=16,
+                            num_kv_heads=1, head_dim=512, page_size=64, kv_dtype="e4m3",
+                            scale_mode=SCALE_TOKEN_HEAD, chunk=8),
+    "fp8t_qfp8_d512_g8": dict(batch=2, rows=[2, 1], kv_lens=[1000, 129], num_qo_heads=8,
+                              num_kv_heads=1, head_dim=512, page_size=32, kv_dtype="e4m3",
+                              q_dtype="e4m3", scale_mode=SCALE_TENSOR),
 }
 # peaked stress cases (Q x 4): compared with the bf16 output's half-ulp added;
 # the running maxima move often, so the lazy O rescale runs
@@ -74,6 +86,11 @@ PEAKED_SMALL = {
     "fp8pth": dict(batch=2, rows=[4, 8], kv_lens=[2000, 900], num_qo_heads=16, num_kv_heads=2,
                    head_dim=256, page_size=16, q_mult=4.0, chunk=16, kv_dtype="e4m3",
                    scale_mode=SCALE_TOKEN_HEAD),
+    "bf16_d512": dict(batch=2, rows=[4, 8], kv_lens=[2000, 900], num_qo_heads=16,
+                      num_kv_heads=1, head_dim=512, page_size=16, q_mult=4.0, chunk=16),
+    "fp8pth_d512": dict(batch=2, rows=[4, 8], kv_lens=[2000, 900], num_qo_heads=16,
+                        num_kv_heads=1, head_dim=512, page_size=16, q_mult=4.0, chunk=16,
+                        kv_dtype="e4m3", scale_mode=SCALE_TOKEN_HEAD),
 }
 
 
@@ -88,8 +105,13 @@ KERNELS = {"mma": B.PDA_KERNEL_MMA, "tc": B.PDA_KERNEL_TC}
 
 
 def _tc_ok(wl):
-    """Shapes the tcgen05 path is built for (head_dim 128/256, pages of >= 8)."""
-    return wl.head_dim in (128, 256) and wl.page_size >= 8
+    """Shapes the tcgen05 path is built for (head_dim 128/256/512, pages of >= 8)."""
+    return wl.head_dim in (128, 256, 512) and wl.page_size >= 8
+
+
+def _mma_ok(wl):
+    """Shapes the mma.sync path is built for (head_dim up to 256)."""
+    return wl.head_dim <= 256
 
 
 @pytest.mark.parametrize("kernel", sorted(KERNELS))
@@ -98,6 +120,8 @@ def test_small_full_parity(name, kernel):
     wl, chunk = _make(name, SMALL[name])
     if kernel == "tc" and not _tc_ok(wl):
         pytest.skip("shape served by the mma.sync path only")
+    if kernel == "mma" and not _mma_ok(wl):
+        pytest.skip("shape served by the tcgen05 path only")
     out, lse, status, dec = run_decode(wl, chunk_pages=chunk, kernel=KERNELS[kernel])
     assert status == 0
     ref_o, ref_l = oracle_ref(wl)
@@ -108,6 +132,8 @@ def test_small_full_parity(name, kernel):
 @pytest.mark.parametrize("kind", sorted(PEAKED_SMALL))
 def test_small_peaked_parity(kind, kernel):
     wl, chunk = _make(f"{kind}_peaked", PEAKED_SMALL[kind])
+    if kernel == "mma" and not _mma_ok(wl):
+        pytest.skip("shape served by the tcgen05 path only")
     out, lse, status, dec = run_decode(wl, chunk_pages=chunk, kernel=KERNELS[kernel])
     assert status == 0
     ref_o, ref_l = oracle_ref(wl)
@@ -139,6 +165,10 @@ CONFIGS = [
     ("longctx_fp8_pth", dict(bs=1, R=8), 64),
     ("longctx_fp8_pth", dict(bs=16, R=8), 64),
     ("mixed", {}, 160),
+    ("d512_mtp_bf16", dict(bs=1, R=4), None),
+    ("d512_mtp_bf16", dict(bs=1, R=8, kv_lens=131072), 48),
+    ("d512_mtp_fp8", dict(bs=1, R=8), None),
+    ("d512_mtp_fp8", dict(bs=1, R=4, kv_lens=131072), 48),
 ]
 
 

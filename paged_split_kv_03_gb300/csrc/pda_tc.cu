@@ -1195,6 +1195,9 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
     x.single = sr.num_splits == 1;
     if constexpr (NMAX <= 16) {
       softmax_role<C, SMODE, 1>(a, x, warp, lane, tid);
+    } else if constexpr (NMAX <= 32) {
+      if (N <= 16) softmax_role<C, SMODE, 1>(a, x, warp, lane, tid);
+      else softmax_role<C, SMODE, 2>(a, x, warp, lane, tid);
     } else {
       switch (N >> 4) {
         case 1: softmax_role<C, SMODE, 1>(a, x, warp, lane, tid); break;
@@ -1252,6 +1255,7 @@ auto tc_select(const pda_plan_t* p, int nmax, F f) {
   }
   if (p->head_dim == 512) {
     if (nmax <= 16) { PDA_TC_CASES(512, 16) }
+    if (nmax <= 32) { PDA_TC_CASES(512, 32) }
     PDA_TC_CASES(512, 64)
   }
   if (nmax <= 16) { PDA_TC_CASES(256, 16) }
@@ -1335,11 +1339,12 @@ bool tc_supported(const pda_plan_t* p) {
 }
 
 // Rows x heads a CTA may hold: 64, except head_dim 512 over an E4M3 cache,
-// whose two-term O accumulator (4 blocks x 2N columns) leaves TMEM room for
-// 16 ("quantized head_dim 512 takes 16 rows x heads", "perf(attention): run
-// up to 8 query rows per request in the triton decode kernel").
+// whose two-term S and O accumulators (2 x 2N + 4 x 2N columns) leave TMEM
+// room for 32. The pages' kernel takes 16 for quantised head_dim 512
+// ("perf(attention): run up to 8 query rows per request in the triton
+// decode kernel"); 32 halves the head blocks that re-read the cache.
 int tc_rows_limit(const pda_plan_t* p) {
-  return p->head_dim == 512 && p->kv_dtype == PDA_E4M3 ? 16 : kTcRowsPerCta;
+  return p->head_dim == 512 && p->kv_dtype == PDA_E4M3 ? 32 : kTcRowsPerCta;
 }
 
 // Largest N (rows x heads, rounded up to 16) a CTA of this plan can hold.
@@ -1353,8 +1358,11 @@ static int plan_nmax(const pda_plan_t* p) {
 }
 
 int tc_variant_rows(const pda_plan_t* p) {
-  // the two-CTAs-per-SM build when every CTA fits 16 columns and it exists
-  if (plan_nmax(p) <= 16 && tc_select(p, 16, GetSmem()) > 0) return 16;
+  // the smallest build that holds every CTA's columns (16: two CTAs per SM
+  // up to head_dim 256; head_dim 512 also has a 32-column build)
+  const int n = plan_nmax(p);
+  if (n <= 16 && tc_select(p, 16, GetSmem()) > 0) return 16;
+  if (p->head_dim == 512 && n <= 32 && tc_select(p, 32, GetSmem()) > 0) return 32;
   return 64;
 }
 

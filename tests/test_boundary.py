@@ -113,11 +113,15 @@ def test_plan_head_dim_512(lib):
     assert rc == 0 and plan.kernel == B.PDA_KERNEL_TC and plan.rows_per_cta == 64
     assert plan.heads_per_cta[1] == 16 and plan.heads_per_cta[8] == 8 and plan.head_blocks == 2
     assert plan.stage1_smem_bytes <= 227 * 1024
-    # E4M3: 16 rows x heads (the two-term O accumulator's TMEM share)
+    # E4M3: 32 rows x heads (the two-term S and O accumulators' TMEM share)
     for sm in (1, 2):
         q, _, rc = B.pda_plan(_params(kv_dtype=1, scale_mode=sm, **D512))
-        assert rc == 0 and q.rows_per_cta == 16
-        assert [q.heads_per_cta[r] for r in (1, 2, 4, 8)] == [16, 8, 4, 2] and q.head_blocks == 8
+        assert rc == 0 and q.rows_per_cta == 32
+        assert [q.heads_per_cta[r] for r in (1, 2, 4, 8)] == [16, 16, 8, 4] and q.head_blocks == 4
+        assert q.stage1_smem_bytes <= 227 * 1024
+    # two rows over bf16: the 32-column build
+    two, _, _ = B.pda_plan(_params(**dict(D512, max_q_len=2)))
+    assert two.rows_per_cta == 32 and two.head_blocks == 1
     # R 1 over bf16 fits 16 columns: the 16-column build, still one CTA per SM
     one, _, _ = B.pda_plan(_params(**dict(D512, max_q_len=1)))
     assert one.rows_per_cta == 16 and one.head_blocks == 1

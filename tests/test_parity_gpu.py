@@ -74,6 +74,8 @@ SMALL = {
     "fp8pth_d512_g16": dict(batch=2, rows=[8, 3], kv_lens=[1300, 260], num_qo_heads=16,
                             num_kv_heads=1, head_dim=512, page_size=64, kv_dtype="e4m3",
                             scale_mode=SCALE_TOKEN_HEAD, chunk=8),
+    "bf16_d512_g16_r2": dict(batch=2, rows=[2, 1], kv_lens=[600, 1300], num_qo_heads=16,
+                             num_kv_heads=1, head_dim=512, page_size=32),
     "fp8t_qfp8_d512_g8": dict(batch=2, rows=[2, 1], kv_lens=[1000, 129], num_qo_heads=8,
                               num_kv_heads=1, head_dim=512, page_size=32, kv_dtype="e4m3",
                               q_dtype="e4m3", scale_mode=SCALE_TENSOR),

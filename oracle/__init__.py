@@ -10,8 +10,8 @@ The arithmetic lives in ``pdo_oracle.c`` (plain C, fp64, OpenMP over output
 items); this module compiles it with gcc on first use and wraps it with
 ctypes. The method it states, and the readings of the pages it takes, are in
 that file's header: per-row causal limit p_i = L - R + i, optional sliding
-window of W keys, contiguous GQA groups, bf16 or OCP E4M3 cache values with
-per-tensor or per-(token, kv head) scales ("perf(attention): run up to 8
+window of W keys, contiguous GQA groups, bf16, OCP E4M3 or int8 cache values
+with per-tensor or per-(token, kv head) scales ("perf(attention): run up to 8
 query rows per request in the triton decode kernel", section "Changes";
 "fp8 support", section "Functionality"; "Naive Support for Hopper FP8
 Prefill Kernel with Per-Head Quantization", item 3).
@@ -78,6 +78,8 @@ def _load(mutation: int = 0):
     lib.pdo_max_threads.restype = i32
     lib.pdo_e4m3_encode.argtypes = [ctypes.c_float]
     lib.pdo_e4m3_encode.restype = ctypes.c_uint8
+    lib.pdo_int8_encode.argtypes = [ctypes.c_float]
+    lib.pdo_int8_encode.restype = ctypes.c_uint8
     lib.pdo_append.argtypes = [i32, i32, i32, i32, i32, i64, i64, i64, i64, vp, vp, vp, vp, vp,
                                vp, vp, vp, vp, vp]
     lib.pdo_append.restype = i32
@@ -118,12 +120,13 @@ def max_threads() -> int:
 def attention(*, q, k_pages, v_pages, page_table, kv_indptr, kv_len, qo_indptr, window,
               sm_scale, k_scale=None, v_scale=None, num_qo_heads, num_kv_heads, head_dim,
               page_size, q_e4m3, kv_e4m3, scale_mode, strides, num_pages, items=None,
-              split_tokens=0, num_threads=0, mutation=0, check=True):
+              split_tokens=0, num_threads=0, mutation=0, check=True, kv_int8=False):
     """fp64 attention for the given (row, q head) items.
 
     Arrays are CPU tensors / numpy arrays holding raw cache payloads (bf16 as
-    16-bit words, e4m3 as bytes). ``strides`` = (page, token, head) in
-    elements. ``items`` = flat indices row*Hq + h (None: every item).
+    16-bit words, e4m3 and int8 as bytes; ``kv_int8`` marks an int8 cache).
+    ``strides`` = (page, token, head) in elements. ``items`` = flat indices
+    row*Hq + h (None: every item).
     Returns (out [n, D] float64, lse [n] float64, status).
     """
     lib = _load(mutation)
@@ -144,8 +147,9 @@ def attention(*, q, k_pages, v_pages, page_table, kv_indptr, kv_len, qo_indptr, 
     out = np.zeros((max(n, 0), head_dim), dtype=np.float64)
     lse = np.zeros((max(n, 0),), dtype=np.float64)
     sp, st, sh = (int(s) for s in strides)
+    kv_dtype = 2 if kv_int8 else int(bool(kv_e4m3))
     rc = lib.pdo_attention(batch, num_qo_heads, num_kv_heads, head_dim, page_size, int(q_e4m3),
-                           int(kv_e4m3), int(scale_mode), sp, st, sh, int(num_pages), _ptr(q_),
+                           kv_dtype, int(scale_mode), sp, st, sh, int(num_pages), _ptr(q_),
                            _ptr(k_), _ptr(v_), _ptr(pt), _ptr(ki), _ptr(kl), _ptr(qi), _ptr(win),
                            float(sm_scale), _ptr(ks), _ptr(vs), int(split_tokens), _ptr(it),
                            n if it is not None else 0, _ptr(out), _ptr(lse), int(num_threads))
@@ -164,7 +168,7 @@ def attention_for(wl, items=None, split_tokens=0, num_threads=0, mutation=0, **o
                 num_qo_heads=wl.num_qo_heads, num_kv_heads=wl.num_kv_heads,
                 head_dim=wl.head_dim, page_size=wl.page_size, q_e4m3=wl.q_e4m3,
                 kv_e4m3=wl.kv_e4m3, scale_mode=wl.scale_mode, strides=wl.strides,
-                num_pages=wl.num_pages)
+                num_pages=wl.num_pages, kv_int8=getattr(wl, "kv_int8", False))
     args.update(overrides)
     return attention(items=items, split_tokens=split_tokens, num_threads=num_threads,
                      mutation=mutation, **args)
@@ -175,7 +179,15 @@ def e4m3_encode(y: float, mutation: int = 0) -> int:
     return int(_load(mutation).pdo_e4m3_encode(float(y)))
 
 
+def int8_encode(y: float, mutation: int = 0) -> int:
+    """Symmetric int8 code (as a signed integer) of the fp32 value y: nearest
+    integer, ties to even, clamped to [-127, 127]."""
+    b = int(_load(mutation).pdo_int8_encode(float(y)))
+    return b - 256 if b >= 128 else b
+
+
 APPEND_BF16, APPEND_TENSOR, APPEND_TOKEN_HEAD = 0, 1, 2
+APPEND_INT8_TENSOR, APPEND_INT8_TOKEN_HEAD = 3, 4
 
 
 def append_kv(*, k_new, v_new, page_table, kv_indptr, kv_len, qo_indptr, k_pages, v_pages,
@@ -186,7 +198,8 @@ def append_kv(*, k_new, v_new, page_table, kv_indptr, kv_len, qo_indptr, k_pages
     ``k_new`` / ``v_new``: bf16 [rows, Hkv, D] (CPU tensors or 16-bit words);
     ``k_pages`` / ``v_pages``: the caches before the append (bytes, or bf16
     words for mode 0); ``k_scale`` / ``v_scale``: fp32 arrays (read for
-    mode 1, written for mode 2, None for mode 0). Returns (k_pages, v_pages,
+    modes 1 and 3, written for modes 2 and 4, None for mode 0). Modes 3 / 4
+    are the int8 counterparts of 1 / 2 (scale amax / 127). Returns (k_pages, v_pages,
     k_scale, v_scale, status) as numpy arrays (caches as raw bytes).
     """
     lib = _load(mutation)

@@ -28,6 +28,9 @@
  *    W <= 0, or no window array, means no lower bound.
  *  - lse is the natural log of sum_j exp(s_j) over the scaled logits.
  *  - FP8 is OCP E4M3 ("e4m3fn": bias 7, no infinities, S.1111.111 is NaN).
+ *  - An int8 cache (named beside bf16 and fp8 in the register-spill check of
+ *    FreeToken PR #900, "Tested on") holds two's-complement bytes; the value
+ *    is the byte times the same per-tensor or per-(token, kv head) scale.
  *
  * Split mode (split_tokens > 0) cuts the key axis into chunks
  * [c*T, (c+1)*T), computes (o_c, lse_c) per chunk with the same two-pass
@@ -81,9 +84,20 @@ double pdo_e4m3_to_double(uint8_t code) {
   return sign ? -mag : mag;
 }
 
+/* Two's-complement signed byte (int8 cache element). */
+static double pdo_int8_to_double(uint8_t byte) {
+  int v = MUT(20) ? (int)byte : (byte >= 128 ? (int)byte - 256 : (int)byte);
+  return (double)v;
+}
+
+#define PDO_KV_BF16 0
+#define PDO_KV_E4M3 1
+#define PDO_KV_INT8 2
+
 typedef struct {
   int batch, hq, hkv, d, page_size;
-  int q_e4m3, kv_e4m3, scale_mode; /* scale_mode: 0 none, 1 per tensor, 2 per (token, kv head) */
+  int q_e4m3, kv_dtype, scale_mode; /* kv_dtype: PDO_KV_*; scale_mode: 0 none, 1 per tensor,
+                                       2 per (token, kv head) */
   int64_t sp, st, sh;              /* cache strides in elements: page, token-in-page, kv head */
   int64_t num_pages;
   const void *q, *k, *v;
@@ -106,8 +120,10 @@ static double pdo_kv_elem(const pdo_problem* p, const void* cache, const float* 
   int64_t idx = MUT(10) ? page * p->sp + slot * p->sh + (int64_t)g * p->st + d
                         : page * p->sp + slot * p->st + (int64_t)g * p->sh + d;
   double x;
-  if (p->kv_e4m3)
+  if (p->kv_dtype == PDO_KV_E4M3)
     x = pdo_e4m3_to_double(((const uint8_t*)cache)[idx]);
+  else if (p->kv_dtype == PDO_KV_INT8)
+    x = pdo_int8_to_double(((const uint8_t*)cache)[idx]);
   else
     x = pdo_bf16_to_double(((const uint16_t*)cache)[idx]);
   if (p->scale_mode == 1) x *= (double)scale[0];
@@ -197,7 +213,8 @@ static int pdo_item(const pdo_problem* p, int64_t row, int h, int64_t split_toke
  * Attention output for the requested (query row, q head) items.
  *   q        [total_rows, hq, d]   bf16 bits (uint16) or e4m3 codes (uint8)
  *   k, v     paged cache, element (page, slot, kv head, c) at
- *            page*sp + slot*st + head*sh + c; bf16 bits or e4m3 codes
+ *            page*sp + slot*st + head*sh + c; bf16 bits, e4m3 codes or int8
+ *            bytes (kv_dtype 0 / 1 / 2)
  *   k_scale, v_scale: NULL (scale_mode 0), [1] (1) or
  *            [num_pages, page_size, hkv] (2)
  *   items    NULL: all total_rows*hq items in order; else flat indices
@@ -205,7 +222,7 @@ static int pdo_item(const pdo_problem* p, int64_t row, int h, int64_t split_toke
  *   out      [n_items, d] fp64; lse [n_items] fp64 (natural log)
  * Returns PDO_OK, PDO_ERR_ARG, or PDO_ERR_KVLEN (some rows set to NaN).
  */
-int pdo_attention(int batch, int hq, int hkv, int d, int page_size, int q_e4m3, int kv_e4m3,
+int pdo_attention(int batch, int hq, int hkv, int d, int page_size, int q_e4m3, int kv_dtype,
                   int scale_mode, int64_t sp, int64_t st, int64_t sh, int64_t num_pages,
                   const void* q, const void* k, const void* v, const int32_t* page_table,
                   const int32_t* kv_indptr, const int32_t* kv_len, const int32_t* qo_indptr,
@@ -213,8 +230,11 @@ int pdo_attention(int batch, int hq, int hkv, int d, int page_size, int q_e4m3, 
                   const float* v_scale, int64_t split_tokens, const int64_t* items,
                   int64_t n_items, double* out, double* lse, int num_threads) {
   if (batch < 0 || hq <= 0 || hkv <= 0 || hq % hkv || d <= 0 || page_size <= 0) return PDO_ERR_ARG;
-  if (scale_mode < 0 || scale_mode > 2 || (scale_mode && !kv_e4m3)) return PDO_ERR_ARG;
-  pdo_problem p = {batch, hq, hkv, d, page_size, q_e4m3, kv_e4m3, scale_mode, sp, st, sh, num_pages,
+  if (kv_dtype < PDO_KV_BF16 || kv_dtype > PDO_KV_INT8) return PDO_ERR_ARG;
+  if (scale_mode < 0 || scale_mode > 2 || ((scale_mode != 0) != (kv_dtype != PDO_KV_BF16)))
+    return PDO_ERR_ARG;
+  if (q_e4m3 && kv_dtype != PDO_KV_E4M3) return PDO_ERR_ARG;
+  pdo_problem p = {batch, hq, hkv, d, page_size, q_e4m3, kv_dtype, scale_mode, sp, st, sh, num_pages,
                    q, k, v, page_table, kv_indptr, kv_len, qo_indptr, window, sm_scale,
                    k_scale, v_scale};
   int64_t total_rows = batch > 0 ? qo_indptr[batch] : 0;
@@ -277,6 +297,28 @@ uint8_t pdo_e4m3_encode(float y) {
   return (uint8_t)(sign | best);
 }
 
+/* Nearest integer to y, ties to the even integer, clamped to [-127, 127]
+ * (symmetric int8; -128 is never produced); NaN -> 0. By comparing the two
+ * integers that bracket y. */
+uint8_t pdo_int8_encode(float y) {
+  if (isnan(y)) return 0;
+  double a = (double)y;
+  double lo = floor(a), hi = ceil(a);
+  double r;
+  if (a - lo < hi - a)
+    r = lo;
+  else if (hi - a < a - lo)
+    r = hi;
+  else /* a tie (or y already an integer: lo == hi) */
+    r = MUT(22) ? (a < 0 ? lo : hi) : (fmod(lo, 2.0) == 0.0 ? lo : hi);
+  if (!MUT(23)) {
+    if (r > 127.0) r = 127.0;
+    if (r < -127.0) r = -127.0;
+  }
+  int v = (int)r;
+  return (uint8_t)(v & 0xFF);
+}
+
 /*
  * pdo_append: writes row i < R_b of every request b (token t = L_b - R_b + i)
  * into page page_table[kv_indptr[b] + t / P], slot t % P, kv head h.
@@ -284,6 +326,9 @@ uint8_t pdo_e4m3_encode(float y) {
  *   mode 1: E4M3 cache, s = k_scale[0] / v_scale[0] (read)
  *   mode 2: E4M3 cache, s per (token, kv head) from the row's amax, written
  *           to k_scale / v_scale [num_pages, page_size, hkv]
+ *   mode 3: int8 cache, s = k_scale[0] / v_scale[0] (read)
+ *   mode 4: int8 cache, s = fp32(amax / 127) per (token, kv head) (1 if amax
+ *           is 0), written like mode 2; code = pdo_int8_encode(fp32(x / s))
  *   k_new, v_new  bf16 bits [total_rows, hkv, d]
  *   k, v          caches (bytes; bf16 cache: 2 bytes per element), strides in elements
  * Returns PDO_OK, PDO_ERR_ARG, PDO_ERR_KVLEN (a request with L < R, skipped)
@@ -294,7 +339,8 @@ int pdo_append(int batch, int hkv, int d, int page_size, int mode, int64_t sp, i
                const int32_t* page_table, const int32_t* kv_indptr, const int32_t* kv_len,
                const int32_t* qo_indptr, uint8_t* k, uint8_t* v, float* k_scale,
                float* v_scale) {
-  if (batch < 0 || hkv <= 0 || d <= 0 || page_size <= 0 || mode < 0 || mode > 2) return PDO_ERR_ARG;
+  if (batch < 0 || hkv <= 0 || d <= 0 || page_size <= 0 || mode < 0 || mode > 4) return PDO_ERR_ARG;
+  if (mode != 0 && (!k_scale || !v_scale)) return PDO_ERR_ARG;
   int status = PDO_OK;
   for (int b = 0; b < batch; ++b) {
     int R = qo_indptr[b + 1] - qo_indptr[b];
@@ -329,16 +375,20 @@ int pdo_append(int batch, int hkv, int d, int page_size, int mode, int64_t sp, i
             float x = (float)pdo_bf16_to_double(src[c]);
             if (fabsf(x) > amax) amax = fabsf(x);
           }
+          const int int8 = mode >= 3;
           float s;
-          if (mode == 1) {
+          if (mode == 1 || mode == 3) {
             s = scale[0];
-          } else {
+          } else if (!int8) {
             s = amax > 0.0f ? amax / (MUT(16) ? 256.0f : 448.0f) : 1.0f;
+            scale[sidx] = s;
+          } else {
+            s = amax > 0.0f ? amax / (MUT(21) ? 128.0f : 127.0f) : 1.0f;
             scale[sidx] = s;
           }
           for (int c = 0; c < d; ++c) {
             float y = (float)pdo_bf16_to_double(src[c]) / s;
-            cache[base + c] = pdo_e4m3_encode(y);
+            cache[base + c] = int8 ? pdo_int8_encode(y) : pdo_e4m3_encode(y);
           }
         }
       }

@@ -1,7 +1,7 @@
 """Seeded synthetic workloads for paged decode attention.
 
-This module only draws inputs: query rows, a paged K/V cache (bf16, or OCP
-E4M3 codes with their scales), a shuffled page table and the CSR offsets. It
+This module only draws inputs: query rows, a paged K/V cache (bf16, OCP
+E4M3 codes or int8 codes, with their scales), a shuffled page table and the CSR offsets. It
 holds none of the attention arithmetic. Both the CUDA library's callers and
 the fp64 oracle consume the arrays it returns, so neither side's arithmetic
 can leak into the other's inputs.
@@ -11,7 +11,9 @@ Recipe (stated once here, used by the tests and the benchmark):
   * bf16 payloads are the round-to-nearest-even bf16 of those values;
   * FP8 payloads: scale = amax / 448 (1 if amax == 0), per tensor or per
     (token, kv head) over head_dim; code = e4m3(clamp(x / scale, +-448))
-    by torch's float8_e4m3fn cast (RNE). A per-tensor E4M3 query folds its
+    by torch's float8_e4m3fn cast (RNE). int8 payloads: scale = amax / 127
+    (1 if amax == 0), code = clamp(round-half-even(x / scale), +-127) by
+    torch.round. A per-tensor E4M3 query folds its
     scale into the returned sm_scale, so a consumer multiplies decoded codes
     by sm_scale only;
   * optional K outliers: round(frac * head_dim) channels per kv head, chosen
@@ -22,7 +24,9 @@ Recipe (stated once here, used by the tests and the benchmark):
     point at poison pages, and ``extra_pages`` poison pages exist;
   * poison: pages no request uses and the tail slots of each request's last
     page hold NaN (bf16 0x7FC0, e4m3 0x7F), and so do their per-token scales,
-    so that any read of them shows up as NaN in the output.
+    so that any read of them shows up as NaN in the output (int8 has no NaN:
+    its poison code is -128, which no quantiser produces, and only the
+    per-token scales of those slots are NaN).
 """
 from __future__ import annotations
 
@@ -35,6 +39,8 @@ import torch
 E4M3_MAX = 448.0
 BF16_NAN_BITS = 0x7FC0
 E4M3_NAN_CODE = 0x7F
+INT8_MAX = 127.0
+INT8_POISON = -128
 
 SCALE_NONE, SCALE_TENSOR, SCALE_TOKEN_HEAD = 0, 1, 2
 
@@ -65,6 +71,7 @@ class Workload:
     sm_scale: float
     q_scale: float = 1.0             # already folded into sm_scale when q_e4m3
     meta: dict = field(default_factory=dict)
+    kv_int8: bool = False            # int8 cache codes (kv_e4m3 is then False)
 
     @property
     def batch(self) -> int:
@@ -99,7 +106,7 @@ class Workload:
                         mv(self.v_pages), mv(self.k_scale), mv(self.v_scale),
                         mv(self.page_table), mv(self.kv_indptr), mv(self.kv_len),
                         mv(self.qo_indptr), mv(self.window), self.sm_scale, self.q_scale,
-                        dict(self.meta))
+                        dict(self.meta), self.kv_int8)
 
 
 def _as_list(x, n):
@@ -123,6 +130,27 @@ def _quant_e4m3(x: torch.Tensor, amax_dims) -> tuple:
         y = x / scale.unsqueeze(-1)
     codes = y.clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).view(torch.uint8)
     return codes, scale.to(torch.float32)
+
+
+def _quant_int8(x: torch.Tensor, amax_dims) -> tuple:
+    """(codes int8, scale float32) with scale = amax/127 over ``amax_dims``
+    (None: whole tensor); codes = clamp(round(x / scale), +-127), ties to even."""
+    if amax_dims is None:
+        amax = x.abs().amax().float()
+    else:
+        amax = x.abs().amax(dim=amax_dims).float()
+    scale = torch.where(amax > 0, amax / INT8_MAX, torch.ones_like(amax))
+    y = x / scale if amax_dims is None else x / scale.unsqueeze(-1)
+    codes = torch.round(y).clamp(-INT8_MAX, INT8_MAX).to(torch.int8)
+    return codes, scale.to(torch.float32)
+
+
+def _exact_int8(x: torch.Tensor) -> torch.Tensor:
+    """int8 codes of integer values in [-127, 127] (asserted)."""
+    codes = x.to(torch.int8)
+    assert torch.equal(codes.to(torch.float32), x), "value not an int8 code"
+    assert int(codes.min()) >= -INT8_MAX, "-128 is the poison code"
+    return codes
 
 
 def _exact_e4m3(x: torch.Tensor) -> torch.Tensor:
@@ -149,11 +177,13 @@ def make_workload(*, name: str = "custom", batch: int, rows: Union[int, Sequence
           shapes [rows, Hq, D] and [num_pages, P, Hkv, D];
       ``token_fn(kind, b, L)`` -- kind in {"k", "v"}: values [L, Hkv, D] of
           request b's tokens in order, scattered through the page table;
-      ``unit_scale`` -- E4M3 scales fixed at 1 (values must be exact E4M3);
+      ``unit_scale`` -- E4M3 / int8 scales fixed at 1 (values must be exact
+          E4M3, or integers in [-127, 127] for int8);
       ``scale_fn(kind, b, L)`` -- per-(token, kv head) scales [L, Hkv] of
           request b (with ``unit_scale``), e.g. to ramp logits per token.
     """
-    assert kv_dtype in ("bf16", "e4m3") and q_dtype in ("bf16", "e4m3")
+    assert kv_dtype in ("bf16", "e4m3", "int8") and q_dtype in ("bf16", "e4m3")
+    assert q_dtype == "bf16" or kv_dtype == "e4m3"
     assert num_qo_heads % num_kv_heads == 0
     if kv_dtype == "bf16":
         assert scale_mode == SCALE_NONE
@@ -235,7 +265,10 @@ def make_workload(*, name: str = "custom", batch: int, rows: Union[int, Sequence
     if kv_dtype == "bf16":
         kc, vc = kf.to(torch.bfloat16), vf.to(torch.bfloat16)
     elif unit_scale:
-        kc, vc = _exact_e4m3(kf), _exact_e4m3(vf)
+        if kv_dtype == "int8":
+            kc, vc = _exact_int8(kf), _exact_int8(vf)
+        else:
+            kc, vc = _exact_e4m3(kf), _exact_e4m3(vf)
         if scale_mode == SCALE_TENSOR:
             k_scale = torch.ones(1, dtype=torch.float32, device=dev)
             v_scale = torch.ones(1, dtype=torch.float32, device=dev)
@@ -253,12 +286,14 @@ def make_workload(*, name: str = "custom", batch: int, rows: Union[int, Sequence
                     k_scale[pg, sl] = scale_fn("k", b, L[b]).to(dev, torch.float32)
                     v_scale[pg, sl] = scale_fn("v", b, L[b]).to(dev, torch.float32)
     elif scale_mode == SCALE_TENSOR:
-        kc, k_scale = _quant_e4m3(kf, None)
-        vc, v_scale = _quant_e4m3(vf, None)
+        quant = _quant_int8 if kv_dtype == "int8" else _quant_e4m3
+        kc, k_scale = quant(kf, None)
+        vc, v_scale = quant(vf, None)
         k_scale, v_scale = k_scale.reshape(1), v_scale.reshape(1)
     else:
-        kc, k_scale = _quant_e4m3(kf, -1)
-        vc, v_scale = _quant_e4m3(vf, -1)
+        quant = _quant_int8 if kv_dtype == "int8" else _quant_e4m3
+        kc, k_scale = quant(kf, -1)
+        vc, v_scale = quant(vf, -1)
     del kf, vf, qf
 
     if poison:
@@ -267,6 +302,9 @@ def make_workload(*, name: str = "custom", batch: int, rows: Union[int, Sequence
             nanb = torch.tensor(BF16_NAN_BITS, dtype=torch.int16, device=dev).view(torch.bfloat16)
             kc[bad] = nanb
             vc[bad] = nanb
+        elif kv_dtype == "int8":
+            kc[bad] = INT8_POISON
+            vc[bad] = INT8_POISON
         else:
             kc[bad] = E4M3_NAN_CODE
             vc[bad] = E4M3_NAN_CODE
@@ -296,7 +334,7 @@ def make_workload(*, name: str = "custom", batch: int, rows: Union[int, Sequence
         kv_indptr=torch.tensor(kv_indptr, **i32), kv_len=torch.tensor(L, **i32),
         qo_indptr=torch.tensor(qo_indptr, **i32), window=win, sm_scale=sm_eff, q_scale=q_scale,
         meta=dict(seed=seed, rows=R, kv_lens=L, outlier_channels=outlier_channels,
-                  poison_pages=poison_pages))
+                  poison_pages=poison_pages), kv_int8=(kv_dtype == "int8"))
 
 
 # ---------------------------------------------------------------------------

@@ -27,6 +27,8 @@ def dequant_cache(wl, which: str) -> torch.Tensor:
         c = c.permute(0, 2, 1, 3)
     if wl.kv_e4m3:
         x = c.contiguous().view(torch.float8_e4m3fn).to(torch.float64)
+    elif getattr(wl, "kv_int8", False):
+        x = c.contiguous().view(torch.int8).to(torch.float64)
     else:
         x = c.to(torch.float64)
     if wl.scale_mode == 1:

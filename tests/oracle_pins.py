@@ -21,6 +21,11 @@ torch's float8_e4m3fn cast (codes within +-448, ties to even), to the
 saturation of the format's largest finite value, to closed forms of the
 scale (amax / 448, 1 for a zero row) and to the page-table placement of
 token L - R + i read independently here.
+
+The int8 cache (beside bf16 and fp8 in the same page's "Tested on") is
+pinned to dense torch attention over torch's own int8 decode, to a closed
+form (a constant negative code times its scale), and its quantiser to
+torch.round (ties to even) with the +-127 clamp and the amax / 127 scale.
 """
 from __future__ import annotations
 
@@ -77,7 +82,8 @@ def bruteforce_cases():
     groups = [(1, 1), (3, 3), (8, 1), (24, 2), (8, 2), (3, 1)]
     kinds = [("bf16", "bf16", SCALE_NONE), ("e4m3", "bf16", SCALE_TENSOR),
              ("e4m3", "bf16", SCALE_TOKEN_HEAD), ("e4m3", "e4m3", SCALE_TENSOR),
-             ("e4m3", "e4m3", SCALE_TOKEN_HEAD)]
+             ("e4m3", "e4m3", SCALE_TOKEN_HEAD), ("int8", "bf16", SCALE_TENSOR),
+             ("int8", "bf16", SCALE_TOKEN_HEAD)]
     n = 0
     for gi, (G, H) in enumerate(groups):
         for ki, (kvd, qd, sm) in enumerate(kinds):
@@ -301,9 +307,9 @@ def _append_case(mode, D=8, P=4, H=2, lens=(9, 5), rows=(3, 2), seed=0):
     k_pages = fill.clone().numpy()
     v_pages = fill.flip(0).clone().numpy()
     ks = vs = None
-    if mode == oracle.APPEND_TENSOR:
+    if mode in (oracle.APPEND_TENSOR, oracle.APPEND_INT8_TENSOR):
         ks, vs = np.array([0.0125], np.float32), np.array([0.02], np.float32)
-    elif mode == oracle.APPEND_TOKEN_HEAD:
+    elif mode in (oracle.APPEND_TOKEN_HEAD, oracle.APPEND_INT8_TOKEN_HEAD):
         ks = np.full(num_pages * P * H, -1.0, np.float32)
         vs = np.full(num_pages * P * H, -2.0, np.float32)
     return dict(k_new=k_new, v_new=v_new, page_table=perm, kv_indptr=kv_indptr,
@@ -386,10 +392,83 @@ def pin_append_bf16_copy(mutation=0):
         assert np.array_equal(v16[page, slot], case["v_new"][row].view(torch.int16).numpy().view(np.uint16))
 
 
+# ------------------------------------------------------------- int8 pins
+def pin_int8_constant_code(mutation=0):
+    """Every V code -3 with v_scale 0.5 gives o = -1.5 exactly, whatever the
+    logits; every K code equal gives lse = ln(visible count) + its logit."""
+    def vals(kind, shape, gen):
+        if kind == "v":
+            return torch.full(shape, -3.0)
+        if kind == "k":
+            return torch.full(shape, -2.0)
+        return torch.randn(shape, generator=gen)
+    wl = make_workload(batch=2, rows=[3, 1], kv_lens=[40, 9], num_qo_heads=4, num_kv_heads=2,
+                       head_dim=16, page_size=8, kv_dtype="int8", scale_mode=SCALE_TENSOR,
+                       unit_scale=True, value_fn=vals, seed=4, poison=True)
+    ks, vs = torch.tensor([0.25]), torch.tensor([0.5])
+    out, lse, rc = _run(wl, mutation, k_scale=ks, v_scale=vs)
+    assert rc == 0
+    _close(out, np.full(out.shape, -1.5), what="int8 constant V")
+    qd = dequant_q(wl)
+    r0 = 0
+    for b, (R, L) in enumerate(zip([3, 1], [40, 9])):
+        for i in range(R):
+            for h in range(4):
+                s = wl.sm_scale * float(qd[r0 + i, h].sum()) * (-2.0 * 0.25)
+                _close(lse[r0 + i, h], math.log(L - R + i + 1) + s, what=f"int8 lse b{b} i{i} h{h}")
+        r0 += R
+
+
+def pin_int8_encode_vs_torch(mutation=0):
+    # integers, half-integers (ties: the even neighbour), random values and
+    # values beyond +-127 (clamped), both signs
+    g = torch.Generator().manual_seed(9)
+    ints = torch.arange(-127, 128).float()
+    halves = torch.arange(-130, 130).float() + 0.5
+    rnd = (torch.rand(3000, generator=g) * 2 - 1) * 140
+    ys = torch.cat([ints, halves, rnd, torch.tensor([1e6, -1e6, 127.5, -127.5])]).float()
+    got = torch.tensor([oracle.int8_encode(float(y), mutation) for y in ys])
+    ref = torch.round(ys).clamp(-127, 127).to(torch.int64)
+    bad = (got != ref).nonzero()
+    assert bad.numel() == 0, f"int8 encode differs from torch.round at {ys[bad[0]].item()!r}"
+
+
+def pin_append_int8(mutation=0):
+    for mode in (oracle.APPEND_INT8_TOKEN_HEAD, oracle.APPEND_INT8_TENSOR):
+        case = _append_case(mode, seed=3)
+        if mode == oracle.APPEND_INT8_TENSOR:
+            case["k_scale"], case["v_scale"] = np.array([0.03], np.float32), np.array([0.05], np.float32)
+        kn = case["k_new"].float()
+        kn[0, 0] = 0                       # a zero row: scale 1, codes 0
+        kn[1, 1] = torch.linspace(-4, 2, 8)  # amax 4 at a negative value
+        case["k_new"] = kn.to(torch.bfloat16)
+        kc, vc, ks, vs, rc = oracle.append_kv(**case, mutation=mutation)
+        assert rc == 0
+        P, H, D = case["page_size"], case["num_kv_heads"], case["head_dim"]
+        for row, page, slot in _slots(case):
+            for h in range(H):
+                for new, cache, scales in ((case["k_new"], kc, ks), (case["v_new"], vc, vs)):
+                    x = new[row, h].float()
+                    if mode == oracle.APPEND_INT8_TENSOR:
+                        s = np.float32(scales[0])
+                    else:
+                        amax = float(x.abs().max())
+                        s = (np.float32(np.float32(amax) / np.float32(127.0)) if amax > 0
+                             else np.float32(1.0))
+                        assert scales[(page * P + slot) * H + h] == s, (row, h)
+                    ref = torch.round(x / torch.tensor(float(s))).clamp(-127, 127).to(torch.int8)
+                    got = cache.reshape(-1, P, H, D)[page, slot, h].view(np.int8)
+                    assert np.array_equal(got, ref.numpy()), (mode, row, h)
+        if mode == oracle.APPEND_INT8_TOKEN_HEAD:
+            r1 = _slots(case)[1]
+            assert kc.reshape(-1, P, H, D)[r1[1], r1[2], 1].view(np.int8)[0] == -127
+
+
 ALL_PINS = [pin_e4m3_all_codes, pin_bruteforce, pin_q_zero_closed_form, pin_single_visible_key,
             pin_constant_v, pin_page_permutation, pin_split_merge, pin_rows_vs_single,
             pin_e4m3_encode_vs_torch, pin_e4m3_encode_saturates, pin_append_token_head,
-            pin_append_per_tensor, pin_append_bf16_copy]
+            pin_append_per_tensor, pin_append_bf16_copy, pin_int8_constant_code,
+            pin_int8_encode_vs_torch, pin_append_int8]
 
 # Planted mistakes compiled into copies of the oracle (see MUT(k) in pdo_oracle.c).
 MUTATIONS = {
@@ -412,4 +491,8 @@ MUTATIONS = {
     17: "append: E4M3 ties go to the odd code",
     18: "append: new row written one token early",
     19: "append: E4M3 sign dropped",
+    20: "int8 cache bytes read as unsigned",
+    21: "append: int8 per-token scale amax / 128",
+    22: "append: int8 ties rounded away from zero",
+    23: "append: int8 codes not clamped to +-127",
 }

@@ -42,7 +42,10 @@ HEADLINE_DESC = ("fp8_decode: bs128, R1, 64 q / 8 kv heads, head_dim 128, ctx 20
 PAGES_NUMBER = {"value": 3672.1, "unit": "GB/s",
                 "source": "hpc-ops FP8 decode on H200 (other hardware; context only)"}
 SWEEP = [("mtp_verify_bf16", 16, R) for R in (1, 4, 8)] + \
-        [("longctx_fp8_pth", 16, R) for R in (1, 4, 8)]
+        [("longctx_fp8_pth", 16, R) for R in (1, 4, 8)] + \
+        [("longctx_int8_pth", 16, R) for R in (1, 8)] + \
+        [("d512_mtp_bf16", 1, R) for R in (1, 4, 8)] + \
+        [("d512_mtp_fp8", 1, R) for R in (1, 4, 8)]
 
 
 def peaks():
@@ -189,7 +192,7 @@ def append_time(name, kw, dev, steps, flush, peak):
     with torch.cuda.graph(graph, stream=s):
         call()
     med = statistics.median(time_graph(graph.replay, steps, 3, flush, s))
-    elt = 1 if wl.kv_e4m3 else 2
+    elt = 1 if (wl.kv_e4m3 or getattr(wl, "kv_int8", False)) else 2
     nbytes = 2 * rows * H * D * (2 + elt) + rows * 4 + 4 * (3 * wl.batch + 2)
     if wl.scale_mode == 2:
         nbytes += 2 * rows * H * 4

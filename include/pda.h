@@ -55,7 +55,11 @@ extern "C" {
 
 typedef struct CUstream_st* pda_stream_t; /* a cudaStream_t; NULL = legacy default stream */
 
-enum { PDA_BF16 = 0, PDA_E4M3 = 1 };
+/* Element types. PDA_INT8 (KV cache only): two's-complement codes whose value
+ * is the code times the per-tensor or per-(token, kv head) scale; an int8
+ * cache is named beside bf16 and fp8 in "perf(attention): run up to 8 query
+ * rows per request in the triton decode kernel", Tested on. */
+enum { PDA_BF16 = 0, PDA_E4M3 = 1, PDA_INT8 = 2 };
 enum { PDA_SCALE_NONE = 0, PDA_SCALE_TENSOR = 1, PDA_SCALE_TOKEN_HEAD = 2 };
 enum { PDA_KERNEL_AUTO = 0, PDA_KERNEL_MMA = 1, PDA_KERNEL_TC = 2 };
 
@@ -89,8 +93,8 @@ typedef struct {
   int32_t head_dim;        /* D: 64, 128, 256 or 512 (512: tcgen05 path, pages >= 8) */
   int32_t page_size;       /* P: power of two in [1, 256] */
   int32_t q_dtype;         /* PDA_BF16, or PDA_E4M3 (then kv_dtype must be PDA_E4M3) */
-  int32_t kv_dtype;        /* PDA_BF16 or PDA_E4M3 */
-  int32_t scale_mode;      /* PDA_SCALE_NONE for bf16 KV; TENSOR or TOKEN_HEAD for E4M3 */
+  int32_t kv_dtype;        /* PDA_BF16, PDA_E4M3 or PDA_INT8 (int8: mma.sync path, D <= 256) */
+  int32_t scale_mode;      /* PDA_SCALE_NONE for bf16 KV; TENSOR or TOKEN_HEAD for E4M3 / int8 */
   int32_t max_batch;       /* upper bound of `batch` over the plan's lifetime */
   int32_t max_q_len;       /* 1..8: rows per request */
   int32_t max_kv_len;      /* upper bound of kv_len[b] */
@@ -153,7 +157,7 @@ int pda_plan(const pda_params* params, pda_plan_t* out_plan, size_t* split_scrat
  * log-sum-exp merge of the chunks of every (query row, q head)).
  *   q          [qo_indptr[batch], Hq, D] bf16, or E4M3 codes (q_dtype), rows
  *              of request b at [qo_indptr[b], qo_indptr[b+1]); 16-B aligned
- *   k_pages,   paged cache, bf16 or E4M3 codes, strides from the plan;
+ *   k_pages,   paged cache, bf16, E4M3 codes or int8 codes, strides from the plan;
  *   v_pages    16-B aligned
  *   page_table int32 CSR: pages of request b at [kv_indptr[b], kv_indptr[b+1]),
  *              at least ceil(kv_len[b] / P) of them; only those are read
@@ -163,6 +167,7 @@ int pda_plan(const pda_params* params, pda_plan_t* out_plan, size_t* split_scrat
  *   window     int32 [batch] sliding window per request (<= 0: none), or NULL
  *   sm_scale   logit scale (times the query's E4M3 scale when q is E4M3)
  *   k_scale,   NULL (bf16), fp32 [1] (per tensor) or fp32 [num_pages, P, Hkv]
+ *              (E4M3 / int8)
  *   v_scale    (per token and kv head), device memory
  *   out        [qo_indptr[batch], Hq, D] bf16
  *   lse        [qo_indptr[batch], Hq] fp32 natural-log LSE, or NULL
@@ -186,7 +191,10 @@ int pda_decode(const pda_plan_t* plan, const void* q, const void* k_pages, const
  *   E4M3, per token-head   s = amax / 448 over the D values of (token, kv head)
  *                          (1 if amax = 0), written to k_scale / v_scale
  *                          [num_pages, P, Hkv], and codes = RNE(sat(x / s)).
- * x / s is one fp32 division; sat clamps to +-448 (E4M3, OCP e4m3fn).
+ *   int8, per tensor       codes = RNE(clamp(x / s, +-127)), s read as for E4M3;
+ *   int8, per token-head   s = amax / 127 (1 if amax = 0), written as for E4M3.
+ * x / s is one fp32 division; sat clamps to +-448 (E4M3, OCP e4m3fn); RNE
+ * ties go to the even code (int8: the even integer).
  *   k_new, v_new  bf16 [qo_indptr[batch], Hkv, D], rows in qo_indptr order
  *   k_pages, v_pages  the cache (written), layout and strides as planned
  *   page_table, kv_indptr, kv_len, qo_indptr  as for pda_decode (kv_len

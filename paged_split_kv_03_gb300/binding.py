@@ -15,7 +15,7 @@ from typing import Optional
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_lib", "libpda.so")
 
-PDA_BF16, PDA_E4M3 = 0, 1
+PDA_BF16, PDA_E4M3, PDA_INT8 = 0, 1, 2
 PDA_SCALE_NONE, PDA_SCALE_TENSOR, PDA_SCALE_TOKEN_HEAD = 0, 1, 2
 PDA_KERNEL_AUTO, PDA_KERNEL_MMA, PDA_KERNEL_TC = 0, 1, 2
 PDA_OK = 0
@@ -209,7 +209,8 @@ def params_for(wl, *, max_batch=None, max_q_len=None, max_kv_len=None, device=0,
     p.head_dim = wl.head_dim
     p.page_size = wl.page_size
     p.q_dtype = PDA_E4M3 if wl.q_e4m3 else PDA_BF16
-    p.kv_dtype = PDA_E4M3 if wl.kv_e4m3 else PDA_BF16
+    p.kv_dtype = (PDA_E4M3 if wl.kv_e4m3 else
+                  PDA_INT8 if getattr(wl, "kv_int8", False) else PDA_BF16)
     p.scale_mode = wl.scale_mode
     p.max_batch = max_batch or wl.batch
     p.max_q_len = max_q_len or max(1, wl.max_q_len)

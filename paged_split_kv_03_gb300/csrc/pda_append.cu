@@ -6,8 +6,9 @@
 // "fp8 support" page (Functionality) uses symmetric per-tensor scales. One
 // warp per (request, row, kv head): it loads the row's D bf16 values of K
 // and of V (D / 32 per lane), takes the amax over D with warp shuffles when
-// the scale is per token, and stores E4M3 codes (or the bf16 values) into
-// the token's page slot. HBM-bound; every access is one contiguous row.
+// the scale is per token, and stores E4M3 or int8 codes (or the bf16
+// values) into the token's page slot. HBM-bound; every access is one
+// contiguous row.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -44,8 +45,20 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
   return r;
 }
 
+// Two floats -> two symmetric int8 codes (nearest, ties to even, clamped to
+// +-127; NaN -> 0): low byte from `lo`.
+__device__ __forceinline__ uint16_t int8x2(float lo, float hi) {
+  auto one = [](float y) -> uint32_t {
+    int v = isnan(y) ? 0 : __float2int_rn(y);
+    v = v > 127 ? 127 : (v < -127 ? -127 : v);
+    return static_cast<uint32_t>(v) & 0xFFu;
+  };
+  return static_cast<uint16_t>(one(lo) | (one(hi) << 8));
+}
+
 // One row (D bf16 values, kPer per lane) into the cache at byte offset `dst`
-// of `pages`; per-token scale written to `scale_out` by lane 0.
+// of `pages`; per-token scale written to `scale_out` by lane 0. MODE: 0 bf16
+// copy, 1 / 2 E4M3 per tensor / per token-head, 3 / 4 int8 likewise.
 template <int D, int MODE>
 __device__ __forceinline__ void put_row(const __nv_bfloat16* src, uint8_t* pages, int64_t elt_off,
                                         const float* scale_in, float* scale_out, int lane) {
@@ -67,8 +80,9 @@ __device__ __forceinline__ void put_row(const __nv_bfloat16* src, uint8_t* pages
       x[2 * e] = __uint_as_float(raw[e] << 16);
       x[2 * e + 1] = __uint_as_float(raw[e] & 0xFFFF0000u);
     }
+    constexpr bool kInt8 = MODE >= 3;
     float s;
-    if constexpr (MODE == 1) {
+    if constexpr (MODE == 1 || MODE == 3) {
       s = __ldg(scale_in);
     } else {
       float amax = 0.f;
@@ -76,12 +90,15 @@ __device__ __forceinline__ void put_row(const __nv_bfloat16* src, uint8_t* pages
       for (int e = 0; e < kPer; ++e) amax = fmaxf(amax, fabsf(x[e]));
 #pragma unroll
       for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+      s = amax > 0.f ? __fdiv_rn(amax, kInt8 ? 127.f : 448.f) : 1.f;
       if (lane == 0) *scale_out = s;
     }
     uint16_t c[kPer / 2];
 #pragma unroll
-    for (int e = 0; e < kPer / 2; ++e) c[e] = e4m3x2(__fdiv_rn(x[2 * e], s), __fdiv_rn(x[2 * e + 1], s));
+    for (int e = 0; e < kPer / 2; ++e) {
+      const float y0 = __fdiv_rn(x[2 * e], s), y1 = __fdiv_rn(x[2 * e + 1], s);
+      c[e] = kInt8 ? int8x2(y0, y1) : e4m3x2(y0, y1);
+    }
     uint8_t* dst = pages + elt_off + lane * kPer;
     if constexpr (kPer == 2) {
       *reinterpret_cast<uint16_t*>(dst) = c[0];
@@ -132,9 +149,10 @@ __global__ void __launch_bounds__(256) append_kv(const __grid_constant__ AppendA
   const int64_t off = page * a.sp + slot * a.st + h * a.sh;  // elements
   const int64_t row = ((int64_t)(q0 + i) * a.hkv + h) * D;
   const int64_t sidx = ((int64_t)page * P + slot) * a.hkv + h;
-  put_row<D, MODE>(a.k_new + row, a.k_pages, off, a.k_scale, a.k_scale + (MODE == 2 ? sidx : 0),
+  constexpr bool kPerToken = MODE == 2 || MODE == 4;
+  put_row<D, MODE>(a.k_new + row, a.k_pages, off, a.k_scale, a.k_scale + (kPerToken ? sidx : 0),
                    lane);
-  put_row<D, MODE>(a.v_new + row, a.v_pages, off, a.v_scale, a.v_scale + (MODE == 2 ? sidx : 0),
+  put_row<D, MODE>(a.v_new + row, a.v_pages, off, a.v_scale, a.v_scale + (kPerToken ? sidx : 0),
                    lane);
 }
 
@@ -145,7 +163,9 @@ AppendFn pick_mode(int mode) {
   switch (mode) {
     case 0: return append_kv<D, 0>;
     case 1: return append_kv<D, 1>;
-    default: return append_kv<D, 2>;
+    case 2: return append_kv<D, 2>;
+    case 3: return append_kv<D, 3>;
+    default: return append_kv<D, 4>;
   }
 }
 
@@ -165,7 +185,7 @@ extern "C" int pda_append_kv(const pda_plan_t* plan, const void* k_new, const vo
   if (!split_scratch) return PDA_ERR_SCRATCH;
   if (reinterpret_cast<uintptr_t>(split_scratch) % 256) return PDA_ERR_SCRATCH;
   if (max_q_len < 1 || max_q_len > plan->max_q_len) return PDA_ERR_INVALID;
-  const bool fp8 = plan->kv_dtype == PDA_E4M3;
+  const bool fp8 = plan->kv_dtype != PDA_BF16;  // one-byte codes (E4M3 or int8) with scales
   if (fp8 && (!k_scale || !v_scale)) return PDA_ERR_NULL;
   if (fp8 && plan->scale_mode == PDA_SCALE_NONE) return PDA_ERR_UNSUPPORTED;
   auto a16 = [](const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
@@ -197,7 +217,9 @@ extern "C" int pda_append_kv(const pda_plan_t* plan, const void* k_new, const vo
   a.page_size = plan->page_size;
   a.num_pages = plan->num_pages;
   a.max_q_len = max_q_len;
-  const int mode = !fp8 ? 0 : plan->scale_mode == PDA_SCALE_TENSOR ? 1 : 2;
+  const int mode = !fp8 ? 0
+                   : (plan->kv_dtype == PDA_INT8 ? 2 : 0) +
+                         (plan->scale_mode == PDA_SCALE_TENSOR ? 1 : 2);
   pda::AppendFn fn = D == 64 ? pda::pick_mode<64>(mode)
                      : D == 128 ? pda::pick_mode<128>(mode)
                      : D == 256 ? pda::pick_mode<256>(mode)

@@ -114,6 +114,23 @@ __device__ __forceinline__ uint32_t e4m3x2_to_ct(uint16_t codes) {
   }
 }
 
+// Two int8 codes (low byte = first element) -> packed bf16 pair. Exact:
+// every integer in [-128, 127] is a bf16 value.
+__device__ __forceinline__ uint32_t int8x2_to_bf16x2(uint16_t codes) {
+  const float lo = static_cast<float>(static_cast<int8_t>(codes & 0xFF));
+  const float hi = static_cast<float>(static_cast<int8_t>(codes >> 8));
+  return pack2<false>(lo, hi);
+}
+
+// Two one-byte cache codes (E4M3 or int8) -> packed compute-type pair.
+template <int KVT, bool kF16>
+__device__ __forceinline__ uint32_t widen2(uint16_t codes) {
+  if constexpr (KVT == PDA_INT8)
+    return int8x2_to_bf16x2(codes);
+  else
+    return e4m3x2_to_ct<kF16>(codes);
+}
+
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 
 // Swizzled byte offset of 16-byte chunk `c` of row `r` in a tile whose rows
@@ -126,7 +143,7 @@ __device__ __forceinline__ uint32_t swz(int r, int c, int row_bytes) {
 // ------------------------------------------------------------ configuration
 template <int D, int KVT, int QT, int SMODE>
 struct Cfg {
-  static constexpr bool kKvFp8 = KVT == PDA_E4M3;
+  static constexpr bool kKvFp8 = KVT == PDA_E4M3 || KVT == PDA_INT8;  // one-byte codes, widened
   static constexpr bool kQFp8 = QT == PDA_E4M3;
   static constexpr bool kF16 = kQFp8;  // MMA operand type: f16 for E4M3 queries, else bf16
   static constexpr int kKvBytes = kKvFp8 ? 1 : 2;
@@ -340,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_mma(const __grid_constant_
     const uint8_t* kt;
     const uint8_t* vt;
     if constexpr (C::kKvFp8) {
-      // widen the E4M3 tile pair to the 16-bit compute type, swizzled
+      // widen the E4M3 / int8 tile pair to the 16-bit compute type, swizzled
       const uint8_t* kraw = ring + st * 2 * C::kTileBytes;
       const uint8_t* vraw = kraw + C::kTileBytes;
       uint8_t* k16 = conv;
@@ -352,10 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_mma(const __grid_constant_
         const uint4 raw = *reinterpret_cast<const uint4*>((which ? vraw : kraw) + r * D + c * 16);
         const uint16_t* cw = reinterpret_cast<const uint16_t*>(&raw);
         uint4 lo, hi;
-        lo.x = e4m3x2_to_ct<kF16>(cw[0]); lo.y = e4m3x2_to_ct<kF16>(cw[1]);
-        lo.z = e4m3x2_to_ct<kF16>(cw[2]); lo.w = e4m3x2_to_ct<kF16>(cw[3]);
-        hi.x = e4m3x2_to_ct<kF16>(cw[4]); hi.y = e4m3x2_to_ct<kF16>(cw[5]);
-        hi.z = e4m3x2_to_ct<kF16>(cw[6]); hi.w = e4m3x2_to_ct<kF16>(cw[7]);
+        lo.x = widen2<KVT, kF16>(cw[0]); lo.y = widen2<KVT, kF16>(cw[1]);
+        lo.z = widen2<KVT, kF16>(cw[2]); lo.w = widen2<KVT, kF16>(cw[3]);
+        hi.x = widen2<KVT, kF16>(cw[4]); hi.y = widen2<KVT, kF16>(cw[5]);
+        hi.z = widen2<KVT, kF16>(cw[6]); hi.w = widen2<KVT, kF16>(cw[7]);
         uint8_t* dst = which ? v16 : k16;
         *reinterpret_cast<uint4*>(dst + swz(r, 2 * c, C::kRow16)) = lo;
         *reinterpret_cast<uint4*>(dst + swz(r, 2 * c + 1, C::kRow16)) = hi;
@@ -661,6 +678,10 @@ using KernelFn = void (*)(DecodeArgs);
 template <int D>
 KernelFn pick_stage1(int kv, int qd, int sm) {
   if (kv == PDA_BF16) return stage1_mma<D, PDA_BF16, PDA_BF16, PDA_SCALE_NONE>;
+  if (kv == PDA_INT8) {
+    if (sm == PDA_SCALE_TENSOR) return stage1_mma<D, PDA_INT8, PDA_BF16, PDA_SCALE_TENSOR>;
+    return stage1_mma<D, PDA_INT8, PDA_BF16, PDA_SCALE_TOKEN_HEAD>;
+  }
   if (qd == PDA_BF16) {
     if (sm == PDA_SCALE_TENSOR) return stage1_mma<D, PDA_E4M3, PDA_BF16, PDA_SCALE_TENSOR>;
     return stage1_mma<D, PDA_E4M3, PDA_BF16, PDA_SCALE_TOKEN_HEAD>;
@@ -672,6 +693,10 @@ KernelFn pick_stage1(int kv, int qd, int sm) {
 template <int D>
 int smem_of(int kv, int qd, int sm) {
   if (kv == PDA_BF16) return Cfg<D, PDA_BF16, PDA_BF16, PDA_SCALE_NONE>::kSmem;
+  if (kv == PDA_INT8) {
+    if (sm == PDA_SCALE_TENSOR) return Cfg<D, PDA_INT8, PDA_BF16, PDA_SCALE_TENSOR>::kSmem;
+    return Cfg<D, PDA_INT8, PDA_BF16, PDA_SCALE_TOKEN_HEAD>::kSmem;
+  }
   if (qd == PDA_BF16) {
     if (sm == PDA_SCALE_TENSOR) return Cfg<D, PDA_E4M3, PDA_BF16, PDA_SCALE_TENSOR>::kSmem;
     return Cfg<D, PDA_E4M3, PDA_BF16, PDA_SCALE_TOKEN_HEAD>::kSmem;

@@ -23,7 +23,7 @@ bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int elem_bytes(int dtype) { return dtype == PDA_E4M3 ? 1 : 2; }
+int elem_bytes(int dtype) { return dtype == PDA_BF16 ? 2 : 1; }
 
 }  // namespace
 
@@ -61,11 +61,12 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
   if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256 && p->head_dim != 512)
     return PDA_ERR_UNSUPPORTED;
   if (!is_pow2(p->page_size) || p->page_size > 256) return PDA_ERR_UNSUPPORTED;
-  if (p->kv_dtype != PDA_BF16 && p->kv_dtype != PDA_E4M3) return PDA_ERR_UNSUPPORTED;
+  if (p->kv_dtype != PDA_BF16 && p->kv_dtype != PDA_E4M3 && p->kv_dtype != PDA_INT8)
+    return PDA_ERR_UNSUPPORTED;
   if (p->q_dtype != PDA_BF16 && p->q_dtype != PDA_E4M3) return PDA_ERR_UNSUPPORTED;
   if (p->q_dtype == PDA_E4M3 && p->kv_dtype != PDA_E4M3) return PDA_ERR_UNSUPPORTED;
   if (p->kv_dtype == PDA_BF16 && p->scale_mode != PDA_SCALE_NONE) return PDA_ERR_UNSUPPORTED;
-  if (p->kv_dtype == PDA_E4M3 && p->scale_mode != PDA_SCALE_TENSOR &&
+  if (p->kv_dtype != PDA_BF16 && p->scale_mode != PDA_SCALE_TENSOR &&
       p->scale_mode != PDA_SCALE_TOKEN_HEAD)
     return PDA_ERR_UNSUPPORTED;
   if (p->max_batch <= 0 || p->max_q_len < 1 || p->max_q_len > pda::kMaxQLen) return PDA_ERR_INVALID;

@@ -1335,7 +1335,7 @@ bool make_map(CUtensorMap* m, const void* base, const pda_plan_t* p, int* slot_d
 
 bool tc_supported(const pda_plan_t* p) {
   return (p->head_dim == 128 || p->head_dim == 256 || p->head_dim == 512) && p->page_size >= 8 &&
-         p->page_size <= 256;
+         p->page_size <= 256 && p->kv_dtype != PDA_INT8;
 }
 
 // Rows x heads a CTA may hold: 64, except head_dim 512 over an E4M3 cache,

@@ -360,10 +360,17 @@ def config_workload(name: str, *, R: Optional[int] = None, bs: Optional[int] = N
                     e4m3 K/V with a scale per (token, kv head), 1% K channels x20, Q bf16
     mixed           bs 64, 48/2 heads, D 128, R_b ~ U{1..8}, ctx_b ~ U[1024, 65536],
                     window 64 on half the requests, page 32, bf16
+    longctx_int8_pth  the longctx_fp8_pth shape with int8 codes (scale amax / 127)
+                    per (token, kv head) (seed 1200)
     d512_mtp_bf16   bs 1 (16), R 4 (1, 8), 16/1 heads, D 512, ctx 32768, page 16, bf16
     d512_mtp_fp8    bs 1 (16), R 4 (1, 8), 16/1 heads, D 512, ctx 32768, page 16, e4m3
                     K/V with a scale per (token, kv head), Q bf16 (seeds 1100 + index)
     """
+    if name == "longctx_int8_pth":
+        # the longctx_fp8_pth shape over an int8 cache (same scale kind)
+        seed = 1200 if seed is None else seed
+        return config_workload("longctx_fp8_pth", R=R, bs=bs, device=device, seed=seed,
+                               **dict(dict(kv_dtype="int8"), **kw))
     if name in D512_NAMES:
         seed = 1100 + D512_NAMES.index(name) if seed is None else seed
         args = dict(batch=bs or 1, rows=R or 4, kv_lens=32768, num_qo_heads=16, num_kv_heads=1,

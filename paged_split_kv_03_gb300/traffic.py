@@ -48,7 +48,7 @@ def call_bytes(wl, chunk_pages: int | None = None, include_scratch: bool = True,
     if plan is not None:
         chunk_pages, tail_from, tail_chunk = plan.chunk_pages, plan.tail_from, plan.tail_chunk_pages
     P, H, D, Hq = wl.page_size, wl.num_kv_heads, wl.head_dim, wl.num_qo_heads
-    kv_elt = 1 if wl.kv_e4m3 else 2
+    kv_elt = 1 if (wl.kv_e4m3 or getattr(wl, "kv_int8", False)) else 2
     q_elt = 1 if wl.q_e4m3 else 2
     lens = wl.kv_len.cpu().tolist()
     qo = wl.qo_indptr.cpu().tolist()

@@ -20,7 +20,10 @@ TOL_FP8 = dict(max=3e-2, mean=3e-3, lse=1e-3)
 
 
 def tol_for(wl):
-    return TOL_FP8 if wl.kv_e4m3 else TOL_BF16
+    # quantised caches (E4M3 or int8) take the bound stated for FP8 KV; int8
+    # widens exactly to bf16 operands, but its per-token v_scale is folded
+    # into the bf16 P, and outlier channels make outputs of magnitude ~4
+    return TOL_FP8 if (wl.kv_e4m3 or getattr(wl, "kv_int8", False)) else TOL_BF16
 
 
 def run_decode(wl, *, chunk_pages=0, kernel=B.PDA_KERNEL_AUTO, max_q_len=None, max_batch=None,

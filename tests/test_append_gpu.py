@@ -1,6 +1,6 @@
 """GPU parity of quantise-on-append (pda_append_kv) against the oracle:
 every byte of both caches and every scale must match exactly, for the three
-cache kinds (bf16 copy, E4M3 per tensor, E4M3 per token and kv head), head
+cache kinds (bf16 copy, E4M3 and int8 per tensor and per token and kv head), head
 dims 64 / 128 / 256 / 512, both cache layouts, ragged rows per request, and the
 status bits of requests the kernel must skip."""
 from __future__ import annotations
@@ -33,6 +33,12 @@ CASES = {
     "pth_d512_p16": dict(kv_dtype="e4m3", scale_mode=SCALE_TOKEN_HEAD, head_dim=512,
                          page_size=16, rows=[2, 8], kv_lens=[40, 300], num_qo_heads=16,
                          num_kv_heads=1),
+    "i8pth_d128_p16": dict(kv_dtype="int8", scale_mode=SCALE_TOKEN_HEAD, head_dim=128,
+                           page_size=16, rows=[8, 1, 3], kv_lens=[300, 17, 3], num_qo_heads=16,
+                           num_kv_heads=2),
+    "i8t_d256_p64_hnd": dict(kv_dtype="int8", scale_mode=SCALE_TENSOR, head_dim=256, page_size=64,
+                             rows=[2, 5], kv_lens=[2, 700], num_qo_heads=16, num_kv_heads=2,
+                             layout="HND"),
     "bf16_d512_p64_hnd": dict(kv_dtype="bf16", scale_mode=SCALE_NONE, head_dim=512,
                               page_size=64, rows=[3], kv_lens=[70], num_qo_heads=4,
                               num_kv_heads=2, layout="HND"),
@@ -40,6 +46,9 @@ CASES = {
 
 
 def _mode(wl):
+    if getattr(wl, "kv_int8", False):
+        return (oracle.APPEND_INT8_TENSOR if wl.scale_mode == SCALE_TENSOR
+                else oracle.APPEND_INT8_TOKEN_HEAD)
     if not wl.kv_e4m3:
         return oracle.APPEND_BF16
     return oracle.APPEND_TENSOR if wl.scale_mode == SCALE_TENSOR else oracle.APPEND_TOKEN_HEAD

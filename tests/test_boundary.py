@@ -130,6 +130,19 @@ def test_plan_head_dim_512(lib):
     assert rc == B.PDA_ERR_UNSUPPORTED
 
 
+def test_plan_int8(lib):
+    # int8 caches take the mma.sync path (widened exactly to bf16), both scale kinds
+    for sm in (1, 2):
+        plan, _, rc = B.pda_plan(_params(kv_dtype=B.PDA_INT8, scale_mode=sm))
+        assert rc == 0 and plan.kernel == B.PDA_KERNEL_MMA and plan.kv_dtype == B.PDA_INT8
+    for bad in (dict(scale_mode=0), dict(q_dtype=1, scale_mode=1),
+                dict(kernel=B.PDA_KERNEL_TC, scale_mode=1), dict(scale_mode=1, **D512)):
+        args = dict(kv_dtype=B.PDA_INT8)
+        args.update(bad)
+        _, _, rc = B.pda_plan(_params(**args), check=False)
+        assert rc == B.PDA_ERR_UNSUPPORTED, bad
+
+
 @pytest.mark.parametrize("bad,code", [
     (dict(num_qo_heads=15), B.PDA_ERR_INVALID),
     (dict(head_dim=96), B.PDA_ERR_UNSUPPORTED),

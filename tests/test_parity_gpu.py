@@ -66,6 +66,16 @@ SMALL = {
     "bf16_p1": dict(batch=2, rows=2, kv_lens=[130, 3], num_qo_heads=4, num_kv_heads=2,
                     head_dim=64, page_size=1, chunk=64),
     # head_dim 512 (tcgen05 path only): one kv head, G = 16 / 8 / 2
+    # int8 caches (mma.sync path): both scale kinds, windows, HND, head_dim 64-256
+    "i8t_d128_g8_win": dict(batch=3, rows=[1, 4, 8], kv_lens=[700, 1500, 33],
+                            windows=[0, 64, 0], num_qo_heads=16, num_kv_heads=2, head_dim=128,
+                            page_size=16, kv_dtype="int8", scale_mode=SCALE_TENSOR),
+    "i8pth_d256_g8_split": dict(batch=2, rows=[8, 2], kv_lens=[2000, 300], num_qo_heads=16,
+                                num_kv_heads=2, head_dim=256, page_size=16, kv_dtype="int8",
+                                scale_mode=SCALE_TOKEN_HEAD, k_outlier_frac=0.01, chunk=16),
+    "i8pth_d64_g3_hnd": dict(batch=3, rows=8, kv_lens=[9, 100, 1000], num_qo_heads=6,
+                             num_kv_heads=2, head_dim=64, page_size=16, layout="HND",
+                             kv_dtype="int8", scale_mode=SCALE_TOKEN_HEAD, chunk=4),
     "bf16_d512_g16_r148": dict(batch=3, rows=[1, 4, 8], kv_lens=[700, 1500, 33],
                                windows=[0, 64, 0], num_qo_heads=16, num_kv_heads=1,
                                head_dim=512, page_size=16, chunk=4),
@@ -88,6 +98,9 @@ PEAKED_SMALL = {
     "fp8pth": dict(batch=2, rows=[4, 8], kv_lens=[2000, 900], num_qo_heads=16, num_kv_heads=2,
                    head_dim=256, page_size=16, q_mult=4.0, chunk=16, kv_dtype="e4m3",
                    scale_mode=SCALE_TOKEN_HEAD),
+    "i8pth": dict(batch=2, rows=[4, 8], kv_lens=[2000, 900], num_qo_heads=16, num_kv_heads=2,
+                  head_dim=256, page_size=16, q_mult=4.0, chunk=16, kv_dtype="int8",
+                  scale_mode=SCALE_TOKEN_HEAD),
     "bf16_d512": dict(batch=2, rows=[4, 8], kv_lens=[2000, 900], num_qo_heads=16,
                       num_kv_heads=1, head_dim=512, page_size=16, q_mult=4.0, chunk=16),
     "fp8pth_d512": dict(batch=2, rows=[4, 8], kv_lens=[2000, 900], num_qo_heads=16,
@@ -107,8 +120,9 @@ KERNELS = {"mma": B.PDA_KERNEL_MMA, "tc": B.PDA_KERNEL_TC}
 
 
 def _tc_ok(wl):
-    """Shapes the tcgen05 path is built for (head_dim 128/256/512, pages of >= 8)."""
-    return wl.head_dim in (128, 256, 512) and wl.page_size >= 8
+    """Shapes the tcgen05 path is built for (head_dim 128/256/512, pages of >= 8,
+    bf16 or E4M3 caches)."""
+    return wl.head_dim in (128, 256, 512) and wl.page_size >= 8 and not wl.kv_int8
 
 
 def _mma_ok(wl):
@@ -136,6 +150,8 @@ def test_small_peaked_parity(kind, kernel):
     wl, chunk = _make(f"{kind}_peaked", PEAKED_SMALL[kind])
     if kernel == "mma" and not _mma_ok(wl):
         pytest.skip("shape served by the tcgen05 path only")
+    if kernel == "tc" and not _tc_ok(wl):
+        pytest.skip("shape served by the mma.sync path only")
     out, lse, status, dec = run_decode(wl, chunk_pages=chunk, kernel=KERNELS[kernel])
     assert status == 0
     ref_o, ref_l = oracle_ref(wl)
@@ -167,6 +183,8 @@ CONFIGS = [
     ("longctx_fp8_pth", dict(bs=1, R=8), 64),
     ("longctx_fp8_pth", dict(bs=16, R=8), 64),
     ("mixed", {}, 160),
+    ("longctx_int8_pth", dict(bs=1, R=8), 64),
+    ("longctx_int8_pth", dict(bs=16, R=1), 64),
     ("d512_mtp_bf16", dict(bs=1, R=4), None),
     ("d512_mtp_bf16", dict(bs=1, R=8, kv_lens=131072), 48),
     ("d512_mtp_fp8", dict(bs=1, R=8), None),

@@ -92,9 +92,9 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor: f32 accumulate, A/B format `fmt` (kind::f16: 1 =
-// bf16; kind::f8f6f4: 0 = E4M3), A (B) MN-major if `a_mn` (`b_mn`), M = 128,
-// N = n.
+// Instruction descriptor: f32 accumulate, A/B format `fmt` (kind::f16: 0 =
+// f16, 1 = bf16; kind::f8f6f4: 0 = E4M3), A (B) MN-major if `a_mn` (`b_mn`),
+// M = 128, N = n.
 __device__ __forceinline__ uint32_t idesc(uint32_t fmt, uint32_t a_mn, uint32_t n,
                                           uint32_t b_mn = 0) {
   return (1u << 4) | (fmt << 7) | (fmt << 10) | (a_mn << 15) | (b_mn << 16) | ((n >> 3) << 17) |
@@ -126,6 +126,27 @@ __device__ __forceinline__ void fence_after() {
 }
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Four int8 codes (byte k = element k) -> two f16 pairs, exactly: with
+// u = x + 128 (the sign bit flipped), the f16 word 0x6400 | u is 1024 + u,
+// and subtracting 1152 leaves x (every integer below 2048 is an f16).
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& e01, uint32_t& e23) {
+  const uint32_t u = w ^ 0x80808080u;
+  uint32_t lo, hi;
+  asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(lo) : "r"(u), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(hi) : "r"(u), "r"(0x64646464u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(e01) : "r"(lo), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(e23) : "r"(hi), "r"(0x64806480u));
+}
+
+// Eight bf16 values -> eight f16 values (RNE; exact inside f16's normal range).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  auto two = [](uint32_t w) -> uint32_t {
+    const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    return *reinterpret_cast<const uint32_t*>(&h);
+  };
+  return make_uint4(two(v.x), two(v.y), two(v.z), two(v.w));
 }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
@@ -338,8 +359,13 @@ template <int D, int KVT, int QT, int SMODE, int NMAX>
 struct TcCfg {
   static constexpr int kD = D;
   static constexpr int kNmax = NMAX;
-  // head_dim 512: a K (or V) tile alone is 64-128 KB, one CTA per SM
-  static constexpr int kCtasPerSm = NMAX <= 16 && D <= 256 ? 2 : 1;
+  // int8 cache: TMA lands the codes in a raw ring, converter warps widen
+  // them exactly to f16 into the MMA ring, and the MMAs are kind::f16 (f16
+  // query, f16 P)
+  static constexpr bool kI8 = KVT == PDA_INT8;
+  // head_dim 512: a K (or V) tile alone is 64-128 KB, one CTA per SM; int8:
+  // one CTA per SM holding both rings
+  static constexpr int kCtasPerSm = NMAX <= 16 && D <= 256 && !kI8 ? 2 : 1;
   // softmax warps: 4 per TMEM lane quadrant when a CTA holds up to 64 columns, else 2
   static constexpr int kSmWarps = NMAX <= 16 ? 8 : 16;
   static constexpr int kSmThreads = 32 * kSmWarps;
@@ -348,15 +374,21 @@ struct TcCfg {
   // per SM on small pages, so the 64-column build splits each chunk's
   // boxes over three warps
   static constexpr int kProducers = NMAX > 16 || kCtasPerSm == 1 ? 3 : 1;
+  static constexpr int kProdThreads = 32 * kProducers;
   static constexpr int kProdWarp1 = 2 + kSmWarps;
-  static constexpr int kThreads = 64 + kSmThreads + 32 * (kProducers - 1);
+  // int8: warps that widen the codes (after the producer warps)
+  static constexpr int kConvWarps = kI8 ? (NMAX <= 16 ? 8 : 4) : 0;
+  static constexpr int kConvThreads = 32 * kConvWarps;
+  static constexpr int kConvWarp0 = kProdWarp1 + kProducers - 1;
+  static constexpr int kThreads = 64 + kSmThreads + 32 * (kProducers - 1) + kConvThreads;
   static constexpr int kColGroups = kSmWarps / 4;   // warps sharing a lane quadrant
   static constexpr bool kF8 = KVT == PDA_E4M3;
   static constexpr bool kQSplit = kF8 && QT == PDA_BF16;  // bf16 query as two E4M3 terms
   static constexpr int kQTerms = kQSplit ? 2 : 1;
-  static constexpr int kElt = kF8 ? 1 : 2;
+  static constexpr int kElt = kF8 ? 1 : 2;            // bytes of an MMA operand element
   static constexpr int kAtom = 128 / kElt;           // elements per 128-byte row
   static constexpr int kChunks = D / kAtom;          // ring slots per K (or V) tile
+  static constexpr int kRawChunks = kI8 ? D / 128 : kChunks;  // TMA chunks per tile
   static constexpr int kTileSlots = 2 * kChunks;
   static constexpr int kQRows = kNmax * kQTerms;
   static constexpr int kQAtomBytes = kQRows * 128;
@@ -384,16 +416,24 @@ struct TcCfg {
   static constexpr int kBudget = kCtasPerSm == 2 ? 228 * 1024 / 2 - 1024 : 227 * 1024;
   // the dynamic window starts 1024-byte aligned (checked at run time)
   static constexpr int kAvail = kBudget - kQBytes - kPBytes - kSmallBytes;
-  static constexpr int kRingRaw = kAvail / kSlot > 12 ? 12 : kAvail / kSlot;
-  // bf16 V blocks span two adjacent slots: keep the ring even so pairs never wrap
+  static constexpr int kAvailSlots = kAvail / kSlot > 12 ? 12 : kAvail / kSlot;
+  // int8: a third of the slots (at least 2) hold TMA'd codes, the rest f16
+  // tiles (the MMA side needs two tiles of those to keep widening ahead)
+  static constexpr int kIRing = kI8 ? (kAvailSlots / 3 < 2 ? 2 : kAvailSlots / 3) : 0;
+  static constexpr int kRingRaw = kAvailSlots - kIRing;
+  // bf16 / f16 V blocks span two adjacent slots: keep the ring even so pairs never wrap
   static constexpr int kRing = kF8 ? kRingRaw : (kRingRaw & ~1);
   // The MMA issuer frees each slot as soon as its MMAs finish, so the ring
   // must hold one whole K (or V) tile (the softmax zeroes the tail rows of
   // the last V tile before its PV); head_dim <= 256 builds keep two tiles
   // in flight, head_dim 512 (a tile of 8 or 4 slots) as many as fit.
-  static constexpr bool kBuildable = kRing >= (D > 256 ? kChunks : kTileSlots) &&
-                                     kTmemNeed <= 512 && kTmemCols * kCtasPerSm <= 512;
-  static constexpr int kSmem = kQBytes + kPBytes + kRing * kSlot + kSmallBytes;
+  // (int8: no tail zeroing, so one tile plus one widened chunk is enough)
+  static constexpr bool kBuildable =
+      kRing >= (kI8 ? kChunks + 2 : (D > 256 ? kChunks : kTileSlots)) && kTmemNeed <= 512 &&
+      kTmemCols * kCtasPerSm <= 512 && (!kI8 || (kIRing >= 1 && D <= 256));
+  static constexpr int kSmem = kQBytes + kPBytes + (kRing + kIRing) * kSlot + kSmallBytes;
+  // barrier words in the small area's first 512 bytes
+  static_assert(2 * (kRing + kIRing) + 10 + 2 <= 64, "barrier area");
 };
 
 // Position of a tile's K or V unit (kChunks ring slots each) in the order
@@ -673,7 +713,8 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
       tmem_wait_st();
     }
     // last tile: rows past the chunk's end may hold stale or poisoned V
-    if (alive && c0 == 0 && tile0 + kTok > x.t_end && tok >= x.t_end) {
+    // (int8 codes are always finite, so their zero P suffices)
+    if (!C::kI8 && alive && c0 == 0 && tile0 + kTok > x.t_end && tok >= x.t_end) {
       const uint32_t gv = static_cast<uint32_t>(unit_pos_v(j, x.ntiles)) * C::kChunks;
       for (int c = 0; c < C::kChunks && alive; ++c) {
         const uint32_t slot = (gv + c) % R_;
@@ -718,8 +759,12 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
       uint8_t* pbase = pb + (r >> 6) * C::kPAtomBytes;
       const uint32_t byte = static_cast<uint32_t>(r & 63) * 2u;
 #pragma unroll
-      for (int i = 0; i < NH; ++i)
-        *reinterpret_cast<__nv_bfloat16*>(pbase + sw128(c0 + i, byte)) = __float2bfloat16_rn(s[i]);
+      for (int i = 0; i < NH; ++i) {
+        if constexpr (C::kI8)
+          *reinterpret_cast<__half*>(pbase + sw128(c0 + i, byte)) = __float2half_rn(s[i]);
+        else
+          *reinterpret_cast<__nv_bfloat16*>(pbase + sw128(c0 + i, byte)) = __float2bfloat16_rn(s[i]);
+      }
     }
     fence_async_smem();
     fence_before();
@@ -806,10 +851,13 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
   uint8_t* q_s = smem;
   uint8_t* p_s = q_s + C::kQBytes;
   uint8_t* ring = p_s + C::kPBytes;
-  uint8_t* small = ring + R_ * kSlot;
+  uint8_t* iring = ring + R_ * kSlot;  // int8: the TMA'd codes (kIRing slots)
+  uint8_t* small = iring + C::kIRing * kSlot;
   uint64_t* full = reinterpret_cast<uint64_t*>(small);
   uint64_t* empty = full + R_;
-  uint64_t* s_full = empty + R_;
+  uint64_t* i_full = empty + R_;           // [kIRing] int8 codes landed
+  uint64_t* i_empty = i_full + C::kIRing;  // [kIRing] ... widened, slot free
+  uint64_t* s_full = i_empty + C::kIRing;
   uint64_t* s_free = s_full + 2;
   uint64_t* p_full = s_free + 2;   // [2]: P of tile j complete, by j & 1
   uint64_t* pv_done = p_full + 2;  // [2]: PV of tile j complete, by j & 1
@@ -864,8 +912,14 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
   // ---- setup: barriers, TMEM, running maxima
   if (tid == 0) {
     for (int s = 0; s < R_; ++s) {
-      bar_init(full + s, C::kProducers);
+      // TMA: one arrive.expect_tx per producer warp; int8: every converter
+      // thread arrives after widening its share into the slot
+      bar_init(full + s, C::kI8 ? C::kConvThreads : C::kProducers);
       bar_init(empty + s, 1);
+    }
+    for (int s = 0; s < C::kIRing; ++s) {
+      bar_init(i_full + s, C::kProducers);
+      bar_init(i_empty + s, C::kConvThreads);
     }
     bar_init(s_full, 1);
     bar_init(s_full + 1, 1);
@@ -937,6 +991,7 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
                                (((int64_t)(q0 + n / hpc) * a.hq + head0 + n % hpc) * D) * C::kElt +
                                cch * 16;
           v = __ldg(reinterpret_cast<const uint4*>(src));
+          if constexpr (C::kI8) v = bf16x8_to_f16x8(v);  // f16 operands beside int8 codes
         }
         const int byte = cch * 16;
         *reinterpret_cast<uint4*>(q_s + (byte / 128) * C::kQAtomBytes + sw128(n, byte % 128)) = v;
@@ -1035,9 +1090,37 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
     };
     ok0 = checked(ok0, pg0);
     ok1 = checked(ok1, pg1);
-    uint32_t g = 0;
+    uint32_t g = 0;   // chunks issued (into the MMA ring; int8: into the int8 ring)
     bool alive = true;
+    // int8: chunk g into the int8 ring once the converters have widened
+    // the chunk whose slot it takes
+    auto emit8 = [&](int kind, bool ok, int pg, int s0) {
+      const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, ok));
+      for (int c = 0; c < C::kRawChunks && alive; ++c, ++g) {
+        const uint32_t slot = g % C::kIRing, round = g / C::kIRing;
+        int good = 1;
+        if (lane == 0) {
+          good = bar_wait(i_empty + slot, (round & 1u) ^ 1u, abort_flag, a.status);
+          if (good) bar_expect_tx(i_full + slot, nvalid * box_bytes);
+        }
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) {
+          alive = false;
+          break;
+        }
+        if (ok) {
+          const uint32_t dst = su32(iring + slot * kSlot) + bx * box_bytes;
+          const int c1 = a.tma_slot_dim == 1 ? s0 : hkv;
+          const int c2 = a.tma_slot_dim == 1 ? hkv : s0;
+          tma_load(dst, maps[kind], c * 128, c1, c2, pg, i_full + slot);
+        }
+      }
+    };
     auto emit = [&](int kind, bool ok, int pg, int s0) {
+      if constexpr (C::kI8) {
+        emit8(kind, ok, pg, s0);
+        return;
+      }
       const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, ok));
       for (int c = 0; c < C::kChunks && alive; ++c, ++g) {
         const uint32_t slot = g % R_, round = g / R_;
@@ -1072,17 +1155,25 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
       pg2 = pg3; s02 = s03; ok2 = ok3;
       ok3 = page_of(j + 4, pg3, s03);
     }
-    // drain: every box issued must have landed before the CTA can exit
-    if (lane == 0) {
-      const uint32_t first = g > (uint32_t)R_ ? g - R_ : 0u;
-      for (uint32_t h = first; h < g; ++h) bar_drain(full + h % R_, (h / R_) & 1u);
+    if constexpr (C::kI8) {
+      // drain: every box issued must have landed before the CTA can exit
+      if (lane == 0) {
+        const uint32_t first = g > (uint32_t)C::kIRing ? g - C::kIRing : 0u;
+        for (uint32_t h = first; h < g; ++h) bar_drain(i_full + h % C::kIRing, (h / C::kIRing) & 1u);
+      }
+    } else {
+      // drain: every box issued must have landed before the CTA can exit
+      if (lane == 0) {
+        const uint32_t first = g > (uint32_t)R_ ? g - R_ : 0u;
+        for (uint32_t h = first; h < g; ++h) bar_drain(full + h % R_, (h / R_) & 1u);
+      }
     }
   } else if (warp == 1) {
     // ===================================================== MMA issuer warp
     if (lane == 0) {
       bool alive = bar_wait(q_ready, 0, abort_flag, a.status);
       fence_after();
-      const uint32_t fmt = kF8 ? 0u : 1u;
+      const uint32_t fmt = kF8 || C::kI8 ? 0u : 1u;  // E4M3, f16 (int8 caches) or bf16
       const uint32_t id_s = idesc(fmt, 0, static_cast<uint32_t>(Nq));
       // E4M3: N = both P terms' columns; bf16: N columns
       const uint32_t id_p = idesc(fmt, 1, static_cast<uint32_t>(kF8 ? 2 * N : N), C::kPMn ? 1u : 0u);
@@ -1156,6 +1247,40 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
       // make sure nothing issued is still running before TMEM is released
       mma_commit(drain);
       bar_drain(drain, 0);
+    }
+  } else if (warp >= C::kConvWarp0) {
+    // =============================== int8 converter warps (kConvWarps > 0)
+    // widen TMA chunk gw (128 tokens x 128 codes) into MMA-ring chunks 2gw
+    // and 2gw + 1 (64 f16 each), 16 codes per thread and step, in FIFO order
+    if constexpr (C::kI8) {
+      const int ct = tid - C::kConvWarp0 * 32;  // 0..kConvThreads-1
+      const uint32_t total = 2u * static_cast<uint32_t>(ntiles) * C::kRawChunks;
+      for (uint32_t gw = 0; gw < total; ++gw) {
+        const uint32_t is = gw % C::kIRing;
+        const uint32_t c0 = 2 * gw, d0 = c0 % R_, d1 = (c0 + 1) % R_;
+        bool ok = bar_wait(i_full + is, (gw / C::kIRing) & 1u, abort_flag, a.status);
+        if (ok) ok = bar_wait(empty + d0, ((c0 / R_) & 1u) ^ 1u, abort_flag, a.status);
+        if (ok) ok = bar_wait(empty + d1, (((c0 + 1) / R_) & 1u) ^ 1u, abort_flag, a.status);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        const uint8_t* src = iring + is * kSlot;
+        for (int idx = ct; idx < kTok * 8; idx += C::kConvThreads) {
+          const int r = idx >> 3, gl = idx & 7;  // token row, 16-code piece
+          const uint4 raw = *reinterpret_cast<const uint4*>(src + r * 128 + ((gl ^ (r & 7)) << 4));
+          uint4 lo, hi;
+          i8x4_to_f16x4(raw.x, lo.x, lo.y);
+          i8x4_to_f16x4(raw.y, lo.z, lo.w);
+          i8x4_to_f16x4(raw.z, hi.x, hi.y);
+          i8x4_to_f16x4(raw.w, hi.z, hi.w);
+          uint8_t* dst = ring + (gl < 4 ? d0 : d1) * kSlot + r * 128;
+          const int p0 = (gl & 3) * 2;  // first 16-byte piece of the f16 row
+          *reinterpret_cast<uint4*>(dst + ((p0 ^ (r & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(dst + (((p0 + 1) ^ (r & 7)) << 4)) = hi;
+        }
+        fence_async_smem();  // the MMAs read these through the async proxy
+        bar_arrive(full + d0);
+        bar_arrive(full + d1);
+        bar_arrive(i_empty + is);
+      }
     }
   } else {
     // ========================================= softmax / epilogue warps
@@ -1242,6 +1367,11 @@ auto tc_select(const pda_plan_t* p, int nmax, F f) {
   const int kv = p->kv_dtype, qd = p->q_dtype, sm = p->scale_mode;
 #define PDA_TC_CASES(DD, NN)                                                              \
   if (kv == PDA_BF16) return f.template get<DD, PDA_BF16, PDA_BF16, PDA_SCALE_NONE, NN>(); \
+  if (kv == PDA_INT8) {                                                                   \
+    if (sm == PDA_SCALE_TENSOR)                                                           \
+      return f.template get<DD, PDA_INT8, PDA_BF16, PDA_SCALE_TENSOR, NN>();              \
+    return f.template get<DD, PDA_INT8, PDA_BF16, PDA_SCALE_TOKEN_HEAD, NN>();            \
+  }                                                                                       \
   if (qd == PDA_BF16) {                                                                   \
     if (sm == PDA_SCALE_TENSOR)                                                           \
       return f.template get<DD, PDA_E4M3, PDA_BF16, PDA_SCALE_TENSOR, NN>();              \
@@ -1298,7 +1428,7 @@ EncodeFn encoder() {
 bool make_map(CUtensorMap* m, const void* base, const pda_plan_t* p, int* slot_dim) {
   EncodeFn enc = encoder();
   if (!enc) return false;
-  const int eb = p->kv_dtype == PDA_E4M3 ? 1 : 2;
+  const int eb = p->kv_dtype == PDA_BF16 ? 2 : 1;  // E4M3 / int8 codes: one byte
   const bool slot_first = p->kv_stride_token <= p->kv_stride_head;
   *slot_dim = slot_first ? 1 : 2;
   const cuuint32_t rows = static_cast<cuuint32_t>(p->page_size < kTok ? p->page_size : kTok);
@@ -1325,7 +1455,7 @@ bool make_map(CUtensorMap* m, const void* base, const pda_plan_t* p, int* slot_d
   strides[2] = static_cast<cuuint64_t>(p->kv_stride_page) * eb;
   box[3] = 1;
   const CUtensorMapDataType dt =
-      p->kv_dtype == PDA_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+      p->kv_dtype == PDA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   return enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -1335,7 +1465,7 @@ bool make_map(CUtensorMap* m, const void* base, const pda_plan_t* p, int* slot_d
 
 bool tc_supported(const pda_plan_t* p) {
   return (p->head_dim == 128 || p->head_dim == 256 || p->head_dim == 512) && p->page_size >= 8 &&
-         p->page_size <= 256 && p->kv_dtype != PDA_INT8;
+         p->page_size <= 256 && (p->kv_dtype != PDA_INT8 || p->head_dim <= 256);
 }
 
 // Rows x heads a CTA may hold: 64, except head_dim 512 over an E4M3 cache,

@@ -131,12 +131,17 @@ def test_plan_head_dim_512(lib):
 
 
 def test_plan_int8(lib):
-    # int8 caches take the mma.sync path (widened exactly to bf16), both scale kinds
+    # int8 caches: the tcgen05 path up to head_dim 256 (codes widened to f16
+    # in shared memory, one CTA per SM), the mma.sync path at head_dim 64
     for sm in (1, 2):
         plan, _, rc = B.pda_plan(_params(kv_dtype=B.PDA_INT8, scale_mode=sm))
-        assert rc == 0 and plan.kernel == B.PDA_KERNEL_MMA and plan.kv_dtype == B.PDA_INT8
-    for bad in (dict(scale_mode=0), dict(q_dtype=1, scale_mode=1),
-                dict(kernel=B.PDA_KERNEL_TC, scale_mode=1), dict(scale_mode=1, **D512)):
+        assert rc == 0 and plan.kernel == B.PDA_KERNEL_TC and plan.kv_dtype == B.PDA_INT8
+        assert plan.stage1_smem_bytes <= 227 * 1024
+        d64, _, rc = B.pda_plan(_params(kv_dtype=B.PDA_INT8, scale_mode=sm, head_dim=64,
+                                        kv_stride_page=16 * 2 * 64, kv_stride_token=2 * 64,
+                                        kv_stride_head=64))
+        assert rc == 0 and d64.kernel == B.PDA_KERNEL_MMA
+    for bad in (dict(scale_mode=0), dict(q_dtype=1, scale_mode=1), dict(scale_mode=1, **D512)):
         args = dict(kv_dtype=B.PDA_INT8)
         args.update(bad)
         _, _, rc = B.pda_plan(_params(**args), check=False)

@@ -66,7 +66,7 @@ SMALL = {
     "bf16_p1": dict(batch=2, rows=2, kv_lens=[130, 3], num_qo_heads=4, num_kv_heads=2,
                     head_dim=64, page_size=1, chunk=64),
     # head_dim 512 (tcgen05 path only): one kv head, G = 16 / 8 / 2
-    # int8 caches (mma.sync path): both scale kinds, windows, HND, head_dim 64-256
+    # int8 caches: both scale kinds, windows, HND, head_dim 64-256
     "i8t_d128_g8_win": dict(batch=3, rows=[1, 4, 8], kv_lens=[700, 1500, 33],
                             windows=[0, 64, 0], num_qo_heads=16, num_kv_heads=2, head_dim=128,
                             page_size=16, kv_dtype="int8", scale_mode=SCALE_TENSOR),
@@ -120,9 +120,10 @@ KERNELS = {"mma": B.PDA_KERNEL_MMA, "tc": B.PDA_KERNEL_TC}
 
 
 def _tc_ok(wl):
-    """Shapes the tcgen05 path is built for (head_dim 128/256/512, pages of >= 8,
-    bf16 or E4M3 caches)."""
-    return wl.head_dim in (128, 256, 512) and wl.page_size >= 8 and not wl.kv_int8
+    """Shapes the tcgen05 path is built for (head_dim 128/256/512, pages of >= 8;
+    int8 caches up to head_dim 256)."""
+    return (wl.head_dim in (128, 256, 512) and wl.page_size >= 8 and
+            (not wl.kv_int8 or wl.head_dim <= 256))
 
 
 def _mma_ok(wl):

@@ -158,9 +158,9 @@ def make_flush(dev):
 
 # Quantise-on-append of one decode step's new rows, timed like a call:
 # (workload, sizes) -- per-tensor E4M3 (bs 128, R 1, 8 kv heads, D 128),
-# per-(token, head) E4M3 (bs 16, R 8, 2 kv heads, D 256), bf16 (same shape).
+# per-(token, head) E4M3 and int8 (bs 16, R 8, 2 kv heads, D 256), bf16 (same shape).
 APPEND_SWEEP = [("fp8_decode", {}), ("longctx_fp8_pth", dict(bs=16, R=8)),
-                ("mtp_verify_bf16", dict(bs=16, R=8))]
+                ("longctx_int8_pth", dict(bs=16, R=8)), ("mtp_verify_bf16", dict(bs=16, R=8))]
 
 
 def append_time(name, kw, dev, steps, flush, peak):

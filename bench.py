@@ -316,6 +316,18 @@ def oracle_rate(wl, budget_s: float, seed: int = 0, max_items=None):
     return gbs, full_s, n, total, oracle.max_threads()
 
 
+def parse_workload(spec):
+    """'name' or 'name:k=v,k=v' (integer values) -> (name, kwargs, description)."""
+    name, _, rest = spec.partition(":")
+    kw = {}
+    for item in filter(None, rest.split(",")):
+        k, _, v = item.partition("=")
+        kw[k.strip()] = int(v)
+    if name == HEADLINE and not kw:
+        return name, kw, HEADLINE_DESC
+    return name, kw, f"{name} {kw}"
+
+
 def run_ours(args, rank, world, dev):
     import torch
 
@@ -325,7 +337,8 @@ def run_ours(args, rank, world, dev):
     peak, peak_kind = peaks()
     flush = make_flush(dev)
 
-    wl = config_workload(HEADLINE, device=dev)
+    wname, wkw, wdesc = parse_workload(args.workload)
+    wl = config_workload(wname, device=dev, **wkw)
     dec, out, lse, stream, graph = setup_call(wl, dev)
     nbytes = call_bytes(wl, plan=dec.plan)
     flops = call_flops(wl)
@@ -354,7 +367,7 @@ def run_ours(args, rank, world, dev):
     stage1_bytes = nbytes["total"] - nbytes["scratch"] // 2
     roof = {"bound": "hbm", "kernel": "stage1", "peak": peak, "unit": "GB/s",
             "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
-            "traffic": recorded_traffic("stage1", HEADLINE)}
+            "traffic": recorded_traffic("stage1", args.workload)}
     if stage1_ms:
         roof["achieved"] = stage1_bytes / (stage1_ms * 1e-3) / 1e9
         roof["frac"] = roof["achieved"] / peak
@@ -396,7 +409,7 @@ def run_ours(args, rank, world, dev):
     if rank == 0 and not args.no_cpu_baseline:
         gbs, full_s, n, total, cores = oracle_rate(wl, budget_s=args.cpu_seconds)
         cpu = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
-               "sample": f"{n} of {total} (row, q head) items of {HEADLINE}, timed and scaled "
+               "sample": f"{n} of {total} (row, q head) items of {wname}, timed and scaled "
                          f"to the whole call ({full_s:.1f} s per call)"}
 
     if rank != 0:
@@ -405,10 +418,13 @@ def run_ours(args, rank, world, dev):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "us_per_call": ms * 1e3,
         "frac_of_peak": value / world / peak, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": value / world / PAGES_NUMBER["value"],
-        "vs_baseline_ref": PAGES_NUMBER, "dtype": "e4m3 (tcgen05 e4m3 x e4m3 MMAs, fp32 accumulate)",
-        "data": "synthetic (seeded N(0,1), e4m3 per-tensor)",
-        "config": {"workload": HEADLINE_DESC, "parallelism": f"replicas x{world}",
+        "vs_baseline": value / world / PAGES_NUMBER["value"] if wdesc == HEADLINE_DESC else None,
+        "vs_baseline_ref": PAGES_NUMBER,
+        "dtype": ("e4m3 (tcgen05 e4m3 x e4m3 MMAs, fp32 accumulate)" if wdesc == HEADLINE_DESC
+                  else ("int8" if wl.kv_int8 else "e4m3" if wl.kv_e4m3 else "bf16")),
+        "data": "synthetic (seeded N(0,1), e4m3 per-tensor)" if wdesc == HEADLINE_DESC
+                else "synthetic (seeded N(0,1))",
+        "config": {"workload": wdesc, "parallelism": f"replicas x{world}",
                    "l2": "flushed before every step (memset of 2x L2, then a read of 2x L2), outside the events",
                    "graph": "stage 1 + stage 2 captured in one CUDA graph",
                    "splits": dec.plan.max_splits, "chunk_pages": dec.plan.chunk_pages,
@@ -459,6 +475,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--workload", default=HEADLINE,
+                    help="workload of the timed step, 'name' or 'name:bs=16,R=8' (default: "
+                         "the FP8 decode headline); other workloads serve profiling")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=4.0)

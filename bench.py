@@ -362,8 +362,20 @@ def run_ours(args, rank, world, dev):
     value = nbytes["total"] * world / (ms * 1e-3) / 1e9
     assert dec.status() == 0, "device status bits set during the benchmark"
 
-    # the dominant kernel: stage 1 (the only launch when the call has one split)
-    stage1_ms = ms if launches_per_step == 1 else None
+    # the dominant kernel: stage 1, timed on its own (a graph of the stage-1
+    # launch alone, pda_decode_stages(PARTIAL), same flush and events) right
+    # after the timed region; with one split it is the whole call
+    if launches_per_step == 1:
+        stage1_ms = ms
+    else:
+        from paged_split_kv_03_gb300 import binding as B
+        g1 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g1, stream=stream):
+            dec.run(wl, out, lse, max_q_len=max(1, wl.max_q_len), stream=stream,
+                    stages=B.PDA_STAGE_PARTIAL)
+        t1 = time_graph(g1.replay, args.steps, args.warmup, flush, stream)
+        stage1_ms = sum(t1) / len(t1)
+        del g1
     stage1_bytes = nbytes["total"] - nbytes["scratch"] // 2
     roof = {"bound": "hbm", "kernel": "stage1", "peak": peak, "unit": "GB/s",
             "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",

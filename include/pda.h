@@ -179,6 +179,23 @@ int pda_decode(const pda_plan_t* plan, const void* q, const void* k_pages, const
                float sm_scale, const float* k_scale, const float* v_scale, void* out,
                float* lse, void* split_scratch, pda_stream_t stream);
 
+/* pda_decode in two halves, for callers that schedule or time them apart.
+ * `stages` is a mask: PDA_STAGE_PARTIAL enqueues stage 1 (the partial
+ * attention of every KV chunk; requests whose rows have one chunk get their
+ * final out / lse here, the others write partials to split_scratch);
+ * PDA_STAGE_MERGE enqueues stage 2 (the per-row merge of those partials; no
+ * launch when plan->max_splits is 1). Both bits = pda_decode. The merge
+ * must follow stage 1 of the same call on the same stream, with the same
+ * arguments. Other bits, or none, return PDA_ERR_INVALID. */
+#define PDA_STAGE_PARTIAL 1u
+#define PDA_STAGE_MERGE 2u
+int pda_decode_stages(const pda_plan_t* plan, const void* q, const void* k_pages,
+                      const void* v_pages, const int32_t* page_table, const int32_t* kv_indptr,
+                      const int32_t* kv_len, const int32_t* qo_indptr, int32_t max_q_len,
+                      const int32_t* window, float sm_scale, const float* k_scale,
+                      const float* v_scale, void* out, float* lse, void* split_scratch,
+                      uint32_t stages, pda_stream_t stream);
+
 /* Quantise-on-append: write the R_b new tokens of every request into the
  * paged cache, the step before decode reads them ("perf(attention): run up
  * to 8 query rows per request in the triton decode kernel", End-to-end A/B:

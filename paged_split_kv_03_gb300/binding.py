@@ -88,6 +88,10 @@ def load_library(path: Optional[str] = None):
     lib.pda_decode.argtypes = [ctypes.POINTER(PdaPlan), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                _i32, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.pda_decode.restype = ctypes.c_int
+    lib.pda_decode_stages.argtypes = [ctypes.POINTER(PdaPlan), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                      _i32, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _u32,
+                                      _vp]
+    lib.pda_decode_stages.restype = ctypes.c_int
     lib.pda_decode_static.argtypes = [ctypes.POINTER(PdaPlan), _vp, _vp, _vp, _vp, _vp, _vp,
                                       _vp, _i32, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp]
     lib.pda_decode_static.restype = ctypes.c_int
@@ -150,6 +154,23 @@ def pda_decode(plan: PdaPlan, q, k_pages, v_pages, page_table, kv_indptr, kv_len
         _stream(stream))
     if check and rc != PDA_OK:
         raise PdaError(rc, "pda_decode")
+    return rc
+
+
+PDA_STAGE_PARTIAL, PDA_STAGE_MERGE = 1, 2
+
+
+def pda_decode_stages(plan: PdaPlan, q, k_pages, v_pages, page_table, kv_indptr, kv_len,
+                      qo_indptr, max_q_len: int, window, sm_scale: float, k_scale, v_scale, out,
+                      lse, split_scratch, stages: int, stream=None, check: bool = True) -> int:
+    """pda_decode's stage 1 (PDA_STAGE_PARTIAL) and / or merge (PDA_STAGE_MERGE)."""
+    rc = load_library().pda_decode_stages(
+        ctypes.byref(plan), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+        _ptr(kv_indptr), _ptr(kv_len), _ptr(qo_indptr), int(max_q_len), _ptr(window),
+        float(sm_scale), _ptr(k_scale), _ptr(v_scale), _ptr(out), _ptr(lse), _ptr(split_scratch),
+        int(stages), _stream(stream))
+    if check and rc != PDA_OK:
+        raise PdaError(rc, "pda_decode_stages")
     return rc
 
 
@@ -236,11 +257,14 @@ class Decoder:
         n = (max(self.scratch_bytes, 256) + 255) // 256 * 256
         self.scratch = torch.zeros(n, dtype=torch.uint8, device=device)
 
-    def run(self, wl, out, lse, max_q_len=None, stream=None, sm_scale=None):
-        return pda_decode(self.plan, wl.q, wl.k_pages, wl.v_pages, wl.page_table, wl.kv_indptr,
-                          wl.kv_len, wl.qo_indptr, max_q_len or max(1, wl.max_q_len), wl.window,
-                          wl.sm_scale if sm_scale is None else sm_scale, wl.k_scale, wl.v_scale,
-                          out, lse, self.scratch, stream)
+    def run(self, wl, out, lse, max_q_len=None, stream=None, sm_scale=None, stages=None):
+        args = (self.plan, wl.q, wl.k_pages, wl.v_pages, wl.page_table, wl.kv_indptr, wl.kv_len,
+                wl.qo_indptr, max_q_len or max(1, wl.max_q_len), wl.window,
+                wl.sm_scale if sm_scale is None else sm_scale, wl.k_scale, wl.v_scale, out, lse,
+                self.scratch)
+        if stages is None:
+            return pda_decode(*args, stream)
+        return pda_decode_stages(*args, stages, stream)
 
     def status(self, stream=None) -> int:
         return pda_get_status(self.plan, self.scratch, stream)

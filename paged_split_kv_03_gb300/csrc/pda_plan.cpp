@@ -280,13 +280,15 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
   return PDA_OK;
 }
 
-extern "C" int pda_decode(const pda_plan_t* plan, const void* q, const void* k_pages,
-                          const void* v_pages, const int32_t* page_table,
-                          const int32_t* kv_indptr, const int32_t* kv_len,
-                          const int32_t* qo_indptr, int32_t max_q_len, const int32_t* window,
-                          float sm_scale, const float* k_scale, const float* v_scale, void* out,
-                          float* lse, void* split_scratch, pda_stream_t stream) {
+extern "C" int pda_decode_stages(const pda_plan_t* plan, const void* q, const void* k_pages,
+                                 const void* v_pages, const int32_t* page_table,
+                                 const int32_t* kv_indptr, const int32_t* kv_len,
+                                 const int32_t* qo_indptr, int32_t max_q_len,
+                                 const int32_t* window, float sm_scale, const float* k_scale,
+                                 const float* v_scale, void* out, float* lse,
+                                 void* split_scratch, uint32_t stages, pda_stream_t stream) {
   if (!plan) return PDA_ERR_NULL;
+  if (stages == 0 || (stages & ~(PDA_STAGE_PARTIAL | PDA_STAGE_MERGE))) return PDA_ERR_INVALID;
   if (plan->magic != PDA_PLAN_MAGIC) return PDA_ERR_PLAN;
   if (!q || !k_pages || !v_pages || !page_table || !kv_indptr || !kv_len || !qo_indptr || !out)
     return PDA_ERR_NULL;
@@ -343,10 +345,24 @@ extern "C" int pda_decode(const pda_plan_t* plan, const void* q, const void* k_p
   a.rows_cap = plan->rows_cap;
   for (int r = 0; r <= pda::kMaxQLen; ++r) a.hpc[r] = plan->heads_per_cta[r];
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  int rc = plan->kernel == PDA_KERNEL_TC ? pda::launch_stage1_tc(plan, a, s)
-                                         : pda::launch_stage1_mma(plan, a, s);
-  if (rc == PDA_OK && plan->max_splits > 1) rc = pda::launch_stage2(plan, a, s);
+  int rc = PDA_OK;
+  if (stages & PDA_STAGE_PARTIAL)
+    rc = plan->kernel == PDA_KERNEL_TC ? pda::launch_stage1_tc(plan, a, s)
+                                       : pda::launch_stage1_mma(plan, a, s);
+  if (rc == PDA_OK && (stages & PDA_STAGE_MERGE) && plan->max_splits > 1)
+    rc = pda::launch_stage2(plan, a, s);
   return rc;
+}
+
+extern "C" int pda_decode(const pda_plan_t* plan, const void* q, const void* k_pages,
+                          const void* v_pages, const int32_t* page_table,
+                          const int32_t* kv_indptr, const int32_t* kv_len,
+                          const int32_t* qo_indptr, int32_t max_q_len, const int32_t* window,
+                          float sm_scale, const float* k_scale, const float* v_scale, void* out,
+                          float* lse, void* split_scratch, pda_stream_t stream) {
+  return pda_decode_stages(plan, q, k_pages, v_pages, page_table, kv_indptr, kv_len, qo_indptr,
+                           max_q_len, window, sm_scale, k_scale, v_scale, out, lse,
+                           split_scratch, PDA_STAGE_PARTIAL | PDA_STAGE_MERGE, stream);
 }
 
 extern "C" int pda_get_status(const pda_plan_t* plan, const void* split_scratch,

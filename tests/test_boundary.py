@@ -190,6 +190,14 @@ def test_decode_host_checks_return_before_any_launch(lib):
     fplan, _, _ = B.pda_plan(_params(kv_dtype=1, scale_mode=2, kv_stride_page=16 * 2 * 256,
                                      kv_stride_token=512, kv_stride_head=256))
     assert B.pda_decode(fplan, check=False, **args) == B.PDA_ERR_NULL  # scales missing
+    # the two-stage entry point: a stage mask of 0 or with unknown bits is refused
+    sargs = dict(args)
+    stream = sargs.pop("stream")
+    for mask in (0, 4, 7):
+        assert B.pda_decode_stages(plan, check=False, stages=mask, stream=stream,
+                                   **sargs) == B.PDA_ERR_INVALID
+    assert B.pda_decode_stages(plan, check=False, stages=1, stream=stream,
+                               **dict(sargs, q=None)) == B.PDA_ERR_NULL
 
 
 def test_strerror(lib):

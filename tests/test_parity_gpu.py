@@ -380,6 +380,28 @@ def test_rows_equal_single_row_requests():
     assert (lse1 - lse).abs().max() <= TOL_BF16["lse"]
 
 
+def test_stages_apart_equal_one_call():
+    """pda_decode_stages(PARTIAL) then (MERGE) on one stream writes the same
+    bytes as pda_decode (a plan with tail splits: both launches run)."""
+    wl = config_workload("fp8_decode", device=DEV, batch=40)
+    dec = B.Decoder(B.params_for(wl), device=DEV)
+    assert dec.plan.max_splits > 1
+    outs = []
+    for stages in (None, "apart"):
+        out = torch.full((wl.total_rows, wl.num_qo_heads, wl.head_dim), float("nan"),
+                         dtype=torch.bfloat16, device=DEV)
+        lse = torch.full((wl.total_rows, wl.num_qo_heads), float("nan"), device=DEV)
+        if stages is None:
+            dec.run(wl, out, lse)
+        else:
+            dec.run(wl, out, lse, stages=B.PDA_STAGE_PARTIAL)
+            dec.run(wl, out, lse, stages=B.PDA_STAGE_MERGE)
+        torch.cuda.synchronize()
+        outs.append((out.view(torch.int16).cpu(), lse.cpu()))
+    assert dec.status() == 0
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
 def test_cuda_graph_replay_with_new_lengths():
     """One plan + one captured graph serve new kv_len / page_table / qo_indptr
     / window contents (same maxima): replay matches the oracle on each."""

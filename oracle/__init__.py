@@ -69,7 +69,7 @@ def _load(mutation: int = 0):
         return _LIBS[mutation]
     lib = ctypes.CDLL(build(mutation))
     i32, i64, vp, dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_double
-    lib.pdo_attention.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i64, i64, i64, i64,
+    lib.pdo_attention.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, i64, i64, i64, i64,
                                   vp, vp, vp, vp, vp, vp, vp, vp, dbl, vp, vp, i64, vp, i64,
                                   vp, vp, i32]
     lib.pdo_attention.restype = i32
@@ -120,13 +120,16 @@ def max_threads() -> int:
 def attention(*, q, k_pages, v_pages, page_table, kv_indptr, kv_len, qo_indptr, window,
               sm_scale, k_scale=None, v_scale=None, num_qo_heads, num_kv_heads, head_dim,
               page_size, q_e4m3, kv_e4m3, scale_mode, strides, num_pages, items=None,
-              split_tokens=0, num_threads=0, mutation=0, check=True, kv_int8=False):
+              split_tokens=0, num_threads=0, mutation=0, check=True, kv_int8=False,
+              head_dim_v=None):
     """fp64 attention for the given (row, q head) items.
 
     Arrays are CPU tensors / numpy arrays holding raw cache payloads (bf16 as
     16-bit words, e4m3 and int8 as bytes; ``kv_int8`` marks an int8 cache).
     ``strides`` = (page, token, head) in elements. ``items`` = flat indices
-    row*Hq + h (None: every item).
+    row*Hq + h (None: every item). ``head_dim_v`` (default ``head_dim``): the
+    value channels, the first ones of each v row (MLA: the latent cache is
+    passed as both k and v, 576 channels, V the first 512).
     Returns (out [n, D] float64, lse [n] float64, status).
     """
     lib = _load(mutation)
@@ -144,11 +147,12 @@ def attention(*, q, k_pages, v_pages, page_table, kv_indptr, kv_len, qo_indptr, 
     batch = int(kl.shape[0])
     total_rows = int(qi[batch]) if batch else 0
     n = int(it.shape[0]) if it is not None else total_rows * num_qo_heads
-    out = np.zeros((max(n, 0), head_dim), dtype=np.float64)
+    dv = int(head_dim_v or head_dim)
+    out = np.zeros((max(n, 0), dv), dtype=np.float64)
     lse = np.zeros((max(n, 0),), dtype=np.float64)
     sp, st, sh = (int(s) for s in strides)
     kv_dtype = 2 if kv_int8 else int(bool(kv_e4m3))
-    rc = lib.pdo_attention(batch, num_qo_heads, num_kv_heads, head_dim, page_size, int(q_e4m3),
+    rc = lib.pdo_attention(batch, num_qo_heads, num_kv_heads, head_dim, dv, page_size, int(q_e4m3),
                            kv_dtype, int(scale_mode), sp, st, sh, int(num_pages), _ptr(q_),
                            _ptr(k_), _ptr(v_), _ptr(pt), _ptr(ki), _ptr(kl), _ptr(qi), _ptr(win),
                            float(sm_scale), _ptr(ks), _ptr(vs), int(split_tokens), _ptr(it),
@@ -168,7 +172,8 @@ def attention_for(wl, items=None, split_tokens=0, num_threads=0, mutation=0, **o
                 num_qo_heads=wl.num_qo_heads, num_kv_heads=wl.num_kv_heads,
                 head_dim=wl.head_dim, page_size=wl.page_size, q_e4m3=wl.q_e4m3,
                 kv_e4m3=wl.kv_e4m3, scale_mode=wl.scale_mode, strides=wl.strides,
-                num_pages=wl.num_pages, kv_int8=getattr(wl, "kv_int8", False))
+                num_pages=wl.num_pages, kv_int8=getattr(wl, "kv_int8", False),
+                head_dim_v=getattr(wl, "head_dim_v", None))
     args.update(overrides)
     return attention(items=items, split_tokens=split_tokens, num_threads=num_threads,
                      mutation=mutation, **args)

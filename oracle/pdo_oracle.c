@@ -28,6 +28,10 @@
  *    W <= 0, or no window array, means no lower bound.
  *  - lse is the natural log of sum_j exp(s_j) over the scaled logits.
  *  - FP8 is OCP E4M3 ("e4m3fn": bias 7, no infinities, S.1111.111 is NaN).
+ *  - MLA decode ("fp8 support", FlashMLA PR #54): the keys are the latent
+ *    vectors of d channels (512 nope + 64 rope, the page's kv_rope) and the
+ *    values are their first dv = 512 channels; a caller passes the latent
+ *    cache as both k and v, and the oracle reads V channels c < dv.
  *  - An int8 cache (named beside bf16 and fp8 in the register-spill check of
  *    FreeToken PR #900, "Tested on") holds two's-complement bytes; the value
  *    is the byte times the same per-tensor or per-(token, kv head) scale.
@@ -96,6 +100,7 @@ static double pdo_int8_to_double(uint8_t byte) {
 
 typedef struct {
   int batch, hq, hkv, d, page_size;
+  int dv;                           /* value channels (<= d): o has dv entries */
   int q_e4m3, kv_dtype, scale_mode; /* kv_dtype: PDO_KV_*; scale_mode: 0 none, 1 per tensor,
                                        2 per (token, kv head) */
   int64_t sp, st, sh;              /* cache strides in elements: page, token-in-page, kv head */
@@ -137,7 +142,7 @@ static double pdo_kv_elem(const pdo_problem* p, const void* cache, const float* 
 static double pdo_attend_range(const pdo_problem* p, int b, int64_t row, int h, int g,
                                int64_t lo, int64_t hi, double* s, double* o) {
   int64_t n = hi - lo + 1;
-  for (int d = 0; d < p->d; ++d) o[d] = 0.0;
+  for (int d = 0; d < p->dv; ++d) o[d] = 0.0;
   if (n <= 0) return -INFINITY;
   double m = -INFINITY;
   for (int64_t j = 0; j < n; ++j) {
@@ -150,10 +155,12 @@ static double pdo_attend_range(const pdo_problem* p, int b, int64_t row, int h, 
   for (int64_t j = 0; j < n; ++j) {
     double w = exp(s[j] - m);
     l += w;
-    for (int d = 0; d < p->d; ++d) o[d] += w * pdo_kv_elem(p, p->v, MUT(9) ? p->k_scale : p->v_scale, b, lo + j, g, d);
+    for (int d = 0; d < p->dv; ++d)
+      o[d] += w * pdo_kv_elem(p, p->v, MUT(9) ? p->k_scale : p->v_scale, b, lo + j, g,
+                              d + MUT(24) * (p->d - p->dv));
   }
   if (!MUT(15))
-    for (int d = 0; d < p->d; ++d) o[d] /= l;
+    for (int d = 0; d < p->dv; ++d) o[d] /= l;
   return MUT(5) ? log(l) : m + log(l);
 }
 
@@ -166,7 +173,7 @@ static int pdo_item(const pdo_problem* p, int64_t row, int h, int64_t split_toke
   int64_t i = row - p->qo_indptr[b];
   int64_t L = p->kv_len[b];
   if (L < rows_b) {
-    for (int d = 0; d < p->d; ++d) out[d] = NAN;
+    for (int d = 0; d < p->dv; ++d) out[d] = NAN;
     *lse_out = NAN;
     return PDO_ERR_KVLEN;
   }
@@ -183,26 +190,26 @@ static int pdo_item(const pdo_problem* p, int64_t row, int h, int64_t split_toke
   /* Split mode: per-chunk partials, then the log-sum-exp merge. */
   int64_t nchunks = pos / split_tokens + 1;
   double* lse_c = (double*)malloc(sizeof(double) * (size_t)nchunks);
-  double* o_c = (double*)malloc(sizeof(double) * (size_t)nchunks * (size_t)p->d);
+  double* o_c = (double*)malloc(sizeof(double) * (size_t)nchunks * (size_t)p->dv);
   double big = -INFINITY;
   for (int64_t c = 0; c < nchunks; ++c) {
     int64_t a = c * split_tokens, e = a + split_tokens - 1;
     if (a < lo) a = lo;
     if (e > pos) e = pos;
     lse_c[c] = pdo_attend_range(p, b, row, h, g, a, e, s, oc);
-    memcpy(o_c + c * p->d, oc, sizeof(double) * (size_t)p->d);
+    memcpy(o_c + c * p->dv, oc, sizeof(double) * (size_t)p->dv);
     if (lse_c[c] > big) big = lse_c[c];
   }
   double wsum = 0.0;
-  for (int d = 0; d < p->d; ++d) out[d] = 0.0;
+  for (int d = 0; d < p->dv; ++d) out[d] = 0.0;
   for (int64_t c = 0; c < nchunks; ++c) {
     if (lse_c[c] == -INFINITY) continue; /* weight 0 */
     double wc = exp(lse_c[c] - big);
     wsum += wc;
-    for (int d = 0; d < p->d; ++d) out[d] += wc * o_c[c * p->d + d];
+    for (int d = 0; d < p->dv; ++d) out[d] += wc * o_c[c * p->dv + d];
   }
   if (!MUT(8))
-    for (int d = 0; d < p->d; ++d) out[d] /= wsum;
+    for (int d = 0; d < p->dv; ++d) out[d] /= wsum;
   *lse_out = big + log(wsum);
   free(lse_c);
   free(o_c);
@@ -217,12 +224,13 @@ static int pdo_item(const pdo_problem* p, int64_t row, int h, int64_t split_toke
  *            bytes (kv_dtype 0 / 1 / 2)
  *   k_scale, v_scale: NULL (scale_mode 0), [1] (1) or
  *            [num_pages, page_size, hkv] (2)
+ *   dv       value channels, 1..d: V is channels [0, dv) of each v row
  *   items    NULL: all total_rows*hq items in order; else flat indices
  *            row*hq + h, n_items of them
- *   out      [n_items, d] fp64; lse [n_items] fp64 (natural log)
+ *   out      [n_items, dv] fp64; lse [n_items] fp64 (natural log)
  * Returns PDO_OK, PDO_ERR_ARG, or PDO_ERR_KVLEN (some rows set to NaN).
  */
-int pdo_attention(int batch, int hq, int hkv, int d, int page_size, int q_e4m3, int kv_dtype,
+int pdo_attention(int batch, int hq, int hkv, int d, int dv, int page_size, int q_e4m3, int kv_dtype,
                   int scale_mode, int64_t sp, int64_t st, int64_t sh, int64_t num_pages,
                   const void* q, const void* k, const void* v, const int32_t* page_table,
                   const int32_t* kv_indptr, const int32_t* kv_len, const int32_t* qo_indptr,
@@ -230,11 +238,12 @@ int pdo_attention(int batch, int hq, int hkv, int d, int page_size, int q_e4m3, 
                   const float* v_scale, int64_t split_tokens, const int64_t* items,
                   int64_t n_items, double* out, double* lse, int num_threads) {
   if (batch < 0 || hq <= 0 || hkv <= 0 || hq % hkv || d <= 0 || page_size <= 0) return PDO_ERR_ARG;
+  if (dv <= 0 || dv > d) return PDO_ERR_ARG;
   if (kv_dtype < PDO_KV_BF16 || kv_dtype > PDO_KV_INT8) return PDO_ERR_ARG;
   if (scale_mode < 0 || scale_mode > 2 || ((scale_mode != 0) != (kv_dtype != PDO_KV_BF16)))
     return PDO_ERR_ARG;
   if (q_e4m3 && kv_dtype != PDO_KV_E4M3) return PDO_ERR_ARG;
-  pdo_problem p = {batch, hq, hkv, d, page_size, q_e4m3, kv_dtype, scale_mode, sp, st, sh, num_pages,
+  pdo_problem p = {batch, hq, hkv, d, page_size, dv, q_e4m3, kv_dtype, scale_mode, sp, st, sh, num_pages,
                    q, k, v, page_table, kv_indptr, kv_len, qo_indptr, window, sm_scale,
                    k_scale, v_scale};
   int64_t total_rows = batch > 0 ? qo_indptr[batch] : 0;
@@ -251,11 +260,11 @@ int pdo_attention(int batch, int hq, int hkv, int d, int page_size, int q_e4m3, 
 #pragma omp parallel
   {
     double* s = (double*)malloc(sizeof(double) * (size_t)(max_len + 1));
-    double* oc = (double*)malloc(sizeof(double) * (size_t)d);
+    double* oc = (double*)malloc(sizeof(double) * (size_t)dv);
 #pragma omp for schedule(dynamic, 1)
     for (int64_t t = 0; t < n; ++t) {
       int64_t flat = items ? items[t] : t;
-      int rc = pdo_item(&p, flat / hq, (int)(flat % hq), split_tokens, s, oc, out + t * d, lse + t);
+      int rc = pdo_item(&p, flat / hq, (int)(flat % hq), split_tokens, s, oc, out + t * dv, lse + t);
       if (rc != PDO_OK) {
 #pragma omp atomic write
         status = rc;

@@ -72,6 +72,7 @@ class Workload:
     q_scale: float = 1.0             # already folded into sm_scale when q_e4m3
     meta: dict = field(default_factory=dict)
     kv_int8: bool = False            # int8 cache codes (kv_e4m3 is then False)
+    head_dim_v: Optional[int] = None # value channels (None: head_dim); MLA: v_pages is k_pages
 
     @property
     def batch(self) -> int:
@@ -100,13 +101,17 @@ class Workload:
     def to(self, device) -> "Workload":
         def mv(t):
             return None if t is None else t.to(device)
+        k_pages, k_scale = mv(self.k_pages), mv(self.k_scale)
+        # an MLA latent cache is one tensor read as K and as V: keep it one
+        v_pages = k_pages if self.v_pages is self.k_pages else mv(self.v_pages)
+        v_scale = k_scale if self.v_scale is self.k_scale else mv(self.v_scale)
         return Workload(self.name, self.num_qo_heads, self.num_kv_heads, self.head_dim,
                         self.page_size, self.num_pages, self.q_e4m3, self.kv_e4m3,
-                        self.scale_mode, self.layout, self.strides, mv(self.q), mv(self.k_pages),
-                        mv(self.v_pages), mv(self.k_scale), mv(self.v_scale),
+                        self.scale_mode, self.layout, self.strides, mv(self.q), k_pages,
+                        v_pages, k_scale, v_scale,
                         mv(self.page_table), mv(self.kv_indptr), mv(self.kv_len),
                         mv(self.qo_indptr), mv(self.window), self.sm_scale, self.q_scale,
-                        dict(self.meta), self.kv_int8)
+                        dict(self.meta), self.kv_int8, self.head_dim_v)
 
 
 def _as_list(x, n):
@@ -169,7 +174,8 @@ def make_workload(*, name: str = "custom", batch: int, rows: Union[int, Sequence
                   k_outlier_frac: float = 0.0, k_outlier_mult: float = 20.0,
                   q_mult: float = 1.0, extra_pages: int = 4, extra_table_entries: int = 1,
                   poison: bool = True, value_fn=None, token_fn=None,
-                  unit_scale: bool = False, scale_fn=None) -> Workload:
+                  unit_scale: bool = False, scale_fn=None, head_dim_v: Optional[int] = None
+                  ) -> Workload:
     """Draw one workload.
 
     Structured tests may replace the N(0,1) draws:
@@ -181,6 +187,8 @@ def make_workload(*, name: str = "custom", batch: int, rows: Union[int, Sequence
           E4M3, or integers in [-127, 127] for int8);
       ``scale_fn(kind, b, L)`` -- per-(token, kv head) scales [L, Hkv] of
           request b (with ``unit_scale``), e.g. to ramp logits per token.
+    ``head_dim_v`` < head_dim makes an MLA latent cache: one tensor (and one
+    scale) serves as K (all head_dim channels) and V (the first head_dim_v).
     """
     assert kv_dtype in ("bf16", "e4m3", "int8") and q_dtype in ("bf16", "e4m3")
     assert q_dtype == "bf16" or kv_dtype == "e4m3"
@@ -219,7 +227,7 @@ def make_workload(*, name: str = "custom", batch: int, rows: Union[int, Sequence
     total_rows = qo_indptr[-1]
     qf = draw("q", (total_rows, num_qo_heads, D)) * q_mult
     kf = draw("k", (num_pages, P, H, D))
-    vf = draw("v", (num_pages, P, H, D))
+    vf = draw("v", (num_pages, P, H, D)) if head_dim_v is None else kf
     if token_fn is not None or scale_fn is not None:
         cursor = 0
         for b in range(batch):
@@ -229,7 +237,8 @@ def make_workload(*, name: str = "custom", batch: int, rows: Union[int, Sequence
             pg, sl = pages[tok // P], tok % P
             if token_fn is not None:
                 kf[pg, sl] = token_fn("k", b, L[b]).to(dev, torch.float32)
-                vf[pg, sl] = token_fn("v", b, L[b]).to(dev, torch.float32)
+                if head_dim_v is None:
+                    vf[pg, sl] = token_fn("v", b, L[b]).to(dev, torch.float32)
     outlier_channels = None
     if k_outlier_frac > 0:
         n_out = max(1, int(round(k_outlier_frac * D)))
@@ -320,6 +329,10 @@ def make_workload(*, name: str = "custom", batch: int, rows: Union[int, Sequence
         strides = (H * P * D, D, P * D)
     else:
         raise ValueError(layout)
+    if head_dim_v is not None:
+        # MLA: one latent cache read as K and as V (its first head_dim_v channels)
+        assert 0 < head_dim_v <= D
+        vc, v_scale = kc, k_scale
 
     win = None
     if windows is not None:
@@ -334,7 +347,8 @@ def make_workload(*, name: str = "custom", batch: int, rows: Union[int, Sequence
         kv_indptr=torch.tensor(kv_indptr, **i32), kv_len=torch.tensor(L, **i32),
         qo_indptr=torch.tensor(qo_indptr, **i32), window=win, sm_scale=sm_eff, q_scale=q_scale,
         meta=dict(seed=seed, rows=R, kv_lens=L, outlier_channels=outlier_channels,
-                  poison_pages=poison_pages), kv_int8=(kv_dtype == "int8"))
+                  poison_pages=poison_pages), kv_int8=(kv_dtype == "int8"),
+        head_dim_v=head_dim_v)
 
 
 # ---------------------------------------------------------------------------

@@ -55,13 +55,14 @@ def visibility_mask(L: int, R: int, window: int) -> torch.Tensor:
 
 
 def dense_attention(wl):
-    """(out [rows, Hq, D], lse [rows, Hq]) in float64."""
+    """(out [rows, Hq, Dv], lse [rows, Hq]) in float64."""
     P, H, Hq = wl.page_size, wl.num_kv_heads, wl.num_qo_heads
     G = Hq // H
     kd, vd = dequant_cache(wl, "k"), dequant_cache(wl, "v")
     qd = dequant_q(wl)
     total = qd.shape[0]
-    out = torch.full((total, Hq, wl.head_dim), float("nan"), dtype=torch.float64)
+    dv = getattr(wl, "head_dim_v", None) or wl.head_dim  # MLA: V = the first dv channels
+    out = torch.full((total, Hq, dv), float("nan"), dtype=torch.float64)
     lse = torch.full((total, Hq), float("nan"), dtype=torch.float64)
     qo = wl.qo_indptr.cpu().tolist()
     kvi = wl.kv_indptr.cpu().tolist()
@@ -75,7 +76,7 @@ def dense_attention(wl):
         npg = math.ceil(L / P)
         pages = table[kvi[b]:kvi[b] + npg]
         K = kd[pages].reshape(npg * P, H, -1)[:L].repeat_interleave(G, dim=1)
-        V = vd[pages].reshape(npg * P, H, -1)[:L].repeat_interleave(G, dim=1)
+        V = vd[pages].reshape(npg * P, H, -1)[:L, :, :dv].repeat_interleave(G, dim=1)
         qb = qd[qo[b]:qo[b + 1]]
         s = torch.einsum("rhd,lhd->rhl", qb, K) * wl.sm_scale
         mask = visibility_mask(L, R, wins[b])

@@ -22,6 +22,10 @@ saturation of the format's largest finite value, to closed forms of the
 scale (amax / 448, 1 for a zero row) and to the page-table placement of
 token L - R + i read independently here.
 
+MLA ("fp8 support", FlashMLA PR #54): a latent cache read as K (all its
+channels) and as V (the first dv) is pinned through the same dense attention
+with V sliced from the latent.
+
 The int8 cache (beside bf16 and fp8 in the same page's "Tested on") is
 pinned to dense torch attention over torch's own int8 decode, to a closed
 form (a constant negative code times its scale), and its quantiser to
@@ -45,8 +49,8 @@ TOL = 1e-12
 def _run(wl, mutation, **kw):
     out, lse, rc = oracle.attention_for(wl, mutation=mutation, **kw)
     total = wl.total_rows
-    return (out.reshape(total, wl.num_qo_heads, wl.head_dim), lse.reshape(total, wl.num_qo_heads),
-            rc)
+    dv = getattr(wl, "head_dim_v", None) or wl.head_dim
+    return out.reshape(total, wl.num_qo_heads, dv), lse.reshape(total, wl.num_qo_heads), rc
 
 
 def _close(a, b, tol=TOL, what=""):
@@ -101,6 +105,12 @@ def bruteforce_cases():
                               layout=("NHD", "HND")[n % 2], seed=100 + n,
                               sm_scale=0.3 + 0.1 * (n % 4), q_mult=1.0 + (n % 2)))
             n += 1
+    # MLA: one latent cache read as K (all channels) and as V (the first dv)
+    for i, (kvd, qd, sm) in enumerate(kinds[:5]):
+        cases.append(dict(batch=2, rows=[1 + i, 2], kv_lens=[30 + 7 * i, 9], num_qo_heads=8,
+                          num_kv_heads=1, head_dim=48, head_dim_v=32, page_size=(4, 16)[i % 2],
+                          kv_dtype=kvd, q_dtype=qd, scale_mode=sm, seed=300 + i,
+                          windows=None if i % 2 else [5, 0]))
     return cases
 
 
@@ -491,6 +501,7 @@ MUTATIONS = {
     17: "append: E4M3 ties go to the odd code",
     18: "append: new row written one token early",
     19: "append: E4M3 sign dropped",
+    24: "MLA: values read from the latent's last dv channels",
     20: "int8 cache bytes read as unsigned",
     21: "append: int8 per-token scale amax / 128",
     22: "append: int8 ties rounded away from zero",

@@ -90,7 +90,7 @@ enum { PDA_KERNEL_AUTO = 0, PDA_KERNEL_MMA = 1, PDA_KERNEL_TC = 2 };
 typedef struct {
   int32_t num_qo_heads;    /* Hq, a multiple of num_kv_heads */
   int32_t num_kv_heads;    /* Hkv >= 1 */
-  int32_t head_dim;        /* D: 64, 128, 256 or 512 (512: tcgen05 path, pages >= 8) */
+  int32_t head_dim;        /* D: 64, 128, 256 or 512 (512: tcgen05 path, pages >= 8); 576 MLA */
   int32_t page_size;       /* P: power of two in [1, 256] */
   int32_t q_dtype;         /* PDA_BF16, or PDA_E4M3 (then kv_dtype must be PDA_E4M3) */
   int32_t kv_dtype;        /* PDA_BF16, PDA_E4M3 or PDA_INT8 (int8: mma.sync path, D <= 256) */
@@ -108,6 +108,10 @@ typedef struct {
   int32_t batch;           /* requests per call, <= max_batch; 0 = max_batch */
   int32_t chunk_pages;     /* 0: planner chooses the KV chunk per CTA; > 0: forced */
   int32_t kernel;          /* PDA_KERNEL_AUTO, _MMA (mma.sync path) or _TC (tcgen05 path) */
+  int32_t head_dim_v;      /* value channels: 0 = head_dim. MLA decode ("fp8 support", FlashMLA
+                              PR #54): head_dim 576 (512 latent + 64 rope), head_dim_v 512,
+                              one latent cache passed as both k_pages and v_pages, V being its
+                              first 512 channels; bf16, or E4M3 with an E4M3 query */
 } pda_params;
 
 /* The plan: plain data, owned by the caller, copied freely. Fields are
@@ -140,7 +144,8 @@ typedef struct {
   int32_t tail_chunk_pages;
   int32_t head_splits;
   int32_t tail_splits;
-  int32_t reserved[11];
+  int32_t head_dim_v;      /* value channels (= head_dim but for MLA) */
+  int32_t reserved[10];
 } pda_plan_t;
 
 #define PDA_PLAN_MAGIC 0x50444131u /* "PDA1" */
@@ -158,7 +163,8 @@ int pda_plan(const pda_params* params, pda_plan_t* out_plan, size_t* split_scrat
  *   q          [qo_indptr[batch], Hq, D] bf16, or E4M3 codes (q_dtype), rows
  *              of request b at [qo_indptr[b], qo_indptr[b+1]); 16-B aligned
  *   k_pages,   paged cache, bf16, E4M3 codes or int8 codes, strides from the plan;
- *   v_pages    16-B aligned
+ *   v_pages    16-B aligned; V is the first head_dim_v channels of each v row (MLA:
+ *              pass the latent cache as both)
  *   page_table int32 CSR: pages of request b at [kv_indptr[b], kv_indptr[b+1]),
  *              at least ceil(kv_len[b] / P) of them; only those are read
  *   kv_indptr  int32 [batch + 1];  kv_len int32 [batch]
@@ -169,7 +175,7 @@ int pda_plan(const pda_params* params, pda_plan_t* out_plan, size_t* split_scrat
  *   k_scale,   NULL (bf16), fp32 [1] (per tensor) or fp32 [num_pages, P, Hkv]
  *              (E4M3 / int8)
  *   v_scale    (per token and kv head), device memory
- *   out        [qo_indptr[batch], Hq, D] bf16
+ *   out        [qo_indptr[batch], Hq, head_dim_v] bf16
  *   lse        [qo_indptr[batch], Hq] fp32 natural-log LSE, or NULL
  *   split_scratch  plan->scratch_bytes of device memory (see pda_plan)
  * All device pointers; nothing is allocated or synchronised. */

@@ -45,7 +45,7 @@ class PdaParams(ctypes.Structure):
                 ("max_kv_len", _i32), ("num_pages", _i32), ("kv_stride_page", _i64),
                 ("kv_stride_token", _i64), ("kv_stride_head", _i64), ("device", _i32),
                 ("num_sms", _i32), ("host_kv_len", ctypes.POINTER(_i32)), ("batch", _i32),
-                ("chunk_pages", _i32), ("kernel", _i32)]
+                ("chunk_pages", _i32), ("kernel", _i32), ("head_dim_v", _i32)]
 
 
 class PdaPlan(ctypes.Structure):
@@ -60,7 +60,7 @@ class PdaPlan(ctypes.Structure):
                 ("rows_cap", _i64), ("scratch_bytes", _i64), ("scratch_lse_offset", _i64),
                 ("scratch_o_offset", _i64), ("stage1_smem_bytes", _i32),
                 ("tail_from", _i32), ("tail_chunk_pages", _i32), ("head_splits", _i32),
-                ("tail_splits", _i32), ("reserved", _i32 * 11)]
+                ("tail_splits", _i32), ("head_dim_v", _i32), ("reserved", _i32 * 10)]
 
 
 class PdaError(RuntimeError):
@@ -243,6 +243,7 @@ def params_for(wl, *, max_batch=None, max_q_len=None, max_kv_len=None, device=0,
     p.batch = batch or wl.batch
     p.chunk_pages = chunk_pages
     p.kernel = kernel
+    p.head_dim_v = getattr(wl, "head_dim_v", None) or 0
     return p
 
 

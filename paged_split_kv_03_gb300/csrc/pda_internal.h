@@ -41,6 +41,7 @@ struct DecodeArgs {
   float sm_scale;
   int64_t sp, st, sh; // cache strides (elements)
   int batch, hq, hkv, group, head_dim, page_size, num_pages;
+  int head_dim_v;  // value channels (MLA: 512 of a 576-channel latent)
   int max_q_len, max_kv_len, max_splits, head_blocks, chunk_pages;
   int tail_from, tail_chunk_pages, head_splits, tail_splits;  // see pda_plan_t
   int64_t rows_cap;

@@ -718,7 +718,7 @@ KernelFn stage1_for(const pda_plan_t* p) {
 // a warp, with at most 16 warps per row (head_dim 512: 4 slices x 4).
 static int stage2_wpi(const pda_plan_t* p) {
   const int w = p->max_splits <= 8 ? 1 : p->max_splits <= 16 ? 2 : p->max_splits <= 32 ? 4 : 8;
-  return p->head_dim == 512 && w > 4 ? 4 : w;
+  return p->head_dim_v == 512 && w > 4 ? 4 : w;
 }
 struct Stage2Launch {
   KernelFn fn;
@@ -740,7 +740,7 @@ Stage2Launch stage2_pick(int wpi) {
 }
 Stage2Launch stage2_for(const pda_plan_t* p) {
   const int wpi = stage2_wpi(p);
-  switch (p->head_dim) {
+  switch (p->head_dim_v) {  // the merged rows have the value channels
     case 64: return stage2_pick<64>(wpi);
     case 128: return stage2_pick<128>(wpi);
     case 256: return stage2_pick<256>(wpi);

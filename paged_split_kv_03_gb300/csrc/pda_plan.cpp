@@ -58,7 +58,14 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
   // ---- shape checks
   if (p->num_qo_heads <= 0 || p->num_kv_heads <= 0 || p->num_qo_heads % p->num_kv_heads)
     return PDA_ERR_INVALID;
-  if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256 && p->head_dim != 512)
+  // MLA: a 576-channel latent (512 + 64 rope) whose first 512 channels are V
+  const int dv = p->head_dim_v ? p->head_dim_v : p->head_dim;
+  const bool mla = p->head_dim == 576 && dv == 512;
+  if (p->head_dim_v < 0 || (dv != p->head_dim && !mla)) return PDA_ERR_UNSUPPORTED;
+  if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256 && p->head_dim != 512 && !mla)
+    return PDA_ERR_UNSUPPORTED;
+  // the latent's E4M3 path takes an E4M3 query (FlashMLA's per-tensor Q/K/V)
+  if (mla && (p->kv_dtype == PDA_INT8 || (p->kv_dtype == PDA_E4M3 && p->q_dtype != PDA_E4M3)))
     return PDA_ERR_UNSUPPORTED;
   if (!is_pow2(p->page_size) || p->page_size > 256) return PDA_ERR_UNSUPPORTED;
   if (p->kv_dtype != PDA_BF16 && p->kv_dtype != PDA_E4M3 && p->kv_dtype != PDA_INT8)
@@ -96,6 +103,7 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
   pl.num_qo_heads = p->num_qo_heads;
   pl.num_kv_heads = p->num_kv_heads;
   pl.head_dim = p->head_dim;
+  pl.head_dim_v = dv;
   pl.page_size = p->page_size;
   pl.q_dtype = p->q_dtype;
   pl.kv_dtype = p->kv_dtype;
@@ -118,7 +126,7 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
     pl.kernel = pda::tc_supported(&pl) ? PDA_KERNEL_TC : PDA_KERNEL_MMA;
   else
     pl.kernel = p->kernel;
-  if (pl.kernel == PDA_KERNEL_MMA && p->head_dim == 512) return PDA_ERR_UNSUPPORTED;
+  if (pl.kernel == PDA_KERNEL_MMA && p->head_dim > 256) return PDA_ERR_UNSUPPORTED;
   pl.rows_per_cta = pl.kernel == PDA_KERNEL_TC ? pda::tc_rows_limit(&pl) : pda::kMmaRowsPerCta;
 
   // Query heads per CTA for a request with R rows: the largest divisor of the
@@ -270,7 +278,7 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
   if (pl.max_splits > 1) {
     off += ceil_div((int64_t)pl.max_splits * pl.rows_cap * pl.num_qo_heads * 4, 256) * 256;
     pl.scratch_o_offset = off;
-    off += (int64_t)pl.max_splits * pl.rows_cap * pl.num_qo_heads * pl.head_dim * 4;
+    off += (int64_t)pl.max_splits * pl.rows_cap * pl.num_qo_heads * pl.head_dim_v * 4;
   } else {
     pl.scratch_o_offset = off;
   }
@@ -331,6 +339,7 @@ extern "C" int pda_decode_stages(const pda_plan_t* plan, const void* q, const vo
   a.hkv = plan->num_kv_heads;
   a.group = plan->group;
   a.head_dim = plan->head_dim;
+  a.head_dim_v = plan->head_dim_v;
   a.page_size = plan->page_size;
   a.num_pages = plan->num_pages;
   a.max_q_len = max_q_len;

@@ -358,6 +358,10 @@ __device__ __forceinline__ void colgroup_sync(uint32_t id) {
 template <int D, int KVT, int QT, int SMODE, int NMAX>
 struct TcCfg {
   static constexpr int kD = D;
+  // MLA (D = 576): the keys are 576-channel latents, the values their first
+  // 512 channels, read from the same cache
+  static constexpr bool kMla = D == 576;
+  static constexpr int kDv = kMla ? 512 : D;
   static constexpr int kNmax = NMAX;
   // int8 cache: TMA lands the codes in a raw ring, converter warps widen
   // them exactly to f16 into the MMA ring, and the MMAs are kind::f16 (f16
@@ -387,9 +391,11 @@ struct TcCfg {
   static constexpr int kQTerms = kQSplit ? 2 : 1;
   static constexpr int kElt = kF8 ? 1 : 2;            // bytes of an MMA operand element
   static constexpr int kAtom = 128 / kElt;           // elements per 128-byte row
-  static constexpr int kChunks = D / kAtom;          // ring slots per K (or V) tile
+  static constexpr int kChunks = (D + kAtom - 1) / kAtom;  // ring slots per K tile (MLA E4M3:
+                                                           // the last half-filled, zeros past 576)
+  static constexpr int kChunksV = kDv / kAtom;       // ring slots per V tile
   static constexpr int kRawChunks = kI8 ? D / 128 : kChunks;  // TMA chunks per tile
-  static constexpr int kTileSlots = 2 * kChunks;
+  static constexpr int kTileSlots = kChunks + kChunksV;
   static constexpr int kQRows = kNmax * kQTerms;
   static constexpr int kQAtomBytes = kQRows * 128;
   static constexpr int kQBytes = kChunks * kQAtomBytes;
@@ -403,7 +409,7 @@ struct TcCfg {
   static constexpr int kPAtomBytes = kNmax * 128;    // [kNmax rows x 128 B]
   static constexpr int kPBufBytes = kPMn ? kTok * 128 : 2 * kPAtomBytes;
   static constexpr int kPBytes = kPBufs * kPBufBytes;
-  static constexpr int kOBlocks = D / 128;
+  static constexpr int kOBlocks = kDv / 128;
   // E4M3: one PV MMA of N = 2 x columns yields both terms' sums side by side
   static constexpr int kOCols = kF8 ? 2 * kNmax : kNmax;  // TMEM columns per O block
   static constexpr int kSCols = kQRows;              // TMEM columns per S buffer
@@ -429,20 +435,30 @@ struct TcCfg {
   // in flight, head_dim 512 (a tile of 8 or 4 slots) as many as fit.
   // (int8: no tail zeroing, so one tile plus one widened chunk is enough)
   static constexpr bool kBuildable =
-      kRing >= (kI8 ? kChunks + 2 : (D > 256 ? kChunks : kTileSlots)) && kTmemNeed <= 512 &&
-      kTmemCols * kCtasPerSm <= 512 && (!kI8 || (kIRing >= 1 && D <= 256));
+      kRing >= (kI8 ? kChunks + 2 : (D > 256 ? kChunksV : kTileSlots)) && kTmemNeed <= 512 &&
+      kTmemCols * kCtasPerSm <= 512 && (!kI8 || (kIRing >= 1 && D <= 256)) &&
+      !(kMla && (kQSplit || kI8));
   static constexpr int kSmem = kQBytes + kPBytes + (kRing + kIRing) * kSlot + kSmallBytes;
   // barrier words in the small area's first 512 bytes
   static_assert(2 * (kRing + kIRing) + 10 + 2 <= 64, "barrier area");
 };
 
-// Position of a tile's K or V unit (kChunks ring slots each) in the order
-// the MMA issuer consumes them: K0, K1, then K_{j+2} followed by V_j for
-// j = 0, 1, ... -- S^T of tile j + 2 is issued as soon as the softmax has
-// read S^T of tile j, before PV of tile j, so the softmax never waits on a
-// PV. The producer loads in the same order, so the ring is a plain FIFO.
-__device__ __forceinline__ int unit_pos_k(int j) { return j < 2 ? j : 2 * j - 2; }
-__device__ __forceinline__ int unit_pos_v(int j, int n) { return min(j + 3, n) + j; }
+// The MMA issuer consumes a tile's K and V units (kChunks and kChunksV ring
+// slots) in the order K0, K1, then K_{j+2} followed by V_j for j = 0, 1, ...
+// -- S^T of tile j + 2 is issued as soon as the softmax has read S^T of tile
+// j, before PV of tile j, so the softmax never waits on a PV. The producer
+// loads in the same order, so the ring is a plain FIFO.
+// First ring chunk of K_j / V_j in that order, for K units of CK chunks and
+// V units of CV (they differ for MLA): K_j follows K_0..K_{j-1} and
+// V_0..V_{j-3}; V_j follows K_0..K_{min(j+2, n-1)} and V_0..V_{j-1}.
+template <int CK, int CV>
+__device__ __forceinline__ uint32_t chunk_pos_k(int j) {
+  return static_cast<uint32_t>(j < 2 ? j * CK : j * CK + (j - 2) * CV);
+}
+template <int CK, int CV>
+__device__ __forceinline__ uint32_t chunk_pos_v(int j, int n) {
+  return static_cast<uint32_t>(min(j + 3, n) * CK + j * CV);
+}
 
 // Everything the softmax / epilogue warps need from the CTA prologue.
 struct SoftmaxCtx {
@@ -715,8 +731,8 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
     // last tile: rows past the chunk's end may hold stale or poisoned V
     // (int8 codes are always finite, so their zero P suffices)
     if (!C::kI8 && alive && c0 == 0 && tile0 + kTok > x.t_end && tok >= x.t_end) {
-      const uint32_t gv = static_cast<uint32_t>(unit_pos_v(j, x.ntiles)) * C::kChunks;
-      for (int c = 0; c < C::kChunks && alive; ++c) {
+      const uint32_t gv = chunk_pos_v<C::kChunks, C::kChunksV>(j, x.ntiles);
+      for (int c = 0; c < C::kChunksV && alive; ++c) {
         const uint32_t slot = (gv + c) % R_;
         alive = bar_wait(x.full + slot, ((gv + c) / R_) & 1u, x.abort_flag, a.status);
         uint4* row = reinterpret_cast<uint4*>(x.ring + slot * kSlot + r * 128);
@@ -822,9 +838,9 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
           const int64_t row = x.q0 + n / hpc;
           const int head = x.head0 + n % hpc;
           if (x.single) {
-            static_cast<__nv_bfloat16*>(a.out)[(row * a.hq + head) * D + d] = __float2bfloat16_rn(o);
+            static_cast<__nv_bfloat16*>(a.out)[(row * a.hq + head) * C::kDv + d] = __float2bfloat16_rn(o);
           } else {
-            a.part_o[(((int64_t)x.split * a.rows_cap + row) * a.hq + head) * D + d] = o;
+            a.part_o[(((int64_t)x.split * a.rows_cap + row) * a.hq + head) * C::kDv + d] = o;
           }
         }
       }
@@ -983,10 +999,11 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
     // ---- query operand Q^T (K-major, 128-byte swizzle), rows n < N (zero past M)
     if constexpr (!C::kQSplit) {
       constexpr int kRowChunks = D * C::kElt / 16;  // 16-byte pieces of one query row
-      for (int idx = st; idx < N * kRowChunks; idx += C::kSmThreads) {
-        const int n = idx / kRowChunks, cch = idx % kRowChunks;
+      constexpr int kPadChunks = C::kChunks * 8;    // ... of its smem rows (MLA E4M3: zeros past D)
+      for (int idx = st; idx < N * kPadChunks; idx += C::kSmThreads) {
+        const int n = idx / kPadChunks, cch = idx % kPadChunks;
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (n < M) {
+        if (n < M && cch < kRowChunks) {
           const uint8_t* src = static_cast<const uint8_t*>(a.q) +
                                (((int64_t)(q0 + n / hpc) * a.hq + head0 + n % hpc) * D) * C::kElt +
                                cch * 16;
@@ -1122,7 +1139,8 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
         return;
       }
       const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, ok));
-      for (int c = 0; c < C::kChunks && alive; ++c, ++g) {
+      const int nch = kind ? C::kChunksV : C::kChunks;
+      for (int c = 0; c < nch && alive; ++c, ++g) {
         const uint32_t slot = g % R_, round = g / R_;
         int good = 1;
         if (lane == 0) {
@@ -1183,7 +1201,7 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
         const int sb = j & 1;
         if (j >= 2 && !bar_wait(s_free + sb, ((j >> 1) - 1) & 1, abort_flag, a.status)) return false;
         fence_after();
-        const uint32_t gk = static_cast<uint32_t>(unit_pos_k(j)) * C::kChunks;
+        const uint32_t gk = chunk_pos_k<C::kChunks, C::kChunksV>(j);
         for (int c = 0; c < C::kChunks; ++c) {
           const uint32_t slot = (gk + c) % R_;
           if (!bar_wait(full + slot, ((gk + c) / R_) & 1u, abort_flag, a.status)) return false;
@@ -1202,7 +1220,7 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
       // O^T += V_j^T P_j^T as soon as the softmax has written P_j
       auto issue_pv = [&](int j) -> bool {
         if (!bar_wait(p_full + (j & 1), (j >> 1) & 1, abort_flag, a.status)) return false;
-        const uint32_t gv = static_cast<uint32_t>(unit_pos_v(j, ntiles)) * C::kChunks;
+        const uint32_t gv = chunk_pos_v<C::kChunks, C::kChunksV>(j, ntiles);
         constexpr int kBlkSlots = kF8 ? 1 : 2;  // ring slots of one 128-d V block
         const uint32_t pbuf = p_addr + static_cast<uint32_t>(j % C::kPBufs) * C::kPBufBytes;
 #pragma unroll
@@ -1388,6 +1406,11 @@ auto tc_select(const pda_plan_t* p, int nmax, F f) {
     if (nmax <= 32) { PDA_TC_CASES(512, 32) }
     PDA_TC_CASES(512, 64)
   }
+  if (p->head_dim == 576) {  // MLA latent
+    if (nmax <= 16) { PDA_TC_CASES(576, 16) }
+    if (nmax <= 32) { PDA_TC_CASES(576, 32) }
+    PDA_TC_CASES(576, 64)
+  }
   if (nmax <= 16) { PDA_TC_CASES(256, 16) }
   PDA_TC_CASES(256, 64)
 #undef PDA_TC_CASES
@@ -1425,7 +1448,7 @@ EncodeFn encoder() {
 // Tensor map over the paged cache: dims (c, slot, head, page) or
 // (c, head, slot, page), ordered by stride; one box = one page's (<= 128)
 // tokens x 128 bytes of one head.
-bool make_map(CUtensorMap* m, const void* base, const pda_plan_t* p, int* slot_dim) {
+bool make_map(CUtensorMap* m, const void* base, const pda_plan_t* p, int* slot_dim, int dim0) {
   EncodeFn enc = encoder();
   if (!enc) return false;
   const int eb = p->kv_dtype == PDA_BF16 ? 2 : 1;  // E4M3 / int8 codes: one byte
@@ -1434,7 +1457,7 @@ bool make_map(CUtensorMap* m, const void* base, const pda_plan_t* p, int* slot_d
   const cuuint32_t rows = static_cast<cuuint32_t>(p->page_size < kTok ? p->page_size : kTok);
   cuuint64_t dims[4], strides[3];
   cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
-  dims[0] = static_cast<cuuint64_t>(p->head_dim);
+  dims[0] = static_cast<cuuint64_t>(dim0);  // channels read (V of MLA: the first 512)
   box[0] = static_cast<cuuint32_t>(128 / eb);
   if (slot_first) {
     dims[1] = p->page_size;
@@ -1464,8 +1487,8 @@ bool make_map(CUtensorMap* m, const void* base, const pda_plan_t* p, int* slot_d
 }  // namespace
 
 bool tc_supported(const pda_plan_t* p) {
-  return (p->head_dim == 128 || p->head_dim == 256 || p->head_dim == 512) && p->page_size >= 8 &&
-         p->page_size <= 256 && (p->kv_dtype != PDA_INT8 || p->head_dim <= 256);
+  return (p->head_dim == 128 || p->head_dim == 256 || p->head_dim == 512 || p->head_dim == 576) &&
+         p->page_size >= 8 && p->page_size <= 256 && (p->kv_dtype != PDA_INT8 || p->head_dim <= 256);
 }
 
 // Rows x heads a CTA may hold: 64, except head_dim 512 over an E4M3 cache,
@@ -1474,7 +1497,8 @@ bool tc_supported(const pda_plan_t* p) {
 // ("perf(attention): run up to 8 query rows per request in the triton
 // decode kernel"); 32 halves the head blocks that re-read the cache.
 int tc_rows_limit(const pda_plan_t* p) {
-  return p->head_dim == 512 && p->kv_dtype == PDA_E4M3 ? 32 : kTcRowsPerCta;
+  // (the MLA latent's E4M3 build likewise: S 2 x N, O 4 x 2N columns)
+  return p->head_dim >= 512 && p->kv_dtype == PDA_E4M3 ? 32 : kTcRowsPerCta;
 }
 
 // Largest N (rows x heads, rounded up to 16) a CTA of this plan can hold.
@@ -1492,7 +1516,7 @@ int tc_variant_rows(const pda_plan_t* p) {
   // up to head_dim 256; head_dim 512 also has a 32-column build)
   const int n = plan_nmax(p);
   if (n <= 16 && tc_select(p, 16, GetSmem()) > 0) return 16;
-  if (p->head_dim == 512 && n <= 32 && tc_select(p, 32, GetSmem()) > 0) return 32;
+  if (p->head_dim >= 512 && n <= 32 && tc_select(p, 32, GetSmem()) > 0) return 32;
   return 64;
 }
 
@@ -1516,7 +1540,8 @@ int launch_stage1_tc(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_
   DecodeArgs a = args;
   CUtensorMap mk, mv;
   int slot_dim = 1;
-  if (!make_map(&mk, args.k, plan, &slot_dim) || !make_map(&mv, args.v, plan, &slot_dim))
+  if (!make_map(&mk, args.k, plan, &slot_dim, plan->head_dim) ||
+      !make_map(&mv, args.v, plan, &slot_dim, plan->head_dim_v))
     return PDA_ERR_CUDA;
   a.tma_slot_dim = slot_dim;
   TcFn k1 = tc_select(plan, plan->rows_per_cta, GetFn());

@@ -360,6 +360,11 @@ CONFIG_NAMES = ("tiny", "fp8_decode", "mtp_verify_bf16", "longctx_fp8_pth", "mix
 # triton decode kernel", "Gemma-4 MTP at long context"); 16 query heads
 # (the page gives no count), bs 1, R 1 / 4 / 8 (no spec, k = 3, k = 7)
 D512_NAMES = ("d512_mtp_bf16", "d512_mtp_fp8")
+# MLA decode ("fp8 support", FlashMLA PR #54): a 576-channel latent (512 +
+# the 64-channel rope) per token, one kv head, V = its first 512 channels;
+# 16 query heads (128 over 8-way tensor parallelism; the page gives none),
+# pages of 64, bs 64, ctx 4096, R 1 (2); bf16, or E4M3 Q/K/V per tensor
+MLA_NAMES = ("mla_bf16", "mla_fp8")
 
 
 def config_workload(name: str, *, R: Optional[int] = None, bs: Optional[int] = None,
@@ -376,6 +381,9 @@ def config_workload(name: str, *, R: Optional[int] = None, bs: Optional[int] = N
                     window 64 on half the requests, page 32, bf16
     longctx_int8_pth  the longctx_fp8_pth shape with int8 codes (scale amax / 127)
                     per (token, kv head) (seed 1200)
+    mla_bf16        bs 64, R 1 (2), 16/1 heads, latent 576 (V its first 512), ctx 4096,
+                    page 64, bf16 (seeds 1300 + index)
+    mla_fp8         the same with E4M3 Q and latent, per-tensor scales
     d512_mtp_bf16   bs 1 (16), R 4 (1, 8), 16/1 heads, D 512, ctx 32768, page 16, bf16
     d512_mtp_fp8    bs 1 (16), R 4 (1, 8), 16/1 heads, D 512, ctx 32768, page 16, e4m3
                     K/V with a scale per (token, kv head), Q bf16 (seeds 1100 + index)
@@ -385,6 +393,14 @@ def config_workload(name: str, *, R: Optional[int] = None, bs: Optional[int] = N
         seed = 1200 if seed is None else seed
         return config_workload("longctx_fp8_pth", R=R, bs=bs, device=device, seed=seed,
                                **dict(dict(kv_dtype="int8"), **kw))
+    if name in MLA_NAMES:
+        seed = 1300 + MLA_NAMES.index(name) if seed is None else seed
+        args = dict(batch=bs or 64, rows=R or 1, kv_lens=4096, num_qo_heads=16, num_kv_heads=1,
+                    head_dim=576, head_dim_v=512, page_size=64)
+        if name == "mla_fp8":
+            args.update(kv_dtype="e4m3", q_dtype="e4m3", scale_mode=SCALE_TENSOR)
+        args.update(kw)
+        return make_workload(name=name, seed=seed, device=device, **args)
     if name in D512_NAMES:
         seed = 1100 + D512_NAMES.index(name) if seed is None else seed
         args = dict(batch=bs or 1, rows=R or 4, kv_lens=32768, num_qo_heads=16, num_kv_heads=1,

@@ -14,7 +14,10 @@ Byte model, per call (GB = 1e9 bytes):
   * page-table entries read (one int32 per streamed page per request) and the
     int32 kv_indptr / kv_len / qo_indptr / window arrays.
   * split scratch: for every request with more than one KV split, each split
-    writes and stage 2 reads (D + 1) fp32 per (row, q head).
+    writes and stage 2 reads (Dv + 1) fp32 per (row, q head).
+  * MLA ("fp8 support", FlashMLA PR #54): one latent cache of D channels is
+    both K and V (V its first Dv); it counts once, as the page's MBU does
+    (the kernel reads V's channels again, from L2). Out has Dv channels.
 
 With the scratch, lse and index terms left out this is the accounting of
 "[Feature Request] Support q_len > 1 for FP8 decode" (hpc-ops issue #4): its
@@ -48,6 +51,9 @@ def call_bytes(wl, chunk_pages: int | None = None, include_scratch: bool = True,
     if plan is not None:
         chunk_pages, tail_from, tail_chunk = plan.chunk_pages, plan.tail_from, plan.tail_chunk_pages
     P, H, D, Hq = wl.page_size, wl.num_kv_heads, wl.head_dim, wl.num_qo_heads
+    Dv = getattr(wl, "head_dim_v", None) or D
+    mla = getattr(wl, "v_pages", None) is not None and wl.v_pages is getattr(wl, "k_pages", None)
+    kv_terms = 1 if mla else 2
     kv_elt = 1 if (wl.kv_e4m3 or getattr(wl, "kv_int8", False)) else 2
     q_elt = 1 if wl.q_e4m3 else 2
     lens = wl.kv_len.cpu().tolist()
@@ -62,16 +68,16 @@ def call_bytes(wl, chunk_pages: int | None = None, include_scratch: bool = True,
         cp = tail_chunk if tail_from is not None and b >= tail_from else chunk_pages
         lo, lo_page, npages, nsplit = _split_range(L, R, wins[b], P, cp or 1 << 30)
         tokens = L - lo_page * P
-        kv += 2 * tokens * H * D * kv_elt
+        kv += kv_terms * tokens * H * D * kv_elt
         if wl.scale_mode == 2:
-            scales += 2 * tokens * H * 4
+            scales += kv_terms * tokens * H * 4
         table += (npages - lo_page) * 4
         if include_scratch and nsplit > 1:
-            scratch += 2 * nsplit * R * Hq * (D + 1) * 4
+            scratch += 2 * nsplit * R * Hq * (Dv + 1) * 4
     if wl.scale_mode == 1:
-        scales += 8
+        scales += 4 * kv_terms
     q = rows_total * Hq * D * q_elt
-    out = rows_total * Hq * D * 2
+    out = rows_total * Hq * Dv * 2
     lse = rows_total * Hq * 4
     index = 4 * (3 * len(lens) + 2) + (4 * len(lens) if wl.window is not None else 0)
     total = kv + scales + q + out + lse + table + index + scratch
@@ -80,8 +86,9 @@ def call_bytes(wl, chunk_pages: int | None = None, include_scratch: bool = True,
 
 
 def call_flops(wl) -> int:
-    """4 * D per (row, q head, visible key)."""
+    """2 * (D + Dv) per (row, q head, visible key): 4 * D unless MLA."""
     D, Hq = wl.head_dim, wl.num_qo_heads
+    Dv = getattr(wl, "head_dim_v", None) or D
     lens = wl.kv_len.cpu().tolist()
     qo = wl.qo_indptr.cpu().tolist()
     wins = wl.window.cpu().tolist() if wl.window is not None else [0] * len(lens)
@@ -92,4 +99,4 @@ def call_flops(wl) -> int:
             pos = L - R + i
             lo = max(0, pos - wins[b] + 1) if wins[b] > 0 else 0
             visible += pos - lo + 1
-    return 4 * D * Hq * visible
+    return 2 * (D + Dv) * Hq * visible

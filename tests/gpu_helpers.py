@@ -26,6 +26,11 @@ def tol_for(wl):
     return TOL_FP8 if (wl.kv_e4m3 or getattr(wl, "kv_int8", False)) else TOL_BF16
 
 
+def dv_of(wl):
+    """Output channels: head_dim, or the value channels of an MLA latent."""
+    return getattr(wl, "head_dim_v", None) or wl.head_dim
+
+
 def run_decode(wl, *, chunk_pages=0, kernel=B.PDA_KERNEL_AUTO, max_q_len=None, max_batch=None,
                max_kv_len=None, decoder=None, fill=float("nan")):
     """Run pda_decode on a device-resident workload; returns (out fp32 CPU
@@ -38,7 +43,7 @@ def run_decode(wl, *, chunk_pages=0, kernel=B.PDA_KERNEL_AUTO, max_q_len=None, m
                               device=dev.index or 0)
         decoder = B.Decoder(params, device=dev)
     rows = wl.total_rows
-    out = torch.full((rows, wl.num_qo_heads, wl.head_dim), fill, dtype=torch.bfloat16, device=dev)
+    out = torch.full((rows, wl.num_qo_heads, dv_of(wl)), fill, dtype=torch.bfloat16, device=dev)
     lse = torch.full((rows, wl.num_qo_heads), fill, dtype=torch.float32, device=dev)
     decoder.run(wl, out, lse, max_q_len=max_q_len)
     torch.cuda.synchronize()
@@ -52,7 +57,7 @@ def oracle_ref(wl, items=None, num_threads=0):
     out, lse, rc = oracle.attention_for(host, items=items, num_threads=num_threads)
     assert rc == 0, f"oracle status {rc}"
     if items is None:
-        out = out.reshape(wl.total_rows, wl.num_qo_heads, wl.head_dim)
+        out = out.reshape(wl.total_rows, wl.num_qo_heads, dv_of(wl))
         lse = lse.reshape(wl.total_rows, wl.num_qo_heads)
     return out, lse
 

@@ -130,6 +130,32 @@ def test_plan_head_dim_512(lib):
     assert rc == B.PDA_ERR_UNSUPPORTED
 
 
+MLA = dict(num_qo_heads=16, num_kv_heads=1, head_dim=576, head_dim_v=512, page_size=64,
+           max_batch=64, max_q_len=2, max_kv_len=4096, kv_stride_page=64 * 576,
+           kv_stride_token=576, kv_stride_head=576)
+
+
+def test_plan_mla(lib):
+    # the latent (576 channels, V its first 512) on the tcgen05 path; scratch
+    # partials hold 512 channels
+    plan, nbytes, rc = B.pda_plan(_params(**MLA))
+    assert rc == 0 and plan.kernel == B.PDA_KERNEL_TC and plan.head_dim_v == 512
+    assert plan.rows_per_cta == 32 and plan.head_blocks == 1
+    rows = 64 * 2
+    assert nbytes >= 256 + plan.max_splits * rows * 16 * (512 + 1) * 4
+    assert plan.stage1_smem_bytes <= 227 * 1024
+    q, _, rc = B.pda_plan(_params(kv_dtype=1, q_dtype=1, scale_mode=1, **MLA))
+    assert rc == 0 and q.rows_per_cta == 32
+    for bad in (dict(kv_dtype=1, scale_mode=1),              # E4M3 latent needs an E4M3 query
+                dict(kv_dtype=2, scale_mode=1),              # no int8 latent
+                dict(kernel=B.PDA_KERNEL_MMA),
+                dict(head_dim_v=500)):
+        _, _, rc = B.pda_plan(_params(**dict(MLA, **bad)), check=False)
+        assert rc == B.PDA_ERR_UNSUPPORTED, bad
+    _, _, rc = B.pda_plan(_params(head_dim_v=64), check=False)  # only the MLA pair differs
+    assert rc == B.PDA_ERR_UNSUPPORTED
+
+
 def test_plan_int8(lib):
     # int8 caches: the tcgen05 path up to head_dim 256 (codes widened to f16
     # in shared memory, one CTA per SM), the mma.sync path at head_dim 64

@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import (TOL_BF16, TOL_FP8, assert_close, oracle_ref, run_decode,
+from gpu_helpers import (TOL_BF16, TOL_FP8, assert_close, dv_of, oracle_ref, run_decode,
                          sample_items, tol_for)
 from paged_split_kv_03_gb300 import binding as B
 from paged_split_kv_03_gb300.synth import (SCALE_NONE, SCALE_TENSOR, SCALE_TOKEN_HEAD,
@@ -86,6 +86,17 @@ SMALL = {
                             scale_mode=SCALE_TOKEN_HEAD, chunk=8),
     "bf16_d512_g16_r2": dict(batch=2, rows=[2, 1], kv_lens=[600, 1300], num_qo_heads=16,
                              num_kv_heads=1, head_dim=512, page_size=32),
+    # MLA latents (576 channels, V = the first 512): bf16, E4M3 per tensor / per token
+    "mla_bf16_split_win": dict(batch=3, rows=[1, 2, 1], kv_lens=[700, 1300, 65],
+                               windows=[0, 0, 32], num_qo_heads=16, num_kv_heads=1,
+                               head_dim=576, head_dim_v=512, page_size=64, chunk=4),
+    "mla_fp8t_g16": dict(batch=2, rows=[2, 1], kv_lens=[1000, 130], num_qo_heads=16,
+                         num_kv_heads=1, head_dim=576, head_dim_v=512, page_size=16,
+                         kv_dtype="e4m3", q_dtype="e4m3", scale_mode=SCALE_TENSOR),
+    "mla_fp8pth_g8_p32": dict(batch=2, rows=[1, 2], kv_lens=[333, 2100], num_qo_heads=8,
+                              num_kv_heads=1, head_dim=576, head_dim_v=512, page_size=32,
+                              kv_dtype="e4m3", q_dtype="e4m3", scale_mode=SCALE_TOKEN_HEAD,
+                              chunk=8),
     "fp8t_qfp8_d512_g8": dict(batch=2, rows=[2, 1], kv_lens=[1000, 129], num_qo_heads=8,
                               num_kv_heads=1, head_dim=512, page_size=32, kv_dtype="e4m3",
                               q_dtype="e4m3", scale_mode=SCALE_TENSOR),
@@ -122,7 +133,7 @@ KERNELS = {"mma": B.PDA_KERNEL_MMA, "tc": B.PDA_KERNEL_TC}
 def _tc_ok(wl):
     """Shapes the tcgen05 path is built for (head_dim 128/256/512, pages of >= 8;
     int8 caches up to head_dim 256)."""
-    return (wl.head_dim in (128, 256, 512) and wl.page_size >= 8 and
+    return (wl.head_dim in (128, 256, 512, 576) and wl.page_size >= 8 and
             (not wl.kv_int8 or wl.head_dim <= 256))
 
 
@@ -186,6 +197,8 @@ CONFIGS = [
     ("mixed", {}, 160),
     ("longctx_int8_pth", dict(bs=1, R=8), 64),
     ("longctx_int8_pth", dict(bs=16, R=1), 64),
+    ("mla_fp8", {}, None),
+    ("mla_bf16", dict(R=2), 96),
     ("d512_mtp_bf16", dict(bs=1, R=4), None),
     ("d512_mtp_bf16", dict(bs=1, R=8, kv_lens=131072), 48),
     ("d512_mtp_fp8", dict(bs=1, R=8), None),
@@ -218,7 +231,7 @@ def test_config_parity(cfg, kw, n_sample, peaked):
         items = sample_items(wl, n_sample, seed=3, must=must)
         ref_o, ref_l = oracle_ref(wl, items=items)
         hq = wl.num_qo_heads
-        o = out.reshape(-1, wl.head_dim)[items]
+        o = out.reshape(-1, dv_of(wl))[items]
         l_ = lse.reshape(-1)[items]
         assert_close(o, l_, ref_o, ref_l, tol_for(wl), what=f"{cfg} sampled",
                      output_rounding=peaked)

@@ -391,14 +391,17 @@ struct TcCfg {
   static constexpr int kQTerms = kQSplit ? 2 : 1;
   static constexpr int kElt = kF8 ? 1 : 2;            // bytes of an MMA operand element
   static constexpr int kAtom = 128 / kElt;           // elements per 128-byte row
-  static constexpr int kChunks = (D + kAtom - 1) / kAtom;  // ring slots per K tile (MLA E4M3:
-                                                           // the last half-filled, zeros past 576)
+  // chunks of a K row (MLA E4M3: the last half-filled, zeros past 576)
+  static constexpr int kChunksQK = (D + kAtom - 1) / kAtom;
+  // ring slots per K tile: 16-bit V blocks take two adjacent slots, so units
+  // keep an even size (MLA bf16: 9 chunks and one empty slot, never loaded)
+  static constexpr int kChunks = kF8 ? kChunksQK : (kChunksQK + 1) & ~1;
   static constexpr int kChunksV = kDv / kAtom;       // ring slots per V tile
   static constexpr int kRawChunks = kI8 ? D / 128 : kChunks;  // TMA chunks per tile
   static constexpr int kTileSlots = kChunks + kChunksV;
   static constexpr int kQRows = kNmax * kQTerms;
   static constexpr int kQAtomBytes = kQRows * 128;
-  static constexpr int kQBytes = kChunks * kQAtomBytes;
+  static constexpr int kQBytes = kChunksQK * kQAtomBytes;
   // P^T operand of PV. K-major: rows n (bf16: two 64-token halves; E4M3: the
   // two terms' rows stacked, 16 + 16). MN-major (E4M3, up to 64 columns):
   // one 128-byte row per token holding term 1 then term 2 of every column,
@@ -999,7 +1002,7 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
     // ---- query operand Q^T (K-major, 128-byte swizzle), rows n < N (zero past M)
     if constexpr (!C::kQSplit) {
       constexpr int kRowChunks = D * C::kElt / 16;  // 16-byte pieces of one query row
-      constexpr int kPadChunks = C::kChunks * 8;    // ... of its smem rows (MLA E4M3: zeros past D)
+      constexpr int kPadChunks = C::kChunksQK * 8;  // ... of its smem rows (MLA E4M3: zeros past D)
       for (int idx = st; idx < N * kPadChunks; idx += C::kSmThreads) {
         const int n = idx / kPadChunks, cch = idx % kPadChunks;
         uint4 v = make_uint4(0, 0, 0, 0);
@@ -1142,17 +1145,18 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
       const int nch = kind ? C::kChunksV : C::kChunks;
       for (int c = 0; c < nch && alive; ++c, ++g) {
         const uint32_t slot = g % R_, round = g / R_;
+        const bool pad = kind == 0 && c >= C::kChunksQK;  // an even-size unit's empty slot
         int good = 1;
         if (lane == 0) {
           good = bar_wait(empty + slot, (round & 1u) ^ 1u, abort_flag, a.status);
-          if (good) bar_expect_tx(full + slot, nvalid * box_bytes);
+          if (good) bar_expect_tx(full + slot, pad ? 0u : nvalid * box_bytes);
         }
         good = __shfl_sync(0xffffffffu, good, 0);
         if (!good) {
           alive = false;
           break;
         }
-        if (ok) {
+        if (ok && !pad) {
           const uint32_t dst = su32(ring + slot * kSlot) + bx * box_bytes;
           const int c1 = a.tma_slot_dim == 1 ? s0 : hkv;
           const int c2 = a.tma_slot_dim == 1 ? hkv : s0;
@@ -1208,10 +1212,12 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
           fence_after();
           const uint32_t abase = ring_addr + slot * kSlot;
           const uint32_t bbase = q_addr + c * C::kQAtomBytes;
+          if (c < C::kChunksQK) {  // (not the empty slot of an even-size unit)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma<kF8>(tmem + sb * C::kSCols, sdesc(abase + kk * 32, 16, 1024),
-                     sdesc(bbase + kk * 32, 16, 1024), id_s, (c | kk) != 0);
+            for (int kk = 0; kk < 4; ++kk)
+              mma<kF8>(tmem + sb * C::kSCols, sdesc(abase + kk * 32, 16, 1024),
+                       sdesc(bbase + kk * 32, 16, 1024), id_s, (c | kk) != 0);
+          }
           mma_commit(empty + slot);  // the slot is free once these MMAs finish
         }
         mma_commit(s_full + sb);

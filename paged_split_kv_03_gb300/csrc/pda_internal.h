@@ -44,6 +44,7 @@ struct DecodeArgs {
   int head_dim_v;  // value channels (MLA: 512 of a 576-channel latent)
   int max_q_len, max_kv_len, max_splits, head_blocks, chunk_pages;
   int tail_from, tail_chunk_pages, head_splits, tail_splits;  // see pda_plan_t
+  int64_t merge_item0;  // first (request, row, q head) item the merge grid covers
   int64_t rows_cap;
   int hpc[kMaxQLen + 1];  // q heads per CTA for R rows
   int tma_slot_dim;       // tcgen05 path: tensor-map coordinate holding the slot (1 or 2)

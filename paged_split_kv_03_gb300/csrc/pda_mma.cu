@@ -575,7 +575,7 @@ __global__ void __launch_bounds__(MergeCfg<D, WPI>::kThreads)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wi = warp % M::kWarpsPerItem;
   const int slice = wi % M::kSlices, sub = wi / M::kSlices;
-  const int64_t item = (int64_t)blockIdx.x * M::kItems + warp / M::kWarpsPerItem;
+  const int64_t item = a.merge_item0 + (int64_t)blockIdx.x * M::kItems + warp / M::kWarpsPerItem;
   const int64_t per_b = (int64_t)a.max_q_len * a.hq;
   bool valid = false;
   int n = 0;
@@ -789,7 +789,13 @@ int launch_stage1_mma(const pda_plan_t* plan, const DecodeArgs& args, cudaStream
 }
 
 int launch_stage2(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_t s) {
-  const int64_t items = (int64_t)plan->batch * args.max_q_len * plan->num_qo_heads;
+  // when only the tail requests are split, the merge covers just their items
+  DecodeArgs a = args;
+  const int64_t per_b = (int64_t)args.max_q_len * plan->num_qo_heads;
+  const int64_t b0 = plan->head_splits == 1 ? plan->tail_from : 0;
+  a.merge_item0 = b0 * per_b;
+  const int64_t items = (int64_t)(plan->batch - b0) * per_b;
+  if (items <= 0) return PDA_OK;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -802,7 +808,7 @@ int launch_stage2(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_t s
   c2.stream = s;
   c2.attrs = attr;
   c2.numAttrs = 1;
-  if (cudaLaunchKernelEx(&c2, l2.fn, args) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&c2, l2.fn, a) != cudaSuccess) {
     cudaGetLastError();
     return PDA_ERR_CUDA;
   }

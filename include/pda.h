@@ -93,7 +93,7 @@ typedef struct {
   int32_t head_dim;        /* D: 64, 128, 256 or 512 (512: tcgen05 path, pages >= 8); 576 MLA */
   int32_t page_size;       /* P: power of two in [1, 256] */
   int32_t q_dtype;         /* PDA_BF16, or PDA_E4M3 (then kv_dtype must be PDA_E4M3) */
-  int32_t kv_dtype;        /* PDA_BF16, PDA_E4M3 or PDA_INT8 (int8: mma.sync path, D <= 256) */
+  int32_t kv_dtype;        /* PDA_BF16, PDA_E4M3 or PDA_INT8 (int8: head_dim <= 256) */
   int32_t scale_mode;      /* PDA_SCALE_NONE for bf16 KV; TENSOR or TOKEN_HEAD for E4M3 / int8 */
   int32_t max_batch;       /* upper bound of `batch` over the plan's lifetime */
   int32_t max_q_len;       /* 1..8: rows per request */

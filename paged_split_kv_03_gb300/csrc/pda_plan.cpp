@@ -119,9 +119,9 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
   pl.group = p->num_qo_heads / p->num_kv_heads;
   pl.num_sms = num_sms;
   if (p->kernel == PDA_KERNEL_TC && !pda::tc_supported(&pl)) return PDA_ERR_UNSUPPORTED;
-  // AUTO takes the tcgen05 path wherever it is built (head_dim 128/256/512,
-  // pages >= 8); head_dim 512 has no mma.sync build (its O tile would not fit
-  // the registers)
+  // AUTO takes the tcgen05 path wherever it is built (head_dim 128/256/512/576,
+  // pages >= 8); head_dims above 256 have no mma.sync build (their O tile
+  // would not fit the registers)
   if (p->kernel == PDA_KERNEL_AUTO)
     pl.kernel = pda::tc_supported(&pl) ? PDA_KERNEL_TC : PDA_KERNEL_MMA;
   else

@@ -499,7 +499,6 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
   constexpr int NCK = NH / KC;
   constexpr int R_ = C::kRing;
   constexpr bool kF8 = C::kF8;
-  constexpr int D = C::kD;
   const int st = tid - 64;       // 0..NT-1
   const int qd = warp & 3;       // TMEM lane quadrant of this warp
   const int r = qd * 32 + lane;  // token row of S^T / d row of O^T
@@ -1115,9 +1114,10 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
     // int8: chunk g into the int8 ring once the converters have widened
     // the chunk whose slot it takes
     auto emit8 = [&](int kind, bool ok, int pg, int s0) {
+      constexpr uint32_t kIR = C::kIRing > 0 ? C::kIRing : 1;  // (other builds never call this)
       const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, ok));
       for (int c = 0; c < C::kRawChunks && alive; ++c, ++g) {
-        const uint32_t slot = g % C::kIRing, round = g / C::kIRing;
+        const uint32_t slot = g % kIR, round = g / kIR;
         int good = 1;
         if (lane == 0) {
           good = bar_wait(i_empty + slot, (round & 1u) ^ 1u, abort_flag, a.status);

@@ -32,6 +32,12 @@
  *    vectors of d channels (512 nope + 64 rope, the page's kv_rope) and the
  *    values are their first dv = 512 channels; a caller passes the latent
  *    cache as both k and v, and the oracle reads V channels c < dv.
+ *  - The mixed-precision latent the FlashMLA page's reviewers accept (the
+ *    nope channels in 8 bits with a scale per token and 128 channels, the
+ *    64 rope channels in 16 bits): scale_mode 3. Reading: one record per
+ *    (token, kv head) of 512 E4M3 codes then 64 bf16 values (640 bytes),
+ *    strides in bytes, scales fp32 [num_pages, page_size, hkv, 4]; channel
+ *    c < 512 is code(c) * scale[c / 128], channel 512 + r the bf16 r.
  *  - An int8 cache (named beside bf16 and fp8 in the register-spill check of
  *    FreeToken PR #900, "Tested on") holds two's-complement bytes; the value
  *    is the byte times the same per-tensor or per-(token, kv head) scale.
@@ -125,6 +131,17 @@ static double pdo_kv_elem(const pdo_problem* p, const void* cache, const float* 
   int64_t idx = MUT(10) ? page * p->sp + slot * p->sh + (int64_t)g * p->st + d
                         : page * p->sp + slot * p->st + (int64_t)g * p->sh + d;
   double x;
+  if (p->scale_mode == 3) { /* MLA record: E4M3 nope with 128-channel scales, bf16 rope */
+    const uint8_t* rec = (const uint8_t*)cache + (page * p->sp + slot * p->st + (int64_t)g * p->sh);
+    if (d < 512) {
+      int blk = MUT(25) ? d / 64 % 4 : d / 128;
+      return pdo_e4m3_to_double(rec[d]) *
+             (double)scale[((page * p->page_size + slot) * p->hkv + g) * 4 + blk];
+    }
+    uint16_t bits;
+    memcpy(&bits, rec + 512 + 2 * (d - 512) - MUT(26) * (d - 512), 2);
+    return pdo_bf16_to_double(bits);
+  }
   if (p->kv_dtype == PDO_KV_E4M3)
     x = pdo_e4m3_to_double(((const uint8_t*)cache)[idx]);
   else if (p->kv_dtype == PDO_KV_INT8)
@@ -240,7 +257,9 @@ int pdo_attention(int batch, int hq, int hkv, int d, int dv, int page_size, int 
   if (batch < 0 || hq <= 0 || hkv <= 0 || hq % hkv || d <= 0 || page_size <= 0) return PDO_ERR_ARG;
   if (dv <= 0 || dv > d) return PDO_ERR_ARG;
   if (kv_dtype < PDO_KV_BF16 || kv_dtype > PDO_KV_INT8) return PDO_ERR_ARG;
-  if (scale_mode < 0 || scale_mode > 2 || ((scale_mode != 0) != (kv_dtype != PDO_KV_BF16)))
+  if (scale_mode < 0 || scale_mode > 3 || ((scale_mode != 0) != (kv_dtype != PDO_KV_BF16)))
+    return PDO_ERR_ARG;
+  if (scale_mode == 3 && (kv_dtype != PDO_KV_E4M3 || d != 576 || dv != 512 || q_e4m3))
     return PDO_ERR_ARG;
   if (q_e4m3 && kv_dtype != PDO_KV_E4M3) return PDO_ERR_ARG;
   pdo_problem p = {batch, hq, hkv, d, page_size, dv, q_e4m3, kv_dtype, scale_mode, sp, st, sh, num_pages,

@@ -43,6 +43,10 @@ INT8_MAX = 127.0
 INT8_POISON = -128
 
 SCALE_NONE, SCALE_TENSOR, SCALE_TOKEN_HEAD = 0, 1, 2
+# MLA latent records: 512 E4M3 nope codes (a scale per token, kv head and 128
+# channels) then the 64 bf16 rope channels, 640 bytes per (token, kv head)
+SCALE_MLA_BLOCK = 3
+MLA_NOPE, MLA_ROPE, MLA_RECORD = 512, 64, 640
 
 
 @dataclass
@@ -191,12 +195,14 @@ def make_workload(*, name: str = "custom", batch: int, rows: Union[int, Sequence
     scale) serves as K (all head_dim channels) and V (the first head_dim_v).
     """
     assert kv_dtype in ("bf16", "e4m3", "int8") and q_dtype in ("bf16", "e4m3")
+    if scale_mode == SCALE_MLA_BLOCK:
+        assert kv_dtype == "e4m3" and q_dtype == "bf16" and head_dim == 576 and head_dim_v == 512
     assert q_dtype == "bf16" or kv_dtype == "e4m3"
     assert num_qo_heads % num_kv_heads == 0
     if kv_dtype == "bf16":
         assert scale_mode == SCALE_NONE
     else:
-        assert scale_mode in (SCALE_TENSOR, SCALE_TOKEN_HEAD)
+        assert scale_mode in (SCALE_TENSOR, SCALE_TOKEN_HEAD, SCALE_MLA_BLOCK)
     dev = torch.device(device)
     gen = torch.Generator(device=dev)
     gen.manual_seed(int(seed))
@@ -294,6 +300,13 @@ def make_workload(*, name: str = "custom", batch: int, rows: Union[int, Sequence
                     pg, sl = pages[tok // P], tok % P
                     k_scale[pg, sl] = scale_fn("k", b, L[b]).to(dev, torch.float32)
                     v_scale[pg, sl] = scale_fn("v", b, L[b]).to(dev, torch.float32)
+    elif scale_mode == SCALE_MLA_BLOCK:
+        # nope: E4M3 with amax/448 per (token, kv head, 128 channels); rope: bf16
+        nope = kf[..., :MLA_NOPE].reshape(num_pages, P, H, MLA_NOPE // 128, 128)
+        codes, k_scale = _quant_e4m3(nope, -1)  # scale [pages, P, H, 4]
+        rope = kf[..., MLA_NOPE:].to(torch.bfloat16).contiguous().view(torch.uint8)
+        kc = torch.cat([codes.reshape(num_pages, P, H, MLA_NOPE), rope], dim=-1).contiguous()
+        vc, v_scale = kc, k_scale
     elif scale_mode == SCALE_TENSOR:
         quant = _quant_int8 if kv_dtype == "int8" else _quant_e4m3
         kc, k_scale = quant(kf, None)
@@ -314,19 +327,24 @@ def make_workload(*, name: str = "custom", batch: int, rows: Union[int, Sequence
         elif kv_dtype == "int8":
             kc[bad] = INT8_POISON
             vc[bad] = INT8_POISON
+        elif scale_mode == SCALE_MLA_BLOCK:
+            kc[..., :MLA_NOPE][bad] = E4M3_NAN_CODE
+            nan_rope = torch.tensor([BF16_NAN_BITS], dtype=torch.int16, device=dev).view(torch.uint8)
+            kc[..., MLA_NOPE:][bad] = nan_rope.repeat(MLA_ROPE)
         else:
             kc[bad] = E4M3_NAN_CODE
             vc[bad] = E4M3_NAN_CODE
-        if scale_mode == SCALE_TOKEN_HEAD:
+        if scale_mode in (SCALE_TOKEN_HEAD, SCALE_MLA_BLOCK):
             k_scale[bad] = float("nan")
             v_scale[bad] = float("nan")
 
+    Dc = MLA_RECORD if scale_mode == SCALE_MLA_BLOCK else D  # elements (bytes) per row
     if layout == "NHD":
-        strides = (P * H * D, H * D, D)
+        strides = (P * H * Dc, H * Dc, Dc)
     elif layout == "HND":
         kc = kc.permute(0, 2, 1, 3).contiguous()
         vc = vc.permute(0, 2, 1, 3).contiguous()
-        strides = (H * P * D, D, P * D)
+        strides = (H * P * Dc, Dc, P * Dc)
     else:
         raise ValueError(layout)
     if head_dim_v is not None:

@@ -25,6 +25,13 @@ def dequant_cache(wl, which: str) -> torch.Tensor:
     c = c.cpu()
     if wl.layout == "HND":
         c = c.permute(0, 2, 1, 3)
+    if wl.scale_mode == 3:
+        # MLA record: 512 E4M3 codes x a scale per 128 channels, then 64 bf16
+        c = c.contiguous()
+        nope = c[..., :512].contiguous().view(torch.float8_e4m3fn).to(torch.float64)
+        sc = s.cpu().to(torch.float64).repeat_interleave(128, dim=-1)
+        rope = c[..., 512:].contiguous().view(torch.bfloat16).to(torch.float64)
+        return torch.cat([nope * sc, rope], dim=-1)
     if wl.kv_e4m3:
         x = c.contiguous().view(torch.float8_e4m3fn).to(torch.float64)
     elif getattr(wl, "kv_int8", False):

@@ -111,6 +111,12 @@ def bruteforce_cases():
                           num_kv_heads=1, head_dim=48, head_dim_v=32, page_size=(4, 16)[i % 2],
                           kv_dtype=kvd, q_dtype=qd, scale_mode=sm, seed=300 + i,
                           windows=None if i % 2 else [5, 0]))
+    # the mixed-precision MLA latent: E4M3 nope with a scale per 128 channels, bf16 rope
+    for i in range(2):
+        cases.append(dict(batch=2, rows=[1 + i, 2], kv_lens=[40 + 9 * i, 17], num_qo_heads=4,
+                          num_kv_heads=1, head_dim=576, head_dim_v=512, page_size=(8, 16)[i],
+                          kv_dtype="e4m3", q_dtype="bf16", scale_mode=3, seed=310 + i,
+                          windows=[0, 6] if i else None, layout=("NHD", "HND")[i]))
     return cases
 
 
@@ -502,6 +508,8 @@ MUTATIONS = {
     18: "append: new row written one token early",
     19: "append: E4M3 sign dropped",
     24: "MLA: values read from the latent's last dv channels",
+    25: "MLA record: nope scale block from 64-channel groups",
+    26: "MLA record: rope read at a one-byte stride",
     20: "int8 cache bytes read as unsigned",
     21: "append: int8 per-token scale amax / 128",
     22: "append: int8 ties rounded away from zero",

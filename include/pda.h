@@ -60,7 +60,14 @@ typedef struct CUstream_st* pda_stream_t; /* a cudaStream_t; NULL = legacy defau
  * cache is named beside bf16 and fp8 in "perf(attention): run up to 8 query
  * rows per request in the triton decode kernel", Tested on. */
 enum { PDA_BF16 = 0, PDA_E4M3 = 1, PDA_INT8 = 2 };
-enum { PDA_SCALE_NONE = 0, PDA_SCALE_TENSOR = 1, PDA_SCALE_TOKEN_HEAD = 2 };
+/* PDA_SCALE_MLA_BLOCK: the mixed-precision MLA latent the FlashMLA page's
+ * reviewers accept ("fp8 support", FlashMLA PR #54: nope in 8 bits per token
+ * and 128 channels, rope in 16 bits). Each (token, kv head) row of the cache
+ * is a 640-byte record: 512 E4M3 nope codes, then the 64 bf16 rope channels;
+ * strides are in bytes; k_scale = v_scale = fp32 [num_pages, P, Hkv, 4], the
+ * scale of each 128-channel nope block. head_dim 576, head_dim_v 512,
+ * kv_dtype PDA_E4M3, q_dtype PDA_BF16. */
+enum { PDA_SCALE_NONE = 0, PDA_SCALE_TENSOR = 1, PDA_SCALE_TOKEN_HEAD = 2, PDA_SCALE_MLA_BLOCK = 3 };
 enum { PDA_KERNEL_AUTO = 0, PDA_KERNEL_MMA = 1, PDA_KERNEL_TC = 2 };
 
 #define PDA_OK 0

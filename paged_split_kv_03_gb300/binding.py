@@ -16,6 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_lib", "libpda.so")
 
 PDA_BF16, PDA_E4M3, PDA_INT8 = 0, 1, 2
+PDA_SCALE_MLA_BLOCK = 3
 PDA_SCALE_NONE, PDA_SCALE_TENSOR, PDA_SCALE_TOKEN_HEAD = 0, 1, 2
 PDA_KERNEL_AUTO, PDA_KERNEL_MMA, PDA_KERNEL_TC = 0, 1, 2
 PDA_OK = 0

@@ -64,8 +64,13 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
   if (p->head_dim_v < 0 || (dv != p->head_dim && !mla)) return PDA_ERR_UNSUPPORTED;
   if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256 && p->head_dim != 512 && !mla)
     return PDA_ERR_UNSUPPORTED;
-  // the latent's E4M3 path takes an E4M3 query (FlashMLA's per-tensor Q/K/V)
-  if (mla && (p->kv_dtype == PDA_INT8 || (p->kv_dtype == PDA_E4M3 && p->q_dtype != PDA_E4M3)))
+  // the latent's E4M3 path takes an E4M3 query (FlashMLA's per-tensor Q/K/V);
+  // the mixed-precision records take a bf16 query, and only they take block scales
+  const bool mla_block = p->scale_mode == PDA_SCALE_MLA_BLOCK;
+  if (mla_block && (!mla || p->kv_dtype != PDA_E4M3 || p->q_dtype != PDA_BF16))
+    return PDA_ERR_UNSUPPORTED;
+  if (mla && !mla_block &&
+      (p->kv_dtype == PDA_INT8 || (p->kv_dtype == PDA_E4M3 && p->q_dtype != PDA_E4M3)))
     return PDA_ERR_UNSUPPORTED;
   if (!is_pow2(p->page_size) || p->page_size > 256) return PDA_ERR_UNSUPPORTED;
   if (p->kv_dtype != PDA_BF16 && p->kv_dtype != PDA_E4M3 && p->kv_dtype != PDA_INT8)
@@ -74,7 +79,7 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
   if (p->q_dtype == PDA_E4M3 && p->kv_dtype != PDA_E4M3) return PDA_ERR_UNSUPPORTED;
   if (p->kv_dtype == PDA_BF16 && p->scale_mode != PDA_SCALE_NONE) return PDA_ERR_UNSUPPORTED;
   if (p->kv_dtype != PDA_BF16 && p->scale_mode != PDA_SCALE_TENSOR &&
-      p->scale_mode != PDA_SCALE_TOKEN_HEAD)
+      p->scale_mode != PDA_SCALE_TOKEN_HEAD && p->scale_mode != PDA_SCALE_MLA_BLOCK)
     return PDA_ERR_UNSUPPORTED;
   if (p->max_batch <= 0 || p->max_q_len < 1 || p->max_q_len > pda::kMaxQLen) return PDA_ERR_INVALID;
   if (p->max_kv_len < 1 || p->num_pages < 1) return PDA_ERR_INVALID;
@@ -309,6 +314,9 @@ extern "C" int pda_decode_stages(const pda_plan_t* plan, const void* q, const vo
   if (lse && reinterpret_cast<uintptr_t>(lse) % 4) return PDA_ERR_ALIGNMENT;
   if (plan->scale_mode != PDA_SCALE_NONE &&
       (reinterpret_cast<uintptr_t>(k_scale) % 4 || reinterpret_cast<uintptr_t>(v_scale) % 4))
+    return PDA_ERR_ALIGNMENT;
+  // MLA records: a token's four block scales are read as one 16-byte vector
+  if (plan->scale_mode == PDA_SCALE_MLA_BLOCK && reinterpret_cast<uintptr_t>(k_scale) % 16)
     return PDA_ERR_ALIGNMENT;
   if (plan->batch == 0) return PDA_OK;
 

@@ -367,6 +367,11 @@ struct TcCfg {
   // them exactly to f16 into the MMA ring, and the MMAs are kind::f16 (f16
   // query, f16 P)
   static constexpr bool kI8 = KVT == PDA_INT8;
+  // mixed-precision MLA records (E4M3 nope with a scale per 128 channels,
+  // bf16 rope): converter warps dequantise the nope chunks and copy the rope
+  // chunk into a bf16 MMA ring, and the MMAs are the bf16 latent's
+  static constexpr bool kMix = SMODE == PDA_SCALE_MLA_BLOCK;
+  static constexpr bool kConv = kI8 || kMix;  // a TMA ring plus converter warps
   // head_dim 512: a K (or V) tile alone is 64-128 KB, one CTA per SM; int8:
   // one CTA per SM holding both rings
   static constexpr int kCtasPerSm = NMAX <= 16 && D <= 256 && !kI8 ? 2 : 1;
@@ -381,12 +386,12 @@ struct TcCfg {
   static constexpr int kProdThreads = 32 * kProducers;
   static constexpr int kProdWarp1 = 2 + kSmWarps;
   // int8: warps that widen the codes (after the producer warps)
-  static constexpr int kConvWarps = kI8 ? (NMAX <= 16 ? 8 : 4) : 0;
+  static constexpr int kConvWarps = kConv ? (NMAX <= 16 ? 8 : 4) : 0;
   static constexpr int kConvThreads = 32 * kConvWarps;
   static constexpr int kConvWarp0 = kProdWarp1 + kProducers - 1;
   static constexpr int kThreads = 64 + kSmThreads + 32 * (kProducers - 1) + kConvThreads;
   static constexpr int kColGroups = kSmWarps / 4;   // warps sharing a lane quadrant
-  static constexpr bool kF8 = KVT == PDA_E4M3;
+  static constexpr bool kF8 = KVT == PDA_E4M3 && !kMix;  // E4M3 MMA operands
   static constexpr bool kQSplit = kF8 && QT == PDA_BF16;  // bf16 query as two E4M3 terms
   static constexpr int kQTerms = kQSplit ? 2 : 1;
   static constexpr int kElt = kF8 ? 1 : 2;            // bytes of an MMA operand element
@@ -398,6 +403,11 @@ struct TcCfg {
   static constexpr int kChunks = kF8 ? kChunksQK : (kChunksQK + 1) & ~1;
   static constexpr int kChunksV = kDv / kAtom;       // ring slots per V tile
   static constexpr int kRawChunks = kI8 ? D / 128 : kChunks;  // TMA chunks per tile
+  // mixed MLA records: a K tile is 4 nope chunks and the rope chunk, a V tile
+  // the 4 nope chunks; each TMA chunk becomes two MMA-ring slots (the rope's
+  // second one is the K unit's empty slot)
+  static constexpr int kRawK = kMix ? 5 : kRawChunks;
+  static constexpr int kRawV = kMix ? 4 : kRawChunks;
   static constexpr int kTileSlots = kChunks + kChunksV;
   static constexpr int kQRows = kNmax * kQTerms;
   static constexpr int kQAtomBytes = kQRows * 128;
@@ -428,7 +438,7 @@ struct TcCfg {
   static constexpr int kAvailSlots = kAvail / kSlot > 12 ? 12 : kAvail / kSlot;
   // int8: a third of the slots (at least 2) hold TMA'd codes, the rest f16
   // tiles (the MMA side needs two tiles of those to keep widening ahead)
-  static constexpr int kIRing = kI8 ? (kAvailSlots / 3 < 2 ? 2 : kAvailSlots / 3) : 0;
+  static constexpr int kIRing = kConv ? (kAvailSlots / 3 < 2 ? 2 : kAvailSlots / 3) : 0;
   static constexpr int kRingRaw = kAvailSlots - kIRing;
   // bf16 / f16 V blocks span two adjacent slots: keep the ring even so pairs never wrap
   static constexpr int kRing = kF8 ? kRingRaw : (kRingRaw & ~1);
@@ -440,7 +450,8 @@ struct TcCfg {
   static constexpr bool kBuildable =
       kRing >= (kI8 ? kChunks + 2 : (D > 256 ? kChunksV : kTileSlots)) && kTmemNeed <= 512 &&
       kTmemCols * kCtasPerSm <= 512 && (!kI8 || (kIRing >= 1 && D <= 256)) &&
-      !(kMla && (kQSplit || kI8));
+      !(kMla && (kQSplit || kI8)) &&
+      (!kMix || (kMla && KVT == PDA_E4M3 && QT == PDA_BF16 && kIRing >= 2));
   static constexpr int kSmem = kQBytes + kPBytes + (kRing + kIRing) * kSlot + kSmallBytes;
   // barrier words in the small area's first 512 bytes
   static_assert(2 * (kRing + kIRing) + 10 + 2 <= 64, "barrier area");
@@ -850,6 +861,130 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
   }
 }
 
+// Mixed-precision MLA records: the converter warps walk the TMA ring in the
+// producer's unit order (K0, K1, then K_{j+2}, V_j, ..., then the last V
+// units). A nope chunk (128 tokens x 128 E4M3 codes of one 128-channel
+// block) becomes two bf16 MMA-ring slots, each code decoded exactly and
+// multiplied by its token's block scale; the rope chunk (64 bf16 per token)
+// is copied to the first of its two slots (the second is the K unit's
+// empty slot). Rows past the chunk's end are written as zeros. A thread
+// keeps one 16-code piece (gl) of kRows rows; their page ids are loaded two
+// units ahead and their scales one unit ahead, so no load is waited on.
+template <class C>
+__device__ __forceinline__ void mla_convert(const DecodeArgs& a, int ntiles, int t_begin,
+                                            int t_end, int P, int hkv, const int32_t* ptab,
+                                            int ct, uint8_t* ring, const uint8_t* iring,
+                                            uint64_t* full, uint64_t* empty, uint64_t* i_full,
+                                            uint64_t* i_empty, volatile int* abort_flag) {
+  constexpr int R_ = C::kRing;
+  constexpr int kRows = kTok * 8 / C::kConvThreads;  // rows of one thread per chunk
+  constexpr int kRowStep = C::kConvThreads / 8;
+  const int gl = ct & 7, r0 = ct >> 3;
+  const int n = ntiles, units = 2 * ntiles;
+  // unit u of the ring order -> (kind 0 = K / 1 = V, tile)
+  auto unit_at = [&](int u, int& kind, int& tile) {
+    if (n == 1 || u < 2) {
+      kind = n == 1 ? u : 0;
+      tile = n == 1 ? 0 : u;
+      return;
+    }
+    const int v = u - 2, pairs = n - 2;
+    if (v < 2 * pairs) {
+      kind = v & 1;
+      tile = (v >> 1) + (kind ? 0 : 2);
+    } else {
+      kind = 1;
+      tile = n - 2 + (v - 2 * pairs);
+    }
+  };
+  auto pages_of = [&](int u, int* pg) {
+    int kind, tile;
+    unit_at(u < units ? u : units - 1, kind, tile);
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+      const int t = t_begin + tile * kTok + r0 + k * kRowStep;
+      pg[k] = t < t_end ? __ldg(ptab + t / P) : -1;
+    }
+  };
+  auto scales_of = [&](int u, const int* pg, float4* sc) {
+    int kind, tile;
+    unit_at(u < units ? u : units - 1, kind, tile);
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+      const int t = t_begin + tile * kTok + r0 + k * kRowStep;
+      sc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (pg[k] >= 0 && pg[k] < a.num_pages)
+        sc[k] = __ldg(reinterpret_cast<const float4*>(a.k_scale) +
+                      ((int64_t)pg[k] * P + t % P) * a.hkv + hkv);
+    }
+  };
+  int pg1[kRows], pg2[kRows];
+  float4 sc0[kRows], sc1[kRows];
+  pages_of(0, pg1);
+  scales_of(0, pg1, sc0);
+  pages_of(1, pg1);
+  uint32_t gw = 0;
+  for (int u = 0; u < units; ++u) {
+    int kind, tile;
+    unit_at(u, kind, tile);
+    pages_of(u + 2, pg2);       // two units ahead
+    scales_of(u + 1, pg1, sc1);  // one unit ahead
+    const int nraw = kind ? C::kRawV : C::kRawK;
+    for (int c = 0; c < nraw; ++c, ++gw) {
+      const uint32_t is = gw % C::kIRing;
+      const uint32_t c0 = 2 * gw, d0 = c0 % R_, d1 = (c0 + 1) % R_;
+      bool ok = bar_wait(i_full + is, (gw / C::kIRing) & 1u, abort_flag, a.status);
+      if (ok) ok = bar_wait(empty + d0, ((c0 / R_) & 1u) ^ 1u, abort_flag, a.status);
+      if (ok) ok = bar_wait(empty + d1, (((c0 + 1) / R_) & 1u) ^ 1u, abort_flag, a.status);
+      if (!__all_sync(0xffffffffu, ok)) return;
+      const uint8_t* src = iring + is * kSlot;
+      const bool rope = kind == 0 && c == 4;
+#pragma unroll
+      for (int k = 0; k < kRows; ++k) {
+        const int r = r0 + k * kRowStep;
+        const uint32_t soff = r * 128 + ((gl ^ (r & 7)) << 4);
+        const bool live = t_begin + tile * kTok + r < t_end;
+        if (rope) {
+          const uint4 v = live ? *reinterpret_cast<const uint4*>(src + soff) : make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(ring + d0 * kSlot + soff) = v;
+        } else {
+          const float sc = c == 0 ? sc0[k].x : c == 1 ? sc0[k].y : c == 2 ? sc0[k].z : sc0[k].w;
+          uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+          if (live) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(src + soff);
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+            uint32_t o[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f01 = e4m3x2_to_f2(static_cast<uint16_t>(w[e] & 0xFFFFu));
+              const float2 f23 = e4m3x2_to_f2(static_cast<uint16_t>(w[e] >> 16));
+              __nv_bfloat162 b01 = __floats2bfloat162_rn(f01.x * sc, f01.y * sc);
+              __nv_bfloat162 b23 = __floats2bfloat162_rn(f23.x * sc, f23.y * sc);
+              o[2 * e] = *reinterpret_cast<uint32_t*>(&b01);
+              o[2 * e + 1] = *reinterpret_cast<uint32_t*>(&b23);
+            }
+            lo = make_uint4(o[0], o[1], o[2], o[3]);
+            hi = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+          uint8_t* dst = ring + (gl < 4 ? d0 : d1) * kSlot + r * 128;
+          const int p0 = (gl & 3) * 2;  // first 16-byte piece of the bf16 row
+          *reinterpret_cast<uint4*>(dst + ((p0 ^ (r & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(dst + (((p0 + 1) ^ (r & 7)) << 4)) = hi;
+        }
+      }
+      fence_async_smem();  // the MMAs read these through the async proxy
+      bar_arrive(full + d0);
+      bar_arrive(full + d1);
+      bar_arrive(i_empty + is);
+    }
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+      sc0[k] = sc1[k];
+      pg1[k] = pg2[k];
+    }
+  }
+}
+
 template <int D, int KVT, int QT, int SMODE, int NMAX>
 __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
                                   TcCfg<D, KVT, QT, SMODE, NMAX>::kCtasPerSm)
@@ -932,7 +1067,7 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
     for (int s = 0; s < R_; ++s) {
       // TMA: one arrive.expect_tx per producer warp; int8: every converter
       // thread arrives after widening its share into the slot
-      bar_init(full + s, C::kI8 ? C::kConvThreads : C::kProducers);
+      bar_init(full + s, C::kConv ? C::kConvThreads : C::kProducers);
       bar_init(empty + s, 1);
     }
     for (int s = 0; s < C::kIRing; ++s) {
@@ -1116,7 +1251,8 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
     auto emit8 = [&](int kind, bool ok, int pg, int s0) {
       constexpr uint32_t kIR = C::kIRing > 0 ? C::kIRing : 1;  // (other builds never call this)
       const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, ok));
-      for (int c = 0; c < C::kRawChunks && alive; ++c, ++g) {
+      const int nraw = kind ? C::kRawV : C::kRawK;
+      for (int c = 0; c < nraw && alive; ++c, ++g) {
         const uint32_t slot = g % kIR, round = g / kIR;
         int good = 1;
         if (lane == 0) {
@@ -1132,12 +1268,18 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
           const uint32_t dst = su32(iring + slot * kSlot) + bx * box_bytes;
           const int c1 = a.tma_slot_dim == 1 ? s0 : hkv;
           const int c2 = a.tma_slot_dim == 1 ? hkv : s0;
-          tma_load(dst, maps[kind], c * 128, c1, c2, pg, i_full + slot);
+          if constexpr (C::kMix) {
+            // nope chunks (K and V) from the code map; the rope chunk from the bf16 map
+            const bool rope = kind == 0 && c == 4;
+            tma_load(dst, rope ? &tmv : &tmk, rope ? 0 : c * 128, c1, c2, pg, i_full + slot);
+          } else {
+            tma_load(dst, maps[kind], c * 128, c1, c2, pg, i_full + slot);
+          }
         }
       }
     };
     auto emit = [&](int kind, bool ok, int pg, int s0) {
-      if constexpr (C::kI8) {
+      if constexpr (C::kConv) {
         emit8(kind, ok, pg, s0);
         return;
       }
@@ -1177,7 +1319,7 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
       pg2 = pg3; s02 = s03; ok2 = ok3;
       ok3 = page_of(j + 4, pg3, s03);
     }
-    if constexpr (C::kI8) {
+    if constexpr (C::kConv) {
       // drain: every box issued must have landed before the CTA can exit
       if (lane == 0) {
         const uint32_t first = g > (uint32_t)C::kIRing ? g - C::kIRing : 0u;
@@ -1305,6 +1447,9 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
         bar_arrive(full + d1);
         bar_arrive(i_empty + is);
       }
+    } else if constexpr (C::kMix) {
+      mla_convert<C>(a, ntiles, t_begin, t_end, P, hkv, ptab, tid - C::kConvWarp0 * 32, ring,
+                     iring, full, empty, i_full, i_empty, abort_flag);
     }
   } else {
     // ========================================= softmax / epilogue warps
@@ -1391,6 +1536,8 @@ auto tc_select(const pda_plan_t* p, int nmax, F f) {
   const int kv = p->kv_dtype, qd = p->q_dtype, sm = p->scale_mode;
 #define PDA_TC_CASES(DD, NN)                                                              \
   if (kv == PDA_BF16) return f.template get<DD, PDA_BF16, PDA_BF16, PDA_SCALE_NONE, NN>(); \
+  if (sm == PDA_SCALE_MLA_BLOCK)                                                          \
+    return f.template get<DD, PDA_E4M3, PDA_BF16, PDA_SCALE_MLA_BLOCK, NN>();             \
   if (kv == PDA_INT8) {                                                                   \
     if (sm == PDA_SCALE_TENSOR)                                                           \
       return f.template get<DD, PDA_INT8, PDA_BF16, PDA_SCALE_TENSOR, NN>();              \
@@ -1454,17 +1601,21 @@ EncodeFn encoder() {
 // Tensor map over the paged cache: dims (c, slot, head, page) or
 // (c, head, slot, page), ordered by stride; one box = one page's (<= 128)
 // tokens x 128 bytes of one head.
-bool make_map(CUtensorMap* m, const void* base, const pda_plan_t* p, int* slot_dim, int dim0) {
+// `bf16_view`: the map reads bf16 values inside one-byte-element rows (the
+// rope channels of a mixed-precision MLA record).
+bool make_map(CUtensorMap* m, const void* base, const pda_plan_t* p, int* slot_dim, int dim0,
+              bool bf16_view = false) {
   EncodeFn enc = encoder();
   if (!enc) return false;
-  const int eb = p->kv_dtype == PDA_BF16 ? 2 : 1;  // E4M3 / int8 codes: one byte
+  const int eb = p->kv_dtype == PDA_BF16 ? 2 : 1;  // E4M3 / int8 codes: one byte (strides)
+  const int ed = bf16_view ? 2 : eb;               // the mapped element
   const bool slot_first = p->kv_stride_token <= p->kv_stride_head;
   *slot_dim = slot_first ? 1 : 2;
   const cuuint32_t rows = static_cast<cuuint32_t>(p->page_size < kTok ? p->page_size : kTok);
   cuuint64_t dims[4], strides[3];
   cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
   dims[0] = static_cast<cuuint64_t>(dim0);  // channels read (V of MLA: the first 512)
-  box[0] = static_cast<cuuint32_t>(128 / eb);
+  box[0] = static_cast<cuuint32_t>(128 / ed);
   if (slot_first) {
     dims[1] = p->page_size;
     dims[2] = p->num_kv_heads;
@@ -1484,7 +1635,7 @@ bool make_map(CUtensorMap* m, const void* base, const pda_plan_t* p, int* slot_d
   strides[2] = static_cast<cuuint64_t>(p->kv_stride_page) * eb;
   box[3] = 1;
   const CUtensorMapDataType dt =
-      p->kv_dtype == PDA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+      ed == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   return enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -1546,8 +1697,13 @@ int launch_stage1_tc(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_
   DecodeArgs a = args;
   CUtensorMap mk, mv;
   int slot_dim = 1;
-  if (!make_map(&mk, args.k, plan, &slot_dim, plan->head_dim) ||
-      !make_map(&mv, args.v, plan, &slot_dim, plan->head_dim_v))
+  const bool rec = plan->scale_mode == PDA_SCALE_MLA_BLOCK;
+  // mixed MLA records: the 512 nope codes (K and V), and the 64 bf16 rope
+  // channels from byte 512 on
+  if (rec ? (!make_map(&mk, args.k, plan, &slot_dim, 512) ||
+             !make_map(&mv, static_cast<const uint8_t*>(args.k) + 512, plan, &slot_dim, 64, true))
+          : (!make_map(&mk, args.k, plan, &slot_dim, plan->head_dim) ||
+             !make_map(&mv, args.v, plan, &slot_dim, plan->head_dim_v)))
     return PDA_ERR_CUDA;
   a.tma_slot_dim = slot_dim;
   TcFn k1 = tc_select(plan, plan->rows_per_cta, GetFn());

@@ -382,7 +382,7 @@ D512_NAMES = ("d512_mtp_bf16", "d512_mtp_fp8")
 # the 64-channel rope) per token, one kv head, V = its first 512 channels;
 # 16 query heads (128 over 8-way tensor parallelism; the page gives none),
 # pages of 64, bs 64, ctx 4096, R 1 (2); bf16, or E4M3 Q/K/V per tensor
-MLA_NAMES = ("mla_bf16", "mla_fp8")
+MLA_NAMES = ("mla_bf16", "mla_fp8", "mla_fp8_mixed")
 
 
 def config_workload(name: str, *, R: Optional[int] = None, bs: Optional[int] = None,
@@ -402,6 +402,8 @@ def config_workload(name: str, *, R: Optional[int] = None, bs: Optional[int] = N
     mla_bf16        bs 64, R 1 (2), 16/1 heads, latent 576 (V its first 512), ctx 4096,
                     page 64, bf16 (seeds 1300 + index)
     mla_fp8         the same with E4M3 Q and latent, per-tensor scales
+    mla_fp8_mixed   the same with latent records: E4M3 nope with a scale per token and
+                    128 channels, bf16 rope; bf16 Q
     d512_mtp_bf16   bs 1 (16), R 4 (1, 8), 16/1 heads, D 512, ctx 32768, page 16, bf16
     d512_mtp_fp8    bs 1 (16), R 4 (1, 8), 16/1 heads, D 512, ctx 32768, page 16, e4m3
                     K/V with a scale per (token, kv head), Q bf16 (seeds 1100 + index)
@@ -417,6 +419,8 @@ def config_workload(name: str, *, R: Optional[int] = None, bs: Optional[int] = N
                     head_dim=576, head_dim_v=512, page_size=64)
         if name == "mla_fp8":
             args.update(kv_dtype="e4m3", q_dtype="e4m3", scale_mode=SCALE_TENSOR)
+        elif name == "mla_fp8_mixed":
+            args.update(kv_dtype="e4m3", q_dtype="bf16", scale_mode=SCALE_MLA_BLOCK)
         args.update(kw)
         return make_workload(name=name, seed=seed, device=device, **args)
     if name in D512_NAMES:

@@ -68,7 +68,11 @@ def call_bytes(wl, chunk_pages: int | None = None, include_scratch: bool = True,
         cp = tail_chunk if tail_from is not None and b >= tail_from else chunk_pages
         lo, lo_page, npages, nsplit = _split_range(L, R, wins[b], P, cp or 1 << 30)
         tokens = L - lo_page * P
-        kv += kv_terms * tokens * H * D * kv_elt
+        if wl.scale_mode == 3:  # MLA records: 512 codes + 64 bf16, four block scales
+            kv += tokens * H * 640
+            scales += tokens * H * 16
+        else:
+            kv += kv_terms * tokens * H * D * kv_elt
         if wl.scale_mode == 2:
             scales += kv_terms * tokens * H * 4
         table += (npages - lo_page) * 4

@@ -154,6 +154,17 @@ def test_plan_mla(lib):
         assert rc == B.PDA_ERR_UNSUPPORTED, bad
     _, _, rc = B.pda_plan(_params(head_dim_v=64), check=False)  # only the MLA pair differs
     assert rc == B.PDA_ERR_UNSUPPORTED
+    # the mixed-precision records: E4M3 codes with block scales, bf16 query
+    mix, _, rc = B.pda_plan(_params(kv_dtype=1, scale_mode=B.PDA_SCALE_MLA_BLOCK,
+                                    **dict(MLA, kv_stride_page=64 * 640, kv_stride_token=640,
+                                           kv_stride_head=640)))
+    assert rc == 0 and mix.kernel == B.PDA_KERNEL_TC and mix.rows_per_cta == 32
+    assert mix.stage1_smem_bytes <= 227 * 1024
+    for bad in (dict(q_dtype=1), dict(kv_dtype=0), dict(head_dim=512, head_dim_v=0)):
+        args = dict(MLA, kv_dtype=1, scale_mode=B.PDA_SCALE_MLA_BLOCK)
+        args.update(bad)
+        _, _, rc = B.pda_plan(_params(**args), check=False)
+        assert rc == B.PDA_ERR_UNSUPPORTED, bad
 
 
 def test_plan_int8(lib):

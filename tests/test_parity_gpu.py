@@ -97,6 +97,13 @@ SMALL = {
                               num_kv_heads=1, head_dim=576, head_dim_v=512, page_size=32,
                               kv_dtype="e4m3", q_dtype="e4m3", scale_mode=SCALE_TOKEN_HEAD,
                               chunk=8),
+    "mla_mix_split_win": dict(batch=3, rows=[1, 2, 1], kv_lens=[700, 1300, 65],
+                              windows=[0, 0, 32], num_qo_heads=16, num_kv_heads=1,
+                              head_dim=576, head_dim_v=512, page_size=64, kv_dtype="e4m3",
+                              scale_mode=3, chunk=4),
+    "mla_mix_g8_hnd_p16": dict(batch=2, rows=[2, 1], kv_lens=[1000, 130], num_qo_heads=8,
+                               num_kv_heads=1, head_dim=576, head_dim_v=512, page_size=16,
+                               kv_dtype="e4m3", scale_mode=3, layout="HND"),
     "fp8t_qfp8_d512_g8": dict(batch=2, rows=[2, 1], kv_lens=[1000, 129], num_qo_heads=8,
                               num_kv_heads=1, head_dim=512, page_size=32, kv_dtype="e4m3",
                               q_dtype="e4m3", scale_mode=SCALE_TENSOR),
@@ -199,6 +206,8 @@ CONFIGS = [
     ("longctx_int8_pth", dict(bs=16, R=1), 64),
     ("mla_fp8", {}, None),
     ("mla_bf16", dict(R=2), 96),
+    ("mla_fp8_mixed", {}, None),
+    ("mla_fp8_mixed", dict(R=2), 96),
     ("d512_mtp_bf16", dict(bs=1, R=4), None),
     ("d512_mtp_bf16", dict(bs=1, R=8, kv_lens=131072), 48),
     ("d512_mtp_fp8", dict(bs=1, R=8), None),

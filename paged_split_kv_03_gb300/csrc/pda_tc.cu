@@ -368,10 +368,11 @@ struct TcCfg {
   // query, f16 P)
   static constexpr bool kI8 = KVT == PDA_INT8;
   // mixed-precision MLA records (E4M3 nope with a scale per 128 channels,
-  // bf16 rope): converter warps dequantise the nope chunks and copy the rope
-  // chunk into a bf16 MMA ring, and the MMAs are the bf16 latent's
+  // bf16 rope): converter warps dequantise the nope chunks and convert the
+  // rope chunk into an f16 MMA ring, and the MMAs are the latent's kind::f16
   static constexpr bool kMix = SMODE == PDA_SCALE_MLA_BLOCK;
   static constexpr bool kConv = kI8 || kMix;  // a TMA ring plus converter warps
+  static constexpr bool kF16Ops = kConv;      // ... whose MMAs take f16 operands (f16 Q and P)
   // head_dim 512: a K (or V) tile alone is 64-128 KB, one CTA per SM; int8:
   // one CTA per SM holding both rings
   static constexpr int kCtasPerSm = NMAX <= 16 && D <= 256 && !kI8 ? 2 : 1;
@@ -789,7 +790,7 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
       const uint32_t byte = static_cast<uint32_t>(r & 63) * 2u;
 #pragma unroll
       for (int i = 0; i < NH; ++i) {
-        if constexpr (C::kI8)
+        if constexpr (C::kF16Ops)
           *reinterpret_cast<__half*>(pbase + sw128(c0 + i, byte)) = __float2half_rn(s[i]);
         else
           *reinterpret_cast<__nv_bfloat16*>(pbase + sw128(c0 + i, byte)) = __float2bfloat16_rn(s[i]);
@@ -864,10 +865,11 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
 // Mixed-precision MLA records: the converter warps walk the TMA ring in the
 // producer's unit order (K0, K1, then K_{j+2}, V_j, ..., then the last V
 // units). A nope chunk (128 tokens x 128 E4M3 codes of one 128-channel
-// block) becomes two bf16 MMA-ring slots, each code decoded exactly and
-// multiplied by its token's block scale; the rope chunk (64 bf16 per token)
-// is copied to the first of its two slots (the second is the K unit's
-// empty slot). Rows past the chunk's end are written as zeros. A thread
+// block) becomes two f16 MMA-ring slots, each code pair decoded exactly to
+// f16 and multiplied by its token's block scale (rounded to f16) in one
+// f16x2 multiply; the rope chunk (64 bf16 per token) is rounded to f16 in
+// the first of its two slots (the second is the K unit's empty slot). Rows
+// past the chunk's end are written as zeros. A thread
 // keeps one 16-code piece (gl) of kRows rows; their page ids are loaded two
 // units ahead and their scales one unit ahead, so no load is waited on.
 template <class C>
@@ -945,10 +947,13 @@ __device__ __forceinline__ void mla_convert(const DecodeArgs& a, int ntiles, int
         const uint32_t soff = r * 128 + ((gl ^ (r & 7)) << 4);
         const bool live = t_begin + tile * kTok + r < t_end;
         if (rope) {
-          const uint4 v = live ? *reinterpret_cast<const uint4*>(src + soff) : make_uint4(0, 0, 0, 0);
+          const uint4 v = live ? bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(src + soff))
+                               : make_uint4(0, 0, 0, 0);
           *reinterpret_cast<uint4*>(ring + d0 * kSlot + soff) = v;
         } else {
           const float sc = c == 0 ? sc0[k].x : c == 1 ? sc0[k].y : c == 2 ? sc0[k].z : sc0[k].w;
+          const __half2 sc2 = __float2half2_rn(sc);
+          const uint32_t sc2u = *reinterpret_cast<const uint32_t*>(&sc2);
           uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
           if (live) {
             const uint4 raw = *reinterpret_cast<const uint4*>(src + soff);
@@ -956,18 +961,17 @@ __device__ __forceinline__ void mla_convert(const DecodeArgs& a, int ntiles, int
             uint32_t o[8];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float2 f01 = e4m3x2_to_f2(static_cast<uint16_t>(w[e] & 0xFFFFu));
-              const float2 f23 = e4m3x2_to_f2(static_cast<uint16_t>(w[e] >> 16));
-              __nv_bfloat162 b01 = __floats2bfloat162_rn(f01.x * sc, f01.y * sc);
-              __nv_bfloat162 b23 = __floats2bfloat162_rn(f23.x * sc, f23.y * sc);
-              o[2 * e] = *reinterpret_cast<uint32_t*>(&b01);
-              o[2 * e + 1] = *reinterpret_cast<uint32_t*>(&b23);
+              uint32_t h01, h23;
+              asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"(static_cast<uint16_t>(w[e] & 0xFFFFu)));
+              asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"(static_cast<uint16_t>(w[e] >> 16)));
+              asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[2 * e]) : "r"(h01), "r"(sc2u));
+              asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[2 * e + 1]) : "r"(h23), "r"(sc2u));
             }
             lo = make_uint4(o[0], o[1], o[2], o[3]);
             hi = make_uint4(o[4], o[5], o[6], o[7]);
           }
           uint8_t* dst = ring + (gl < 4 ? d0 : d1) * kSlot + r * 128;
-          const int p0 = (gl & 3) * 2;  // first 16-byte piece of the bf16 row
+          const int p0 = (gl & 3) * 2;  // first 16-byte piece of the f16 row
           *reinterpret_cast<uint4*>(dst + ((p0 ^ (r & 7)) << 4)) = lo;
           *reinterpret_cast<uint4*>(dst + (((p0 + 1) ^ (r & 7)) << 4)) = hi;
         }
@@ -1145,7 +1149,7 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
                                (((int64_t)(q0 + n / hpc) * a.hq + head0 + n % hpc) * D) * C::kElt +
                                cch * 16;
           v = __ldg(reinterpret_cast<const uint4*>(src));
-          if constexpr (C::kI8) v = bf16x8_to_f16x8(v);  // f16 operands beside int8 codes
+          if constexpr (C::kF16Ops) v = bf16x8_to_f16x8(v);  // f16 operands (converted caches)
         }
         const int byte = cch * 16;
         *reinterpret_cast<uint4*>(q_s + (byte / 128) * C::kQAtomBytes + sw128(n, byte % 128)) = v;
@@ -1337,7 +1341,7 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
     if (lane == 0) {
       bool alive = bar_wait(q_ready, 0, abort_flag, a.status);
       fence_after();
-      const uint32_t fmt = kF8 || C::kI8 ? 0u : 1u;  // E4M3, f16 (int8 caches) or bf16
+      const uint32_t fmt = kF8 || C::kF16Ops ? 0u : 1u;  // E4M3, f16 (converted caches) or bf16
       const uint32_t id_s = idesc(fmt, 0, static_cast<uint32_t>(Nq));
       // E4M3: N = both P terms' columns; bf16: N columns
       const uint32_t id_p = idesc(fmt, 1, static_cast<uint32_t>(kF8 ? 2 * N : N), C::kPMn ? 1u : 0u);

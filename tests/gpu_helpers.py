@@ -70,8 +70,9 @@ def bf16_half_ulp(x):
 
 def mla_record_lse_bound(wl, items=None):
     """Extra lse allowance for mixed-precision MLA records: the kernel's key
-    operand is bf16(code x block scale), off by at most 2^-9 relative per
-    channel, so a key's logit moves by at most 2^-9 * sm_scale * sum_c
+    operand is f16(code x f16(block scale)), off by at most about 2^-10
+    relative per channel (2^-9 is used, which also covers f16's subnormal
+    steps), so a key's logit moves by at most 2^-9 * sm_scale * sum_c
     |q_c k_c| and the lse (a smooth maximum) by at most the largest such move
     over the request's keys. Computed from the oracle-side decode of the
     records; zeros for other workloads."""

@@ -46,7 +46,7 @@ SWEEP = [("mtp_verify_bf16", 16, R) for R in (1, 4, 8)] + \
         [("longctx_int8_pth", 16, R) for R in (1, 8)] + \
         [("d512_mtp_bf16", 1, R) for R in (1, 4, 8)] + \
         [("d512_mtp_fp8", 1, R) for R in (1, 4, 8)] + \
-        [("mla_bf16", 64, 1), ("mla_fp8", 64, 1), ("mla_fp8", 64, 2)]
+        [("mla_bf16", 64, 1), ("mla_fp8", 64, 1), ("mla_fp8", 64, 2), ("mla_fp8_mixed", 64, 1)]
 
 
 def peaks():

@@ -329,6 +329,24 @@ def parse_workload(spec):
     return name, kw, f"{name} {kw}"
 
 
+def max_over_ranks(ms, device):
+    """The slowest replica's step time (ms): the job's time when ranks run in
+    a process group (any backend), else ``ms`` itself."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank, world, ms):
+    """Whole-job throughput: the bytes every replica moved / the slowest
+    replica's time (weak scaling: each rank runs the full workload)."""
+    return bytes_per_rank * world / (ms * 1e-3) / 1e9
+
+
 def run_ours(args, rank, world, dev):
     import torch
 
@@ -355,12 +373,8 @@ def run_ours(args, rank, world, dev):
     torch.cuda.synchronize()
     if dist:
         tdist.barrier()
-    ms = sum(times) / len(times)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = nbytes["total"] * world / (ms * 1e-3) / 1e9
+    ms = max_over_ranks(sum(times) / len(times), dev)
+    value = whole_job_gbs(nbytes["total"], world, ms)
     assert dec.status() == 0, "device status bits set during the benchmark"
 
     # the dominant kernel: stage 1, timed on its own (a graph of the stage-1

@@ -405,6 +405,49 @@ def test_rows_equal_single_row_requests():
     assert (lse1 - lse).abs().max() <= TOL_BF16["lse"]
 
 
+GRAPH_CASES = {
+    "int8_pth_d256": dict(batch=2, rows=[3, 8], kv_lens=[1500, 700], num_qo_heads=16,
+                          num_kv_heads=2, head_dim=256, page_size=16, kv_dtype="int8",
+                          scale_mode=SCALE_TOKEN_HEAD),
+    "mla_records": dict(batch=2, rows=[1, 2], kv_lens=[900, 333], num_qo_heads=16,
+                        num_kv_heads=1, head_dim=576, head_dim_v=512, page_size=64,
+                        kv_dtype="e4m3", scale_mode=3),
+    "mla_bf16": dict(batch=2, rows=[2, 1], kv_lens=[1200, 64], num_qo_heads=16,
+                     num_kv_heads=1, head_dim=576, head_dim_v=512, page_size=16),
+}
+
+
+@pytest.mark.parametrize("name", sorted(GRAPH_CASES))
+def test_graph_replay_new_queries(name):
+    """A captured call replayed with new query values (same buffers) matches
+    the oracle each time: the converter and latent pipelines carry no state
+    from one call to the next."""
+    wl, _ = _make(name, GRAPH_CASES[name])
+    dec = B.Decoder(B.params_for(wl), device=DEV)
+    out = torch.empty(wl.total_rows, wl.num_qo_heads, dv_of(wl), dtype=torch.bfloat16,
+                      device=DEV)
+    lse = torch.empty(wl.total_rows, wl.num_qo_heads, dtype=torch.float32, device=DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        dec.run(wl, out, lse, stream=s)
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        dec.run(wl, out, lse, stream=s)
+    g = torch.Generator(device="cpu").manual_seed(5)
+    for step in range(3):
+        if step:
+            wl.q.copy_(torch.randn(wl.q.shape, generator=g).to(wl.q.dtype))
+        out.fill_(float("nan"))
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        ref_o, ref_l = oracle_ref(wl)
+        assert_close(out.float().cpu(), lse.cpu(), ref_o, ref_l, tol_for(wl),
+                     what=f"{name} replay {step}")
+    assert dec.status() == 0
+
+
 def test_stages_apart_equal_one_call():
     """pda_decode_stages(PARTIAL) then (MERGE) on one stream writes the same
     bytes as pda_decode (a plan with tail splits: both launches run)."""

@@ -193,6 +193,7 @@ def int8_encode(y: float, mutation: int = 0) -> int:
 
 APPEND_BF16, APPEND_TENSOR, APPEND_TOKEN_HEAD = 0, 1, 2
 APPEND_INT8_TENSOR, APPEND_INT8_TOKEN_HEAD = 3, 4
+APPEND_MLA_RECORD = 5  # 576-channel latent -> 640-byte record + four block scales
 
 
 def append_kv(*, k_new, v_new, page_table, kv_indptr, kv_len, qo_indptr, k_pages, v_pages,
@@ -204,14 +205,16 @@ def append_kv(*, k_new, v_new, page_table, kv_indptr, kv_len, qo_indptr, k_pages
     ``k_pages`` / ``v_pages``: the caches before the append (bytes, or bf16
     words for mode 0); ``k_scale`` / ``v_scale``: fp32 arrays (read for
     modes 1 and 3, written for modes 2 and 4, None for mode 0). Modes 3 / 4
-    are the int8 counterparts of 1 / 2 (scale amax / 127). Returns (k_pages, v_pages,
+    are the int8 counterparts of 1 / 2 (scale amax / 127). Mode 5 writes MLA
+    records (head_dim 576: E4M3 nope with a scale per 128 channels, bf16
+    rope) from ``k_new`` alone into ``k_pages`` / ``k_scale``. Returns (k_pages, v_pages,
     k_scale, v_scale, status) as numpy arrays (caches as raw bytes).
     """
     lib = _load(mutation)
     kn = _np(k_new).view(np.uint16)
-    vn = _np(v_new).view(np.uint16)
+    vn = _np(v_new if v_new is not None else k_new).view(np.uint16)
     kc = np.array(_np(k_pages), copy=True).view(np.uint8)
-    vc = np.array(_np(v_pages), copy=True).view(np.uint8)
+    vc = kc if v_pages is None else np.array(_np(v_pages), copy=True).view(np.uint8)
     ks = None if k_scale is None else np.array(_np(k_scale, np.float32), copy=True)
     vs = None if v_scale is None else np.array(_np(v_scale, np.float32), copy=True)
     pt = _np(page_table, np.int32)

@@ -357,6 +357,11 @@ uint8_t pdo_int8_encode(float y) {
  *   mode 3: int8 cache, s = k_scale[0] / v_scale[0] (read)
  *   mode 4: int8 cache, s = fp32(amax / 127) per (token, kv head) (1 if amax
  *           is 0), written like mode 2; code = pdo_int8_encode(fp32(x / s))
+ *   mode 5: MLA records (d = 576): per 128-channel block of the first 512
+ *           channels s = fp32(amax / 448) (1 if 0), written to k_scale
+ *           [num_pages, page_size, hkv, 4], codes as mode 2 at record bytes
+ *           [0, 512); the 64 rope channels copied as bf16 to bytes [512, 640);
+ *           v_new and v are not used (the latent is both K and V)
  *   k_new, v_new  bf16 bits [total_rows, hkv, d]
  *   k, v          caches (bytes; bf16 cache: 2 bytes per element), strides in elements
  * Returns PDO_OK, PDO_ERR_ARG, PDO_ERR_KVLEN (a request with L < R, skipped)
@@ -367,8 +372,9 @@ int pdo_append(int batch, int hkv, int d, int page_size, int mode, int64_t sp, i
                const int32_t* page_table, const int32_t* kv_indptr, const int32_t* kv_len,
                const int32_t* qo_indptr, uint8_t* k, uint8_t* v, float* k_scale,
                float* v_scale) {
-  if (batch < 0 || hkv <= 0 || d <= 0 || page_size <= 0 || mode < 0 || mode > 4) return PDO_ERR_ARG;
-  if (mode != 0 && (!k_scale || !v_scale)) return PDO_ERR_ARG;
+  if (batch < 0 || hkv <= 0 || d <= 0 || page_size <= 0 || mode < 0 || mode > 5) return PDO_ERR_ARG;
+  if (mode == 5 && d != 576) return PDO_ERR_ARG;
+  if (mode != 0 && (!k_scale || (mode != 5 && !v_scale))) return PDO_ERR_ARG;
   int status = PDO_OK;
   for (int b = 0; b < batch; ++b) {
     int R = qo_indptr[b + 1] - qo_indptr[b];
@@ -390,6 +396,24 @@ int pdo_append(int batch, int hkv, int d, int page_size, int mode, int64_t sp, i
         int64_t row = ((int64_t)(qo_indptr[b] + i) * hkv + h) * d;
         int64_t base = (int64_t)page * sp + slot * st + (int64_t)h * sh;
         int64_t sidx = ((int64_t)page * page_size + slot) * hkv + h;
+        if (mode == 5) {
+          const uint16_t* src = k_new + row;
+          for (int blk = 0; blk < 4; ++blk) {
+            float amax = 0.0f;
+            for (int c = 128 * blk; c < 128 * blk + (MUT(27) ? 64 : 128); ++c) {
+              float x = (float)pdo_bf16_to_double(src[c]);
+              if (fabsf(x) > amax) amax = fabsf(x);
+            }
+            float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+            k_scale[sidx * 4 + blk] = sc;
+            for (int c = 128 * blk; c < 128 * (blk + 1); ++c) {
+              float y = (float)pdo_bf16_to_double(src[c]) / sc;
+              k[base + c] = pdo_e4m3_encode(y);
+            }
+          }
+          for (int c = 0; c < 64; ++c) memcpy(k + base + 512 + 2 * c, src + 512 + c, 2);
+          continue;
+        }
         for (int kv = 0; kv < 2; ++kv) {
           const uint16_t* src = (kv ? v_new : k_new) + row;
           uint8_t* cache = kv ? v : k;

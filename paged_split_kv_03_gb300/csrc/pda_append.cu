@@ -116,6 +116,41 @@ __device__ __forceinline__ void put_row(const __nv_bfloat16* src, uint8_t* pages
   }
 }
 
+// One MLA record (MODE 5): the row's 576 bf16 latent values -> 512 E4M3
+// nope codes, each 128-channel block with its own amax / 448 scale (lane l
+// holds channels 16l .. 16l + 15 of block l / 8; the block's amax is a
+// shuffle over its 8 lanes), then the 64 rope values copied as bf16.
+__device__ __forceinline__ void put_mla_record(const __nv_bfloat16* src, uint8_t* rec,
+                                               float* scales, int lane) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src + lane * 16);
+  const uint4 w0 = __ldg(s4), w1 = __ldg(s4 + 1);
+  const uint32_t raw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+  float x[16];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    x[2 * e] = __uint_as_float(raw[e] << 16);
+    x[2 * e + 1] = __uint_as_float(raw[e] & 0xFFFF0000u);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+  for (int off = 1; off < 8; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const float sc = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  if ((lane & 7) == 0) scales[lane >> 3] = sc;
+  uint32_t c[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const uint16_t lo = e4m3x2(__fdiv_rn(x[4 * e], sc), __fdiv_rn(x[4 * e + 1], sc));
+    const uint16_t hi = e4m3x2(__fdiv_rn(x[4 * e + 2], sc), __fdiv_rn(x[4 * e + 3], sc));
+    c[e] = lo | (static_cast<uint32_t>(hi) << 16);
+  }
+  *reinterpret_cast<uint4*>(rec + lane * 16) = make_uint4(c[0], c[1], c[2], c[3]);
+  // rope: two bf16 per lane
+  *reinterpret_cast<uint32_t*>(rec + 512 + lane * 4) =
+      __ldg(reinterpret_cast<const uint32_t*>(src + 512) + lane);
+}
+
 template <int D, int MODE>
 __global__ void __launch_bounds__(256) append_kv(const __grid_constant__ AppendArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -149,6 +184,10 @@ __global__ void __launch_bounds__(256) append_kv(const __grid_constant__ AppendA
   const int64_t off = page * a.sp + slot * a.st + h * a.sh;  // elements
   const int64_t row = ((int64_t)(q0 + i) * a.hkv + h) * D;
   const int64_t sidx = ((int64_t)page * P + slot) * a.hkv + h;
+  if constexpr (MODE == 5) {  // MLA record: the latent is both K and V
+    put_mla_record(a.k_new + row, a.k_pages + off, a.k_scale + sidx * 4, lane);
+    return;
+  }
   constexpr bool kPerToken = MODE == 2 || MODE == 4;
   put_row<D, MODE>(a.k_new + row, a.k_pages, off, a.k_scale, a.k_scale + (kPerToken ? sidx : 0),
                    lane);
@@ -160,12 +199,16 @@ using AppendFn = void (*)(AppendArgs);
 
 template <int D>
 AppendFn pick_mode(int mode) {
-  switch (mode) {
-    case 0: return append_kv<D, 0>;
-    case 1: return append_kv<D, 1>;
-    case 2: return append_kv<D, 2>;
-    case 3: return append_kv<D, 3>;
-    default: return append_kv<D, 4>;
+  if constexpr (D == 576) {
+    return append_kv<576, 5>;  // MLA records only
+  } else {
+    switch (mode) {
+      case 0: return append_kv<D, 0>;
+      case 1: return append_kv<D, 1>;
+      case 2: return append_kv<D, 2>;
+      case 3: return append_kv<D, 3>;
+      default: return append_kv<D, 4>;
+    }
   }
 }
 
@@ -179,21 +222,29 @@ extern "C" int pda_append_kv(const pda_plan_t* plan, const void* k_new, const vo
                              void* split_scratch, pda_stream_t stream) {
   if (!plan) return PDA_ERR_NULL;
   if (plan->magic != PDA_PLAN_MAGIC) return PDA_ERR_PLAN;
-  if (!k_new || !v_new || !page_table || !kv_indptr || !kv_len || !qo_indptr || !k_pages ||
-      !v_pages)
+  // MLA records: one latent (k_new into k_pages, scales into k_scale); the
+  // v arguments are not used
+  const bool rec = plan->scale_mode == PDA_SCALE_MLA_BLOCK;
+  if (!k_new || (!v_new && !rec) || !page_table || !kv_indptr || !kv_len || !qo_indptr ||
+      !k_pages || (!v_pages && !rec))
     return PDA_ERR_NULL;
   if (!split_scratch) return PDA_ERR_SCRATCH;
   if (reinterpret_cast<uintptr_t>(split_scratch) % 256) return PDA_ERR_SCRATCH;
   if (max_q_len < 1 || max_q_len > plan->max_q_len) return PDA_ERR_INVALID;
   const bool fp8 = plan->kv_dtype != PDA_BF16;  // one-byte codes (E4M3 or int8) with scales
-  if (fp8 && (!k_scale || !v_scale)) return PDA_ERR_NULL;
+  if (fp8 && (!k_scale || (!v_scale && !rec))) return PDA_ERR_NULL;
   if (fp8 && plan->scale_mode == PDA_SCALE_NONE) return PDA_ERR_UNSUPPORTED;
   auto a16 = [](const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
-  if (!a16(k_new) || !a16(v_new) || !a16(k_pages) || !a16(v_pages)) return PDA_ERR_ALIGNMENT;
-  if (fp8 && (reinterpret_cast<uintptr_t>(k_scale) % 4 || reinterpret_cast<uintptr_t>(v_scale) % 4))
-    return PDA_ERR_ALIGNMENT;
+  if (rec) {
+    if (!a16(k_new) || !a16(k_pages) || !a16(k_scale)) return PDA_ERR_ALIGNMENT;
+  } else {
+    if (!a16(k_new) || !a16(v_new) || !a16(k_pages) || !a16(v_pages)) return PDA_ERR_ALIGNMENT;
+    if (fp8 && (reinterpret_cast<uintptr_t>(k_scale) % 4 || reinterpret_cast<uintptr_t>(v_scale) % 4))
+      return PDA_ERR_ALIGNMENT;
+  }
   const int D = plan->head_dim;
-  if (D != 64 && D != 128 && D != 256 && D != 512) return PDA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256 && D != 512 && !(D == 576 && rec)) return PDA_ERR_UNSUPPORTED;
+  if (rec && D != 576) return PDA_ERR_UNSUPPORTED;
   if (plan->batch == 0) return PDA_OK;
 
   pda::AppendArgs a;
@@ -217,13 +268,15 @@ extern "C" int pda_append_kv(const pda_plan_t* plan, const void* k_new, const vo
   a.page_size = plan->page_size;
   a.num_pages = plan->num_pages;
   a.max_q_len = max_q_len;
-  const int mode = !fp8 ? 0
-                   : (plan->kv_dtype == PDA_INT8 ? 2 : 0) +
-                         (plan->scale_mode == PDA_SCALE_TENSOR ? 1 : 2);
+  const int mode = rec ? 5
+                 : !fp8 ? 0
+                        : (plan->kv_dtype == PDA_INT8 ? 2 : 0) +
+                              (plan->scale_mode == PDA_SCALE_TENSOR ? 1 : 2);
   pda::AppendFn fn = D == 64 ? pda::pick_mode<64>(mode)
                      : D == 128 ? pda::pick_mode<128>(mode)
                      : D == 256 ? pda::pick_mode<256>(mode)
-                                : pda::pick_mode<512>(mode);
+                     : D == 512 ? pda::pick_mode<512>(mode)
+                                : pda::pick_mode<576>(mode);
   const int64_t warps = (int64_t)plan->batch * max_q_len * plan->num_kv_heads;
   const int64_t blocks = (warps + 7) / 8;
   if (blocks > 0x7fffffffLL) return PDA_ERR_INVALID;

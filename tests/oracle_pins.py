@@ -480,11 +480,58 @@ def pin_append_int8(mutation=0):
             assert kc.reshape(-1, P, H, D)[r1[1], r1[2], 1].view(np.int8)[0] == -127
 
 
+def pin_append_mla_record(mutation=0):
+    """MLA records: per 128-channel block s = fp32(amax / 448), codes = the
+    E4M3 cast of x / s, the rope channels' bf16 bytes at byte 512; nothing
+    else changes. A block's largest value sits in its second half."""
+    g = torch.Generator().manual_seed(8)
+    P, H, D, rec = 4, 2, 576, 640
+    lens, rows = (9, 5), (3, 2)
+    pages_per = [math.ceil(L / P) for L in lens]
+    num_pages = sum(pages_per) + 2
+    perm = torch.randperm(num_pages, generator=g)[:sum(pages_per)].to(torch.int32)
+    kv_indptr = torch.tensor([0] + list(np.cumsum(pages_per)), dtype=torch.int32)
+    qo = torch.tensor([0] + list(np.cumsum(rows)), dtype=torch.int32)
+    n = int(qo[-1])
+    x = torch.randn(n, H, D, generator=g)
+    x[:, :, 100] = 9.0   # block 0's maximum in its second 64 channels
+    x[1, 0, 256:384] = 0  # a zero block: scale 1, codes 0
+    k_new = x.to(torch.bfloat16)
+    fill = torch.randint(0, 256, (num_pages * P * H * rec,), generator=g, dtype=torch.uint8)
+    case = dict(k_new=k_new, v_new=None, page_table=perm, kv_indptr=kv_indptr,
+                kv_len=torch.tensor(lens, dtype=torch.int32), qo_indptr=qo,
+                k_pages=fill.clone().numpy(), v_pages=None,
+                k_scale=np.full(num_pages * P * H * 4, -1.0, np.float32), v_scale=None,
+                num_kv_heads=H, head_dim=D, page_size=P, mode=oracle.APPEND_MLA_RECORD,
+                strides=(P * H * rec, H * rec, rec), num_pages=num_pages)
+    kc, _, ks, _, rc = oracle.append_kv(**case, mutation=mutation)
+    assert rc == 0
+    kc = kc.reshape(num_pages, P, H, rec)
+    ks = ks.reshape(num_pages, P, H, 4)
+    touched = np.zeros((num_pages, P), bool)
+    for row, page, slot in _slots(case):
+        touched[page, slot] = True
+        for h in range(H):
+            xr = k_new[row, h].float()
+            for b in range(4):
+                blk = xr[128 * b:128 * (b + 1)]
+                amax = float(blk.abs().max())
+                sc = np.float32(np.float32(amax) / np.float32(448.0)) if amax > 0 else np.float32(1.0)
+                assert ks[page, slot, h, b] == sc, (row, h, b)
+                ref = _e4m3_torch((blk / torch.tensor(float(sc))).clamp(-448, 448)).numpy()
+                assert np.array_equal(kc[page, slot, h, 128 * b:128 * (b + 1)], ref), (row, h, b)
+            rope = k_new[row, h, 512:].contiguous().view(torch.uint8).numpy()
+            assert np.array_equal(kc[page, slot, h, 512:], rope), (row, h)
+    before = fill.numpy().reshape(num_pages, P, H, rec)
+    assert np.array_equal(kc[~touched], before[~touched])
+    assert np.all(ks[~touched] == -1.0)
+
+
 ALL_PINS = [pin_e4m3_all_codes, pin_bruteforce, pin_q_zero_closed_form, pin_single_visible_key,
             pin_constant_v, pin_page_permutation, pin_split_merge, pin_rows_vs_single,
             pin_e4m3_encode_vs_torch, pin_e4m3_encode_saturates, pin_append_token_head,
             pin_append_per_tensor, pin_append_bf16_copy, pin_int8_constant_code,
-            pin_int8_encode_vs_torch, pin_append_int8]
+            pin_int8_encode_vs_torch, pin_append_int8, pin_append_mla_record]
 
 # Planted mistakes compiled into copies of the oracle (see MUT(k) in pdo_oracle.c).
 MUTATIONS = {
@@ -510,6 +557,7 @@ MUTATIONS = {
     24: "MLA: values read from the latent's last dv channels",
     25: "MLA record: nope scale block from 64-channel groups",
     26: "MLA record: rope read at a one-byte stride",
+    27: "append: MLA record block amax over its first 64 channels only",
     20: "int8 cache bytes read as unsigned",
     21: "append: int8 per-token scale amax / 128",
     22: "append: int8 ties rounded away from zero",

@@ -137,6 +137,49 @@ def test_append_then_decode_reads_the_new_tokens():
     assert np.abs(lse.cpu().numpy().reshape(-1) - ref_l).max() <= 1e-3
 
 
+def test_append_mla_records_bit_exact_then_decode():
+    """MLA records: the new rows' latents -> E4M3 nope codes with a scale per
+    128 channels and bf16 rope, byte-exact against the oracle; decode over the
+    appended cache then matches the oracle on it."""
+    args = dict(batch=3, rows=[2, 1, 1], kv_lens=[300, 65, 2], num_qo_heads=16, num_kv_heads=1,
+                head_dim=576, head_dim_v=512, page_size=64, kv_dtype="e4m3", scale_mode=3)
+    wl = make_workload(name="append_mla", seed=41, device="cpu", **args)
+    g = torch.Generator().manual_seed(42)
+    k_new = (torch.randn(wl.total_rows, 1, 576, generator=g) * 2).to(torch.bfloat16)
+    k_new[0, 0, 128:256] = 0  # a zero block: scale 1, codes 0
+    dwl = wl.to(DEV)
+    dec = B.Decoder(B.params_for(dwl), device=DEV)
+    dec.reset_status()
+    pages, scales = dwl.k_pages.clone(), dwl.k_scale.clone()
+    B.pda_append_kv(dec.plan, k_new.to(DEV), None, dwl.page_table, dwl.kv_indptr, dwl.kv_len,
+                    dwl.qo_indptr, max(1, wl.max_q_len), pages, None, scales, None, dec.scratch)
+    torch.cuda.synchronize()
+    assert dec.status() == 0
+    kc, _, ks, _, rc = oracle.append_kv(
+        k_new=k_new, v_new=None, page_table=wl.page_table, kv_indptr=wl.kv_indptr,
+        kv_len=wl.kv_len, qo_indptr=wl.qo_indptr, k_pages=wl.k_pages, v_pages=None,
+        k_scale=wl.k_scale, v_scale=None, num_kv_heads=1, head_dim=576, page_size=64,
+        mode=oracle.APPEND_MLA_RECORD, strides=wl.strides, num_pages=wl.num_pages)
+    assert rc == 0
+    assert np.array_equal(_bytes(pages.cpu()), kc.reshape(-1)), "record bytes differ"
+    assert np.array_equal(scales.cpu().numpy().reshape(-1).view(np.uint32),
+                          ks.reshape(-1).view(np.uint32)), "block scales differ"
+    # decode over the appended records
+    wl.k_pages = wl.v_pages = pages.cpu()
+    wl.k_scale = wl.v_scale = scales.cpu()
+    dwl = wl.to(DEV)
+    out = torch.empty(wl.total_rows, 16, 512, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(wl.total_rows, 16, dtype=torch.float32, device=DEV)
+    dec.run(dwl, out, lse)
+    torch.cuda.synchronize()
+    assert dec.status() == 0
+    ref_o, ref_l, rc = oracle.attention_for(wl)
+    assert rc == 0
+    err = np.abs(out.float().cpu().numpy().reshape(ref_o.shape) - ref_o)
+    assert err.max() <= 3e-2 and err.mean() <= 3e-3
+    assert np.abs(lse.cpu().numpy().reshape(-1) - ref_l).max() <= 1e-3
+
+
 def test_append_status_and_isolation():
     """A request whose page id is out of range, and one with kv_len < rows,
     set their status bits and are skipped; the other requests are written."""

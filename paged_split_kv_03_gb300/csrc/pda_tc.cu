@@ -24,13 +24,21 @@
 // from its [token][d] tile, so no transpose is needed on this hardware. The
 // softmax denominator always sums the exact fp32 probabilities.
 //
-// Warp roles (192 threads): warp 0 issues the TMA page gathers (one 128-byte
-// swizzled box per page and 128-byte column of the head) into a ring of 16 KB
-// slots and owns the TMEM allocation; warp 1 issues the MMAs from one thread;
-// warps 2..5 run the online softmax out of TMEM (thread = token row of S^T),
-// write P to shared memory and finish the output (thread = head_dim row of
-// O^T). All hand-offs are mbarriers; every wait is bounded and a timeout sets
-// PDA_STATUS_WAIT_TIMEOUT and unwinds without hanging.
+// Warp roles: warp 0 (with two more warps in the one-CTA-per-SM builds)
+// issues the TMA page gathers (one 128-byte swizzled box per page and
+// 128-byte column of the head) into a ring of 16 KB slots, and warp 0 owns the
+// TMEM allocation; warp 1 issues the MMAs from one thread; 8 or 16 warps run
+// the online softmax out of TMEM (thread = token row of S^T, a share of the
+// columns), write P to shared memory and finish the output (thread = head_dim
+// row of O^T). All hand-offs are mbarriers; every wait is bounded and a
+// timeout sets PDA_STATUS_WAIT_TIMEOUT and unwinds without hanging.
+//
+// Converted caches add a TMA ring and converter warps in front of the MMA
+// ring: int8 codes widen exactly to f16, and the mixed-precision MLA records
+// dequantise their E4M3 nope chunks (a scale per token and 128 channels) and
+// round their bf16 rope to f16; those builds run kind::f16 MMAs with an f16
+// query and P. The MLA latent (head_dim 576) is read twice from the same
+// cache: as K over all its channels and as V over its first 512.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>

@@ -7,8 +7,10 @@
 // warp per (request, row, kv head): it loads the row's D bf16 values of K
 // and of V (D / 32 per lane), takes the amax over D with warp shuffles when
 // the scale is per token, and stores E4M3 or int8 codes (or the bf16
-// values) into the token's page slot. HBM-bound; every access is one
-// contiguous row.
+// values) into the token's page slot. MLA records ("fp8 support", the
+// reviewers' 8-bit nope per 128 channels with 16-bit rope) take the latent
+// alone: a scale per 128-channel block, then the rope copied. HBM-bound;
+// every access is one contiguous row.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

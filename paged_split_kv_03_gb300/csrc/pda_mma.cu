@@ -10,7 +10,8 @@
 // follow the page table; it masks every row at its own causal position and
 // window; it keeps an online softmax per row; and it writes either the final
 // output (one chunk) or a normalised partial (o, lse) for stage 2.
-// FP8 (OCP E4M3) caches are widened exactly to 16 bits in shared memory;
+// FP8 (OCP E4M3) and int8 caches are widened exactly to 16 bits in shared
+// memory;
 // per-tensor K scales fold into the logit scale and per-tensor V scales into
 // the finalize step ("Naive Support for Hopper FP8 Prefill Kernel with
 // Per-Head Quantization", item 3); per-(token, kv head) scales multiply the

@@ -36,3 +36,17 @@ def test_byte_and_flop_model_reproduce_printed_numbers(idx):
     assert abs(call_flops(wl) * r["iter_per_s"] / 1e12 - r["TFLOPS"]) < 0.005
     # the printed average time is the inverse of the printed rate
     assert abs(1e3 / r["iter_per_s"] - r["avg_ms"]) < 0.0006
+
+
+def test_mla_latent_counts_once():
+    """MLA: the latent is read as K and as V but moves from HBM once (the
+    FlashMLA page's MBU); bf16 latent 576 x 2 B per token, records 640 B plus
+    four fp32 block scales per token; out has the 512 value channels."""
+    from paged_split_kv_03_gb300.synth import config_workload
+    for name, per_tok in (("mla_bf16", 576 * 2), ("mla_fp8", 576), ("mla_fp8_mixed", 640 + 16)):
+        wl = config_workload(name, bs=2, kv_lens=640)
+        assert wl.v_pages is wl.k_pages
+        b = call_bytes(wl)
+        assert b["kv"] + (b["scales"] if name == "mla_fp8_mixed" else 0) == 2 * 640 * per_tok
+        assert b["out"] == 2 * 16 * 512 * 2
+        assert call_flops(wl) == 2 * (576 + 512) * 16 * 2 * 640

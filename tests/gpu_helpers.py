@@ -2,7 +2,7 @@
 C ABI, run the fp64 oracle on the same arrays, compare with the stated
 tolerances.
 
-Tolerances (stated by the task's target and restated here): bf16 KV --
+Tolerances of the decode path's accuracy target: bf16 KV --
 max |err| <= 1e-2 and mean |err| <= 1e-3 over all output elements, lse
 |err| <= 1e-3; FP8 KV -- max |err| <= 3e-2 against the oracle on the
 dequantised values (mean <= 3e-3), lse |err| <= 1e-3.

@@ -241,3 +241,9 @@ def test_strerror(lib):
     for code in range(0, -8, -1):
         assert B.pda_strerror(code)
     assert "unknown" in B.pda_strerror(-99)
+
+
+def test_missing_library_raises(tmp_path):
+    # no fallback: a binding pointed at an absent library refuses to load
+    with pytest.raises(RuntimeError, match="no fallback"):
+        B.load_library(str(tmp_path / "libpda.so"))

@@ -231,8 +231,8 @@ def setup_call(wl, dev):
     import torch
     from paged_split_kv_03_gb300 import binding as B
     dec = B.Decoder(B.params_for(wl, device=dev.index or 0), device=dev)
-    out = torch.empty(wl.total_rows, wl.num_qo_heads, wl.head_dim, dtype=torch.bfloat16,
-                      device=dev)
+    dv = getattr(wl, "head_dim_v", None) or wl.head_dim
+    out = torch.empty(wl.total_rows, wl.num_qo_heads, dv, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(wl.total_rows, wl.num_qo_heads, dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
     mq = max(1, wl.max_q_len)
@@ -251,10 +251,14 @@ def e2e_time(wl, dec, steps, warmup, dev):
     import torch
     names = ["q", "k_pages", "v_pages", "k_scale", "v_scale", "page_table", "kv_indptr",
              "kv_len", "qo_indptr", "window"]
-    host = {n: getattr(wl, n).cpu().pin_memory() for n in names if getattr(wl, n) is not None}
+    alias = wl.v_pages is wl.k_pages  # an MLA latent is both caches: copied once
+    host = {n: getattr(wl, n).cpu().pin_memory() for n in names
+            if getattr(wl, n) is not None and not (alias and n == "v_pages")}
     devb = {n: torch.empty_like(getattr(wl, n)) for n in host}
-    out = torch.empty(wl.total_rows, wl.num_qo_heads, wl.head_dim, dtype=torch.bfloat16,
-                      device=dev)
+    if alias:
+        devb["v_pages"] = devb["k_pages"]
+    dv = getattr(wl, "head_dim_v", None) or wl.head_dim
+    out = torch.empty(wl.total_rows, wl.num_qo_heads, dv, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(wl.total_rows, wl.num_qo_heads, dtype=torch.float32, device=dev)
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()

@@ -101,7 +101,8 @@ typedef struct {
   int32_t page_size;       /* P: power of two in [1, 256] */
   int32_t q_dtype;         /* PDA_BF16, or PDA_E4M3 (then kv_dtype must be PDA_E4M3) */
   int32_t kv_dtype;        /* PDA_BF16, PDA_E4M3 or PDA_INT8 (int8: head_dim <= 256) */
-  int32_t scale_mode;      /* PDA_SCALE_NONE for bf16 KV; TENSOR or TOKEN_HEAD for E4M3 / int8 */
+  int32_t scale_mode;      /* PDA_SCALE_NONE for bf16 KV; TENSOR or TOKEN_HEAD for E4M3 / int8;
+                              MLA_BLOCK for MLA latent records (E4M3 KV, bf16 Q, 576 / 512) */
   int32_t max_batch;       /* upper bound of `batch` over the plan's lifetime */
   int32_t max_q_len;       /* 1..8: rows per request */
   int32_t max_kv_len;      /* upper bound of kv_len[b] */

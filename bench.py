@@ -139,6 +139,25 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+THROTTLE_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def clocks_ok(summary) -> bool:
+    """False when the clock record of a timed region disqualifies its number:
+    a hardware or thermal slowdown was active, or the median SM clock sat
+    below 90 % of its maximum with no reason given (a clock lock left by
+    someone else). sw_power_cap alone is kept. No record (no nvidia-smi):
+    nothing to judge, True."""
+    if not summary:
+        return True
+    if any(r in THROTTLE_REASONS for r in summary.get("reasons", ())):
+        return False
+    mx = summary.get("sm_max_mhz") or 0.0
+    if mx > 0 and summary.get("sm_mhz", mx) < 0.9 * mx and not summary.get("reasons"):
+        return False
+    return True
+
+
 # ------------------------------------------------------------------ GPU arm
 def make_flush(dev):
     """L2 flush for timing: a memset of 2x L2, then a read of another 2x L2
@@ -377,6 +396,18 @@ def run_ours(args, rank, world, dev):
     torch.cuda.synchronize()
     if dist:
         tdist.barrier()
+    clocks = clk.summary()
+    if max_over_ranks(0.0 if clocks_ok(clocks) else 1.0, dev) > 0:  # every rank agrees
+        # a throttled or clock-locked timed region is taken once more; the
+        # line reports the second one and keeps the first one's record
+        first = clocks
+        with ClockSampler(dev.index or 0) as clk:
+            times = time_graph(graph.replay, args.steps, args.warmup, flush, stream)
+        torch.cuda.synchronize()
+        if dist:
+            tdist.barrier()
+        clocks = clk.summary() or {}
+        clocks = dict(clocks, remeasured_after=first)
     ms = max_over_ranks(sum(times) / len(times), dev)
     value = whole_job_gbs(nbytes["total"], world, ms)
     assert dec.status() == 0, "device status bits set during the benchmark"
@@ -462,7 +493,7 @@ def run_ours(args, rank, world, dev):
                    "grid_ctas": dec.plan.grid_ctas, "bytes_per_call": nbytes,
                    "flops_per_call": flops, "tflops": flops / (ms * 1e-3) / 1e12},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": launches_per_step * args.steps, "clocks": clk.summary(),
+        "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
         "r_sweep": sweep, "append": append, "source_sha": source_sha(),
     }
 

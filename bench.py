@@ -341,12 +341,14 @@ def oracle_rate(wl, budget_s: float, seed: int = 0, max_items=None):
 
 
 def parse_workload(spec):
-    """'name' or 'name:k=v,k=v' (integer values) -> (name, kwargs, description)."""
+    """'name' or 'name:k=v,k=v' (integer values, else strings such as
+    layout=HND) -> (name, kwargs, description)."""
     name, _, rest = spec.partition(":")
     kw = {}
     for item in filter(None, rest.split(",")):
         k, _, v = item.partition("=")
-        kw[k.strip()] = int(v)
+        v = v.strip()
+        kw[k.strip()] = int(v) if v.lstrip("-").isdigit() else v
     if name == HEADLINE and not kw:
         return name, kw, HEADLINE_DESC
     return name, kw, f"{name} {kw}"

@@ -68,3 +68,14 @@ def test_recorded_traffic_keys_on_source_hash(tmp_path, monkeypatch):
     assert bench.recorded_traffic("stage1", "mixed") is None          # never captured
     (csrc / "pda_tc.cu").write_bytes(b"// changed\n" + (csrc / "pda_tc.cu").read_bytes())
     assert bench.recorded_traffic("stage1", "fp8_decode") is None     # kernel changed since
+
+
+def test_parse_workload():
+    assert bench.parse_workload(bench.HEADLINE)[:2] == (bench.HEADLINE, {})
+    name, kw, desc = bench.parse_workload("longctx_fp8_pth:bs=16,R=8")
+    assert (name, kw) == ("longctx_fp8_pth", {"bs": 16, "R": 8})
+    name, kw, _ = bench.parse_workload("fp8_decode:layout=HND")
+    assert kw == {"layout": "HND"}
+    from paged_split_kv_03_gb300.synth import config_workload
+    wl = config_workload("tiny", **kw)
+    assert wl.layout == "HND"

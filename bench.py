@@ -366,6 +366,19 @@ def max_over_ranks(ms, device):
     return float(t.item())
 
 
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal (context beside the measured peak)
+
+
+def step_stats(times_ms):
+    """Median and interquartile mean (the mean of the middle half of the sorted
+    samples) of per-step times, in microseconds."""
+    xs = sorted(times_ms)
+    n = len(xs)
+    q = n // 4
+    mid = xs[q:n - q] if n - 2 * q > 0 else xs
+    return {"us_median": statistics.median(xs) * 1e3, "us_iqm": sum(mid) / len(mid) * 1e3}
+
+
 def whole_job_gbs(bytes_per_rank, world, ms):
     """Whole-job throughput: the bytes every replica moved / the slowest
     replica's time (weak scaling: each rank runs the full workload)."""
@@ -481,7 +494,10 @@ def run_ours(args, rank, world, dev):
     return {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "us_per_call": ms * 1e3,
-        "frac_of_peak": value / world / peak, "higher_is_better": True, "scaling": "weak",
+        "step_stats": step_stats(times),
+        "frac_of_peak": value / world / peak,
+        "frac_of_nominal_8tbs": value / world / NOMINAL_HBM_GBS,
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": value / world / PAGES_NUMBER["value"] if wdesc == HEADLINE_DESC else None,
         "vs_baseline_ref": PAGES_NUMBER,
         "dtype": ("e4m3 (tcgen05 e4m3 x e4m3 MMAs, fp32 accumulate)" if wdesc == HEADLINE_DESC

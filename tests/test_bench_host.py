@@ -79,3 +79,14 @@ def test_parse_workload():
     from paged_split_kv_03_gb300.synth import config_workload
     wl = config_workload("tiny", **kw)
     assert wl.layout == "HND"
+
+
+def test_step_stats():
+    st = bench.step_stats([0.1, 0.2, 0.3, 0.4, 10.0, 0.25, 0.15, 0.35])
+    # sorted: .1 .15 .2 .25 .3 .35 .4 10 -> middle half .2 .25 .3 .35
+    assert abs(st["us_median"] - 275.0) < 1e-9
+    assert abs(st["us_iqm"] - 275.0) < 1e-9
+    one = bench.step_stats([0.5])
+    assert one == {"us_median": 500.0, "us_iqm": 500.0}
+    three = bench.step_stats([0.3, 0.1, 0.2])
+    assert abs(three["us_iqm"] - 200.0) < 1e-9 and abs(three["us_median"] - 200.0) < 1e-9

@@ -33,8 +33,10 @@ PDA_STATUS_WAIT_TIMEOUT = 0x20
 PDA_STATUS_SMEM_MISALIGNED = 0x40
 PDA_PLAN_MAGIC = 0x50444131
 
-EXPORTED = ("pda_plan", "pda_decode", "pda_get_status", "pda_reset_status", "pda_strerror",
-            "pda_version", "pda_struct_sizes", "pda_decode_static")
+# every entry point include/pda.h declares
+EXPORTED = ("pda_plan", "pda_decode", "pda_decode_stages", "pda_decode_static", "pda_append_kv",
+            "pda_get_status", "pda_reset_status", "pda_strerror", "pda_version",
+            "pda_struct_sizes")
 
 _i32, _i64, _u32, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_void_p
 

@@ -31,6 +31,7 @@ def test_exports_every_declared_symbol(lib):
             "pda_strerror"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in pda.h but not exported"
+    assert sorted(B.EXPORTED) == names, "binding's list of entry points differs from pda.h"
 
 
 def test_struct_layouts_match(lib):

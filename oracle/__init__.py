@@ -19,7 +19,9 @@ Prefill Kernel with Per-Head Quantization", item 3).
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import os
+import platform
 import subprocess
 import threading
 
@@ -50,9 +52,14 @@ def build(mutation: int = 0, force: bool = False) -> str:
     pins catch each such mistake. The default build has none.
     """
     out = lib_path(mutation)
+    stamp_path = out + ".stamp"
+    with open(_SRC, "rb") as f:  # the source and the machine type it was built on
+        stamp = hashlib.sha256(platform.machine().encode() + f.read()).hexdigest()
     with _LOCK:
-        if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
-            return out
+        if not force and os.path.exists(out) and os.path.exists(stamp_path):
+            with open(stamp_path) as f:
+                if f.read().strip() == stamp:
+                    return out
         os.makedirs(_BUILD, exist_ok=True)
         tmp = out + f".tmp{os.getpid()}"
         cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
@@ -61,6 +68,8 @@ def build(mutation: int = 0, force: bool = False) -> str:
             cmd.insert(1, f"-DPDO_MUTATION={mutation}")
         subprocess.run(cmd, check=True)
         os.replace(tmp, out)
+        with open(stamp_path, "w") as f:
+            f.write(stamp + "\n")
     return out
 
 

@@ -8,7 +8,9 @@ the first CUDA call).
 """
 from __future__ import annotations
 
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -37,16 +39,33 @@ def _flags(extra=()):
             *ARCH, *extra]
 
 
-def _deps_mtime():
-    paths = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    paths.append(os.path.join(INCLUDE, "pda.h"))
-    paths.append(os.path.abspath(__file__))
-    return max(os.path.getmtime(p) for p in paths if os.path.isfile(p))
+STAMP = os.path.join(LIBDIR, "stamp")
+
+
+def _stamp() -> str:
+    """The host architecture plus a hash of every input of the build: a
+    library built from other sources, or on another machine type, is stale."""
+    h = hashlib.sha256(platform.machine().encode())
+    paths = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC))
+    paths += [os.path.join(INCLUDE, "pda.h"), os.path.abspath(__file__)]
+    for p in paths:
+        if os.path.isfile(p):
+            h.update(os.path.basename(p).encode())
+            with open(p, "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def _current() -> bool:
+    if not (os.path.exists(LIB) and os.path.exists(STAMP)):
+        return False
+    with open(STAMP) as f:
+        return f.read().strip() == _stamp()
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     """Compile (if stale) and return the path of libpda.so."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
+    if not force and _current():
         return LIB
     objdir = os.path.join(LIBDIR, "obj")
     os.makedirs(objdir, exist_ok=True)
@@ -73,6 +92,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(_stamp() + "\n")
     return LIB
 
 

@@ -149,14 +149,19 @@ def _mma_ok(wl):
     return wl.head_dim <= 256
 
 
+def _refused(wl, chunk, kernel):
+    """A shape one path is not built for: its plan is refused up front with
+    PDA_ERR_UNSUPPORTED (nothing is launched)."""
+    p = B.params_for(wl, chunk_pages=chunk, kernel=KERNELS[kernel])
+    assert B.pda_plan(p, check=False)[2] == B.PDA_ERR_UNSUPPORTED
+
+
 @pytest.mark.parametrize("kernel", sorted(KERNELS))
 @pytest.mark.parametrize("name", sorted(SMALL))
 def test_small_full_parity(name, kernel):
     wl, chunk = _make(name, SMALL[name])
-    if kernel == "tc" and not _tc_ok(wl):
-        pytest.skip("shape served by the mma.sync path only")
-    if kernel == "mma" and not _mma_ok(wl):
-        pytest.skip("shape served by the tcgen05 path only")
+    if not (_tc_ok(wl) if kernel == "tc" else _mma_ok(wl)):
+        return _refused(wl, chunk, kernel)
     out, lse, status, dec = run_decode(wl, chunk_pages=chunk, kernel=KERNELS[kernel])
     assert status == 0
     ref_o, ref_l = oracle_ref(wl)
@@ -167,10 +172,8 @@ def test_small_full_parity(name, kernel):
 @pytest.mark.parametrize("kind", sorted(PEAKED_SMALL))
 def test_small_peaked_parity(kind, kernel):
     wl, chunk = _make(f"{kind}_peaked", PEAKED_SMALL[kind])
-    if kernel == "mma" and not _mma_ok(wl):
-        pytest.skip("shape served by the tcgen05 path only")
-    if kernel == "tc" and not _tc_ok(wl):
-        pytest.skip("shape served by the mma.sync path only")
+    if not (_tc_ok(wl) if kernel == "tc" else _mma_ok(wl)):
+        return _refused(wl, chunk, kernel)
     out, lse, status, dec = run_decode(wl, chunk_pages=chunk, kernel=KERNELS[kernel])
     assert status == 0
     ref_o, ref_l = oracle_ref(wl)

@@ -248,3 +248,65 @@ def test_missing_library_raises(tmp_path):
     # no fallback: a binding pointed at an absent library refuses to load
     with pytest.raises(RuntimeError, match="no fallback"):
         B.load_library(str(tmp_path / "libpda.so"))
+
+
+def _random_params(rng):
+    D = rng.choice([64, 128, 256, 512, 576])
+    mla = D == 576
+    hkv = 1 if (D >= 512 and rng.random() < 0.8) else rng.choice([1, 2, 4, 8])
+    G = rng.choice([1, 2, 3, 4, 6, 8, 12, 16, 24, 48, 64])
+    P = rng.choice([1, 2, 4, 8, 16, 32, 64, 128, 256])
+    kvt = rng.choice([B.PDA_BF16, B.PDA_E4M3, B.PDA_INT8])
+    qt = B.PDA_E4M3 if (kvt == B.PDA_E4M3 and rng.random() < 0.4) else B.PDA_BF16
+    sm = B.PDA_SCALE_NONE if kvt == B.PDA_BF16 else rng.choice([1, 2])
+    if mla and kvt == B.PDA_E4M3 and rng.random() < 0.5:
+        sm, qt = B.PDA_SCALE_MLA_BLOCK, B.PDA_BF16
+    Dc = 640 if sm == B.PDA_SCALE_MLA_BLOCK else D      # row elements (record bytes)
+    mq, mb = rng.randint(1, 8), rng.choice([1, 2, 3, 7, 16, 64, 128, 256])
+    L = rng.choice([1, 7, 64, 1000, 2048, 4096, 32768, 131072])
+    return _params(num_qo_heads=G * hkv, num_kv_heads=hkv, head_dim=D, page_size=P,
+                   q_dtype=qt, kv_dtype=kvt, scale_mode=sm, max_batch=mb, max_q_len=mq,
+                   max_kv_len=L, num_pages=mb * -(-L // P) + 4, kv_stride_page=P * hkv * Dc,
+                   kv_stride_token=hkv * Dc, kv_stride_head=Dc, batch=0,
+                   chunk_pages=rng.choice([0, 0, 0, 1, 5, 64]), head_dim_v=512 if mla else 0)
+
+
+def test_plan_invariants_random_shapes(lib):
+    """Seeded sweep over shapes, dtypes, page sizes, rows and forced chunks:
+    every accepted plan tiles its heads and tokens exactly, sizes its grid
+    and scratch for them and fits shared memory; every refusal is a
+    documented code."""
+    import random
+    rng = random.Random(5)
+    accepted = 0
+    for _ in range(800):
+        p = _random_params(rng)
+        plan, nbytes, rc = B.pda_plan(p, check=False)
+        if rc != B.PDA_OK:
+            assert rc in (B.PDA_ERR_UNSUPPORTED, B.PDA_ERR_INVALID, B.PDA_ERR_ALIGNMENT), rc
+            continue
+        accepted += 1
+        G, mq, Hq = p.num_qo_heads // p.num_kv_heads, p.max_q_len, p.num_qo_heads
+        for R in range(1, mq + 1):                      # q heads per CTA divide the group
+            h = plan.heads_per_cta[R]
+            assert G % h == 0 and R * h <= plan.rows_per_cta
+        assert plan.head_blocks * plan.heads_per_cta[mq] == G
+        pages = -(-p.max_kv_len // p.page_size)         # splits cover the context, none empty
+        assert plan.head_splits * plan.chunk_pages >= pages
+        assert (plan.head_splits - 1) * plan.chunk_pages < pages
+        assert plan.tail_splits * plan.tail_chunk_pages >= pages
+        tail = plan.tail_from < plan.batch
+        assert plan.max_splits == max(plan.head_splits, plan.tail_splits if tail else 0)
+        assert plan.grid_ctas == ((plan.tail_from * plan.head_splits +
+                                   (plan.batch - plan.tail_from) * plan.tail_splits) *
+                                  p.num_kv_heads * plan.head_blocks)
+        assert plan.rows_cap == p.max_batch * mq
+        dv = p.head_dim_v or p.head_dim
+        assert plan.scratch_lse_offset >= 256 and plan.scratch_lse_offset % 16 == 0
+        assert plan.scratch_o_offset % 16 == 0 and nbytes == plan.scratch_bytes
+        if plan.max_splits > 1:
+            n = plan.max_splits * plan.rows_cap * Hq
+            assert plan.scratch_o_offset >= plan.scratch_lse_offset + 4 * n
+            assert nbytes >= plan.scratch_o_offset + 4 * n * dv
+        assert plan.stage1_smem_bytes <= 227 * 1024
+    assert accepted > 500

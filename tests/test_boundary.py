@@ -310,3 +310,39 @@ def test_plan_invariants_random_shapes(lib):
             assert nbytes >= plan.scratch_o_offset + 4 * n * dv
         assert plan.stage1_smem_bytes <= 227 * 1024
     assert accepted > 500
+
+
+def test_append_host_checks_return_before_any_launch(lib):
+    fake = 1 << 20  # 16-byte aligned non-null address; never dereferenced on these paths
+    args = dict(k_new=fake, v_new=fake, page_table=fake, kv_indptr=fake, kv_len=fake,
+                qo_indptr=fake, max_q_len=4, k_pages=fake, v_pages=fake, k_scale=fake,
+                v_scale=fake, split_scratch=fake, stream=0)
+
+    def call(plan, **over):
+        return B.pda_append_kv(plan, check=False, **dict(args, **over))
+
+    fp8, _, _ = B.pda_plan(_params(kv_dtype=1, scale_mode=2, kv_stride_page=16 * 2 * 256,
+                                   kv_stride_token=512, kv_stride_head=256))
+    assert call(B.PdaPlan()) == B.PDA_ERR_PLAN
+    assert call(fp8, k_new=None) == B.PDA_ERR_NULL
+    assert call(fp8, v_new=None) == B.PDA_ERR_NULL
+    assert call(fp8, v_pages=None) == B.PDA_ERR_NULL
+    assert call(fp8, k_scale=None) == B.PDA_ERR_NULL
+    assert call(fp8, split_scratch=None) == B.PDA_ERR_SCRATCH
+    assert call(fp8, split_scratch=fake + 16) == B.PDA_ERR_SCRATCH
+    assert call(fp8, max_q_len=0) == B.PDA_ERR_INVALID
+    assert call(fp8, max_q_len=9) == B.PDA_ERR_INVALID
+    assert call(fp8, k_new=fake + 2) == B.PDA_ERR_ALIGNMENT
+    assert call(fp8, v_pages=fake + 8) == B.PDA_ERR_ALIGNMENT
+    assert call(fp8, v_scale=fake + 2) == B.PDA_ERR_ALIGNMENT
+    # MLA records: one latent, so the v arguments may be NULL; the block
+    # scales are read as 16-byte vectors
+    rec, _, _ = B.pda_plan(_params(**dict(MLA, kv_dtype=1, scale_mode=B.PDA_SCALE_MLA_BLOCK,
+                                          kv_stride_page=64 * 640, kv_stride_token=640,
+                                          kv_stride_head=640)))
+    assert call(rec, v_new=None, v_pages=None, v_scale=None, k_scale=fake + 4,
+                max_q_len=2) == B.PDA_ERR_ALIGNMENT
+    assert call(rec, k_scale=None, max_q_len=2) == B.PDA_ERR_NULL
+    # a latent without records has no append kernel
+    lat, _, _ = B.pda_plan(_params(**MLA))
+    assert call(lat, max_q_len=2) == B.PDA_ERR_UNSUPPORTED

@@ -11,8 +11,10 @@ size (which writes the memset's dirty lines back), both outside the CUDA
 events that time the step, so each step starts from a cold, clean L2.
 `value` is the algorithmic HBM bytes of the call (paged_split_kv_03_gb300.
 traffic) over its measured time, summed over ranks; the line also carries the
-R = 1 / 4 / 8 sweep of the two bs-16 workloads at 16 query / 2 kv heads and
-head_dim 256 (bf16 ctx 32768 and E4M3 per-(token, head) ctx 131072).
+R = 1 / 4 / 8 sweep at bs 1 and bs 16 of the two workloads at 16 query / 2 kv
+heads and head_dim 256 (bf16 ctx 32768 and E4M3 per-(token, head) ctx 131072)
+with their R8 / R1 time ratios, the mixed batch (bs 64, 48 / 2 heads, R 1..8,
+ctx 1K..64K, half windowed), and the int8, head_dim 512 and MLA workloads.
 
 `--impl reference` times the fp64 CPU oracle on the host cores instead, on a
 bounded sample of (row, q head) items per step, scaled to the same metric.
@@ -41,8 +43,9 @@ HEADLINE_DESC = ("fp8_decode: bs128, R1, 64 q / 8 kv heads, head_dim 128, ctx 20
                  "page 64, Q/K/V e4m3 per-tensor scales, bf16 out")
 PAGES_NUMBER = {"value": 3672.1, "unit": "GB/s",
                 "source": "hpc-ops FP8 decode on H200 (other hardware; context only)"}
-SWEEP = [("mtp_verify_bf16", 16, R) for R in (1, 4, 8)] + \
-        [("longctx_fp8_pth", 16, R) for R in (1, 4, 8)] + \
+SWEEP = [("mtp_verify_bf16", bs, R) for bs in (1, 16) for R in (1, 4, 8)] + \
+        [("longctx_fp8_pth", bs, R) for bs in (1, 16) for R in (1, 4, 8)] + \
+        [("mixed", 64, None)] + \
         [("longctx_int8_pth", 16, R) for R in (1, 8)] + \
         [("d512_mtp_bf16", 1, R) for R in (1, 4, 8)] + \
         [("d512_mtp_fp8", 1, R) for R in (1, 4, 8)] + \
@@ -458,7 +461,8 @@ def run_ours(args, rank, world, dev):
             t2 = time_graph(g2.replay, max(10, args.steps), 3, flush, s2)
             b2 = call_bytes(w2, plan=d2.plan)["total"]
             med = statistics.median(t2)
-            sweep.append({"workload": f"{name} bs{bs} R{R}", "us_per_call": med * 1e3,
+            label = f"{name} bs{bs} R{R}" if R else f"{name} bs{bs} R1..8"
+            sweep.append({"workload": label, "us_per_call": med * 1e3,
                           "GB_s": b2 / (med * 1e-3) / 1e9,
                           "frac_of_peak": b2 / (med * 1e-3) / 1e9 / peak, "bytes": b2,
                           "splits": d2.plan.max_splits})
@@ -466,9 +470,10 @@ def run_ours(args, rank, world, dev):
             torch.cuda.empty_cache()
         by = {s["workload"]: s["us_per_call"] for s in sweep}
         for name in ("mtp_verify_bf16", "longctx_fp8_pth"):
-            r1, r8 = by.get(f"{name} bs16 R1"), by.get(f"{name} bs16 R8")
-            if r1 and r8:
-                sweep.append({"workload": f"{name} bs16", "R8_over_R1": r8 / r1})
+            for bs in (1, 16):
+                r1, r8 = by.get(f"{name} bs{bs} R1"), by.get(f"{name} bs{bs} R8")
+                if r1 and r8:
+                    sweep.append({"workload": f"{name} bs{bs}", "R8_over_R1": r8 / r1})
 
     append = []
     if rank == 0 and not args.no_sweep:
@@ -504,12 +509,13 @@ def run_ours(args, rank, world, dev):
                   else ("int8" if wl.kv_int8 else "e4m3" if wl.kv_e4m3 else "bf16")),
         "data": "synthetic (seeded N(0,1), e4m3 per-tensor)" if wdesc == HEADLINE_DESC
                 else "synthetic (seeded N(0,1))",
-        "config": {"workload": wdesc, "parallelism": f"replicas x{world}",
-                   "l2": "flushed before every step (memset of 2x L2, then a read of 2x L2), outside the events",
-                   "graph": "stage 1 + stage 2 captured in one CUDA graph",
-                   "splits": dec.plan.max_splits, "chunk_pages": dec.plan.chunk_pages,
-                   "grid_ctas": dec.plan.grid_ctas, "bytes_per_call": nbytes,
-                   "flops_per_call": flops, "tflops": flops / (ms * 1e-3) / 1e12},
+        "config": {"workload": wdesc},
+        "setup": {"parallelism": f"replicas x{world}",
+                  "l2": "flushed before every step (memset of 2x L2, then a read of 2x L2), outside the events",
+                  "graph": "stage 1 + stage 2 captured in one CUDA graph",
+                  "splits": dec.plan.max_splits, "chunk_pages": dec.plan.chunk_pages,
+                  "grid_ctas": dec.plan.grid_ctas, "bytes_per_call": nbytes,
+                  "flops_per_call": flops, "tflops": flops / (ms * 1e-3) / 1e12},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
         "r_sweep": sweep, "append": append, "source_sha": source_sha(),

@@ -120,7 +120,17 @@ typedef struct {
                               PR #54): head_dim 576 (512 latent + 64 rope), head_dim_v 512,
                               one latent cache passed as both k_pages and v_pages, V being its
                               first 512 channels; bf16, or E4M3 with an E4M3 query */
+  int32_t wait_limit_us;   /* bound of every stage-1 pipeline wait (tcgen05 path), in
+                              microseconds; 0 = 2 s. A wait that runs out sets
+                              PDA_STATUS_WAIT_TIMEOUT and its CTA gives up, writing nothing */
+  uint32_t inject;         /* test hooks, 0 in normal use: PDA_INJECT_WITHHOLD_KV */
 } pda_params;
+
+/* Test hook (pda_params.inject): the tcgen05 stage-1 CTAs issue no K/V
+ * loads at all, so their consumers' waits run out after wait_limit_us and
+ * every CTA returns with PDA_STATUS_WAIT_TIMEOUT set and nothing written.
+ * It exercises the timeout path without a device fault. */
+#define PDA_INJECT_WITHHOLD_KV 0x1u
 
 /* The plan: plain data, owned by the caller, copied freely. Fields are
  * documented for inspection; pda_decode reads only what pda_plan wrote. */
@@ -153,7 +163,10 @@ typedef struct {
   int32_t head_splits;
   int32_t tail_splits;
   int32_t head_dim_v;      /* value channels (= head_dim but for MLA) */
-  int32_t reserved[10];
+  int32_t device;          /* pda_params.device */
+  int32_t wait_limit_us;   /* pda_params.wait_limit_us, 0 resolved to 2 s */
+  uint32_t inject;         /* pda_params.inject */
+  int32_t reserved[7];
 } pda_plan_t;
 
 #define PDA_PLAN_MAGIC 0x50444131u /* "PDA1" */
@@ -255,14 +268,18 @@ int pda_append_kv(const pda_plan_t* plan, const void* k_new, const void* v_new,
  * host's memory budget). The split scratch lives in a fixed
  * PDA_STATIC_SCRATCH_BYTES array of the library's own device memory, which
  * every GPU that loads the library holds until the process exits. Arguments
- * are those of pda_decode minus split_scratch. Returns PDA_ERR_TOO_LARGE
- * when plan->scratch_bytes exceeds the array. Allocates nothing. All calls
- * share the array and it keeps the last call's contents; each call first
- * clears the status word (an async memset on `stream`). Calls whose GPU
- * work overlaps race on the array: serialise them (one stream). The first
- * call on a device looks up the array's address with that device current;
- * make it before any stream capture. The status bits are not readable by the
- * caller through this entry point. */
+ * are those of pda_decode minus split_scratch; the host-side checks are
+ * pda_decode's and run before anything is enqueued. Returns
+ * PDA_ERR_TOO_LARGE when plan->scratch_bytes exceeds the array, and
+ * PDA_ERR_INVALID when the current device is not the plan's device (the
+ * array is per device). Allocates nothing. All calls share the array and it
+ * keeps the last call's contents; each call first clears the status word (an
+ * async memset on `stream`). Calls whose GPU work overlaps race on the
+ * array: serialise them (one stream). The array's device address is looked
+ * up on every call made outside a stream capture; a call made while `stream`
+ * is capturing reuses the last lookup on that device, so make the first call
+ * on a device before any stream capture. Read or clear the array's status
+ * bits with pda_get_status / pda_reset_status and split_scratch = NULL. */
 int pda_decode_static(const pda_plan_t* plan, const void* q, const void* k_pages,
                       const void* v_pages, const int32_t* page_table, const int32_t* kv_indptr,
                       const int32_t* kv_len, const int32_t* qo_indptr, int32_t max_q_len,
@@ -270,11 +287,13 @@ int pda_decode_static(const pda_plan_t* plan, const void* q, const void* k_pages
                       const float* v_scale, void* out, float* lse, pda_stream_t stream);
 
 /* Copy the device status word of `split_scratch` to *host_bits. Synchronises
- * `stream`. */
+ * `stream`. split_scratch = NULL reads the status of pda_decode_static's
+ * built-in array on the plan's device (which must be current). */
 int pda_get_status(const pda_plan_t* plan, const void* split_scratch, uint32_t* host_bits,
                    pda_stream_t stream);
 
-/* Clear the device status word (an async memset on `stream`). */
+/* Clear the device status word (an async memset on `stream`); NULL clears
+ * that of pda_decode_static's built-in array, as for pda_get_status. */
 int pda_reset_status(const pda_plan_t* plan, void* split_scratch, pda_stream_t stream);
 
 /* Static text for a PDA_ERR_* code. */

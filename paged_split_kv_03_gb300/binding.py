@@ -32,6 +32,7 @@ PDA_STATUS_ROWS_GT_CAP = 0x10
 PDA_STATUS_WAIT_TIMEOUT = 0x20
 PDA_STATUS_SMEM_MISALIGNED = 0x40
 PDA_PLAN_MAGIC = 0x50444131
+PDA_INJECT_WITHHOLD_KV = 0x1
 
 # every entry point include/pda.h declares
 EXPORTED = ("pda_plan", "pda_decode", "pda_decode_stages", "pda_decode_static", "pda_append_kv",
@@ -48,7 +49,8 @@ class PdaParams(ctypes.Structure):
                 ("max_kv_len", _i32), ("num_pages", _i32), ("kv_stride_page", _i64),
                 ("kv_stride_token", _i64), ("kv_stride_head", _i64), ("device", _i32),
                 ("num_sms", _i32), ("host_kv_len", ctypes.POINTER(_i32)), ("batch", _i32),
-                ("chunk_pages", _i32), ("kernel", _i32), ("head_dim_v", _i32)]
+                ("chunk_pages", _i32), ("kernel", _i32), ("head_dim_v", _i32),
+                ("wait_limit_us", _i32), ("inject", _u32)]
 
 
 class PdaPlan(ctypes.Structure):
@@ -63,7 +65,8 @@ class PdaPlan(ctypes.Structure):
                 ("rows_cap", _i64), ("scratch_bytes", _i64), ("scratch_lse_offset", _i64),
                 ("scratch_o_offset", _i64), ("stage1_smem_bytes", _i32),
                 ("tail_from", _i32), ("tail_chunk_pages", _i32), ("head_splits", _i32),
-                ("tail_splits", _i32), ("head_dim_v", _i32), ("reserved", _i32 * 10)]
+                ("tail_splits", _i32), ("head_dim_v", _i32), ("device", _i32),
+                ("wait_limit_us", _i32), ("inject", _u32), ("reserved", _i32 * 7)]
 
 
 class PdaError(RuntimeError):
@@ -207,6 +210,8 @@ def pda_append_kv(plan: PdaPlan, k_new, v_new, page_table, kv_indptr, kv_len, qo
 
 
 def pda_get_status(plan: PdaPlan, split_scratch, stream=None) -> int:
+    """Device status bits; ``split_scratch=None`` reads those of the
+    built-in array that pda_decode_static uses."""
     bits = _u32(0)
     rc = load_library().pda_get_status(ctypes.byref(plan), _ptr(split_scratch),
                                        ctypes.byref(bits), _stream(stream))
@@ -225,7 +230,8 @@ def pda_reset_status(plan: PdaPlan, split_scratch, stream=None) -> None:
 # ---------------------------------------------------------------- helpers
 
 def params_for(wl, *, max_batch=None, max_q_len=None, max_kv_len=None, device=0, num_sms=0,
-               chunk_pages=0, kernel=PDA_KERNEL_AUTO, batch=0) -> PdaParams:
+               chunk_pages=0, kernel=PDA_KERNEL_AUTO, batch=0, wait_limit_us=0,
+               inject=0) -> PdaParams:
     """PdaParams describing a workload object (synth.Workload or alike)."""
     p = PdaParams()
     p.num_qo_heads = wl.num_qo_heads
@@ -247,6 +253,8 @@ def params_for(wl, *, max_batch=None, max_q_len=None, max_kv_len=None, device=0,
     p.chunk_pages = chunk_pages
     p.kernel = kernel
     p.head_dim_v = getattr(wl, "head_dim_v", None) or 0
+    p.wait_limit_us = wait_limit_us
+    p.inject = inject
     return p
 
 

@@ -63,6 +63,31 @@ def _current() -> bool:
         return f.read().strip() == _stamp()
 
 
+def ptxas_reports():
+    """{kernel (mangled name): (registers, stack bytes, spill store bytes,
+    spill load bytes)} from the ptxas reports of the last build."""
+    import re
+    out = {}
+    for f in sorted(os.listdir(LIBDIR)):
+        if not (f.startswith("ptxas_") and f.endswith(".txt")):
+            continue
+        name = None
+        for line in open(os.path.join(LIBDIR, f)):
+            m = re.search(r"Function properties for (\S+)", line)
+            if m:
+                name = m.group(1)
+                continue
+            m = re.search(r"(\d+) bytes stack frame, (\d+) bytes spill stores, "
+                          r"(\d+) bytes spill loads", line)
+            if m and name:
+                out[name] = [None, *(int(x) for x in m.groups())]
+                continue
+            m = re.search(r"Used (\d+) registers", line)
+            if m and name in out and out[name][0] is None:
+                out[name][0] = int(m.group(1))
+    return {k: tuple(v) for k, v in out.items()}
+
+
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     """Compile (if stale) and return the path of libpda.so."""
     if not force and _current():
@@ -73,12 +98,17 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     def compile_one(src):
         obj = os.path.join(objdir, os.path.splitext(src)[0] + ".o")
-        extra = ["-Xptxas", "-v"] if (ptxas_info and src.endswith(".cu")) else []
+        # ptxas's resource report (registers, stack, spills) of every kernel
+        # is kept beside the library for the build checks
+        extra = ["-Xptxas", "-v"] if src.endswith(".cu") else []
         cmd = [cc, *_flags(extra), "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stderr}")
-        return obj, r.stderr
+        if src.endswith(".cu"):
+            with open(os.path.join(LIBDIR, "ptxas_" + os.path.splitext(src)[0] + ".txt"), "w") as f:
+                f.write(r.stderr)
+        return obj, r.stderr if ptxas_info else ""
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         results = list(ex.map(compile_one, SOURCES))

@@ -48,6 +48,8 @@ struct DecodeArgs {
   int64_t rows_cap;
   int hpc[kMaxQLen + 1];  // q heads per CTA for R rows
   int tma_slot_dim;       // tcgen05 path: tensor-map coordinate holding the slot (1 or 2)
+  uint64_t wait_limit_ns; // tcgen05 path: bound of every pipeline wait
+  uint32_t inject;        // PDA_INJECT_* test hooks set by the host (0 in normal use)
 };
 
 // The KV range one (request, split) covers. Every kernel derives it from the
@@ -111,5 +113,18 @@ int tc_smem_bytes(const pda_plan_t* plan);
 int tc_ctas_per_sm(const pda_plan_t* plan);
 int launch_stage1_tc(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_t s);
 int launch_stage2(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_t s);
+
+// Host-side checks of pda_decode's arguments (plan, pointers, alignment,
+// max_q_len); PDA_OK or the PDA_ERR_* code pda_decode returns for them.
+int check_decode_args(const pda_plan_t* plan, const void* q, const void* k_pages,
+                      const void* v_pages, const int32_t* page_table, const int32_t* kv_indptr,
+                      const int32_t* kv_len, const int32_t* qo_indptr, int32_t max_q_len,
+                      const float* k_scale, const float* v_scale, const void* out,
+                      const float* lse);
+
+// Device address of the library's built-in split scratch (the array behind
+// pda_decode_static) on the current device, which must be `device`; looked
+// up afresh unless `s` is capturing a graph (then the last lookup is used).
+int static_scratch(int device, cudaStream_t s, void** out);
 
 }  // namespace pda

@@ -15,9 +15,15 @@
 // whatever the last call wrote: each call clears its status word first, and
 // calls whose GPU work overlaps (two streams, or two host threads) race on
 // it, so the caller must order them on one stream or otherwise serialise
-// them. The first call on a device looks up the array's device address (with
-// that device current) and caches it; make that first call before any
-// stream capture begins.
+// them. The status word of the array is read and cleared by pda_get_status
+// and pda_reset_status with split_scratch = NULL.
+//
+// Host code cannot use the array's symbol as a device address: its device
+// address is looked up with the plan's device current, on every call whose
+// stream is not capturing a graph (so a device reset, which may move the
+// array, is followed). A call made while its stream is capturing reuses the
+// address of the last lookup on that device, so the first call on a device
+// must come before any stream capture.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -33,28 +39,39 @@ constexpr int kMaxDevices = 64;
 std::mutex g_lock;
 void* g_addr[kMaxDevices] = {};
 
-// Device address of g_static_scratch on the current device (looked up once
-// per device; host code cannot use the symbol itself as a device address).
-int static_scratch(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+}  // namespace
+
+namespace pda {
+
+int static_scratch(int device, cudaStream_t s, void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return PDA_ERR_CUDA;
+  }
+  // the array is per device: the plan's device must be the current one
+  if (dev != device || dev < 0 || dev >= kMaxDevices) return PDA_ERR_INVALID;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
     cudaGetLastError();
     return PDA_ERR_CUDA;
   }
   std::lock_guard<std::mutex> guard(g_lock);
-  if (!g_addr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) {
       cudaGetLastError();
       return PDA_ERR_CUDA;
     }
     g_addr[dev] = p;
+  } else if (!g_addr[dev]) {
+    return PDA_ERR_CUDA;  // never looked up outside a capture
   }
   *out = g_addr[dev];
   return PDA_OK;
 }
 
-}  // namespace
+}  // namespace pda
 
 extern "C" int pda_decode_static(const pda_plan_t* plan, const void* q, const void* k_pages,
                                  const void* v_pages, const int32_t* page_table,
@@ -63,15 +80,17 @@ extern "C" int pda_decode_static(const pda_plan_t* plan, const void* q, const vo
                                  const int32_t* window, float sm_scale, const float* k_scale,
                                  const float* v_scale, void* out, float* lse,
                                  pda_stream_t stream) {
-  if (!plan) return PDA_ERR_NULL;
-  if (plan->magic != PDA_PLAN_MAGIC) return PDA_ERR_PLAN;
+  // every host-side check first: a refused call touches nothing on the device
+  int rc = pda::check_decode_args(plan, q, k_pages, v_pages, page_table, kv_indptr, kv_len,
+                                  qo_indptr, max_q_len, k_scale, v_scale, out, lse);
+  if (rc != PDA_OK) return rc;
   if (plan->scratch_bytes > (int64_t)PDA_STATIC_SCRATCH_BYTES) return PDA_ERR_TOO_LARGE;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   void* scratch = nullptr;
-  int rc = static_scratch(&scratch);
+  rc = pda::static_scratch(plan->device, s, &scratch);
   if (rc != PDA_OK) return rc;
   // The status word is the only part that must start at zero.
-  if (cudaMemsetAsync(scratch, 0, sizeof(uint32_t), reinterpret_cast<cudaStream_t>(stream)) !=
-      cudaSuccess) {
+  if (cudaMemsetAsync(scratch, 0, sizeof(uint32_t), s) != cudaSuccess) {
     cudaGetLastError();
     return PDA_ERR_CUDA;
   }

@@ -88,6 +88,7 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
     return PDA_ERR_INVALID;
   if (p->chunk_pages < 0) return PDA_ERR_INVALID;
   if (p->kernel < PDA_KERNEL_AUTO || p->kernel > PDA_KERNEL_TC) return PDA_ERR_INVALID;
+  if (p->wait_limit_us < 0 || (p->inject & ~PDA_INJECT_WITHHOLD_KV)) return PDA_ERR_INVALID;
   // 16-byte alignment of every stride ("require 16-byte aligned cache bases
   // and strides", follow-up commit on the FreeToken page)
   const int eb = elem_bytes(p->kv_dtype);
@@ -123,6 +124,9 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
   pl.kv_stride_head = p->kv_stride_head;
   pl.group = p->num_qo_heads / p->num_kv_heads;
   pl.num_sms = num_sms;
+  pl.device = p->device;
+  pl.wait_limit_us = p->wait_limit_us > 0 ? p->wait_limit_us : 2000000;
+  pl.inject = p->inject;
   if (p->kernel == PDA_KERNEL_TC && !pda::tc_supported(&pl)) return PDA_ERR_UNSUPPORTED;
   // AUTO takes the tcgen05 path wherever it is built (head_dim 128/256/512/576,
   // pages >= 8); head_dims above 256 have no mma.sync build (their O tile
@@ -293,6 +297,33 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
   return PDA_OK;
 }
 
+namespace pda {
+
+int check_decode_args(const pda_plan_t* plan, const void* q, const void* k_pages,
+                      const void* v_pages, const int32_t* page_table, const int32_t* kv_indptr,
+                      const int32_t* kv_len, const int32_t* qo_indptr, int32_t max_q_len,
+                      const float* k_scale, const float* v_scale, const void* out,
+                      const float* lse) {
+  if (!plan) return PDA_ERR_NULL;
+  if (plan->magic != PDA_PLAN_MAGIC) return PDA_ERR_PLAN;
+  if (!q || !k_pages || !v_pages || !page_table || !kv_indptr || !kv_len || !qo_indptr || !out)
+    return PDA_ERR_NULL;
+  if (max_q_len < 1 || max_q_len > plan->max_q_len) return PDA_ERR_INVALID;
+  if (plan->scale_mode != PDA_SCALE_NONE && (!k_scale || !v_scale)) return PDA_ERR_NULL;
+  auto a16 = [](const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
+  if (!a16(q) || !a16(k_pages) || !a16(v_pages) || !a16(out)) return PDA_ERR_ALIGNMENT;
+  if (lse && reinterpret_cast<uintptr_t>(lse) % 4) return PDA_ERR_ALIGNMENT;
+  if (plan->scale_mode != PDA_SCALE_NONE &&
+      (reinterpret_cast<uintptr_t>(k_scale) % 4 || reinterpret_cast<uintptr_t>(v_scale) % 4))
+    return PDA_ERR_ALIGNMENT;
+  // MLA records: a token's four block scales are read as one 16-byte vector
+  if (plan->scale_mode == PDA_SCALE_MLA_BLOCK && reinterpret_cast<uintptr_t>(k_scale) % 16)
+    return PDA_ERR_ALIGNMENT;
+  return PDA_OK;
+}
+
+}  // namespace pda
+
 extern "C" int pda_decode_stages(const pda_plan_t* plan, const void* q, const void* k_pages,
                                  const void* v_pages, const int32_t* page_table,
                                  const int32_t* kv_indptr, const int32_t* kv_len,
@@ -307,17 +338,9 @@ extern "C" int pda_decode_stages(const pda_plan_t* plan, const void* q, const vo
     return PDA_ERR_NULL;
   if (!split_scratch) return PDA_ERR_SCRATCH;
   if (reinterpret_cast<uintptr_t>(split_scratch) % 256) return PDA_ERR_SCRATCH;
-  if (max_q_len < 1 || max_q_len > plan->max_q_len) return PDA_ERR_INVALID;
-  if (plan->scale_mode != PDA_SCALE_NONE && (!k_scale || !v_scale)) return PDA_ERR_NULL;
-  auto a16 = [](const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
-  if (!a16(q) || !a16(k_pages) || !a16(v_pages) || !a16(out)) return PDA_ERR_ALIGNMENT;
-  if (lse && reinterpret_cast<uintptr_t>(lse) % 4) return PDA_ERR_ALIGNMENT;
-  if (plan->scale_mode != PDA_SCALE_NONE &&
-      (reinterpret_cast<uintptr_t>(k_scale) % 4 || reinterpret_cast<uintptr_t>(v_scale) % 4))
-    return PDA_ERR_ALIGNMENT;
-  // MLA records: a token's four block scales are read as one 16-byte vector
-  if (plan->scale_mode == PDA_SCALE_MLA_BLOCK && reinterpret_cast<uintptr_t>(k_scale) % 16)
-    return PDA_ERR_ALIGNMENT;
+  const int rc0 = pda::check_decode_args(plan, q, k_pages, v_pages, page_table, kv_indptr, kv_len,
+                                         qo_indptr, max_q_len, k_scale, v_scale, out, lse);
+  if (rc0 != PDA_OK) return rc0;
   if (plan->batch == 0) return PDA_OK;
 
   pda::DecodeArgs a;
@@ -360,6 +383,9 @@ extern "C" int pda_decode_stages(const pda_plan_t* plan, const void* q, const vo
   a.head_splits = plan->head_splits;
   a.tail_splits = plan->tail_splits;
   a.rows_cap = plan->rows_cap;
+  a.wait_limit_ns = static_cast<uint64_t>(plan->wait_limit_us > 0 ? plan->wait_limit_us : 2000000) *
+                    1000ull;
+  a.inject = plan->inject;
   for (int r = 0; r <= pda::kMaxQLen; ++r) a.hpc[r] = plan->heads_per_cta[r];
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int rc = PDA_OK;
@@ -386,7 +412,13 @@ extern "C" int pda_get_status(const pda_plan_t* plan, const void* split_scratch,
                               uint32_t* host_bits, pda_stream_t stream) {
   if (!plan || !host_bits) return PDA_ERR_NULL;
   if (plan->magic != PDA_PLAN_MAGIC) return PDA_ERR_PLAN;
-  if (!split_scratch) return PDA_ERR_SCRATCH;
+  void* fixed = nullptr;
+  if (!split_scratch) {  // the built-in array of pda_decode_static
+    const int rc =
+        pda::static_scratch(plan->device, reinterpret_cast<cudaStream_t>(stream), &fixed);
+    if (rc != PDA_OK) return rc;
+    split_scratch = fixed;
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemcpyAsync(host_bits, split_scratch, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) !=
           cudaSuccess ||
@@ -400,7 +432,11 @@ extern "C" int pda_get_status(const pda_plan_t* plan, const void* split_scratch,
 extern "C" int pda_reset_status(const pda_plan_t* plan, void* split_scratch, pda_stream_t stream) {
   if (!plan) return PDA_ERR_NULL;
   if (plan->magic != PDA_PLAN_MAGIC) return PDA_ERR_PLAN;
-  if (!split_scratch) return PDA_ERR_SCRATCH;
+  if (!split_scratch) {  // the built-in array of pda_decode_static
+    const int rc = pda::static_scratch(plan->device, reinterpret_cast<cudaStream_t>(stream),
+                                       &split_scratch);
+    if (rc != PDA_OK) return rc;
+  }
   if (cudaMemsetAsync(split_scratch, 0, sizeof(uint32_t),
                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
     cudaGetLastError();

@@ -264,19 +264,22 @@ __device__ __forceinline__ uint64_t global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s of wall time per wait
-// Bounded wait: false if another role aborted or the limit ran out (which
-// records PDA_STATUS_WAIT_TIMEOUT and aborts the CTA).
+// Bound of a drain (a wait for copies already issued) and the default bound
+// of every other pipeline wait: 2 s of wall time.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Bounded wait: false if another role aborted or the call's wait limit
+// (a.wait_limit_ns) ran out, which records PDA_STATUS_WAIT_TIMEOUT and
+// aborts the CTA.
 __device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag,
-                                         uint32_t* status) {
+                                         const DecodeArgs& a) {
   if (bar_try(b, parity)) return true;
   const uint64_t t0 = global_ns();
   for (;;) {
     if (bar_try_sleep(b, parity, 20000u)) return true;
     if (*abort_flag) return false;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > a.wait_limit_ns) {
       *abort_flag = 1;
-      atomicOr(status, PDA_STATUS_WAIT_TIMEOUT);
+      atomicOr(a.status, PDA_STATUS_WAIT_TIMEOUT);
       return false;
     }
   }
@@ -616,7 +619,7 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
     // past M then hold finite values that are never written out)
     const bool full = tile0 >= all_lo && tile0 + kTok - 1 <= all_hi;
 
-    if (alive) alive = bar_wait(x.s_full + (j & 1), (j >> 1) & 1, x.abort_flag, a.status);
+    if (alive) alive = bar_wait(x.s_full + (j & 1), (j >> 1) & 1, x.abort_flag, a);
     alive = __all_sync(0xffffffffu, alive);
     fence_after();
     float s[NH];
@@ -726,7 +729,7 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
     {
       const int need = fired ? j - 1 : j - C::kPBufs;
       if (need >= 0)
-        alive = bar_wait(x.pv_done + (need & 1), (need >> 1) & 1, x.abort_flag, a.status);
+        alive = bar_wait(x.pv_done + (need & 1), (need >> 1) & 1, x.abort_flag, a);
     }
     alive = __all_sync(0xffffffffu, alive);
     fence_after();
@@ -756,7 +759,7 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
       const uint32_t gv = chunk_pos_v<C::kChunks, C::kChunksV>(j, x.ntiles);
       for (int c = 0; c < C::kChunksV && alive; ++c) {
         const uint32_t slot = (gv + c) % R_;
-        alive = bar_wait(x.full + slot, ((gv + c) / R_) & 1u, x.abort_flag, a.status);
+        alive = bar_wait(x.full + slot, ((gv + c) / R_) & 1u, x.abort_flag, a);
         uint4* row = reinterpret_cast<uint4*>(x.ring + slot * kSlot + r * 128);
 #pragma unroll
         for (int e = 0; e < 8; ++e) row[e] = make_uint4(0, 0, 0, 0);
@@ -811,7 +814,7 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
   // ---------------------------------------------------------- epilogue
   if (alive && x.ntiles > 0)
     alive = bar_wait(x.pv_done + ((x.ntiles - 1) & 1), ((x.ntiles - 1) >> 1) & 1, x.abort_flag,
-                     a.status);
+                     a);
   fence_after();
   if (group_or<NT>(!alive)) return;
   // column sums of the per-token partial denominators
@@ -943,9 +946,9 @@ __device__ __forceinline__ void mla_convert(const DecodeArgs& a, int ntiles, int
     for (int c = 0; c < nraw; ++c, ++gw) {
       const uint32_t is = gw % C::kIRing;
       const uint32_t c0 = 2 * gw, d0 = c0 % R_, d1 = (c0 + 1) % R_;
-      bool ok = bar_wait(i_full + is, (gw / C::kIRing) & 1u, abort_flag, a.status);
-      if (ok) ok = bar_wait(empty + d0, ((c0 / R_) & 1u) ^ 1u, abort_flag, a.status);
-      if (ok) ok = bar_wait(empty + d1, (((c0 + 1) / R_) & 1u) ^ 1u, abort_flag, a.status);
+      bool ok = bar_wait(i_full + is, (gw / C::kIRing) & 1u, abort_flag, a);
+      if (ok) ok = bar_wait(empty + d0, ((c0 / R_) & 1u) ^ 1u, abort_flag, a);
+      if (ok) ok = bar_wait(empty + d1, (((c0 + 1) / R_) & 1u) ^ 1u, abort_flag, a);
       if (!__all_sync(0xffffffffu, ok)) return;
       const uint8_t* src = iring + is * kSlot;
       const bool rope = kind == 0 && c == 4;
@@ -1268,7 +1271,7 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
         const uint32_t slot = g % kIR, round = g / kIR;
         int good = 1;
         if (lane == 0) {
-          good = bar_wait(i_empty + slot, (round & 1u) ^ 1u, abort_flag, a.status);
+          good = bar_wait(i_empty + slot, (round & 1u) ^ 1u, abort_flag, a);
           if (good) bar_expect_tx(i_full + slot, nvalid * box_bytes);
         }
         good = __shfl_sync(0xffffffffu, good, 0);
@@ -1302,7 +1305,7 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
         const bool pad = kind == 0 && c >= C::kChunksQK;  // an even-size unit's empty slot
         int good = 1;
         if (lane == 0) {
-          good = bar_wait(empty + slot, (round & 1u) ^ 1u, abort_flag, a.status);
+          good = bar_wait(empty + slot, (round & 1u) ^ 1u, abort_flag, a);
           if (good) bar_expect_tx(full + slot, pad ? 0u : nvalid * box_bytes);
         }
         good = __shfl_sync(0xffffffffu, good, 0);
@@ -1318,9 +1321,14 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
         }
       }
     };
-    emit(0, ok0, pg0, s00);
-    if (ntiles > 1) emit(0, ok1, pg1, s01);
-    for (int j = 0; j < ntiles && alive; ++j) {
+    // PDA_INJECT_WITHHOLD_KV (a host-set test hook): issue nothing at all,
+    // so that the consumers' first waits run out with nothing in flight
+    const bool withhold = (a.inject & PDA_INJECT_WITHHOLD_KV) != 0u;
+    if (!withhold) {
+      emit(0, ok0, pg0, s00);
+      if (ntiles > 1) emit(0, ok1, pg1, s01);
+    }
+    for (int j = 0; j < ntiles && alive && !withhold; ++j) {
       if (j + 2 < ntiles) {
         ok2 = checked(ok2, pg2);
         emit(0, ok2, pg2, s02);                     // K_{j+2}
@@ -1347,7 +1355,7 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
   } else if (warp == 1) {
     // ===================================================== MMA issuer warp
     if (lane == 0) {
-      bool alive = bar_wait(q_ready, 0, abort_flag, a.status);
+      bool alive = bar_wait(q_ready, 0, abort_flag, a);
       fence_after();
       const uint32_t fmt = kF8 || C::kF16Ops ? 0u : 1u;  // E4M3, f16 (converted caches) or bf16
       const uint32_t id_s = idesc(fmt, 0, static_cast<uint32_t>(Nq));
@@ -1357,12 +1365,12 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
       // S^T of tile j into TMEM buffer j & 1 (the softmax has freed it)
       auto issue_s = [&](int j) -> bool {
         const int sb = j & 1;
-        if (j >= 2 && !bar_wait(s_free + sb, ((j >> 1) - 1) & 1, abort_flag, a.status)) return false;
+        if (j >= 2 && !bar_wait(s_free + sb, ((j >> 1) - 1) & 1, abort_flag, a)) return false;
         fence_after();
         const uint32_t gk = chunk_pos_k<C::kChunks, C::kChunksV>(j);
         for (int c = 0; c < C::kChunks; ++c) {
           const uint32_t slot = (gk + c) % R_;
-          if (!bar_wait(full + slot, ((gk + c) / R_) & 1u, abort_flag, a.status)) return false;
+          if (!bar_wait(full + slot, ((gk + c) / R_) & 1u, abort_flag, a)) return false;
           fence_after();
           const uint32_t abase = ring_addr + slot * kSlot;
           const uint32_t bbase = q_addr + c * C::kQAtomBytes;
@@ -1379,14 +1387,14 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
       };
       // O^T += V_j^T P_j^T as soon as the softmax has written P_j
       auto issue_pv = [&](int j) -> bool {
-        if (!bar_wait(p_full + (j & 1), (j >> 1) & 1, abort_flag, a.status)) return false;
+        if (!bar_wait(p_full + (j & 1), (j >> 1) & 1, abort_flag, a)) return false;
         const uint32_t gv = chunk_pos_v<C::kChunks, C::kChunksV>(j, ntiles);
         constexpr int kBlkSlots = kF8 ? 1 : 2;  // ring slots of one 128-d V block
         const uint32_t pbuf = p_addr + static_cast<uint32_t>(j % C::kPBufs) * C::kPBufBytes;
 #pragma unroll
         for (int blk = 0; blk < C::kOBlocks; ++blk) {
           for (int c = blk * kBlkSlots; c < (blk + 1) * kBlkSlots; ++c)
-            if (!bar_wait(full + (gv + c) % R_, ((gv + c) / R_) & 1u, abort_flag, a.status))
+            if (!bar_wait(full + (gv + c) % R_, ((gv + c) / R_) & 1u, abort_flag, a))
               return false;
           fence_after();
           if constexpr (kF8) {
@@ -1436,9 +1444,9 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
       for (uint32_t gw = 0; gw < total; ++gw) {
         const uint32_t is = gw % C::kIRing;
         const uint32_t c0 = 2 * gw, d0 = c0 % R_, d1 = (c0 + 1) % R_;
-        bool ok = bar_wait(i_full + is, (gw / C::kIRing) & 1u, abort_flag, a.status);
-        if (ok) ok = bar_wait(empty + d0, ((c0 / R_) & 1u) ^ 1u, abort_flag, a.status);
-        if (ok) ok = bar_wait(empty + d1, (((c0 + 1) / R_) & 1u) ^ 1u, abort_flag, a.status);
+        bool ok = bar_wait(i_full + is, (gw / C::kIRing) & 1u, abort_flag, a);
+        if (ok) ok = bar_wait(empty + d0, ((c0 / R_) & 1u) ^ 1u, abort_flag, a);
+        if (ok) ok = bar_wait(empty + d1, (((c0 + 1) / R_) & 1u) ^ 1u, abort_flag, a);
         if (!__all_sync(0xffffffffu, ok)) break;
         const uint8_t* src = iring + is * kSlot;
         for (int idx = ct; idx < kTok * 8; idx += C::kConvThreads) {

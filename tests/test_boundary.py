@@ -198,6 +198,8 @@ def test_plan_int8(lib):
     (dict(kv_stride_head=260), B.PDA_ERR_ALIGNMENT),   # 520 B: not a multiple of 16
     (dict(batch=17), B.PDA_ERR_INVALID),
     (dict(max_kv_len=0), B.PDA_ERR_INVALID),
+    (dict(wait_limit_us=-1), B.PDA_ERR_INVALID),
+    (dict(inject=0x80), B.PDA_ERR_INVALID),            # an unknown test hook
 ])
 def test_plan_rejects(lib, bad, code):
     _, _, rc = B.pda_plan(_params(**bad), check=False)

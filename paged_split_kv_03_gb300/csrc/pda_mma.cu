@@ -554,8 +554,11 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_mma(const __grid_constant_
 // q head) ("Stage 2 merges per row"). A warp owns a slice of 32 x VW
 // consecutive floats of the row (VW = 4, or 2 at head_dim 64), so each
 // partial is one coalesced vector load per lane; WPI warps per slice share
-// the row's splits (WPI grows with the split count), each keeping eight
-// partials in flight, and combine through shared memory.
+// the row's splits. Each warp merges its own splits online -- a running
+// maximum of their LSEs, its sums rescaled when the maximum rises -- with all
+// of a batch's loads (LSE and partial output) in flight at once, so a warp
+// with at most kBatch splits waits for one round of loads; the WPI warps then
+// combine their (maximum, sum, output) triples through shared memory.
 template <int D, int WPI>
 struct MergeCfg {
   static constexpr int kVW = D >= 128 ? 4 : 2;                  // floats per lane
@@ -563,7 +566,7 @@ struct MergeCfg {
   static constexpr int kWarpsPerItem = kSlices * WPI;           // <= 32
   static constexpr int kItems = kWarpsPerItem >= 8 ? 1 : 8 / kWarpsPerItem;  // rows per CTA
   static constexpr int kThreads = kItems * kWarpsPerItem * 32;
-  static constexpr int kBatch = 8;                              // partials in flight
+  static constexpr int kBatch = 12;                             // partials in flight
 };
 
 template <int D, int WPI>
@@ -572,7 +575,8 @@ __global__ void __launch_bounds__(MergeCfg<D, WPI>::kThreads)
   using M = MergeCfg<D, WPI>;
   constexpr int kVW = M::kVW;
   __shared__ __align__(16) float sh_acc[M::kThreads / 32][32 * kVW];
-  __shared__ float sh_w[M::kThreads / 32];
+  __shared__ float sh_m[M::kThreads / 32];
+  __shared__ float sh_l[M::kThreads / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wi = warp % M::kWarpsPerItem;
   const int slice = wi % M::kSlices, sub = wi / M::kSlices;
@@ -588,76 +592,96 @@ __global__ void __launch_bounds__(MergeCfg<D, WPI>::kThreads)
     const int q0 = a.qo_indptr[b];
     const int R = a.qo_indptr[b + 1] - q0;
     const int L = a.kv_len[b];
+    const int W = a.window ? a.window[b] : 0;
     if (i < R && R <= a.max_q_len && L >= R && L <= a.max_kv_len && q0 + R <= a.rows_cap) {
-      const int W = a.window ? a.window[b] : 0;
       const SplitRange sr = split_range(L, R, W, a.page_size, chunk_for(a, b));
       n = sr.num_splits;
       valid = n > 1;  // one split: stage 1 wrote the final result
       base = (int64_t)(q0 + i) * a.hq + head;
     }
   }
+  // everything above overlaps stage 1's tail; its partials are read below
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
   const int64_t stride = a.rows_cap * a.hq;  // partial rows per split
   const int col = slice * 32 * kVW + lane * kVW;
-  float mx = -INFINITY;
+  float m = -INFINITY, l = 0.f;  // running maximum (log2) and sum of this warp's splits
   float acc[kVW];
 #pragma unroll
   for (int e = 0; e < kVW; ++e) acc[e] = 0.f;
-  float wsum = 0.f;
   if (valid) {
-    for (int s = lane; s < n; s += 32) mx = fmaxf(mx, a.part_lse[s * stride + base]);
+    for (int s0 = sub; s0 < n; s0 += M::kBatch * WPI) {
+      float ls[M::kBatch];
+      float x[M::kBatch][kVW];
+      // issue the batch's loads first, then combine
 #pragma unroll
-    for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (mx != -INFINITY) {
-      for (int s0 = sub; s0 < n; s0 += M::kBatch * WPI) {
-        float ls[M::kBatch];
-        float x[M::kBatch][kVW];
-        // issue the batch's loads first, then combine
+      for (int u = 0; u < M::kBatch; ++u) {
+        const int s = s0 + u * WPI;
+        ls[u] = -INFINITY;
 #pragma unroll
-        for (int u = 0; u < M::kBatch; ++u) {
-          const int s = s0 + u * WPI;
-          ls[u] = -INFINITY;
-#pragma unroll
-          for (int e = 0; e < kVW; ++e) x[u][e] = 0.f;
-          if (s < n) {
-            ls[u] = a.part_lse[s * stride + base];
-            const float* src = a.part_o + (s * stride + base) * D + col;
-            if constexpr (kVW == 4) {
-              const float4 v = *reinterpret_cast<const float4*>(src);
-              x[u][0] = v.x; x[u][1] = v.y; x[u][2] = v.z; x[u][3] = v.w;
-            } else {
-              const float2 v = *reinterpret_cast<const float2*>(src);
-              x[u][0] = v.x; x[u][1] = v.y;
-            }
+        for (int e = 0; e < kVW; ++e) x[u][e] = 0.f;
+        if (s < n) {
+          ls[u] = a.part_lse[s * stride + base];
+          const float* src = a.part_o + (s * stride + base) * D + col;
+          if constexpr (kVW == 4) {
+            const float4 v = *reinterpret_cast<const float4*>(src);
+            x[u][0] = v.x; x[u][1] = v.y; x[u][2] = v.z; x[u][3] = v.w;
+          } else {
+            const float2 v = *reinterpret_cast<const float2*>(src);
+            x[u][0] = v.x; x[u][1] = v.y;
           }
         }
+      }
+      float bm = m;
 #pragma unroll
-        for (int u = 0; u < M::kBatch; ++u) {
-          const float w = ls[u] == -INFINITY ? 0.f : exp2f(ls[u] - mx);
-          wsum += w;
-          // an empty split's partial may hold anything: select, do not scale
+      for (int u = 0; u < M::kBatch; ++u) bm = fmaxf(bm, ls[u]);
+      if (bm > m) {  // the maximum rose: rescale what this warp has summed
+        const float f = exp2f(m - bm);  // m = -inf: nothing summed yet, f = 0
+        l *= f;
 #pragma unroll
-          for (int e = 0; e < kVW; ++e) acc[e] = w > 0.f ? fmaf(w, x[u][e], acc[e]) : acc[e];
-        }
+        for (int e = 0; e < kVW; ++e) acc[e] *= f;
+        m = bm;
+      }
+#pragma unroll
+      for (int u = 0; u < M::kBatch; ++u) {
+        const float w = ls[u] == -INFINITY ? 0.f : exp2f(ls[u] - m);
+        l += w;
+        // an empty split's partial may hold anything: select, do not scale
+#pragma unroll
+        for (int e = 0; e < kVW; ++e) acc[e] = w > 0.f ? fmaf(w, x[u][e], acc[e]) : acc[e];
       }
     }
   }
   if constexpr (WPI > 1) {
 #pragma unroll
     for (int e = 0; e < kVW; ++e) sh_acc[warp][lane * kVW + e] = acc[e];
-    if (lane == 0) sh_w[warp] = wsum;
+    if (lane == 0) {
+      sh_m[warp] = m;
+      sh_l[warp] = l;
+    }
     __syncthreads();
     if (sub == 0) {
-      for (int k = 1; k < WPI; ++k) {
-        const int w2 = warp + k * M::kSlices;  // same slice, split group k
+      float mx = m;
+      for (int k = 1; k < WPI; ++k) mx = fmaxf(mx, sh_m[warp + k * M::kSlices]);
+      if (mx != -INFINITY) {
+        const float f0 = exp2f(m - mx);
+        l *= f0;
 #pragma unroll
-        for (int e = 0; e < kVW; ++e) acc[e] += sh_acc[w2][lane * kVW + e];
-        wsum += sh_w[w2];
+        for (int e = 0; e < kVW; ++e) acc[e] *= f0;
+        for (int k = 1; k < WPI; ++k) {
+          const int w2 = warp + k * M::kSlices;  // same slice, split group k
+          const float mk = sh_m[w2];
+          if (mk == -INFINITY) continue;
+          const float f = exp2f(mk - mx);
+          l = fmaf(f, sh_l[w2], l);
+#pragma unroll
+          for (int e = 0; e < kVW; ++e) acc[e] = fmaf(f, sh_acc[w2][lane * kVW + e], acc[e]);
+        }
       }
+      m = mx;
     }
   }
   if (!valid || sub != 0) return;
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  const float inv = l > 0.f ? 1.f / l : 0.f;
   __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + base * D + col;
   if constexpr (kVW == 4) {
     __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
@@ -670,7 +694,7 @@ __global__ void __launch_bounds__(MergeCfg<D, WPI>::kThreads)
     *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
   }
   if (slice == 0 && lane == 0 && a.lse)
-    a.lse[base] = wsum > 0.f ? (mx + __log2f(wsum)) * kLn2 : -INFINITY;
+    a.lse[base] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
 }
 
 // ---------------------------------------------------------------- dispatch
@@ -715,10 +739,13 @@ KernelFn stage1_for(const pda_plan_t* p) {
   }
 }
 
-// Warps per slice of a merged row: one up to 8 splits, then up to 8 splits
-// a warp, with at most 16 warps per row (head_dim 512: 4 slices x 4).
+// Warps per slice of a merged row: one up to 12 splits, then up to 12
+// splits a warp (one round of loads each), with at most 16 warps per row
+// (head_dim 512: 4 slices x 4), so that a CTA of 512 threads keeps its
+// batch of partials in registers.
 static int stage2_wpi(const pda_plan_t* p) {
-  const int w = p->max_splits <= 8 ? 1 : p->max_splits <= 16 ? 2 : p->max_splits <= 32 ? 4 : 8;
+  const int s = p->max_splits;
+  const int w = s <= 12 ? 1 : s <= 24 ? 2 : s <= 48 ? 4 : 8;
   return p->head_dim_v == 512 && w > 4 ? 4 : w;
 }
 struct Stage2Launch {

@@ -1045,9 +1045,13 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
   WorkItem wi;
   if (!work_item(a, blockIdx.x, wi)) return;
   const int hb = wi.hb, split = wi.split, hkv = wi.hkv, b = wi.b;
+  // the request's scalars, loaded together (one round trip)
   const int q0 = a.qo_indptr[b];
-  const int R = a.qo_indptr[b + 1] - q0;
+  const int q1 = a.qo_indptr[b + 1];
   const int L = a.kv_len[b];
+  const int W = a.window ? a.window[b] : 0;
+  const int kv0 = a.kv_indptr[b];
+  const int R = q1 - q0;
   if (R <= 0 || R > a.max_q_len || L < R || L > a.max_kv_len || q0 + R > a.rows_cap) {
     if (tid == 0 && split == 0 && hb == 0 && hkv == 0) {
       uint32_t bits = 0;
@@ -1061,7 +1065,6 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
   }
   const int hpc = a.hpc[R];
   if (hb >= a.group / hpc) return;
-  const int W = a.window ? a.window[b] : 0;
   const int P = a.page_size;
   const SplitRange sr = split_range(L, R, W, P, chunk_for(a, b));
   if (split >= sr.num_splits) return;
@@ -1075,43 +1078,13 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
   const int N = (M + 15) & ~15;   // MMA N of PV (and of each Q term)
   const int Nq = N * C::kQTerms;  // MMA N of S^T
   const int head0 = hkv * a.group + hb * hpc;
-  const int32_t* ptab = a.page_table + a.kv_indptr[b];
+  const int32_t* ptab = a.page_table + kv0;
 
-  // ---- setup: barriers, TMEM, running maxima
-  if (tid == 0) {
-    for (int s = 0; s < R_; ++s) {
-      // TMA: one arrive.expect_tx per producer warp; int8: every converter
-      // thread arrives after widening its share into the slot
-      bar_init(full + s, C::kConv ? C::kConvThreads : C::kProducers);
-      bar_init(empty + s, 1);
-    }
-    for (int s = 0; s < C::kIRing; ++s) {
-      bar_init(i_full + s, C::kProducers);
-      bar_init(i_empty + s, C::kConvThreads);
-    }
-    bar_init(s_full, 1);
-    bar_init(s_full + 1, 1);
-    bar_init(s_free, C::kSmThreads);
-    bar_init(s_free + 1, C::kSmThreads);
-    bar_init(p_full, C::kSmThreads);
-    bar_init(p_full + 1, C::kSmThreads);
-    bar_init(pv_done, 1);
-    bar_init(pv_done + 1, 1);
-    bar_init(q_ready, C::kSmThreads);
-    bar_init(drain, 1);
-    *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     su32(tmem_slot)),
-                 "r"(C::kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  // Before the CTA-wide sync, so that their latency overlaps the setup:
-  // producer warps prefetch the tensor maps and load the first page ids;
-  // softmax warps reset the running maxima and build the query tile.
+  // ---- setup. The producer warps load the first page ids, then (once
+  // warp 0 has initialised the barriers) start the first ring fill without
+  // waiting for the rest of the CTA; the MMA warp allocates TMEM and the
+  // softmax warps build the query tile meanwhile. Named barrier 7 is the
+  // CTA's setup barrier: producers only arrive on it, the others wait.
   const bool producer = warp == 0 || (warp >= C::kProdWarp1 && warp < C::kProdWarp1 + C::kProducers - 1);
   const int pw = warp == 0 ? 0 : warp - C::kProdWarp1 + 1;  // producer index
   const int box_rows = P < kTok ? P : kTok;
@@ -1141,109 +1114,185 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
     ok1 = page_of(1, pg1, s01);
     ok2 = page_of(2, pg2, s02);
     ok3 = page_of(3, pg3, s03);
-  } else if (warp >= 2 && warp < 2 + C::kSmWarps) {
-    const int st = tid - 64;  // 0..kSmThreads-1
-    const int sw = warp - 2;  // softmax warp index
-    if (st < C::kNmax) {
-      m_used[st] = kMInit;
-      colscale[st] = 1.f;
+  }
+  if (tid == 0) {
+    for (int s = 0; s < R_; ++s) {
+      // TMA: one arrive.expect_tx per producer warp; int8: every converter
+      // thread arrives after widening its share into the slot
+      bar_init(full + s, C::kConv ? C::kConvThreads : C::kProducers);
+      bar_init(empty + s, 1);
     }
-    // ---- query operand Q^T (K-major, 128-byte swizzle), rows n < N (zero past M)
-    if constexpr (!C::kQSplit) {
-      constexpr int kRowChunks = D * C::kElt / 16;  // 16-byte pieces of one query row
-      constexpr int kPadChunks = C::kChunksQK * 8;  // ... of its smem rows (MLA E4M3: zeros past D)
-      for (int idx = st; idx < N * kPadChunks; idx += C::kSmThreads) {
-        const int n = idx / kPadChunks, cch = idx % kPadChunks;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (n < M && cch < kRowChunks) {
-          const uint8_t* src = static_cast<const uint8_t*>(a.q) +
-                               (((int64_t)(q0 + n / hpc) * a.hq + head0 + n % hpc) * D) * C::kElt +
-                               cch * 16;
-          v = __ldg(reinterpret_cast<const uint4*>(src));
-          if constexpr (C::kF16Ops) v = bf16x8_to_f16x8(v);  // f16 operands (converted caches)
-        }
-        const int byte = cch * 16;
-        *reinterpret_cast<uint4*>(q_s + (byte / 128) * C::kQAtomBytes + sw128(n, byte % 128)) = v;
-      }
+    for (int s = 0; s < C::kIRing; ++s) {
+      bar_init(i_full + s, C::kProducers);
+      bar_init(i_empty + s, C::kConvThreads);
+    }
+    bar_init(s_full, 1);
+    bar_init(s_full + 1, 1);
+    bar_init(s_free, C::kSmThreads);
+    bar_init(s_free + 1, C::kSmThreads);
+    bar_init(p_full, C::kSmThreads);
+    bar_init(p_full + 1, C::kSmThreads);
+    bar_init(pv_done, 1);
+    bar_init(pv_done + 1, 1);
+    bar_init(q_ready, C::kSmThreads);
+    bar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (producer) {
+    __syncwarp();  // warp 0 reconverges after the barrier setup
+    // the other producer warps may use the barriers once warp 0 has made them
+    if constexpr (C::kProducers > 1) {
+      if (warp == 0)
+        asm volatile("bar.arrive 6, %0;" ::"n"(C::kProdThreads) : "memory");
+      else
+        asm volatile("bar.sync 6, %0;" ::"n"(C::kProdThreads) : "memory");
     } else {
-      // bf16 query -> Q * 2^a = Q1 + Q2/16 in E4M3 (rows n and N + n), with
-      // one exponent a for the CTA, from its largest |Q|
-      constexpr int kPer = D / 32;  // elements per lane (16, 8 or 4)
-      auto load_row = [&](int n, float* xv) {
-        if (n < M) {
-          const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(a.q) +
-                                     ((int64_t)(q0 + n / hpc) * a.hq + head0 + n % hpc) * D +
-                                     lane * kPer;
-#pragma unroll
-          for (int e = 0; e < kPer; ++e) xv[e] = __bfloat162float(src[e]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < kPer; ++e) xv[e] = 0.f;
-        }
-      };
-      float amax = 0.f;
-      for (int n = sw; n < M; n += C::kSmWarps) {
-        float xv[kPer];
-        load_row(n, xv);
-#pragma unroll
-        for (int e = 0; e < kPer; ++e) amax = fmaxf(amax, fabsf(xv[e]));
+      __syncwarp();
+    }
+    asm volatile("bar.arrive 7, %0;" ::"n"(C::kThreads) : "memory");
+  } else {
+    if (warp == 1) {  // the MMA warp owns the TMEM allocation
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       su32(tmem_slot)),
+                   "r"(C::kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    } else if (warp >= 2 && warp < 2 + C::kSmWarps) {
+      const int st = tid - 64;  // 0..kSmThreads-1
+      const int sw = warp - 2;  // softmax warp index
+      if (st < C::kNmax) {
+        m_used[st] = kMInit;
+        colscale[st] = 1.f;
       }
+      // ---- query operand Q^T (K-major, 128-byte swizzle), rows n < N (zero
+      // past M); every load is issued before the first store, so the tile
+      // costs one round trip to memory
+      if constexpr (!C::kQSplit) {
+        constexpr int kRowChunks = D * C::kElt / 16;  // 16-byte pieces of one query row
+        constexpr int kPadChunks = C::kChunksQK * 8;  // ... of its smem rows (MLA E4M3: zeros past D)
+        constexpr int kIters = (C::kNmax * kPadChunks + C::kSmThreads - 1) / C::kSmThreads;
+        uint4 qv[kIters];
 #pragma unroll
-      for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      if (lane == 0) red[sw] = amax;
-      group_sync<C::kSmThreads>();
-      amax = 0.f;
-      for (int w = 0; w < C::kSmWarps; ++w) amax = fmaxf(amax, red[w]);
-      int ex = 0;
-      if (amax > 0.f) ex = static_cast<int>(floorf(__log2f(448.f / amax)));
-      ex = ex > 126 ? 126 : ex;
-      // keep the scaled maximum inside E4M3's finite range despite log2 rounding
-      while (ex > -126 && amax * exp2f(static_cast<float>(ex)) > 448.f) --ex;
-      const float up = exp2f(static_cast<float>(ex));
-      if (st == 0) colscale[0] = 1.f / up;
-      for (int n = sw; n < N; n += C::kSmWarps) {
-        float xv[kPer];
-        load_row(n, xv);
-        uint8_t codes[2][kPer];
+        for (int it = 0; it < kIters; ++it) {
+          const int idx = st + it * C::kSmThreads;
+          const int n = idx / kPadChunks, cch = idx % kPadChunks;
+          qv[it] = make_uint4(0, 0, 0, 0);
+          if (n < M && cch < kRowChunks)
+            qv[it] = __ldg(reinterpret_cast<const uint4*>(
+                static_cast<const uint8_t*>(a.q) +
+                (((int64_t)(q0 + n / hpc) * a.hq + head0 + n % hpc) * D) * C::kElt + cch * 16));
+        }
 #pragma unroll
-        for (int e = 0; e < kPer; e += 2) {
-          float v0 = xv[e] * up, v1 = xv[e + 1] * up;
+        for (int it = 0; it < kIters; ++it) {
+          const int idx = st + it * C::kSmThreads;
+          const int n = idx / kPadChunks, cch = idx % kPadChunks;
+          if (n < N) {
+            uint4 v = qv[it];
+            if constexpr (C::kF16Ops) v = bf16x8_to_f16x8(v);  // f16 operands (converted caches)
+            const int byte = cch * 16;
+            *reinterpret_cast<uint4*>(q_s + (byte / 128) * C::kQAtomBytes + sw128(n, byte % 128)) = v;
+          }
+        }
+      } else {
+        // bf16 query -> Q * 2^a = Q1 + Q2/16 in E4M3 (rows n and N + n), with
+        // one exponent a for the CTA, from its largest |Q|. A lane holds kPer
+        // elements of each of its warp's rows (n = sw + k * kSmWarps).
+        constexpr int kPer = D / 32;  // elements per lane (16, 8 or 4)
+        constexpr int kRowsW = C::kNmax / C::kSmWarps;
+        uint32_t raw[kRowsW][kPer / 2];  // bf16 pairs, low half first
+#pragma unroll
+        for (int k = 0; k < kRowsW; ++k) {
+          const int n = sw + k * C::kSmWarps;
+#pragma unroll
+          for (int e = 0; e < kPer / 2; ++e) raw[k][e] = 0u;
+          if (n < M) {
+            const uint8_t* src = static_cast<const uint8_t*>(a.q) +
+                                 (((int64_t)(q0 + n / hpc) * a.hq + head0 + n % hpc) * D +
+                                  lane * kPer) * 2;
+            if constexpr (kPer >= 8) {
+#pragma unroll
+              for (int v4 = 0; v4 < kPer / 8; ++v4) {
+                const uint4 w = __ldg(reinterpret_cast<const uint4*>(src) + v4);
+                raw[k][4 * v4] = w.x;
+                raw[k][4 * v4 + 1] = w.y;
+                raw[k][4 * v4 + 2] = w.z;
+                raw[k][4 * v4 + 3] = w.w;
+              }
+            } else {
+              const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
+              raw[k][0] = w.x;
+              raw[k][1] = w.y;
+            }
+          }
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int k = 0; k < kRowsW; ++k)
+#pragma unroll
+          for (int e = 0; e < kPer / 2; ++e)
+            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(raw[k][e] << 16)),
+                                     fabsf(__uint_as_float(raw[k][e] & 0xFFFF0000u))));
+#pragma unroll
+        for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        if (lane == 0) red[sw] = amax;
+        group_sync<C::kSmThreads>();
+        amax = 0.f;
+        for (int w = 0; w < C::kSmWarps; ++w) amax = fmaxf(amax, red[w]);
+        int ex = 0;
+        if (amax > 0.f) ex = static_cast<int>(floorf(__log2f(448.f / amax)));
+        ex = ex > 126 ? 126 : ex;
+        // keep the scaled maximum inside E4M3's finite range despite log2 rounding
+        while (ex > -126 && amax * exp2f(static_cast<float>(ex)) > 448.f) --ex;
+        const float up = exp2f(static_cast<float>(ex));
+        if (st == 0) colscale[0] = 1.f / up;
+#pragma unroll
+        for (int k = 0; k < kRowsW; ++k) {
+          const int n = sw + k * C::kSmWarps;
+          if (n >= N) continue;
+          uint8_t codes[2][kPer];
+#pragma unroll
+          for (int e = 0; e < kPer; e += 2) {
+            float v0 = __uint_as_float(raw[k][e / 2] << 16) * up;
+            float v1 = __uint_as_float(raw[k][e / 2] & 0xFFFF0000u) * up;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const uint16_t c2 = f2_to_e4m3x2(v0, v1);
+              const float2 back = e4m3x2_to_f2(c2);
+              codes[t][e] = static_cast<uint8_t>(c2 & 0xFF);
+              codes[t][e + 1] = static_cast<uint8_t>(c2 >> 8);
+              v0 = (v0 - back.x) * 16.f;
+              v1 = (v1 - back.y) * 16.f;
+            }
+          }
+          const int byte = lane * kPer;  // d of this lane's first element (1 byte each)
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
-            const uint16_t c2 = f2_to_e4m3x2(v0, v1);
-            const float2 back = e4m3x2_to_f2(c2);
-            codes[t][e] = static_cast<uint8_t>(c2 & 0xFF);
-            codes[t][e + 1] = static_cast<uint8_t>(c2 >> 8);
-            v0 = (v0 - back.x) * 16.f;
-            v1 = (v1 - back.y) * 16.f;
-          }
-        }
-        const int byte = lane * kPer;  // d of this lane's first element (1 byte each)
+            uint8_t* dst = q_s + (byte / 128) * C::kQAtomBytes + sw128(t * N + n, byte % 128);
+            uint32_t w[kPer / 4];
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          uint8_t* dst = q_s + (byte / 128) * C::kQAtomBytes + sw128(t * N + n, byte % 128);
-          uint32_t w[kPer / 4];
-#pragma unroll
-          for (int e = 0; e < kPer / 4; ++e)
-            w[e] = codes[t][4 * e] | (codes[t][4 * e + 1] << 8) | (codes[t][4 * e + 2] << 16) |
-                   ((uint32_t)codes[t][4 * e + 3] << 24);
-          if constexpr (kPer == 16) {
-            *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-          } else if constexpr (kPer == 8) {
-            *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
-          } else {
-            *reinterpret_cast<uint32_t*>(dst) = w[0];
+            for (int e = 0; e < kPer / 4; ++e)
+              w[e] = codes[t][4 * e] | (codes[t][4 * e + 1] << 8) | (codes[t][4 * e + 2] << 16) |
+                     ((uint32_t)codes[t][4 * e + 3] << 24);
+            if constexpr (kPer == 16) {
+              *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+            } else if constexpr (kPer == 8) {
+              *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+            } else {
+              *reinterpret_cast<uint32_t*>(dst) = w[0];
+            }
           }
         }
       }
+      fence_async_smem();
+      group_sync<C::kSmThreads>();  // the query scale visible to the whole group
     }
-    fence_async_smem();
-    group_sync<C::kSmThreads>();  // the query scale visible to the whole group
+    fence_before();
+    asm volatile("bar.sync 7, %0;" ::"n"(C::kThreads) : "memory");
+    fence_after();
   }
-  fence_before();
-  __syncthreads();
-  fence_after();
-  const uint32_t tmem = *tmem_slot;
+  // TMEM address (the MMA and softmax warps only; producers never use it)
+  const uint32_t tmem = producer ? 0u : *tmem_slot;
   const uint32_t tmem_o = tmem + 2 * C::kSCols;
 
   if (warp == 0 || (warp >= C::kProdWarp1 && warp < C::kProdWarp1 + C::kProducers - 1)) {
@@ -1528,7 +1577,7 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
   fence_before();
   __syncthreads();
   fence_after();
-  if (warp == 0)
+  if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(C::kTmemCols)
                  : "memory");

@@ -228,6 +228,24 @@ def append_time(name, kw, dev, steps, flush, peak):
             "bytes": nbytes, "status": status}
 
 
+def append_once(name, kw, dev):
+    """One eager pda_append_kv on the workload (a profiler's target)."""
+    import torch
+    from paged_split_kv_03_gb300 import binding as B
+    from paged_split_kv_03_gb300.synth import config_workload
+    wl = config_workload(name, device=dev, **kw)
+    dec = B.Decoder(B.params_for(wl, device=dev.index or 0), device=dev)
+    g = torch.Generator(device=dev).manual_seed(11)
+    shape = (wl.total_rows, wl.num_kv_heads, wl.head_dim)
+    k_new = torch.randn(shape, generator=g, device=dev).to(torch.bfloat16)
+    v_new = torch.randn(shape, generator=g, device=dev).to(torch.bfloat16)
+    B.pda_append_kv(dec.plan, k_new, v_new, wl.page_table, wl.kv_indptr, wl.kv_len, wl.qo_indptr,
+                    max(1, wl.max_q_len), wl.k_pages, wl.v_pages, wl.k_scale, wl.v_scale,
+                    dec.scratch)
+    torch.cuda.synchronize()
+    assert dec.status() == 0
+
+
 def time_graph(fn, steps, warmup, flush, stream):
     """Per-step CUDA-event times (ms) of ``fn`` replayed on ``stream``, with an
     L2 flush enqueued before every step outside the events."""
@@ -567,6 +585,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=4.0)
+    ap.add_argument("--profile-append", action="store_true",
+                    help="profiling aid: run one pda_append_kv of each append workload and "
+                         "exit (no timing, no JSON line)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -574,6 +595,11 @@ def main(argv=None):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.profile_append:
+        import torch
+        for name, kw in APPEND_SWEEP:
+            append_once(name, kw, torch.device("cuda", local))
+        return
     if args.impl == "reference":
         res = run_reference(args, rank, world)
     else:

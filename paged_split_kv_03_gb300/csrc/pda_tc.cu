@@ -839,6 +839,13 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
     }
   }
   group_sync<NT>();
+  // O^T out of TMEM (thread = one d row of each 128-row block, its columns),
+  // times 1/l. Where the idle ring holds the whole [M][Dv] fp32 tile, it is
+  // staged there first, so that every (row, head) output row leaves as
+  // 16-byte stores of consecutive channels with one index computation per 4
+  // channels; otherwise each element is stored straight from its thread.
+  constexpr bool kStage = C::kNmax * C::kDv * 4 <= C::kRing * kSlot;
+  float* ostage = reinterpret_cast<float*>(x.ring);
 #pragma unroll
   for (int blk = 0; blk < C::kOBlocks; ++blk) {
     const int d = blk * 128 + r;
@@ -860,14 +867,40 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
         const int n = c0 + ch * KC + e;
         if (n < M) {
           const float o = v[e] * x.linv[n];
-          const int64_t row = x.q0 + n / hpc;
-          const int head = x.head0 + n % hpc;
-          if (x.single) {
-            static_cast<__nv_bfloat16*>(a.out)[(row * a.hq + head) * C::kDv + d] = __float2bfloat16_rn(o);
+          if constexpr (kStage) {
+            ostage[n * C::kDv + d] = o;
           } else {
-            a.part_o[(((int64_t)x.split * a.rows_cap + row) * a.hq + head) * C::kDv + d] = o;
+            const int64_t row = x.q0 + n / hpc;
+            const int head = x.head0 + n % hpc;
+            if (x.single) {
+              static_cast<__nv_bfloat16*>(a.out)[(row * a.hq + head) * C::kDv + d] = __float2bfloat16_rn(o);
+            } else {
+              a.part_o[(((int64_t)x.split * a.rows_cap + row) * a.hq + head) * C::kDv + d] = o;
+            }
           }
         }
+      }
+    }
+  }
+  if constexpr (kStage) {
+    group_sync<NT>();
+    constexpr int kQ = C::kDv / 4;  // 4-channel groups of one output row
+    for (int q = st; q < M * kQ; q += NT) {
+      const int n = q / kQ, c4 = q % kQ;
+      const float4 o = reinterpret_cast<const float4*>(ostage)[q];
+      const int64_t row = x.q0 + n / hpc;
+      const int head = x.head0 + n % hpc;
+      if (x.single) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(o.z, o.w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + (row * a.hq + head) * C::kDv +
+                                  4 * c4) = pk;
+      } else {
+        *reinterpret_cast<float4*>(a.part_o + (((int64_t)x.split * a.rows_cap + row) * a.hq + head) *
+                                                  C::kDv + 4 * c4) = o;
       }
     }
   }
@@ -1294,6 +1327,8 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
   // TMEM address (the MMA and softmax warps only; producers never use it)
   const uint32_t tmem = producer ? 0u : *tmem_slot;
   const uint32_t tmem_o = tmem + 2 * C::kSCols;
+  // every warp reconverges here, before the (warp-uniform) role dispatch
+  __syncwarp();
 
   if (warp == 0 || (warp >= C::kProdWarp1 && warp < C::kProdWarp1 + C::kProducers - 1)) {
     // ================================================ TMA producer warps

@@ -266,11 +266,18 @@ def time_graph(fn, steps, warmup, flush, stream):
     return [a.elapsed_time(b) for a, b in evs]
 
 
+# workloads planned from the batch's host lengths, rows and windows (their
+# lengths vary; a serving step plans each batch this way), the others from
+# their maxima (one plan for any lengths)
+HOST_PLANNED = ("mixed",)
+
+
 def setup_call(wl, dev):
     """Plan, scratch, outputs and a captured CUDA graph of one pda_decode."""
     import torch
     from paged_split_kv_03_gb300 import binding as B
-    dec = B.Decoder(B.params_for(wl, device=dev.index or 0), device=dev)
+    dec = B.Decoder(B.params_for(wl, device=dev.index or 0, host_plan=wl.name in HOST_PLANNED),
+                    device=dev)
     dv = getattr(wl, "head_dim_v", None) or wl.head_dim
     out = torch.empty(wl.total_rows, wl.num_qo_heads, dv, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(wl.total_rows, wl.num_qo_heads, dtype=torch.float32, device=dev)

@@ -124,6 +124,12 @@ typedef struct {
                               microseconds; 0 = 2 s. A wait that runs out sets
                               PDA_STATUS_WAIT_TIMEOUT and its CTA gives up, writing nothing */
   uint32_t inject;         /* test hooks, 0 in normal use: PDA_INJECT_WITHHOLD_KV */
+  /* optional host copies for exact eager planning, used with host_kv_len:
+   * qo_indptr[batch + 1] (rows of each request) and window[batch]; NULL = every
+   * request has max_q_len rows / no window. The plan stays valid for any
+   * device contents within its maxima; these only tune its KV chunk. */
+  const int32_t* host_qo_indptr;
+  const int32_t* host_window;
 } pda_params;
 
 /* Test hook (pda_params.inject): the tcgen05 stage-1 CTAs issue no K/V

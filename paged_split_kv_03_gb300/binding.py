@@ -50,7 +50,8 @@ class PdaParams(ctypes.Structure):
                 ("kv_stride_token", _i64), ("kv_stride_head", _i64), ("device", _i32),
                 ("num_sms", _i32), ("host_kv_len", ctypes.POINTER(_i32)), ("batch", _i32),
                 ("chunk_pages", _i32), ("kernel", _i32), ("head_dim_v", _i32),
-                ("wait_limit_us", _i32), ("inject", _u32)]
+                ("wait_limit_us", _i32), ("inject", _u32),
+                ("host_qo_indptr", ctypes.POINTER(_i32)), ("host_window", ctypes.POINTER(_i32))]
 
 
 class PdaPlan(ctypes.Structure):
@@ -231,8 +232,11 @@ def pda_reset_status(plan: PdaPlan, split_scratch, stream=None) -> None:
 
 def params_for(wl, *, max_batch=None, max_q_len=None, max_kv_len=None, device=0, num_sms=0,
                chunk_pages=0, kernel=PDA_KERNEL_AUTO, batch=0, wait_limit_us=0,
-               inject=0) -> PdaParams:
-    """PdaParams describing a workload object (synth.Workload or alike)."""
+               inject=0, host_plan=False) -> PdaParams:
+    """PdaParams describing a workload object (synth.Workload or alike).
+    ``host_plan``: pass the batch's host lengths, rows and windows, so the
+    planner sizes the KV chunk for this batch (the plan still serves any
+    lengths within its maxima)."""
     p = PdaParams()
     p.num_qo_heads = wl.num_qo_heads
     p.num_kv_heads = wl.num_kv_heads
@@ -255,6 +259,15 @@ def params_for(wl, *, max_batch=None, max_q_len=None, max_kv_len=None, device=0,
     p.head_dim_v = getattr(wl, "head_dim_v", None) or 0
     p.wait_limit_us = wait_limit_us
     p.inject = inject
+    if host_plan:
+        def arr(xs):
+            a = (_i32 * len(xs))(*[int(x) for x in xs])
+            return a, ctypes.cast(a, ctypes.POINTER(_i32))
+        p._keep = [arr(wl.kv_len.cpu().tolist()), arr(wl.qo_indptr.cpu().tolist())]
+        p.host_kv_len, p.host_qo_indptr = p._keep[0][1], p._keep[1][1]
+        if wl.window is not None:
+            p._keep.append(arr(wl.window.cpu().tolist()))
+            p.host_window = p._keep[2][1]
     return p
 
 

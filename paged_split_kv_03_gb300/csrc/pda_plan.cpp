@@ -178,8 +178,58 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
   const double cta_overhead_us = 4.0;
   const double merge_us = 3.0;
   const double rows_heads = (double)pl.batch * pl.max_q_len * pl.num_qo_heads;
+  // Exact eager planning (host copies of the lengths, rows and windows):
+  // each request's visible pages and its own head blocks, the grid's CTAs
+  // in launch order (request, kv head, split, head block) taken greedily by
+  // `slots` SM slots (a CTA with no work costs a launch), and the merge of
+  // the requests that split.
+  struct HostReq {
+    int64_t pages;
+    int nhb, rows;
+  };
+  std::vector<HostReq> hreq;
+  if (p->host_kv_len) {
+    hreq.resize(pl.batch);
+    for (int b = 0; b < pl.batch; ++b) {
+      const int64_t L = std::max<int64_t>(0, std::min<int64_t>(p->host_kv_len[b], max_len));
+      int R = p->host_qo_indptr ? p->host_qo_indptr[b + 1] - p->host_qo_indptr[b] : pl.max_q_len;
+      R = std::max(0, std::min(R, pl.max_q_len));
+      const int W = p->host_window ? p->host_window[b] : 0;
+      const int64_t lo = W > 0 ? std::max<int64_t>(0, L - R - W + 1) : 0;
+      hreq[b].pages = R > 0 && L > 0 ? ceil_div(L, p->page_size) - lo / p->page_size : 0;
+      hreq[b].nhb = R > 0 ? pl.group / pl.heads_per_cta[R] : 0;
+      hreq[b].rows = R;
+    }
+  }
+  const int64_t exact_ctas = (int64_t)pl.batch * hb_units;  // times the split count
+  auto exact_cost = [&](int64_t chunk) -> double {
+    const int64_t nsplit = ceil_div(pages_max, chunk);
+    std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+    for (int64_t i = 0; i < slots; ++i) free_at.push(0.0);
+    double end = 0.0, merge_bytes = 0.0;
+    for (int b = 0; b < pl.batch; ++b) {
+      const HostReq& h = hreq[b];
+      const int64_t ns = h.pages > 0 ? ceil_div(h.pages, chunk) : 0;
+      if (ns > 1) merge_bytes += 2.0 * ns * h.rows * pl.num_qo_heads * (p->head_dim + 1) * 4;
+      for (int kvh = 0; kvh < pl.num_kv_heads; ++kvh)
+        for (int64_t sp = 0; sp < nsplit; ++sp)
+          for (int hb = 0; hb < pl.head_blocks; ++hb) {
+            double w = 0.5;  // a CTA without work: launch and exit
+            if (sp < ns && hb < h.nhb)
+              w = cta_overhead_us + std::min<int64_t>(chunk, h.pages - sp * chunk) * page_kv_bytes /
+                                        sm_bytes_per_us;
+            const double s0 = free_at.top();
+            free_at.pop();
+            free_at.push(s0 + w);
+            end = std::max(end, s0 + w);
+          }
+    }
+    if (nsplit > 1) end += merge_us + merge_bytes / 6.0e6;
+    return end;
+  };
   auto cost = [&](int64_t chunk) -> double {
     const int64_t nsplit = ceil_div(pages_max, chunk);
+    if (!hreq.empty() && exact_ctas * nsplit <= 400000) return exact_cost(chunk);
     double t;
     if (p->host_kv_len) {
       double total = 0.0, longest = 0.0;
@@ -210,6 +260,9 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
     for (int64_t n = 2; n <= max_split; ++n) {
       const int64_t c = ceil_div(pages_max, n);
       if (ceil_div(pages_max, c) != n) continue;  // same chunk as a smaller n
+      // the exact model simulates the grid: try split counts 2..16, then
+      // about 12 % apart
+      if (!hreq.empty() && n > 16 && n % std::max<int64_t>(1, n / 8) != 0) continue;
       const double t = cost(c);
       if (t < best * 0.999) {
         best = t;
@@ -230,7 +283,7 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
   // (k ~ slots / their CTAs) and run last, if a greedy schedule of the CTAs
   // (each SM slot takes the next CTA when free) finishes sooner, merge
   // included.
-  if (p->chunk_pages == 0 && pl.batch > 0) {
+  if (p->chunk_pages == 0 && pl.batch > 0 && hreq.empty()) {
     const int64_t per_req = hb_units * pl.head_splits;  // CTAs of one request
     const int64_t total = (int64_t)pl.batch * per_req;
     const int64_t rem = total % slots;

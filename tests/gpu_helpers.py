@@ -32,7 +32,7 @@ def dv_of(wl):
 
 
 def run_decode(wl, *, chunk_pages=0, kernel=B.PDA_KERNEL_AUTO, max_q_len=None, max_batch=None,
-               max_kv_len=None, decoder=None, fill=float("nan")):
+               max_kv_len=None, decoder=None, fill=float("nan"), host_plan=False):
     """Run pda_decode on a device-resident workload; returns (out fp32 CPU
     [rows, Hq, D], lse CPU [rows, Hq], status bits, decoder)."""
     dev = wl.q.device
@@ -40,7 +40,7 @@ def run_decode(wl, *, chunk_pages=0, kernel=B.PDA_KERNEL_AUTO, max_q_len=None, m
     if decoder is None:
         params = B.params_for(wl, chunk_pages=chunk_pages, kernel=kernel, max_q_len=max_q_len,
                               max_batch=max_batch, max_kv_len=max_kv_len,
-                              device=dev.index or 0)
+                              device=dev.index or 0, host_plan=host_plan)
         decoder = B.Decoder(params, device=dev)
     rows = wl.total_rows
     out = torch.full((rows, wl.num_qo_heads, dv_of(wl)), fill, dtype=torch.bfloat16, device=dev)

@@ -348,3 +348,45 @@ def test_append_host_checks_return_before_any_launch(lib):
     # a latent without records has no append kernel
     lat, _, _ = B.pda_plan(_params(**MLA))
     assert call(lat, max_q_len=2) == B.PDA_ERR_UNSUPPORTED
+
+
+def test_plan_from_host_lengths(lib):
+    """Eager planning from the batch's host lengths, rows and windows (the
+    mixed batch's shape: 48 / 2 heads, R 1..8, ctx 1K..64K, half windowed):
+    the plan is a valid split plan for the same maxima, its chunk covers the
+    longest request, and a batch of tiny windowed requests is not split."""
+    import random
+    rng = random.Random(3)
+    bs = 64
+    lens = [rng.randint(1024, 65536) for _ in range(bs)]
+    rows = [rng.randint(1, 8) for _ in range(bs)]
+    wins = [64 if b % 2 == 0 else 0 for b in range(bs)]
+    qo = [0]
+    for r in rows:
+        qo.append(qo[-1] + r)
+
+    def params(lens_, qo_, wins_):
+        p = _params(num_qo_heads=48, num_kv_heads=2, head_dim=128, page_size=32, max_batch=bs,
+                    max_q_len=8, max_kv_len=65536, num_pages=bs * 2048 + 4,
+                    kv_stride_page=32 * 2 * 128, kv_stride_token=2 * 128, kv_stride_head=128)
+        keep = [(ctypes.c_int32 * len(x))(*x) for x in (lens_, qo_, wins_)]
+        p.host_kv_len, p.host_qo_indptr, p.host_window = (
+            ctypes.cast(k, ctypes.POINTER(ctypes.c_int32)) for k in keep)
+        return p, keep
+
+    p, keep = params(lens, qo, wins)
+    plan, nbytes, rc = B.pda_plan(p)
+    assert rc == 0 and plan.kernel == B.PDA_KERNEL_TC
+    pages_max = -(-max(lens) // 32)
+    assert plan.head_splits * plan.chunk_pages >= pages_max
+    assert plan.tail_from == plan.batch  # the simulated grid replaces the tail split
+    assert plan.grid_ctas == bs * 2 * plan.head_blocks * plan.head_splits
+    base, _ = B.pda_plan(_params(num_qo_heads=48, num_kv_heads=2, head_dim=128, page_size=32,
+                                 max_batch=bs, max_q_len=8, max_kv_len=65536,
+                                 num_pages=bs * 2048 + 4, kv_stride_page=32 * 2 * 128,
+                                 kv_stride_token=2 * 128, kv_stride_head=128))[:2]
+    assert plan.max_kv_len <= base.max_kv_len and plan.head_blocks == base.head_blocks
+    # every request windowed to 64 keys: one or two pages each, no split
+    p2, keep2 = params(lens, qo, [64] * bs)
+    small, _, rc = B.pda_plan(p2)
+    assert rc == 0 and small.max_splits == 1

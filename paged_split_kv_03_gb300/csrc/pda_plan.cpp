@@ -163,8 +163,8 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
 
   // Split planning: pick the KV chunk (pages per CTA) that minimises a small
   // cost model of stage 1 + stage 2 on this GPU. A CTA costs a fixed
-  // overhead (prologue, pipeline fill, epilogue) plus its K/V bytes at the
-  // SM's share of HBM bandwidth; CTAs run in waves of `slots`; more than one
+  // overhead (prologue, pipeline fill, epilogue) plus its K/V bytes at its
+  // slot's streaming rate; CTAs run in waves of `slots`; more than one
   // split adds the merge (stage 2 launch plus partials written and read).
   // With host lengths, per-request work replaces the uniform worst case.
   const bool tc = pl.kernel == PDA_KERNEL_TC;
@@ -174,8 +174,35 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
   const int64_t hb_units = (int64_t)pl.num_kv_heads * pl.head_blocks;  // CTAs per (request, split)
   const int64_t units = (int64_t)pl.batch * hb_units;
   const double page_kv_bytes = 2.0 * p->page_size * p->head_dim * eb;  // K+V of one head, one page
-  const double sm_bytes_per_us = 44000.0 / per_sm;                       // ~6.7 TB/s over 152 SMs
-  const double cta_overhead_us = 4.0;
+  const double hbm_bytes_per_us = 44000.0 * num_sms;  // ~6.7 TB/s over 152 SMs
+  const double sm_bytes_per_us = 44000.0 / per_sm;     // a slot's share
+  // What the CTA of a one-per-SM build can consume when HBM is not the
+  // limit (bytes/us, measured on GB300 with fewer CTAs than SMs): head_dim
+  // 256 bf16 ~56 KB/us at 16-64 columns; E4M3 ~46 KB/us at 32 columns and
+  // ~40 at 64 (two-term S and P); int8 ~24 (the widening pass). Elsewhere
+  // (two CTAs per SM, whose siblings share an SM's loads unevenly when
+  // fewer than all slots are busy; head_dim 512; MLA) a slot is taken to
+  // stream at its share of HBM whatever the number of busy slots.
+  double slot_cap = sm_bytes_per_us;
+  bool capped = false;
+  if (tc && per_sm == 1 && pl.head_dim <= 256 && pl.scale_mode != PDA_SCALE_MLA_BLOCK) {
+    const int ncols = ((pl.max_q_len * pl.heads_per_cta[pl.max_q_len] + 15) / 16) * 16;
+    capped = true;
+    if (pl.kv_dtype == PDA_INT8) slot_cap = 24000.0;
+    else if (pl.kv_dtype == PDA_E4M3) slot_cap = 40000.0 + 200.0 * (64 - std::min(ncols, 64));
+    else slot_cap = 56000.0;
+  }
+  // a slot's rate while `active` slots stream at once
+  auto slot_rate = [&](int64_t active) {
+    if (!capped) return sm_bytes_per_us;
+    const int64_t a = std::max<int64_t>(1, std::min(active, slots));
+    return std::min(slot_cap, hbm_bytes_per_us / a);
+  };
+  // The second CTA of an SM streams through its sibling's prologue and
+  // epilogue; with one CTA per SM nothing does, and each CTA's start-up
+  // (launch, request scalars, page ids, the first tile's round trip) and
+  // drain (the last tiles' MMAs, softmax and output) leave its SM idle.
+  const double cta_overhead_us = per_sm >= 2 ? 4.0 : 8.0;
   const double merge_us = 3.0;
   const double rows_heads = (double)pl.batch * pl.max_q_len * pl.num_qo_heads;
   // Exact eager planning (host copies of the lengths, rows and windows):
@@ -217,7 +244,7 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
             double w = 0.5;  // a CTA without work: launch and exit
             if (sp < ns && hb < h.nhb)
               w = cta_overhead_us + std::min<int64_t>(chunk, h.pages - sp * chunk) * page_kv_bytes /
-                                        sm_bytes_per_us;
+                                        slot_rate(slots);
             const double s0 = free_at.top();
             free_at.pop();
             free_at.push(s0 + w);
@@ -237,15 +264,18 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
         const int64_t pages = std::max<int64_t>(1, ceil_div(p->host_kv_len[b], p->page_size));
         for (int64_t s0 = 0; s0 < pages; s0 += chunk) {
           const double w = cta_overhead_us + std::min<int64_t>(chunk, pages - s0) * page_kv_bytes /
-                                                 sm_bytes_per_us;
+                                                 slot_rate(slots);
           total += w * hb_units;
           longest = std::max(longest, w);
         }
       }
       t = std::max(total / slots, longest);
     } else {
-      const double w = cta_overhead_us + chunk * page_kv_bytes / sm_bytes_per_us;
-      t = (double)ceil_div(units * nsplit, slots) * w;
+      // full waves at the all-slots rate, then a partial one at its own
+      const int64_t n = units * nsplit;
+      const double bytes = chunk * page_kv_bytes;
+      t = (double)(n / slots) * (cta_overhead_us + bytes / slot_rate(slots));
+      if (n % slots) t += cta_overhead_us + bytes / slot_rate(n % slots);
     }
     if (nsplit > 1) t += merge_us + 2.0 * nsplit * rows_heads * (p->head_dim + 1) * 4 / 6.0e6;
     return t;
@@ -288,7 +318,7 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
     const int64_t total = (int64_t)pl.batch * per_req;
     const int64_t rem = total % slots;
     auto cta_us = [&](int64_t c) {
-      return cta_overhead_us + std::min<int64_t>(c, pages_max) * page_kv_bytes / sm_bytes_per_us;
+      return cta_overhead_us + std::min<int64_t>(c, pages_max) * page_kv_bytes / slot_rate(slots);
     };
     // makespan of n1 CTAs of t1 then n2 of t2 when each of `slots` slots
     // takes the next CTA as soon as it is free

@@ -104,6 +104,26 @@ def test_plan_tail_split(lib):
     assert even.tail_from == even.batch and even.grid_ctas == 76 * 8
 
 
+def test_plan_one_per_sm_waves(lib):
+    # bf16 head_dim 256 runs one CTA per SM; its CTAs start and drain in
+    # step, so each wave costs a start-up with the SM idle, and one CTA can
+    # stream faster than a 1/152 share of HBM: bs 16 x 2 kv heads at 32K
+    # takes one wave of 4 splits (128 CTAs), not three
+    plan, _, rc = B.pda_plan(_params(max_q_len=1))
+    assert rc == 0 and plan.kernel == B.PDA_KERNEL_TC
+    assert plan.rows_per_cta == 64 and plan.grid_ctas <= 152
+    assert (plan.head_splits, plan.grid_ctas) == (4, 128)
+    # int8 widens its codes at ~24 KB/us per CTA, below the SM's share of
+    # HBM: more CTAs than SMs still pays, and it keeps several waves
+    i8, _, rc = B.pda_plan(_params(max_q_len=1, kv_dtype=B.PDA_INT8, scale_mode=2,
+                                   max_kv_len=131072, num_pages=140000))
+    assert rc == 0 and i8.grid_ctas > 2 * 152
+    # two CTAs per SM (E4M3 head_dim 256 at 16 columns): unchanged share model
+    f8, _, rc = B.pda_plan(_params(max_q_len=1, kv_dtype=1, q_dtype=0, scale_mode=2,
+                                   max_kv_len=131072, num_pages=140000))
+    assert rc == 0 and f8.grid_ctas == 608
+
+
 D512 = dict(num_qo_heads=16, num_kv_heads=1, head_dim=512, page_size=16, max_batch=1,
             max_kv_len=131072, kv_stride_page=16 * 512, kv_stride_token=512, kv_stride_head=512)
 

@@ -50,6 +50,9 @@ SWEEP = [("mtp_verify_bf16", bs, R) for bs in (1, 16) for R in (1, 4, 8)] + \
         [("d512_mtp_bf16", 1, R) for R in (1, 4, 8)] + \
         [("d512_mtp_fp8", 1, R) for R in (1, 4, 8)] + \
         [("mla_bf16", 64, 1), ("mla_fp8", 64, 1), ("mla_fp8", 64, 2), ("mla_fp8_mixed", 64, 1)]
+# the same FP8 decode batch with the cache in HND order (one kv head's page
+# contiguous) beside the NHD headline: the access-pattern check
+LAYOUT_SWEEP = [("fp8_decode", dict(layout="HND"), "fp8_decode bs128 R1 HND")]
 
 
 def peaks():
@@ -480,13 +483,14 @@ def run_ours(args, rank, world, dev):
 
     sweep = []
     if rank == 0 and not args.no_sweep:
-        for name, bs, R in SWEEP:
-            w2 = config_workload(name, R=R, bs=bs, device=dev)
+        runs = [(name, dict(R=R, bs=bs), f"{name} bs{bs} R{R}" if R else f"{name} bs{bs} R1..8")
+                for name, bs, R in SWEEP] + LAYOUT_SWEEP
+        for name, kw, label in runs:
+            w2 = config_workload(name, device=dev, **kw)
             d2, o2, l2_, s2, g2 = setup_call(w2, dev)
             t2 = time_graph(g2.replay, max(10, args.steps), 3, flush, s2)
             b2 = call_bytes(w2, plan=d2.plan)["total"]
             med = statistics.median(t2)
-            label = f"{name} bs{bs} R{R}" if R else f"{name} bs{bs} R1..8"
             sweep.append({"workload": label, "us_per_call": med * 1e3,
                           "GB_s": b2 / (med * 1e-3) / 1e9,
                           "frac_of_peak": b2 / (med * 1e-3) / 1e9 / peak, "bytes": b2,

@@ -200,6 +200,7 @@ def test_split_count_invariance(chunk, kernel):
 CONFIGS = [
     ("tiny", {}, None, None),
     ("fp8_decode", {}, None, None),
+    ("fp8_decode", dict(layout="HND"), None, None),
     ("mtp_verify_bf16", dict(bs=1, R=1), None, None),
     ("mtp_verify_bf16", dict(bs=1, R=4), None, None),
     ("mtp_verify_bf16", dict(bs=1, R=8), None, None),

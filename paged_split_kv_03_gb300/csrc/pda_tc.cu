@@ -1597,11 +1597,22 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
       if (N <= 16) softmax_role<C, SMODE, 1>(a, x, warp, lane, tid);
       else softmax_role<C, SMODE, 2>(a, x, warp, lane, tid);
     } else {
-      switch (N >> 4) {
-        case 1: softmax_role<C, SMODE, 1>(a, x, warp, lane, tid); break;
-        case 2: softmax_role<C, SMODE, 2>(a, x, warp, lane, tid); break;
-        case 3: softmax_role<C, SMODE, 3>(a, x, warp, lane, tid); break;
-        default: softmax_role<C, SMODE, 4>(a, x, warp, lane, tid); break;
+      if constexpr (NMAX > 64) {
+        switch (N >> 4) {
+          case 1: softmax_role<C, SMODE, 1>(a, x, warp, lane, tid); break;
+          case 2: softmax_role<C, SMODE, 2>(a, x, warp, lane, tid); break;
+          case 3: softmax_role<C, SMODE, 3>(a, x, warp, lane, tid); break;
+          case 4: softmax_role<C, SMODE, 4>(a, x, warp, lane, tid); break;
+          case 5: softmax_role<C, SMODE, 5>(a, x, warp, lane, tid); break;
+          default: softmax_role<C, SMODE, 6>(a, x, warp, lane, tid); break;
+        }
+      } else {
+        switch (N >> 4) {
+          case 1: softmax_role<C, SMODE, 1>(a, x, warp, lane, tid); break;
+          case 2: softmax_role<C, SMODE, 2>(a, x, warp, lane, tid); break;
+          case 3: softmax_role<C, SMODE, 3>(a, x, warp, lane, tid); break;
+          default: softmax_role<C, SMODE, 4>(a, x, warp, lane, tid); break;
+        }
       }
     }
   }
@@ -1656,6 +1667,10 @@ auto tc_select(const pda_plan_t* p, int nmax, F f) {
   return f.template get<DD, PDA_E4M3, PDA_E4M3, PDA_SCALE_TOKEN_HEAD, NN>();
   if (p->head_dim == 128) {
     if (nmax <= 16) { PDA_TC_CASES(128, 16) }
+    // bf16 caches without scales also have a 96-column build (large GQA
+    // groups with several rows: fewer head blocks re-reading the same K/V)
+    if (nmax > 64 && kv == PDA_BF16)
+      return f.template get<128, PDA_BF16, PDA_BF16, PDA_SCALE_NONE, 96>();
     PDA_TC_CASES(128, 64)
   }
   if (p->head_dim == 512) {
@@ -1754,11 +1769,18 @@ bool tc_supported(const pda_plan_t* p) {
 
 // Rows x heads a CTA may hold: 64, except head_dim 512 over an E4M3 cache,
 // whose two-term S and O accumulators (2 x 2N + 4 x 2N columns) leave TMEM
-// room for 32. The pages' kernel takes 16 for quantised head_dim 512
+// room for 32, and head_dim 128 over a bf16 cache, which has a 96-column
+// build. The pages' kernel takes 16 for quantised head_dim 512
 // ("perf(attention): run up to 8 query rows per request in the triton
-// decode kernel"); 32 halves the head blocks that re-read the cache.
+// decode kernel"); 32 halves the head blocks that re-read the cache. A
+// head block streams its kv head's whole chunk whatever its columns (a CTA's
+// pace is set by its K/V bytes, not by its 16-96 columns, measured on the
+// 48 / 2-head mixed batch), so fewer, wider head blocks cut the bytes the
+// SMs read for a large GQA group with several rows; 96 columns is the widest
+// whose softmax state fits the 96 registers a thread has at 640 threads.
 int tc_rows_limit(const pda_plan_t* p) {
   // (the MLA latent's E4M3 build likewise: S 2 x N, O 4 x 2N columns)
+  if (p->head_dim == 128 && p->kv_dtype == PDA_BF16) return 96;
   return p->head_dim >= 512 && p->kv_dtype == PDA_E4M3 ? 32 : kTcRowsPerCta;
 }
 
@@ -1774,10 +1796,12 @@ static int plan_nmax(const pda_plan_t* p) {
 
 int tc_variant_rows(const pda_plan_t* p) {
   // the smallest build that holds every CTA's columns (16: two CTAs per SM
-  // up to head_dim 256; head_dim 512 also has a 32-column build)
+  // up to head_dim 256; head_dim 512 also has a 32-column build, bf16
+  // head_dim 128 a 96-column one)
   const int n = plan_nmax(p);
   if (n <= 16 && tc_select(p, 16, GetSmem()) > 0) return 16;
   if (p->head_dim >= 512 && n <= 32 && tc_select(p, 32, GetSmem()) > 0) return 32;
+  if (n > 64 && tc_select(p, 96, GetSmem()) > 0) return 96;
   return 64;
 }
 

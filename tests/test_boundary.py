@@ -55,12 +55,20 @@ def _params(**kw):
 
 def test_plan_heads_divide_group(lib):
     # 48 query / 2 kv heads: group 24; heads per CTA must divide 24 at every R
+    # (bf16 head_dim 128: the 96-column build, 24 heads up to R = 4, then 12)
     plan, nbytes, rc = B.pda_plan(_params(num_qo_heads=48, num_kv_heads=2, head_dim=128))
+    assert plan.rows_per_cta == 96
     for R in range(1, 9):
         h = plan.heads_per_cta[R]
         assert 24 % h == 0 and R * h <= plan.rows_per_cta
-    assert plan.heads_per_cta[1] == 24 and plan.heads_per_cta[8] == 8
-    assert plan.head_blocks == 3
+    assert plan.heads_per_cta[1] == 24 and plan.heads_per_cta[4] == 24
+    assert plan.heads_per_cta[5] == 12 and plan.heads_per_cta[8] == 12
+    assert plan.head_blocks == 2
+    # E4M3 at head_dim 128 keeps 64 columns: 8 heads at R = 8, 3 head blocks
+    f8, _, rc = B.pda_plan(_params(num_qo_heads=48, num_kv_heads=2, head_dim=128, kv_dtype=1,
+                                   scale_mode=1, kv_stride_page=16 * 2 * 128,
+                                   kv_stride_token=2 * 128, kv_stride_head=128))
+    assert rc == 0 and f8.rows_per_cta == 64 and f8.heads_per_cta[8] == 8 and f8.head_blocks == 3
 
 
 def test_plan_splits_and_scratch(lib):

@@ -31,7 +31,7 @@ KNOWN_SPILLS = {
 # longctx_fp8_pth and mixed
 STATED = [("stage1_tc", (128, 1, 1, 1, 16)), ("stage1_tc", (256, 0, 0, 0, 64)),
           ("stage1_tc", (256, 1, 0, 2, 16)), ("stage1_tc", (256, 1, 0, 2, 64)),
-          ("stage1_tc", (128, 0, 0, 0, 64))]
+          ("stage1_tc", (128, 0, 0, 0, 96))]
 
 
 def _key(mangled):

@@ -447,7 +447,10 @@ struct TcCfg {
   static constexpr int kBudget = kCtasPerSm == 2 ? 228 * 1024 / 2 - 1024 : 227 * 1024;
   // the dynamic window starts 1024-byte aligned (checked at run time)
   static constexpr int kAvail = kBudget - kQBytes - kPBytes - kSmallBytes;
-  static constexpr int kAvailSlots = kAvail / kSlot > 12 ? 12 : kAvail / kSlot;
+  // (at most 12 slots, but for the E4M3 MLA latent, whose aliased K units
+  // want all the room there is)
+  static constexpr int kMaxSlots = kMla && kF8 ? 16 : 12;
+  static constexpr int kAvailSlots = kAvail / kSlot > kMaxSlots ? kMaxSlots : kAvail / kSlot;
   // int8: a third of the slots (at least 2) hold TMA'd codes, the rest f16
   // tiles (the MMA side needs two tiles of those to keep widening ahead)
   static constexpr int kIRing = kConv ? (kAvailSlots / 3 < 2 ? 2 : kAvailSlots / 3) : 0;
@@ -465,6 +468,13 @@ struct TcCfg {
       !(kMla && (kQSplit || kI8)) &&
       (!kMix || (kMla && KVT == PDA_E4M3 && QT == PDA_BF16 && kIRing >= 2));
   static constexpr int kSmem = kQBytes + kPBytes + (kRing + kIRing) * kSlot + kSmallBytes;
+  // E4M3 MLA latent: V is the first 512 channels of the K tile already in
+  // the ring, so no V unit is loaded; each K unit stays until its PV (the
+  // rope chunk goes after its S^T), and S^T runs one tile ahead instead of
+  // two, which needs two K units in the ring and pays only with a few slots
+  // more to load ahead (with exactly two, R = 2's 32-column build measured
+  // 10 % slower; with 13 slots R = 1 is 6 % faster)
+  static constexpr bool kVAlias = kMla && kF8 && kRing >= 2 * kChunks + 3;
   // barrier words in the small area's first 512 bytes
   static_assert(2 * (kRing + kIRing) + 10 + 2 <= 64, "barrier area");
 };
@@ -484,6 +494,19 @@ __device__ __forceinline__ uint32_t chunk_pos_k(int j) {
 template <int CK, int CV>
 __device__ __forceinline__ uint32_t chunk_pos_v(int j, int n) {
   return static_cast<uint32_t>(min(j + 3, n) * CK + j * CV);
+}
+
+// The same for a configuration whose V units alias their K units (the ring
+// then holds K_0, K_1, K_2, ... only).
+template <class C>
+__device__ __forceinline__ uint32_t unit_pos_k(int j) {
+  if constexpr (C::kVAlias) return static_cast<uint32_t>(j * C::kChunks);
+  else return chunk_pos_k<C::kChunks, C::kChunksV>(j);
+}
+template <class C>
+__device__ __forceinline__ uint32_t unit_pos_v(int j, int n) {
+  if constexpr (C::kVAlias) return static_cast<uint32_t>(j * C::kChunks);
+  else return chunk_pos_v<C::kChunks, C::kChunksV>(j, n);
 }
 
 // Everything the softmax / epilogue warps need from the CTA prologue.
@@ -756,7 +779,7 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
     // last tile: rows past the chunk's end may hold stale or poisoned V
     // (int8 codes are always finite, so their zero P suffices)
     if (!C::kI8 && alive && c0 == 0 && tile0 + kTok > x.t_end && tok >= x.t_end) {
-      const uint32_t gv = chunk_pos_v<C::kChunks, C::kChunksV>(j, x.ntiles);
+      const uint32_t gv = unit_pos_v<C>(j, x.ntiles);
       for (int c = 0; c < C::kChunksV && alive; ++c) {
         const uint32_t slot = (gv + c) % R_;
         alive = bar_wait(x.full + slot, ((gv + c) / R_) & 1u, x.abort_flag, a);
@@ -1417,7 +1440,7 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
         ok2 = checked(ok2, pg2);
         emit(0, ok2, pg2, s02);                     // K_{j+2}
       }
-      emit(1, ok0, pg0, s00);                       // V_j
+      if constexpr (!C::kVAlias) emit(1, ok0, pg0, s00);  // V_j
       pg0 = pg1; s00 = s01; ok0 = ok1;
       pg1 = pg2; s01 = s02; ok1 = ok2;
       pg2 = pg3; s02 = s03; ok2 = ok3;
@@ -1451,7 +1474,7 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
         const int sb = j & 1;
         if (j >= 2 && !bar_wait(s_free + sb, ((j >> 1) - 1) & 1, abort_flag, a)) return false;
         fence_after();
-        const uint32_t gk = chunk_pos_k<C::kChunks, C::kChunksV>(j);
+        const uint32_t gk = unit_pos_k<C>(j);
         for (int c = 0; c < C::kChunks; ++c) {
           const uint32_t slot = (gk + c) % R_;
           if (!bar_wait(full + slot, ((gk + c) / R_) & 1u, abort_flag, a)) return false;
@@ -1464,7 +1487,9 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
               mma<kF8>(tmem + sb * C::kSCols, sdesc(abase + kk * 32, 16, 1024),
                        sdesc(bbase + kk * 32, 16, 1024), id_s, (c | kk) != 0);
           }
-          mma_commit(empty + slot);  // the slot is free once these MMAs finish
+          // the slot is free once these MMAs finish (an aliased K unit's V
+          // chunks once its PV has run)
+          if (!C::kVAlias || c >= C::kChunksV) mma_commit(empty + slot);
         }
         mma_commit(s_full + sb);
         return true;
@@ -1472,7 +1497,7 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
       // O^T += V_j^T P_j^T as soon as the softmax has written P_j
       auto issue_pv = [&](int j) -> bool {
         if (!bar_wait(p_full + (j & 1), (j >> 1) & 1, abort_flag, a)) return false;
-        const uint32_t gv = chunk_pos_v<C::kChunks, C::kChunksV>(j, ntiles);
+        const uint32_t gv = unit_pos_v<C>(j, ntiles);
         constexpr int kBlkSlots = kF8 ? 1 : 2;  // ring slots of one 128-d V block
         const uint32_t pbuf = p_addr + static_cast<uint32_t>(j % C::kPBufs) * C::kPBufBytes;
 #pragma unroll
@@ -1508,11 +1533,19 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
         return true;
       };
       if (alive) alive = issue_s(0);
-      if (alive && ntiles > 1) alive = issue_s(1);
-      for (int j = 0; j < ntiles && alive; ++j) {
-        // S^T of tile j + 2 once the softmax has read tile j's buffer
-        if (j + 2 < ntiles) alive = issue_s(j + 2);
-        if (alive) alive = issue_pv(j);
+      if constexpr (C::kVAlias) {
+        for (int j = 0; j < ntiles && alive; ++j) {
+          // S^T of tile j + 1 (its K unit is in the ring beside K_j)
+          if (j + 1 < ntiles) alive = issue_s(j + 1);
+          if (alive) alive = issue_pv(j);
+        }
+      } else {
+        if (alive && ntiles > 1) alive = issue_s(1);
+        for (int j = 0; j < ntiles && alive; ++j) {
+          // S^T of tile j + 2 once the softmax has read tile j's buffer
+          if (j + 2 < ntiles) alive = issue_s(j + 2);
+          if (alive) alive = issue_pv(j);
+        }
       }
       // make sure nothing issued is still running before TMEM is released
       mma_commit(drain);

@@ -180,6 +180,23 @@ def test_small_peaked_parity(kind, kernel):
     assert_close(out, lse, ref_o, ref_l, tol_for(wl), what=f"{kind} peaked", output_rounding=True)
 
 
+@pytest.mark.parametrize("chunk", [3, 16, 0])
+def test_wide_head_blocks(chunk):
+    """bf16 head_dim 128 with a GQA group of 24: the 96-column build holds
+    all 24 heads of a request with up to 4 rows (72 or 96 columns) and 12
+    heads for 5-8 rows (two head blocks), over one or several splits, with
+    windows; every output element against the oracle."""
+    wl, _ = _make("wide", dict(batch=6, rows=[1, 3, 4, 5, 7, 8], kv_lens=[700, 3000, 2049, 1500, 4096, 900],
+                               num_qo_heads=48, num_kv_heads=2, head_dim=128, page_size=32,
+                               windows=[0, 0, 100, 0, 0, 40]))
+    out, lse, status, dec = run_decode(wl, chunk_pages=chunk, kernel=B.PDA_KERNEL_TC)
+    assert status == 0
+    assert dec.plan.rows_per_cta == 96 and dec.plan.heads_per_cta[4] == 24
+    assert dec.plan.heads_per_cta[5] == 12 and dec.plan.head_blocks == 2
+    ref_o, ref_l = oracle_ref(wl)
+    assert_close(out, lse, ref_o, ref_l, TOL_BF16, what=f"96 columns, chunk {chunk}")
+
+
 @pytest.mark.parametrize("kernel", sorted(KERNELS))
 @pytest.mark.parametrize("chunk", [4, 16, 64, 0])
 def test_split_count_invariance(chunk, kernel):
@@ -218,6 +235,7 @@ CONFIGS = [
     ("longctx_int8_pth", dict(bs=16, R=1), 256, 64),
     ("longctx_int8_pth", dict(bs=16, R=8), None, 64),
     ("mla_fp8", {}, None, None),
+    ("mla_fp8", dict(R=2), None, 96),
     ("mla_bf16", {}, None, 96),
     ("mla_bf16", dict(R=2), 96, 96),
     ("mla_fp8_mixed", {}, None, None),

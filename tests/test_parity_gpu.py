@@ -367,7 +367,7 @@ def test_window_lower_bound_bit_exact(kind, kernel):
     key of each row outweighs the next by e^-128 (below the smallest fp32),
     and the key just below the window would dominate it if it were admitted.
     Output must be v at p_i - W + 1 bit for bit."""
-    R_list, L_list, W_list = [8, 4, 2, 1], [200, 70, 33, 129], [1, 5, 64, 17]
+    R_list, L_list, W_list = [8, 4, 2, 1, 3, 5], [200, 70, 33, 129, 250, 180], [1, 5, 64, 17, 63, 65]
     H, G, D, P = 2, 3, 128, 16
 
     def token_fn(which, b, L):
@@ -390,7 +390,7 @@ def test_window_lower_bound_bit_exact(kind, kernel):
         return x
 
     kv, sm = ("bf16", SCALE_NONE) if kind == "bf16" else ("e4m3", SCALE_TOKEN_HEAD)
-    wl = make_workload(batch=4, rows=R_list, kv_lens=L_list, windows=W_list,
+    wl = make_workload(batch=len(R_list), rows=R_list, kv_lens=L_list, windows=W_list,
                        num_qo_heads=H * G, num_kv_heads=H, head_dim=D, page_size=P, kv_dtype=kv,
                        scale_mode=sm, sm_scale=1.0, value_fn=value_fn, token_fn=token_fn,
                        scale_fn=scale_fn if kind != "bf16" else None, unit_scale=True, seed=9,

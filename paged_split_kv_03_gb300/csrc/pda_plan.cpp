@@ -174,6 +174,13 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
   const int64_t hb_units = (int64_t)pl.num_kv_heads * pl.head_blocks;  // CTAs per (request, split)
   const int64_t units = (int64_t)pl.batch * hb_units;
   const double page_kv_bytes = 2.0 * p->page_size * p->head_dim * eb;  // K+V of one head, one page
+  // A CTA works in tiles of 128 tokens: the bytes it costs are those of its
+  // pages rounded up to whole tiles (a chunk of 560 tokens costs five tiles,
+  // one of 512 four: measured 4 % apart at bs 1)
+  auto chunk_cost_bytes = [&](int64_t pages) {
+    const int64_t tiles = ceil_div(pages * p->page_size, 128);
+    return static_cast<double>(tiles) * 128.0 * (page_kv_bytes / p->page_size);
+  };
   const double hbm_bytes_per_us = 44000.0 * num_sms;  // ~6.7 TB/s over 152 SMs
   const double sm_bytes_per_us = 44000.0 / per_sm;     // a slot's share
   // What the CTA of a one-per-SM build can consume when HBM is not the
@@ -243,8 +250,8 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
           for (int hb = 0; hb < pl.head_blocks; ++hb) {
             double w = 0.5;  // a CTA without work: launch and exit
             if (sp < ns && hb < h.nhb)
-              w = cta_overhead_us + std::min<int64_t>(chunk, h.pages - sp * chunk) * page_kv_bytes /
-                                        slot_rate(slots);
+              w = cta_overhead_us +
+                  chunk_cost_bytes(std::min<int64_t>(chunk, h.pages - sp * chunk)) / slot_rate(slots);
             const double s0 = free_at.top();
             free_at.pop();
             free_at.push(s0 + w);
@@ -263,8 +270,8 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
       for (int b = 0; b < pl.batch; ++b) {
         const int64_t pages = std::max<int64_t>(1, ceil_div(p->host_kv_len[b], p->page_size));
         for (int64_t s0 = 0; s0 < pages; s0 += chunk) {
-          const double w = cta_overhead_us + std::min<int64_t>(chunk, pages - s0) * page_kv_bytes /
-                                                 slot_rate(slots);
+          const double w =
+              cta_overhead_us + chunk_cost_bytes(std::min<int64_t>(chunk, pages - s0)) / slot_rate(slots);
           total += w * hb_units;
           longest = std::max(longest, w);
         }
@@ -273,7 +280,7 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
     } else {
       // full waves at the all-slots rate, then a partial one at its own
       const int64_t n = units * nsplit;
-      const double bytes = chunk * page_kv_bytes;
+      const double bytes = chunk_cost_bytes(chunk);
       t = (double)(n / slots) * (cta_overhead_us + bytes / slot_rate(slots));
       if (n % slots) t += cta_overhead_us + bytes / slot_rate(n % slots);
     }
@@ -318,7 +325,7 @@ extern "C" int pda_plan(const pda_params* p, pda_plan_t* out, size_t* split_scra
     const int64_t total = (int64_t)pl.batch * per_req;
     const int64_t rem = total % slots;
     auto cta_us = [&](int64_t c) {
-      return cta_overhead_us + std::min<int64_t>(c, pages_max) * page_kv_bytes / slot_rate(slots);
+      return cta_overhead_us + chunk_cost_bytes(std::min<int64_t>(c, pages_max)) / slot_rate(slots);
     };
     // makespan of n1 CTAs of t1 then n2 of t2 when each of `slots` slots
     // takes the next CTA as soon as it is free

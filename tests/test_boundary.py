@@ -132,6 +132,17 @@ def test_plan_one_per_sm_waves(lib):
     assert rc == 0 and f8.grid_ctas == 608
 
 
+def test_plan_whole_tiles(lib):
+    # a CTA works in 128-token tiles, so the planner's chunks at bs 1 cover
+    # whole tiles (560 tokens would cost five tiles, 512 four)
+    for kw in (dict(max_batch=1, max_q_len=8), dict(max_batch=1, max_q_len=1),
+               dict(max_batch=1, max_q_len=4, kv_dtype=1, scale_mode=2, max_kv_len=131072,
+                    num_pages=140000)):
+        plan, _, rc = B.pda_plan(_params(**kw))
+        assert rc == 0 and plan.max_splits > 1
+        assert plan.chunk_pages * 16 % 128 == 0, (kw, plan.chunk_pages)
+
+
 D512 = dict(num_qo_heads=16, num_kv_heads=1, head_dim=512, page_size=16, max_batch=1,
             max_kv_len=131072, kv_stride_page=16 * 512, kv_stride_token=512, kv_stride_head=512)
 

@@ -244,9 +244,11 @@ int pda_decode_stages(const pda_plan_t* plan, const void* q, const void* k_pages
  *   int8, per tensor       codes = RNE(clamp(x / s, +-127)), s read as for E4M3;
  *   int8, per token-head   s = amax / 127 (1 if amax = 0), written as for E4M3;
  *   MLA records            (PDA_SCALE_MLA_BLOCK, head_dim 576) k_new holds the latents:
- *                          per 128-channel block of the first 512, s = amax / 448 (1 if
- *                          0) to k_scale [num_pages, P, Hkv, 4] and codes = RNE(sat(x / s))
- *                          at record bytes [0, 512); the 64 rope values copied as bf16 to
+ *                          per 128-channel block of the first 512, s = amax / 448 to
+ *                          k_scale [num_pages, P, Hkv, 4] and codes = RNE(sat(x / s))
+ *                          (a zero block: s = 0 and zero codes, so that it adds nothing
+ *                          to any sum of the decode) at record bytes [0, 512); the 64
+ *                          rope values copied as bf16 to
  *                          bytes [512, 640); v_new, v_pages and v_scale are not used and
  *                          may be NULL; k_new, k_pages and k_scale 16-byte aligned.
  * x / s is one fp32 division; sat clamps to +-448 (E4M3, OCP e4m3fn); RNE

@@ -404,10 +404,12 @@ int pdo_append(int batch, int hkv, int d, int page_size, int mode, int64_t sp, i
               float x = (float)pdo_bf16_to_double(src[c]);
               if (fabsf(x) > amax) amax = fabsf(x);
             }
-            float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+            /* a zero block: scale 0 and zero codes (its decoded values are
+               zero, and a scale of 0 gives it no weight in any sum) */
+            float sc = amax > 0.0f ? amax / 448.0f : (MUT(28) ? 1.0f : 0.0f);
             k_scale[sidx * 4 + blk] = sc;
             for (int c = 128 * blk; c < 128 * (blk + 1); ++c) {
-              float y = (float)pdo_bf16_to_double(src[c]) / sc;
+              float y = (float)pdo_bf16_to_double(src[c]) / (amax > 0.0f ? sc : 1.0f);
               k[base + c] = pdo_e4m3_encode(y);
             }
           }

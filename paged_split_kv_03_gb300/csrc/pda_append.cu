@@ -138,13 +138,15 @@ __device__ __forceinline__ void put_mla_record(const __nv_bfloat16* src, uint8_t
   for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(x[e]));
 #pragma unroll
   for (int off = 1; off < 8; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  const float sc = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  // a zero block: scale 0 (no weight in the decode's sums) and zero codes
+  const float sc = amax > 0.f ? __fdiv_rn(amax, 448.f) : 0.f;
+  const float dv = amax > 0.f ? sc : 1.f;
   if ((lane & 7) == 0) scales[lane >> 3] = sc;
   uint32_t c[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const uint16_t lo = e4m3x2(__fdiv_rn(x[4 * e], sc), __fdiv_rn(x[4 * e + 1], sc));
-    const uint16_t hi = e4m3x2(__fdiv_rn(x[4 * e + 2], sc), __fdiv_rn(x[4 * e + 3], sc));
+    const uint16_t lo = e4m3x2(__fdiv_rn(x[4 * e], dv), __fdiv_rn(x[4 * e + 1], dv));
+    const uint16_t hi = e4m3x2(__fdiv_rn(x[4 * e + 2], dv), __fdiv_rn(x[4 * e + 3], dv));
     c[e] = lo | (static_cast<uint32_t>(hi) << 16);
   }
   *reinterpret_cast<uint4*>(rec + lane * 16) = make_uint4(c[0], c[1], c[2], c[3]);

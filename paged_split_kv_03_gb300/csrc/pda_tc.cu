@@ -33,12 +33,15 @@
 // row of O^T). All hand-offs are mbarriers; every wait is bounded and a
 // timeout sets PDA_STATUS_WAIT_TIMEOUT and unwinds without hanging.
 //
-// Converted caches add a TMA ring and converter warps in front of the MMA
-// ring: int8 codes widen exactly to f16, and the mixed-precision MLA records
-// dequantise their E4M3 nope chunks (a scale per token and 128 channels) and
-// round their bf16 rope to f16; those builds run kind::f16 MMAs with an f16
-// query and P. The MLA latent (head_dim 576) is read twice from the same
-// cache: as K over all its channels and as V over its first 512.
+// int8 caches add a TMA ring and converter warps in front of the MMA ring:
+// the codes widen exactly to f16, and those builds run kind::f16 MMAs with
+// an f16 query and P. The MLA latent (head_dim 576) is read twice from the
+// same cache: as K over all its channels and as V over its first 512. The
+// mixed-precision MLA records (E4M3 nope with a scale per token and 128
+// channels, bf16 rope) keep the codes as MMA operands too: each nope block's
+// S^T has TMEM columns of its own, the softmax weighs the blocks by their
+// tokens' scales, and each 128-d block of V takes its own P, the weights
+// times that block's scales.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -157,30 +160,6 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
   return make_uint4(two(v.x), two(v.y), two(v.z), two(v.w));
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16};" ::"r"(taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15]))
-      : "memory");
-}
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
   uint32_t r[8];
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
@@ -378,12 +357,16 @@ struct TcCfg {
   // them exactly to f16 into the MMA ring, and the MMAs are kind::f16 (f16
   // query, f16 P)
   static constexpr bool kI8 = KVT == PDA_INT8;
-  // mixed-precision MLA records (E4M3 nope with a scale per 128 channels,
-  // bf16 rope): converter warps dequantise the nope chunks and convert the
-  // rope chunk into an f16 MMA ring, and the MMAs are the latent's kind::f16
+  // mixed-precision MLA records (E4M3 nope with a scale per token and 128
+  // channels, bf16 rope): the nope codes are MMA operands as they are, each
+  // 128-channel block's S^T in TMEM columns of its own (kind::f8f6f4, the
+  // bf16 query as two E4M3 terms), the rope's S^T beside them (kind::f16,
+  // bf16); the softmax weighs the blocks by their tokens' scales, and PV
+  // takes one P per block (P times the block's scale), so that the block
+  // scales never meet the codes in shared memory
   static constexpr bool kMix = SMODE == PDA_SCALE_MLA_BLOCK;
-  static constexpr bool kConv = kI8 || kMix;  // a TMA ring plus converter warps
-  static constexpr bool kF16Ops = kConv;      // ... whose MMAs take f16 operands (f16 Q and P)
+  static constexpr bool kConv = kI8;      // a TMA ring plus converter warps
+  static constexpr bool kF16Ops = kConv;  // ... whose MMAs take f16 operands (f16 Q and P)
   // head_dim 512: a K (or V) tile alone is 64-128 KB, one CTA per SM; int8:
   // one CTA per SM holding both rings
   static constexpr int kCtasPerSm = NMAX <= 16 && D <= 256 && !kI8 ? 2 : 1;
@@ -403,23 +386,19 @@ struct TcCfg {
   static constexpr int kConvWarp0 = kProdWarp1 + kProducers - 1;
   static constexpr int kThreads = 64 + kSmThreads + 32 * (kProducers - 1) + kConvThreads;
   static constexpr int kColGroups = kSmWarps / 4;   // warps sharing a lane quadrant
-  static constexpr bool kF8 = KVT == PDA_E4M3 && !kMix;  // E4M3 MMA operands
+  static constexpr bool kF8 = KVT == PDA_E4M3;  // E4M3 MMA operands
   static constexpr bool kQSplit = kF8 && QT == PDA_BF16;  // bf16 query as two E4M3 terms
   static constexpr int kQTerms = kQSplit ? 2 : 1;
   static constexpr int kElt = kF8 ? 1 : 2;            // bytes of an MMA operand element
   static constexpr int kAtom = 128 / kElt;           // elements per 128-byte row
-  // chunks of a K row (MLA E4M3: the last half-filled, zeros past 576)
+  // chunks of a K row (MLA E4M3: the last half-filled, zeros past 576;
+  // records: the last one the 64 bf16 rope channels)
   static constexpr int kChunksQK = (D + kAtom - 1) / kAtom;
   // ring slots per K tile: 16-bit V blocks take two adjacent slots, so units
   // keep an even size (MLA bf16: 9 chunks and one empty slot, never loaded)
   static constexpr int kChunks = kF8 ? kChunksQK : (kChunksQK + 1) & ~1;
   static constexpr int kChunksV = kDv / kAtom;       // ring slots per V tile
   static constexpr int kRawChunks = kI8 ? D / 128 : kChunks;  // TMA chunks per tile
-  // mixed MLA records: a K tile is 4 nope chunks and the rope chunk, a V tile
-  // the 4 nope chunks; each TMA chunk becomes two MMA-ring slots (the rope's
-  // second one is the K unit's empty slot)
-  static constexpr int kRawK = kMix ? 5 : kRawChunks;
-  static constexpr int kRawV = kMix ? 4 : kRawChunks;
   static constexpr int kTileSlots = kChunks + kChunksV;
   static constexpr int kQRows = kNmax * kQTerms;
   static constexpr int kQAtomBytes = kQRows * 128;
@@ -433,17 +412,25 @@ struct TcCfg {
   static constexpr int kPBufs = kPMn ? 2 : 1;
   static constexpr int kPAtomBytes = kNmax * 128;    // [kNmax rows x 128 B]
   static constexpr int kPBufBytes = kPMn ? kTok * 128 : 2 * kPAtomBytes;
-  static constexpr int kPBytes = kPBufs * kPBufBytes;
   static constexpr int kOBlocks = kDv / 128;
+  // records: one P per 128-d block of V (P times that block's scales)
+  static constexpr int kPSets = kMix ? kOBlocks : 1;
+  static constexpr int kPBytes = kPBufs * kPBufBytes * kPSets;
   // E4M3: one PV MMA of N = 2 x columns yields both terms' sums side by side
   static constexpr int kOCols = kF8 ? 2 * kNmax : kNmax;  // TMEM columns per O block
-  static constexpr int kSCols = kQRows;              // TMEM columns per S buffer
+  // TMEM columns per S buffer (records: the 4 nope blocks' two-term sums,
+  // then the rope's N columns, padded to 32)
+  static constexpr int kSCols = kMix ? kOBlocks * kQRows + 32 : kQRows;
+  // running maxima kept per column: one, or for records the denominator's
+  // and one per 128-d block of O (each block's P carries its own scales)
+  static constexpr int kFrames = kMix ? kOBlocks + 1 : 1;
   static constexpr int kTmemNeed = 2 * kSCols + kOBlocks * kOCols;
   static constexpr int kTmemCols =
       kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
   // two CTAs of an SM share its 512 columns
-  // barriers (512 B), then m_used, alpha, colscale, red[4], linv (kNmax floats each)
-  static constexpr int kSmallBytes = 512 + 8 * kNmax * 4;
+  // barriers (512 B), then m_used [kFrames], alpha [kFrames], colscale,
+  // red [4][kFrames], linv [kPSets] (kNmax floats each)
+  static constexpr int kSmallBytes = 512 + (6 * kFrames + 1 + kPSets) * kNmax * 4;
   static constexpr int kBudget = kCtasPerSm == 2 ? 228 * 1024 / 2 - 1024 : 227 * 1024;
   // the dynamic window starts 1024-byte aligned (checked at run time)
   static constexpr int kAvail = kBudget - kQBytes - kPBytes - kSmallBytes;
@@ -465,8 +452,8 @@ struct TcCfg {
   static constexpr bool kBuildable =
       kRing >= (kI8 ? kChunks + 2 : (D > 256 ? kChunksV : kTileSlots)) && kTmemNeed <= 512 &&
       kTmemCols * kCtasPerSm <= 512 && (!kI8 || (kIRing >= 1 && D <= 256)) &&
-      !(kMla && (kQSplit || kI8)) &&
-      (!kMix || (kMla && KVT == PDA_E4M3 && QT == PDA_BF16 && kIRing >= 2));
+      !(kMla && !kMix && (kQSplit || kI8)) &&
+      (!kMix || (kMla && KVT == PDA_E4M3 && QT == PDA_BF16 && NMAX == 16));
   static constexpr int kSmem = kQBytes + kPBytes + (kRing + kIRing) * kSlot + kSmallBytes;
   // E4M3 MLA latent: V is the first 512 channels of the K tile already in
   // the ring, so no V unit is loaded; each K unit stays until its PV (the
@@ -929,129 +916,314 @@ __device__ __forceinline__ void softmax_role(const DecodeArgs& a, const SoftmaxC
   }
 }
 
-// Mixed-precision MLA records: the converter warps walk the TMA ring in the
-// producer's unit order (K0, K1, then K_{j+2}, V_j, ..., then the last V
-// units). A nope chunk (128 tokens x 128 E4M3 codes of one 128-channel
-// block) becomes two f16 MMA-ring slots, each code pair decoded exactly to
-// f16 and multiplied by its token's block scale (rounded to f16) in one
-// f16x2 multiply; the rope chunk (64 bf16 per token) is rounded to f16 in
-// the first of its two slots (the second is the K unit's empty slot). Rows
-// past the chunk's end are written as zeros. A thread
-// keeps one 16-code piece (gl) of kRows rows; their page ids are loaded two
-// units ahead and their scales one unit ahead, so no load is waited on.
+// Online softmax of the mixed-precision MLA records (the 16-column build).
+// A token's logit is the rope's S^T plus, over the 4 nope blocks, the
+// token's block scale times that block's S^T (both query terms). The
+// denominator sums the plain weights 2^(y - m_0); block b's P holds the
+// weights times the token's scale of block b, 2^(y + log2 s_b - m_b), so
+// that PV of the block's raw codes yields that block of the output. Each of
+// the five sums runs against a running maximum of its own (frame 0: the
+// denominator's, frame 1 + b: block b's), so every P stays <= 2^kTh however
+// the scales range; the epilogue brings each O block into frame 0.
 template <class C>
-__device__ __forceinline__ void mla_convert(const DecodeArgs& a, int ntiles, int t_begin,
-                                            int t_end, int P, int hkv, const int32_t* ptab,
-                                            int ct, uint8_t* ring, const uint8_t* iring,
-                                            uint64_t* full, uint64_t* empty, uint64_t* i_full,
-                                            uint64_t* i_empty, volatile int* abort_flag) {
+__device__ __forceinline__ void softmax_rec(const DecodeArgs& a, const SoftmaxCtx& x, int warp,
+                                            int lane, int tid) {
+  constexpr int N = 16;                  // columns (rows x heads, padded)
+  constexpr int NT = C::kSmThreads;
+  constexpr int NH = N / C::kColGroups;  // columns of this thread
+  constexpr int NB = C::kOBlocks;        // nope blocks
+  constexpr int NF = C::kFrames;         // NB + 1 running maxima per column
+  constexpr int NM = C::kNmax;
   constexpr int R_ = C::kRing;
-  constexpr int kRows = kTok * 8 / C::kConvThreads;  // rows of one thread per chunk
-  constexpr int kRowStep = C::kConvThreads / 8;
-  const int gl = ct & 7, r0 = ct >> 3;
-  const int n = ntiles, units = 2 * ntiles;
-  // unit u of the ring order -> (kind 0 = K / 1 = V, tile)
-  auto unit_at = [&](int u, int& kind, int& tile) {
-    if (n == 1 || u < 2) {
-      kind = n == 1 ? u : 0;
-      tile = n == 1 ? 0 : u;
-      return;
+  static_assert(NH == 8 && NM == N && NF == NB + 1 && C::kPBufs == 1, "one 16-column records build");
+  const int st = tid - 64;       // 0..NT-1
+  const int qd = warp & 3;       // TMEM lane quadrant of this warp
+  const int r = qd * 32 + lane;  // token row of S^T / d row of O^T
+  const int sw = (warp - 2) & 3; // warp index within the column group
+  const int c0 = ((warp - 2) >> 2) * NH;  // first column of this thread
+  const uint32_t bar_id = 2u + static_cast<uint32_t>((warp - 2) >> 2);
+  const int gi = sw * 32 + lane;          // thread index within the column group
+  const uint32_t tl = x.tmem + (static_cast<uint32_t>(qd * 32) << 16);
+  const uint32_t tl_o = tl + 2 * C::kSCols;
+  const int M = x.M, hpc = x.hpc, R = x.R;
+
+  const float qk = a.sm_scale * kLog2e;        // logits in log2 units
+  const float qk_nope = qk * x.colscale[0];    // ... of the nope terms (the query's 2^-a)
+  const int p_first = x.L - R;                   // position of row 0
+  const int all_hi = min(p_first, x.t_end - 1);  // every real row sees keys <= all_hi
+  const int all_lo = x.W > 0 ? x.L - x.W : 0;    // ... and >= all_lo
+
+  float lsum[NH];
+#pragma unroll
+  for (int i = 0; i < NH; ++i) lsum[i] = 0.f;
+  bool alive = true;
+
+  // block scales of this thread's key: page ids three tiles ahead, scales
+  // two (the cursor advances by (kTok / P, kTok % P) per tile)
+  const int sP = x.P;
+  const int dq = kTok / sP, dr = kTok % sP;
+  int cur_pi = (x.t_begin + r) / sP, cur_ps = (x.t_begin + r) % sP, cur_j = 0;
+  auto next_page = [&](int& slot) -> int {
+    const int tok = x.t_begin + cur_j * kTok + r;
+    const int pg = (cur_j < x.ntiles && tok < x.t_end) ? __ldg(x.ptab + cur_pi) : -1;
+    slot = cur_ps;
+    ++cur_j;
+    cur_pi += dq;
+    cur_ps += dr;
+    if (cur_ps >= sP) {
+      cur_ps -= sP;
+      ++cur_pi;
     }
-    const int v = u - 2, pairs = n - 2;
-    if (v < 2 * pairs) {
-      kind = v & 1;
-      tile = (v >> 1) + (kind ? 0 : 2);
-    } else {
-      kind = 1;
-      tile = n - 2 + (v - 2 * pairs);
-    }
+    return pg;
   };
-  auto pages_of = [&](int u, int* pg) {
-    int kind, tile;
-    unit_at(u < units ? u : units - 1, kind, tile);
-#pragma unroll
-    for (int k = 0; k < kRows; ++k) {
-      const int t = t_begin + tile * kTok + r0 + k * kRowStep;
-      pg[k] = t < t_end ? __ldg(ptab + t / P) : -1;
-    }
+  auto scales_for = [&](int page, int slot) -> float4 {
+    if (page < 0 || page >= a.num_pages) return make_float4(0.f, 0.f, 0.f, 0.f);
+    return __ldg(reinterpret_cast<const float4*>(a.k_scale) +
+                 ((int64_t)page * sP + slot) * a.hkv + x.hkv);
   };
-  auto scales_of = [&](int u, const int* pg, float4* sc) {
-    int kind, tile;
-    unit_at(u < units ? u : units - 1, kind, tile);
+  int sl0, sl1, sl_c;
+  const int pg0 = next_page(sl0), pg1 = next_page(sl1);
+  int pg_c = next_page(sl_c);
+  float4 sc_a = scales_for(pg0, sl0), sc_b = scales_for(pg1, sl1);
+
+  // this thread's running maxima (they change only when a vote fires)
+  float mu[NF][NH];
+  auto load_mu = [&]() {
 #pragma unroll
-    for (int k = 0; k < kRows; ++k) {
-      const int t = t_begin + tile * kTok + r0 + k * kRowStep;
-      sc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (pg[k] >= 0 && pg[k] < a.num_pages)
-        sc[k] = __ldg(reinterpret_cast<const float4*>(a.k_scale) +
-                      ((int64_t)pg[k] * P + t % P) * a.hkv + hkv);
-    }
+    for (int f = 0; f < NF; ++f)
+#pragma unroll
+      for (int i = 0; i < NH; i += 4) {
+        const float4 m4 = *reinterpret_cast<const float4*>(x.m_used + f * NM + c0 + i);
+        mu[f][i] = m4.x;
+        mu[f][i + 1] = m4.y;
+        mu[f][i + 2] = m4.z;
+        mu[f][i + 3] = m4.w;
+      }
   };
-  int pg1[kRows], pg2[kRows];
-  float4 sc0[kRows], sc1[kRows];
-  pages_of(0, pg1);
-  scales_of(0, pg1, sc0);
-  pages_of(1, pg1);
-  uint32_t gw = 0;
-  for (int u = 0; u < units; ++u) {
-    int kind, tile;
-    unit_at(u, kind, tile);
-    pages_of(u + 2, pg2);       // two units ahead
-    scales_of(u + 1, pg1, sc1);  // one unit ahead
-    const int nraw = kind ? C::kRawV : C::kRawK;
-    for (int c = 0; c < nraw; ++c, ++gw) {
-      const uint32_t is = gw % C::kIRing;
-      const uint32_t c0 = 2 * gw, d0 = c0 % R_, d1 = (c0 + 1) % R_;
-      bool ok = bar_wait(i_full + is, (gw / C::kIRing) & 1u, abort_flag, a);
-      if (ok) ok = bar_wait(empty + d0, ((c0 / R_) & 1u) ^ 1u, abort_flag, a);
-      if (ok) ok = bar_wait(empty + d1, (((c0 + 1) / R_) & 1u) ^ 1u, abort_flag, a);
-      if (!__all_sync(0xffffffffu, ok)) return;
-      const uint8_t* src = iring + is * kSlot;
-      const bool rope = kind == 0 && c == 4;
+  load_mu();
+
+  for (int j = 0; j < x.ntiles; ++j) {
+    const int tok = x.t_begin + j * kTok + r;
+    const float4 sc = sc_a;
+    sc_a = sc_b;
+    sc_b = scales_for(pg_c, sl_c);
+    pg_c = next_page(sl_c);
+    const float sb[NB] = {sc.x, sc.y, sc.z, sc.w};
+    // columns this key is visible to: rows i with lo_i <= tok <= pos_i
+    int n_lo = M, n_hi = 0;  // empty
+    if (tok < x.t_end) {
+      const int i_lo = max(0, tok - p_first);
+      const int i_hi = x.W > 0 ? min(R - 1, tok + x.W - 1 - p_first) : R - 1;
+      if (i_lo <= i_hi) {
+        n_lo = i_lo * hpc;
+        n_hi = (i_hi + 1) * hpc;
+      }
+    }
+    const int tile0 = x.t_begin + j * kTok;
+    const bool full = tile0 >= all_lo && tile0 + kTok - 1 <= all_hi;
+
+    if (alive) alive = bar_wait(x.s_full + (j & 1), (j >> 1) & 1, x.abort_flag, a);
+    alive = __all_sync(0xffffffffu, alive);
+    fence_after();
+    float y[NH];
 #pragma unroll
-      for (int k = 0; k < kRows; ++k) {
-        const int r = r0 + k * kRowStep;
-        const uint32_t soff = r * 128 + ((gl ^ (r & 7)) << 4);
-        const bool live = t_begin + tile * kTok + r < t_end;
-        if (rope) {
-          const uint4 v = live ? bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(src + soff))
-                               : make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(ring + d0 * kSlot + soff) = v;
-        } else {
-          const float sc = c == 0 ? sc0[k].x : c == 1 ? sc0[k].y : c == 2 ? sc0[k].z : sc0[k].w;
-          const __half2 sc2 = __float2half2_rn(sc);
-          const uint32_t sc2u = *reinterpret_cast<const uint32_t*>(&sc2);
-          uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-          if (live) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(src + soff);
-            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-            uint32_t o[8];
+    for (int i = 0; i < NH; ++i) y[i] = 0.f;
+    if (alive) {
+      const uint32_t scol = tl + (j & 1) * C::kSCols + c0;
+      float v[NB][2][NH], vr[NH];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              uint32_t h01, h23;
-              asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"(static_cast<uint16_t>(w[e] & 0xFFFFu)));
-              asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"(static_cast<uint16_t>(w[e] >> 16)));
-              asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[2 * e]) : "r"(h01), "r"(sc2u));
-              asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[2 * e + 1]) : "r"(h23), "r"(sc2u));
-            }
-            lo = make_uint4(o[0], o[1], o[2], o[3]);
-            hi = make_uint4(o[4], o[5], o[6], o[7]);
-          }
-          uint8_t* dst = ring + (gl < 4 ? d0 : d1) * kSlot + r * 128;
-          const int p0 = (gl & 3) * 2;  // first 16-byte piece of the f16 row
-          *reinterpret_cast<uint4*>(dst + ((p0 ^ (r & 7)) << 4)) = lo;
-          *reinterpret_cast<uint4*>(dst + (((p0 + 1) ^ (r & 7)) << 4)) = hi;
+      for (int b = 0; b < NB; ++b) {
+        tmem_ld8(scol + b * C::kQRows, v[b][0]);
+        tmem_ld8(scol + b * C::kQRows + N, v[b][1]);
+      }
+      tmem_ld8(scol + NB * C::kQRows, vr);
+      tmem_wait_ld();
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        const float w = qk_nope * sb[b];
+#pragma unroll
+        for (int i = 0; i < NH; ++i) y[i] = fmaf(fmaf(v[b][1][i], 0.0625f, v[b][0][i]), w, y[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < NH; ++i) y[i] = fmaf(vr[i], qk, y[i]);
+    }
+    fence_before();
+    bar_arrive(x.s_free + (j & 1));
+    if (!full) {
+#pragma unroll
+      for (int i = 0; i < NH; ++i) {
+        const int n = c0 + i;
+        if (n < n_lo || n >= n_hi) y[i] = -INFINITY;
+      }
+    }
+    // log2 of the block scales (a zero scale: the block adds nothing)
+    float ls[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) ls[b] = sb[b] > 0.f ? __log2f(sb[b]) : -INFINITY;
+
+    // the lazy-rescale vote over all five frames (as in the other builds)
+    float dmax = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < NH; ++i) {
+      dmax = fmaxf(dmax, y[i] - mu[0][i]);
+#pragma unroll
+      for (int b = 0; b < NB; ++b) dmax = fmaxf(dmax, y[i] + ls[b] - mu[1 + b][i]);
+    }
+    const bool fired = colgroup_or(dmax > kTh || !alive || *x.abort_flag != 0, bar_id);
+    if (fired && colgroup_or(!alive || *x.abort_flag != 0, bar_id)) {
+      alive = false;
+      break;
+    }
+    if (fired) {
+      // exact maxima of every frame over the tile's 128 keys
+#pragma unroll
+      for (int f = 0; f < NF; ++f)
+#pragma unroll
+        for (int i = 0; i < NH; ++i) {
+          float v = f == 0 ? y[i] : y[i] + ls[f - 1];
+#pragma unroll
+          for (int off = 16; off; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+          if (lane == 0) x.red[(f * 4 + sw) * NM + c0 + i] = v;
+        }
+      colgroup_sync(bar_id);
+      if (gi < NF * NH) {  // one (frame, column) per thread
+        const int f = gi / NH, c = c0 + gi % NH;
+        const float* rd = x.red + f * 4 * NM + c;
+        const float mx = fmaxf(fmaxf(rd[0], rd[NM]), fmaxf(rd[2 * NM], rd[3 * NM]));
+        const float mo = x.m_used[f * NM + c];
+        const float mn = fmaxf(mo, mx);  // finite: kMInit bounds it below
+        x.alpha[f * NM + c] = ex2(mo - mn);
+        x.m_used[f * NM + c] = mn;
+      }
+      colgroup_sync(bar_id);
+#pragma unroll
+      for (int i = 0; i < NH; ++i) lsum[i] *= x.alpha[c0 + i];
+      load_mu();
+    }
+#pragma unroll
+    for (int i = 0; i < NH; ++i) lsum[i] += ex2(y[i] - mu[0][i]);
+    // the P buffers and O are free once PV of tile j - 1 has finished
+    if (j >= 1) alive = bar_wait(x.pv_done + ((j - 1) & 1), ((j - 1) >> 1) & 1, x.abort_flag, a);
+    alive = __all_sync(0xffffffffu, alive);
+    fence_after();
+    if (alive && fired && j >= 1) {
+      // rescale each O^T block (this thread's d row, both terms) by its frame's alpha
+#pragma unroll
+      for (int blk = 0; blk < NB; ++blk) {
+        float al[NH];
+#pragma unroll
+        for (int i = 0; i < NH; ++i) al[i] = x.alpha[(1 + blk) * NM + c0 + i];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t col = tl_o + blk * C::kOCols + half * N + c0;
+          float v[NH];
+          tmem_ld8(col, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < NH; ++i) v[i] *= al[i];
+          tmem_st8(col, v);
         }
       }
-      fence_async_smem();  // the MMAs read these through the async proxy
-      bar_arrive(full + d0);
-      bar_arrive(full + d1);
-      bar_arrive(i_empty + is);
+      tmem_wait_st();
     }
+    // last tile: rows past the chunk's end may hold stale or poisoned codes
+    if (alive && c0 == 0 && tile0 + kTok > x.t_end && tok >= x.t_end) {
+      const uint32_t gv = unit_pos_v<C>(j, x.ntiles);
+      for (int c = 0; c < C::kChunksV && alive; ++c) {
+        const uint32_t slot = (gv + c) % R_;
+        alive = bar_wait(x.full + slot, ((gv + c) / R_) & 1u, x.abort_flag, a);
+        uint4* row = reinterpret_cast<uint4*>(x.ring + slot * kSlot + r * 128);
 #pragma unroll
-    for (int k = 0; k < kRows; ++k) {
-      sc0[k] = sc1[k];
-      pg1[k] = pg2[k];
+        for (int e = 0; e < 8; ++e) row[e] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    // P^T of each block (K-major, two E4M3 terms: term t of column n in row t * N + n)
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      uint8_t* pb = x.p_s + b * C::kPBufBytes;
+#pragma unroll
+      for (int i = 0; i < NH; i += 2) {
+        uint16_t c1, c2;
+        p_terms(ex2(y[i] + ls[b] - mu[1 + b][i]), ex2(y[i + 1] + ls[b] - mu[1 + b][i + 1]), c1, c2);
+        const int n = c0 + i;
+        pb[sw128(n, r)] = static_cast<uint8_t>(c1 & 0xFF);
+        pb[sw128(n + 1, r)] = static_cast<uint8_t>(c1 >> 8);
+        pb[N * 128 + sw128(n, r)] = static_cast<uint8_t>(c2 & 0xFF);
+        pb[N * 128 + sw128(n + 1, r)] = static_cast<uint8_t>(c2 >> 8);
+      }
+    }
+    fence_async_smem();
+    fence_before();
+    bar_arrive(x.p_full + (j & 1));
+  }
+  // ---------------------------------------------------------- epilogue
+  if (alive && x.ntiles > 0)
+    alive = bar_wait(x.pv_done + ((x.ntiles - 1) & 1), ((x.ntiles - 1) >> 1) & 1, x.abort_flag,
+                     a);
+  fence_after();
+  if (group_or<NT>(!alive)) return;
+  // column sums of the per-token partial denominators
+#pragma unroll
+  for (int i = 0; i < NH; ++i) {
+    float v = lsum[i];
+#pragma unroll
+    for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0) x.red[sw * NM + c0 + i] = v;
+  }
+  group_sync<NT>();
+  if (st < M) {
+    const float lt = x.red[st] + x.red[NM + st] + x.red[2 * NM + st] + x.red[3 * NM + st];
+    const float m0 = x.m_used[st];
+    // block b's O is in frame 1 + b: 2^(m_b - m_0) brings it to the denominator's
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+      x.linv[b * NM + st] = lt > 0.f ? ex2(x.m_used[(1 + b) * NM + st] - m0) / lt : 0.f;
+    const float lse2 = lt > 0.f ? m0 + __log2f(lt) : -INFINITY;
+    const int64_t row = x.q0 + st / hpc;
+    const int head = x.head0 + st % hpc;
+    if (x.single) {
+      if (a.lse) a.lse[row * a.hq + head] = lse2 * kLn2;
+    } else {
+      a.part_lse[((int64_t)x.split * a.rows_cap + row) * a.hq + head] = lse2;
+    }
+  }
+  group_sync<NT>();
+  // O^T out of TMEM (thread = one d row of each block, its columns) through
+  // the idle ring, so that every (row, head) output row leaves as 16-byte
+  // stores of consecutive channels
+  static_assert(NM * C::kDv * 4 <= C::kRing * kSlot, "the ring stages the output");
+  float* ostage = reinterpret_cast<float*>(x.ring);
+#pragma unroll
+  for (int blk = 0; blk < NB; ++blk) {
+    const int d = blk * 128 + r;
+    float v[NH], v2[NH];
+    tmem_ld8(tl_o + blk * C::kOCols + c0, v);
+    tmem_ld8(tl_o + blk * C::kOCols + N + c0, v2);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < NH; ++i) {
+      const int n = c0 + i;
+      if (n < M) ostage[n * C::kDv + d] = (v[i] + v2[i]) * x.linv[blk * NM + n];
+    }
+  }
+  group_sync<NT>();
+  constexpr int kQ = C::kDv / 4;  // 4-channel groups of one output row
+  for (int q = st; q < M * kQ; q += NT) {
+    const int n = q / kQ, c4 = q % kQ;
+    const float4 o = reinterpret_cast<const float4*>(ostage)[q];
+    const int64_t row = x.q0 + n / hpc;
+    const int head = x.head0 + n % hpc;
+    if (x.single) {
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y);
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(o.z, o.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + (row * a.hq + head) * C::kDv +
+                                4 * c4) = pk;
+    } else {
+      *reinterpret_cast<float4*>(a.part_o + (((int64_t)x.split * a.rows_cap + row) * a.hq + head) *
+                                                C::kDv + 4 * c4) = o;
     }
   }
 }
@@ -1089,11 +1261,11 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
   uint64_t* drain = q_ready + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* m_used = reinterpret_cast<float*>(small + 512);
-  float* alpha = m_used + C::kNmax;
-  float* colscale = alpha + C::kNmax;
-  float* red = colscale + C::kNmax;  // [4][C::kNmax]
-  float* linv = red + 4 * C::kNmax;
+  float* m_used = reinterpret_cast<float*>(small + 512);  // [kFrames][kNmax]
+  float* alpha = m_used + C::kFrames * C::kNmax;          // [kFrames][kNmax]
+  float* colscale = alpha + C::kFrames * C::kNmax;
+  float* red = colscale + C::kNmax;  // [4][kFrames][kNmax]
+  float* linv = red + 4 * C::kFrames * C::kNmax;  // [kPSets][kNmax]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -1218,7 +1390,8 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
       const int st = tid - 64;  // 0..kSmThreads-1
       const int sw = warp - 2;  // softmax warp index
       if (st < C::kNmax) {
-        m_used[st] = kMInit;
+#pragma unroll
+        for (int f = 0; f < C::kFrames; ++f) m_used[f * C::kNmax + st] = kMInit;
         colscale[st] = 1.f;
       }
       // ---- query operand Q^T (K-major, 128-byte swizzle), rows n < N (zero
@@ -1254,14 +1427,25 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
         // bf16 query -> Q * 2^a = Q1 + Q2/16 in E4M3 (rows n and N + n), with
         // one exponent a for the CTA, from its largest |Q|. A lane holds kPer
         // elements of each of its warp's rows (n = sw + k * kSmWarps).
-        constexpr int kPer = D / 32;  // elements per lane (16, 8 or 4)
+        // (records: the 512 nope channels; the 64 rope channels stay bf16)
+        constexpr int kDq = C::kMix ? C::kDv : D;
+        constexpr int kPer = kDq / 32;  // elements per lane (16, 8 or 4)
         constexpr int kRowsW = C::kNmax / C::kSmWarps;
         uint32_t raw[kRowsW][kPer / 2];  // bf16 pairs, low half first
+        uint4 rope[kRowsW];              // records: 8 rope channels of lanes 0-7
 #pragma unroll
         for (int k = 0; k < kRowsW; ++k) {
           const int n = sw + k * C::kSmWarps;
 #pragma unroll
           for (int e = 0; e < kPer / 2; ++e) raw[k][e] = 0u;
+          rope[k] = make_uint4(0, 0, 0, 0);
+          if constexpr (C::kMix) {
+            if (n < M && lane < 8)
+              rope[k] = __ldg(reinterpret_cast<const uint4*>(
+                                  static_cast<const uint8_t*>(a.q) +
+                                  (((int64_t)(q0 + n / hpc) * a.hq + head0 + n % hpc) * D + kDq) * 2) +
+                              lane);
+          }
           if (n < M) {
             const uint8_t* src = static_cast<const uint8_t*>(a.q) +
                                  (((int64_t)(q0 + n / hpc) * a.hq + head0 + n % hpc) * D +
@@ -1338,6 +1522,12 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
               *reinterpret_cast<uint32_t*>(dst) = w[0];
             }
           }
+          // records: the rope rows n (bf16, unscaled) in the last atom
+          if constexpr (C::kMix) {
+            if (lane < 8)
+              *reinterpret_cast<uint4*>(q_s + C::kOBlocks * C::kQAtomBytes + sw128(n, lane * 16)) =
+                  rope[k];
+          }
         }
       }
       fence_async_smem();
@@ -1373,8 +1563,7 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
     auto emit8 = [&](int kind, bool ok, int pg, int s0) {
       constexpr uint32_t kIR = C::kIRing > 0 ? C::kIRing : 1;  // (other builds never call this)
       const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, ok));
-      const int nraw = kind ? C::kRawV : C::kRawK;
-      for (int c = 0; c < nraw && alive; ++c, ++g) {
+      for (int c = 0; c < C::kRawChunks && alive; ++c, ++g) {
         const uint32_t slot = g % kIR, round = g / kIR;
         int good = 1;
         if (lane == 0) {
@@ -1390,13 +1579,7 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
           const uint32_t dst = su32(iring + slot * kSlot) + bx * box_bytes;
           const int c1 = a.tma_slot_dim == 1 ? s0 : hkv;
           const int c2 = a.tma_slot_dim == 1 ? hkv : s0;
-          if constexpr (C::kMix) {
-            // nope chunks (K and V) from the code map; the rope chunk from the bf16 map
-            const bool rope = kind == 0 && c == 4;
-            tma_load(dst, rope ? &tmv : &tmk, rope ? 0 : c * 128, c1, c2, pg, i_full + slot);
-          } else {
-            tma_load(dst, maps[kind], c * 128, c1, c2, pg, i_full + slot);
-          }
+          tma_load(dst, maps[kind], c * 128, c1, c2, pg, i_full + slot);
         }
       }
     };
@@ -1424,7 +1607,14 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
           const uint32_t dst = su32(ring + slot * kSlot) + bx * box_bytes;
           const int c1 = a.tma_slot_dim == 1 ? s0 : hkv;
           const int c2 = a.tma_slot_dim == 1 ? hkv : s0;
-          tma_load(dst, maps[kind], c * C::kAtom, c1, c2, pg, full + slot);
+          if constexpr (C::kMix) {
+            // records: nope chunks (K and V) from the code map, the rope
+            // chunk from the bf16 map
+            const bool rp = kind == 0 && c == C::kOBlocks;
+            tma_load(dst, rp ? &tmv : &tmk, rp ? 0 : c * 128, c1, c2, pg, full + slot);
+          } else {
+            tma_load(dst, maps[kind], c * C::kAtom, c1, c2, pg, full + slot);
+          }
         }
       }
     };
@@ -1468,6 +1658,8 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
       const uint32_t id_s = idesc(fmt, 0, static_cast<uint32_t>(Nq));
       // E4M3: N = both P terms' columns; bf16: N columns
       const uint32_t id_p = idesc(fmt, 1, static_cast<uint32_t>(kF8 ? 2 * N : N), C::kPMn ? 1u : 0u);
+      // records: the rope chunk's S^T, bf16 x bf16 (kind::f16), N columns
+      const uint32_t id_rope = idesc(1u, 0, static_cast<uint32_t>(N));
       const uint32_t q_addr = su32(q_s), p_addr = su32(p_s), ring_addr = su32(ring);
       // S^T of tile j into TMEM buffer j & 1 (the softmax has freed it)
       auto issue_s = [&](int j) -> bool {
@@ -1481,7 +1673,17 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
           fence_after();
           const uint32_t abase = ring_addr + slot * kSlot;
           const uint32_t bbase = q_addr + c * C::kQAtomBytes;
-          if (c < C::kChunksQK) {  // (not the empty slot of an even-size unit)
+          if constexpr (C::kMix) {
+            // records: nope block c into its own columns, the rope after them
+            const bool rp = c == C::kOBlocks;
+            const uint32_t d = tmem + sb * C::kSCols + c * C::kQRows;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = sdesc(abase + kk * 32, 16, 1024), bd = sdesc(bbase + kk * 32, 16, 1024);
+              if (rp) mma<false>(d, ad, bd, id_rope, kk != 0);
+              else mma<true>(d, ad, bd, id_s, kk != 0);
+            }
+          } else if (c < C::kChunksQK) {  // (not the empty slot of an even-size unit)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma<kF8>(tmem + sb * C::kSCols, sdesc(abase + kk * 32, 16, 1024),
@@ -1510,10 +1712,12 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
             // V block = one slot (128 d); K = 32 tokens per MMA; both P terms
             // in one MMA (B rows 0..N-1 term 1, N..2N-1 term 2)
             const uint32_t vbase = ring_addr + ((gv + blk) % R_) * kSlot;
+            // (records: block blk's own P)
+            const uint32_t pb = pbuf + (C::kMix ? blk * C::kPBufBytes : 0);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t bd = C::kPMn ? sdesc(pbuf + kk * 4096, 16384, 1024)
-                                          : sdesc(pbuf + kk * 32, 16, 1024);
+              const uint64_t bd = C::kPMn ? sdesc(pb + kk * 4096, 16384, 1024)
+                                          : sdesc(pb + kk * 32, 16, 1024);
               mma<true>(tmem_o + blk * C::kOCols, sdesc(vbase + kk * 4096, kSlot, 1024), bd,
                         id_p, !(j == 0 && kk == 0));
             }
@@ -1584,9 +1788,6 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
         bar_arrive(full + d1);
         bar_arrive(i_empty + is);
       }
-    } else if constexpr (C::kMix) {
-      mla_convert<C>(a, ntiles, t_begin, t_end, P, hkv, ptab, tid - C::kConvWarp0 * 32, ring,
-                     iring, full, empty, i_full, i_empty, abort_flag);
     }
   } else {
     // ========================================= softmax / epilogue warps
@@ -1624,7 +1825,9 @@ __global__ void __launch_bounds__(TcCfg<D, KVT, QT, SMODE, NMAX>::kThreads,
     x.t_end = t_end;
     x.ntiles = ntiles;
     x.single = sr.num_splits == 1;
-    if constexpr (NMAX <= 16) {
+    if constexpr (C::kMix) {
+      softmax_rec<C>(a, x, warp, lane, tid);
+    } else if constexpr (NMAX <= 16) {
       softmax_role<C, SMODE, 1>(a, x, warp, lane, tid);
     } else if constexpr (NMAX <= 32) {
       if (N <= 16) softmax_role<C, SMODE, 1>(a, x, warp, lane, tid);
@@ -1812,8 +2015,10 @@ bool tc_supported(const pda_plan_t* p) {
 // SMs read for a large GQA group with several rows; 96 columns is the widest
 // whose softmax state fits the 96 registers a thread has at 640 threads.
 int tc_rows_limit(const pda_plan_t* p) {
-  // (the MLA latent's E4M3 build likewise: S 2 x N, O 4 x 2N columns)
+  // (the MLA latent's E4M3 build likewise: S 2 x N, O 4 x 2N columns; the
+  // records' per-block S^T, 2 x (4 x 2N + 32) columns, leaves room for 16)
   if (p->head_dim == 128 && p->kv_dtype == PDA_BF16) return 96;
+  if (p->scale_mode == PDA_SCALE_MLA_BLOCK) return 16;
   return p->head_dim >= 512 && p->kv_dtype == PDA_E4M3 ? 32 : kTcRowsPerCta;
 }
 

@@ -495,7 +495,7 @@ def pin_append_mla_record(mutation=0):
     n = int(qo[-1])
     x = torch.randn(n, H, D, generator=g)
     x[:, :, 100] = 9.0   # block 0's maximum in its second 64 channels
-    x[1, 0, 256:384] = 0  # a zero block: scale 1, codes 0
+    x[1, 0, 256:384] = 0  # a zero block: scale 0, codes 0
     k_new = x.to(torch.bfloat16)
     fill = torch.randint(0, 256, (num_pages * P * H * rec,), generator=g, dtype=torch.uint8)
     case = dict(k_new=k_new, v_new=None, page_table=perm, kv_indptr=kv_indptr,
@@ -516,9 +516,10 @@ def pin_append_mla_record(mutation=0):
             for b in range(4):
                 blk = xr[128 * b:128 * (b + 1)]
                 amax = float(blk.abs().max())
-                sc = np.float32(np.float32(amax) / np.float32(448.0)) if amax > 0 else np.float32(1.0)
+                sc = np.float32(np.float32(amax) / np.float32(448.0)) if amax > 0 else np.float32(0.0)
                 assert ks[page, slot, h, b] == sc, (row, h, b)
-                ref = _e4m3_torch((blk / torch.tensor(float(sc))).clamp(-448, 448)).numpy()
+                div = float(sc) if amax > 0 else 1.0
+                ref = _e4m3_torch((blk / torch.tensor(div)).clamp(-448, 448)).numpy()
                 assert np.array_equal(kc[page, slot, h, 128 * b:128 * (b + 1)], ref), (row, h, b)
             rope = k_new[row, h, 512:].contiguous().view(torch.uint8).numpy()
             assert np.array_equal(kc[page, slot, h, 512:], rope), (row, h)
@@ -558,6 +559,7 @@ MUTATIONS = {
     25: "MLA record: nope scale block from 64-channel groups",
     26: "MLA record: rope read at a one-byte stride",
     27: "append: MLA record block amax over its first 64 channels only",
+    28: "append: MLA record zero block given scale 1",
     20: "int8 cache bytes read as unsigned",
     21: "append: int8 per-token scale amax / 128",
     22: "append: int8 ties rounded away from zero",

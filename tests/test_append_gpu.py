@@ -146,7 +146,7 @@ def test_append_mla_records_bit_exact_then_decode():
     wl = make_workload(name="append_mla", seed=41, device="cpu", **args)
     g = torch.Generator().manual_seed(42)
     k_new = (torch.randn(wl.total_rows, 1, 576, generator=g) * 2).to(torch.bfloat16)
-    k_new[0, 0, 128:256] = 0  # a zero block: scale 1, codes 0
+    k_new[0, 0, 128:256] = 0  # a zero block: scale 0, codes 0
     dwl = wl.to(DEV)
     dec = B.Decoder(B.params_for(dwl), device=DEV)
     dec.reset_status()

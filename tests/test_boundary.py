@@ -200,7 +200,9 @@ def test_plan_mla(lib):
     mix, _, rc = B.pda_plan(_params(kv_dtype=1, scale_mode=B.PDA_SCALE_MLA_BLOCK,
                                     **dict(MLA, kv_stride_page=64 * 640, kv_stride_token=640,
                                            kv_stride_head=640)))
-    assert rc == 0 and mix.kernel == B.PDA_KERNEL_TC and mix.rows_per_cta == 32
+    # (their per-block S^T fits TMEM at 16 columns: R = 2 runs two head blocks)
+    assert rc == 0 and mix.kernel == B.PDA_KERNEL_TC and mix.rows_per_cta == 16
+    assert list(mix.heads_per_cta)[1:3] == [16, 8] and mix.head_blocks == 2
     assert mix.stage1_smem_bytes <= 227 * 1024
     for bad in (dict(q_dtype=1), dict(kv_dtype=0), dict(head_dim=512, head_dim_v=0)):
         args = dict(MLA, kv_dtype=1, scale_mode=B.PDA_SCALE_MLA_BLOCK)

@@ -22,7 +22,6 @@ KNOWN_SPILLS = {
     ("stage1_tc", (128, 2, 0, 1, 64)): 8,      # int8 caches, one CTA per SM at 80
     ("stage1_tc", (128, 2, 0, 2, 64)): 24,     # registers a thread
     ("stage1_tc", (256, 2, 0, 2, 64)): 8,
-    ("stage1_tc", (576, 1, 0, 3, 32)): 280,    # MLA records, 32 columns
     ("stage1_mma", (256, 0, 0, 0)): 8,         # mma.sync fallback at head_dim 256
     ("stage1_mma", (256, 1, 1, 1)): 36,
     ("stage1_mma", (256, 2, 0, 1)): 12,

@@ -14,8 +14,8 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import (TOL_BF16, TOL_FP8, assert_close, dv_of, mla_record_lse_bound,
-                         oracle_ref, run_decode, sample_items, tol_for)
+from gpu_helpers import (TOL_BF16, TOL_FP8, assert_close, dv_of, oracle_ref, run_decode,
+                         sample_items, tol_for)
 from paged_split_kv_03_gb300 import binding as B
 from paged_split_kv_03_gb300.synth import (SCALE_NONE, SCALE_TENSOR, SCALE_TOKEN_HEAD,
                                            config_workload, make_workload)
@@ -272,9 +272,7 @@ def test_config_parity(cfg, kw, n_normal, n_peaked, peaked):
     assert torch.isfinite(out).all() and torch.isfinite(lse).all()
     if n_sample is None:
         ref_o, ref_l = oracle_ref(wl)
-        extra = mla_record_lse_bound(wl) if peaked else None
-        assert_close(out, lse, ref_o, ref_l, tol_for(wl), what=cfg, output_rounding=peaked,
-                     lse_extra=extra)
+        assert_close(out, lse, ref_o, ref_l, tol_for(wl), what=cfg, output_rounding=peaked)
     else:
         must = []
         if wl.window is not None:
@@ -285,8 +283,7 @@ def test_config_parity(cfg, kw, n_normal, n_peaked, peaked):
         o = out.reshape(-1, dv_of(wl))[items]
         l_ = lse.reshape(-1)[items]
         assert_close(o, l_, ref_o, ref_l, tol_for(wl), what=f"{cfg} sampled",
-                     output_rounding=peaked,
-                     lse_extra=mla_record_lse_bound(wl, items) if peaked else None)
+                     output_rounding=peaked)
 
 
 def test_tail_split_parity():

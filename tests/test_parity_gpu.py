@@ -180,6 +180,25 @@ def test_small_peaked_parity(kind, kernel):
     assert_close(out, lse, ref_o, ref_l, tol_for(wl), what=f"{kind} peaked", output_rounding=True)
 
 
+@pytest.mark.parametrize("name", ["mla_mix_split_win", "mla_mix_g8_hnd_p16"])
+def test_records_wide_block_scales(name):
+    """MLA records whose block scales are shrunk by 2^0 .. 2^-8, independently
+    per token and 128-channel block (the codes unchanged, so every block still
+    reaches the code 448): the records build weighs each block's P against a
+    running maximum of that block's own, so a token whose scale in one block is
+    far below the block's largest still gets its share. Compared in full with
+    the oracle on the same records."""
+    wl, chunk = _make(name, SMALL[name], seed=9)
+    g = torch.Generator().manual_seed(23)
+    e = torch.randint(-8, 1, tuple(wl.k_scale.shape), generator=g).to(torch.float32)
+    wl.k_scale = wl.k_scale * torch.exp2(e).to(wl.k_scale.device)
+    wl.v_scale = wl.k_scale
+    out, lse, status, dec = run_decode(wl, chunk_pages=chunk)
+    assert status == 0 and dec.plan.kernel == B.PDA_KERNEL_TC
+    ref_o, ref_l = oracle_ref(wl)
+    assert_close(out, lse, ref_o, ref_l, TOL_FP8, what=f"{name} wide block scales")
+
+
 @pytest.mark.parametrize("chunk", [3, 16, 0])
 def test_wide_head_blocks(chunk):
     """bf16 head_dim 128 with a GQA group of 24: the 96-column build holds

@@ -49,7 +49,8 @@ SWEEP = [("mtp_verify_bf16", bs, R) for bs in (1, 16) for R in (1, 4, 8)] + \
         [("longctx_int8_pth", 16, R) for R in (1, 8)] + \
         [("d512_mtp_bf16", 1, R) for R in (1, 4, 8)] + \
         [("d512_mtp_fp8", 1, R) for R in (1, 4, 8)] + \
-        [("mla_bf16", 64, 1), ("mla_fp8", 64, 1), ("mla_fp8", 64, 2), ("mla_fp8_mixed", 64, 1)]
+        [("mla_bf16", 64, 1), ("mla_fp8", 64, 1), ("mla_fp8", 64, 2), ("mla_fp8_mixed", 64, 1),
+         ("mla_fp8_mixed", 64, 2)]
 # the same FP8 decode batch with the cache in HND order (one kv head's page
 # contiguous) beside the NHD headline: the access-pattern check
 LAYOUT_SWEEP = [("fp8_decode", dict(layout="HND"), "fp8_decode bs128 R1 HND")]

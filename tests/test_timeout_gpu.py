@@ -13,9 +13,10 @@ must again match the oracle.
 import pytest
 import torch
 
-from gpu_helpers import TOL_BF16, TOL_FP8, assert_close, oracle_ref
+from gpu_helpers import TOL_BF16, TOL_FP8, assert_close, dv_of, oracle_ref
 from paged_split_kv_03_gb300 import binding as B
-from paged_split_kv_03_gb300.synth import SCALE_TOKEN_HEAD, make_workload
+from paged_split_kv_03_gb300.synth import (SCALE_MLA_BLOCK, SCALE_TENSOR, SCALE_TOKEN_HEAD,
+                                           make_workload)
 
 pytestmark = pytest.mark.gpu
 
@@ -25,6 +26,14 @@ CASES = {
     "fp8pth_d256": (dict(batch=2, rows=[4, 8], kv_lens=[900, 400], num_qo_heads=16,
                          num_kv_heads=2, head_dim=256, page_size=16, kv_dtype="e4m3",
                          scale_mode=SCALE_TOKEN_HEAD), TOL_FP8),
+    # the E4M3 MLA latent (V taken from the K unit in the ring) and the
+    # mixed-precision records (their own softmax with five running maxima)
+    "mla_fp8": (dict(batch=2, rows=[1, 1], kv_lens=[700, 300], num_qo_heads=16,
+                     num_kv_heads=1, head_dim=576, head_dim_v=512, page_size=64,
+                     kv_dtype="e4m3", q_dtype="e4m3", scale_mode=SCALE_TENSOR), TOL_FP8),
+    "mla_records": (dict(batch=2, rows=[1, 2], kv_lens=[700, 300], num_qo_heads=16,
+                         num_kv_heads=1, head_dim=576, head_dim_v=512, page_size=64,
+                         kv_dtype="e4m3", scale_mode=SCALE_MLA_BLOCK), TOL_FP8),
 }
 
 
@@ -37,7 +46,7 @@ def test_withheld_loads_time_out_and_the_next_call_is_correct(name):
     bad = B.Decoder(B.params_for(wl, chunk_pages=chunk, kernel=B.PDA_KERNEL_TC,
                                  wait_limit_us=2000, inject=B.PDA_INJECT_WITHHOLD_KV))
     assert bad.plan.max_splits == 1 and bad.plan.wait_limit_us == 2000
-    out = torch.full((wl.total_rows, wl.num_qo_heads, wl.head_dim), float("nan"),
+    out = torch.full((wl.total_rows, wl.num_qo_heads, dv_of(wl)), float("nan"),
                      dtype=torch.bfloat16, device="cuda")
     lse = torch.full((wl.total_rows, wl.num_qo_heads), float("nan"), device="cuda")
     bad.run(wl, out, lse)

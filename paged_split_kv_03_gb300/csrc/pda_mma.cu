@@ -558,29 +558,35 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_mma(const __grid_constant_
 // maximum of their LSEs, its sums rescaled when the maximum rises -- with all
 // of a batch's loads (LSE and partial output) in flight at once, so a warp
 // with at most kBatch splits waits for one round of loads; the WPI warps then
-// combine their (maximum, sum, output) triples through shared memory.
-template <int D, int WPI>
+// combine their (maximum, sum, output) triples through shared memory. With
+// SPLIT, a CTA holds one slice of a row (its WPI warps), so that a row of
+// many splits spreads over kSlices CTAs and more warps share its splits.
+template <int D, int WPI, int SPLIT = 0>
 struct MergeCfg {
   static constexpr int kVW = D >= 128 ? 4 : 2;                  // floats per lane
   static constexpr int kSlices = D / (32 * kVW);                // warps across the row
-  static constexpr int kWarpsPerItem = kSlices * WPI;           // <= 32
-  static constexpr int kItems = kWarpsPerItem >= 8 ? 1 : 8 / kWarpsPerItem;  // rows per CTA
+  static constexpr int kSlicesCta = SPLIT ? 1 : kSlices;        // ... within one CTA
+  static constexpr int kWarpsPerItem = kSlicesCta * WPI;        // <= 32
+  // (row, or with SPLIT (row, slice)) units per CTA
+  static constexpr int kItems = kWarpsPerItem >= 8 ? 1 : 8 / kWarpsPerItem;
   static constexpr int kThreads = kItems * kWarpsPerItem * 32;
   static constexpr int kBatch = 12;                             // partials in flight
 };
 
-template <int D, int WPI>
-__global__ void __launch_bounds__(MergeCfg<D, WPI>::kThreads)
+template <int D, int WPI, int SPLIT>
+__global__ void __launch_bounds__(MergeCfg<D, WPI, SPLIT>::kThreads)
     stage2_merge(const __grid_constant__ DecodeArgs a) {
-  using M = MergeCfg<D, WPI>;
+  using M = MergeCfg<D, WPI, SPLIT>;
   constexpr int kVW = M::kVW;
   __shared__ __align__(16) float sh_acc[M::kThreads / 32][32 * kVW];
   __shared__ float sh_m[M::kThreads / 32];
   __shared__ float sh_l[M::kThreads / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wi = warp % M::kWarpsPerItem;
-  const int slice = wi % M::kSlices, sub = wi / M::kSlices;
-  const int64_t item = a.merge_item0 + (int64_t)blockIdx.x * M::kItems + warp / M::kWarpsPerItem;
+  const int64_t unit = (int64_t)blockIdx.x * M::kItems + warp / M::kWarpsPerItem;
+  const int sub = wi / M::kSlicesCta;
+  const int slice = SPLIT ? static_cast<int>(unit % M::kSlices) : wi % M::kSlices;
+  const int64_t item = a.merge_item0 + (SPLIT ? unit / M::kSlices : unit);
   const int64_t per_b = (int64_t)a.max_q_len * a.hq;
   bool valid = false;
   int n = 0;
@@ -661,14 +667,14 @@ __global__ void __launch_bounds__(MergeCfg<D, WPI>::kThreads)
     __syncthreads();
     if (sub == 0) {
       float mx = m;
-      for (int k = 1; k < WPI; ++k) mx = fmaxf(mx, sh_m[warp + k * M::kSlices]);
+      for (int k = 1; k < WPI; ++k) mx = fmaxf(mx, sh_m[warp + k * M::kSlicesCta]);
       if (mx != -INFINITY) {
         const float f0 = exp2f(m - mx);
         l *= f0;
 #pragma unroll
         for (int e = 0; e < kVW; ++e) acc[e] *= f0;
         for (int k = 1; k < WPI; ++k) {
-          const int w2 = warp + k * M::kSlices;  // same slice, split group k
+          const int w2 = warp + k * M::kSlicesCta;  // same slice, split group k
           const float mk = sh_m[w2];
           if (mk == -INFINITY) continue;
           const float f = exp2f(mk - mx);
@@ -740,35 +746,54 @@ KernelFn stage1_for(const pda_plan_t* p) {
 }
 
 // Warps per slice of a merged row: one up to 12 splits, then up to 12
-// splits a warp (one round of loads each), with at most 16 warps per row
-// (head_dim 512: 4 slices x 4), so that a CTA of 512 threads keeps its
-// batch of partials in registers.
-static int stage2_wpi(const pda_plan_t* p) {
+// splits a warp (one round of loads each), up to 8 warps (16 where each
+// slice has a CTA of its own) so that a CTA of at most 512 threads keeps
+// its batch of partials in registers. Rows of 256 or 512 channels with more
+// than 12 splits give each slice its own CTA (SPLIT: up to 16 warps share a
+// slice's splits) when the rows' slices still fit one CTA per SM -- few
+// rows of many splits, as at bs 1 with 4 to 16 rows x heads (measured:
+// head_dim 512 bf16 bs 1 R 1 38.9 -> 35.3 us per call); with more rows the
+// extra CTAs cost more than the shorter rounds save (bs 1 R 8: +1.3 to
+// +1.7 us).
+static int stage2_wpi(const pda_plan_t* p, bool split) {
   const int s = p->max_splits;
-  const int w = s <= 12 ? 1 : s <= 24 ? 2 : s <= 48 ? 4 : 8;
-  return p->head_dim_v == 512 && w > 4 ? 4 : w;
+  const int w = s <= 12 ? 1 : s <= 24 ? 2 : s <= 48 ? 4 : s <= 96 ? 8 : 16;
+  return split ? w : (w > 8 ? 8 : (p->head_dim_v == 512 && w > 4 ? 4 : w));
 }
 struct Stage2Launch {
   KernelFn fn;
-  int items_per_cta, threads;
+  int units_per_cta, threads, slices;  // slices: CTAs per row (1 unless SPLIT)
 };
-template <int D, int WPI>
+template <int D, int WPI, int SPLIT>
 Stage2Launch stage2_entry() {
-  using M = MergeCfg<D, WPI>;
-  return {stage2_merge<D, WPI>, M::kItems, M::kThreads};
+  using M = MergeCfg<D, WPI, SPLIT>;
+  return {stage2_merge<D, WPI, SPLIT>, M::kItems, M::kThreads, SPLIT ? M::kSlices : 1};
 }
 template <int D>
 Stage2Launch stage2_pick(int wpi) {
   switch (wpi) {
-    case 1: return stage2_entry<D, 1>();
-    case 2: return stage2_entry<D, 2>();
-    case 4: return stage2_entry<D, 4>();
-    default: return stage2_entry<D, (D == 512 ? 4 : 8)>();
+    case 1: return stage2_entry<D, 1, 0>();
+    case 2: return stage2_entry<D, 2, 0>();
+    case 4: return stage2_entry<D, 4, 0>();
+    default: return stage2_entry<D, (D == 512 ? 4 : 8), 0>();
   }
 }
-Stage2Launch stage2_for(const pda_plan_t* p) {
-  const int wpi = stage2_wpi(p);
-  switch (p->head_dim_v) {  // the merged rows have the value channels
+template <int D>
+Stage2Launch stage2_pick_split(int wpi) {
+  switch (wpi) {
+    case 2: return stage2_entry<D, 2, 1>();
+    case 4: return stage2_entry<D, 4, 1>();
+    case 8: return stage2_entry<D, 8, 1>();
+    default: return stage2_entry<D, 16, 1>();
+  }
+}
+Stage2Launch stage2_for(const pda_plan_t* p, int64_t items) {
+  // the merged rows have the value channels
+  const bool split = p->head_dim_v >= 256 && p->max_splits > 12 &&
+                     items * (p->head_dim_v / 128) <= p->num_sms;
+  const int wpi = stage2_wpi(p, split);
+  if (split) return p->head_dim_v == 256 ? stage2_pick_split<256>(wpi) : stage2_pick_split<512>(wpi);
+  switch (p->head_dim_v) {
     case 64: return stage2_pick<64>(wpi);
     case 128: return stage2_pick<128>(wpi);
     case 256: return stage2_pick<256>(wpi);
@@ -828,9 +853,10 @@ int launch_stage2(const pda_plan_t* plan, const DecodeArgs& args, cudaStream_t s
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t c2 = {};
-  const Stage2Launch l2 = stage2_for(plan);
-  const int per_cta = l2.items_per_cta;
-  c2.gridDim = dim3(static_cast<unsigned>((items + per_cta - 1) / per_cta));
+  const Stage2Launch l2 = stage2_for(plan, items);
+  const int64_t units = items * l2.slices;
+  const int per_cta = l2.units_per_cta;
+  c2.gridDim = dim3(static_cast<unsigned>((units + per_cta - 1) / per_cta));
   c2.blockDim = dim3(static_cast<unsigned>(l2.threads));
   c2.dynamicSmemBytes = 0;
   c2.stream = s;

@@ -748,13 +748,13 @@ KernelFn stage1_for(const pda_plan_t* p) {
 // Warps per slice of a merged row: one up to 12 splits, then up to 12
 // splits a warp (one round of loads each), up to 8 warps (16 where each
 // slice has a CTA of its own) so that a CTA of at most 512 threads keeps
-// its batch of partials in registers. Rows of 256 or 512 channels with more
-// than 12 splits give each slice its own CTA (SPLIT: up to 16 warps share a
+// its batch of partials in registers. Rows of 512 channels with more than
+// 12 splits give each slice its own CTA (SPLIT: up to 16 warps share a
 // slice's splits) when the rows' slices still fit one CTA per SM -- few
-// rows of many splits, as at bs 1 with 4 to 16 rows x heads (measured:
-// head_dim 512 bf16 bs 1 R 1 38.9 -> 35.3 us per call); with more rows the
-// extra CTAs cost more than the shorter rounds save (bs 1 R 8: +1.3 to
-// +1.7 us).
+// rows of many splits, as at bs 1 with 16 rows x heads (measured: head_dim
+// 512 bf16 bs 1 R 1 37.6 -> 34.8 us per call); with more rows the extra CTAs
+// cost more than the shorter rounds save (bs 1 R 8: +1.3 to +1.7 us), and
+// at 256 channels (two slices) the call moved by less than its noise.
 static int stage2_wpi(const pda_plan_t* p, bool split) {
   const int s = p->max_splits;
   const int w = s <= 12 ? 1 : s <= 24 ? 2 : s <= 48 ? 4 : s <= 96 ? 8 : 16;
@@ -789,10 +789,9 @@ Stage2Launch stage2_pick_split(int wpi) {
 }
 Stage2Launch stage2_for(const pda_plan_t* p, int64_t items) {
   // the merged rows have the value channels
-  const bool split = p->head_dim_v >= 256 && p->max_splits > 12 &&
-                     items * (p->head_dim_v / 128) <= p->num_sms;
+  const bool split = p->head_dim_v == 512 && p->max_splits > 12 && items * 4 <= p->num_sms;
   const int wpi = stage2_wpi(p, split);
-  if (split) return p->head_dim_v == 256 ? stage2_pick_split<256>(wpi) : stage2_pick_split<512>(wpi);
+  if (split) return stage2_pick_split<512>(wpi);
   switch (p->head_dim_v) {
     case 64: return stage2_pick<64>(wpi);
     case 128: return stage2_pick<128>(wpi);
